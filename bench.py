@@ -1,0 +1,506 @@
+#!/usr/bin/env python3
+"""Benchmark of the masked GQA attention library on synthetic engine-shaped
+workloads; prints ONE JSON line (rank 0).
+
+Headline workload (one "step"): the OmniVoice-shaped padded
+classifier-free-guidance prefill -- batch 2 (conditional row: 1024 valid keys;
+unconditional row: 384 valid keys, rest padded), 16 query heads, 8 KV heads,
+head_dim 128, 1024 positions, bf16, 4D key-padding mask as packed bits --
+called 32 times (the 32 unmasking steps), each call on the next of 8
+rotating input sets (201 MB > L2) so every call reads HBM. The step is
+captured once in a CUDA graph and replayed.
+
+Also measured in the same run and reported under "decode" and
+"other_workloads": static-cache decode (8 requests, 16/2 heads, dim 64,
+8192-slot cache, filled 256..3100, 16 rotating cache sets of 33.5 MB),
+packed-guidance prefill (one 1408-position row, segments 1024 + 384), and the
+DiT batch (32 rows x 4096 positions, 1..6 segments per row).
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "masked GQA prefill TFLOP/s & cache-decode GB/s, as % of GB300 roofline"
+CALLS_PER_STEP = 32
+PREFILL_SETS = 8
+DECODE_SETS = 16
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(d, *keys):
+    for k in keys:
+        if k in d and isinstance(d[k], (int, float)):
+            return float(d[k])
+        for sub in d.values():
+            if isinstance(sub, dict) and k in sub and isinstance(sub[k], (int, float)):
+                return float(sub[k])
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def device_inputs(wl, dev):
+    d = {}
+    for n in ("q", "k", "v", "mask_bits", "kv_len", "seg_q", "seg_k"):
+        t = getattr(wl, n)
+        d[n] = None if t is None else t.to(dev)
+    return d
+
+
+def make_args(M, d, out, wl, lse=None):
+    return M.make_args(d["q"], d["k"], d["v"], out, scale=wl.scale, mask_bits=d["mask_bits"],
+                       kv_len=d["kv_len"], seg_q=d["seg_q"], seg_k=d["seg_k"], lse=lse)
+
+
+def time_graph(step_fn, steps, warmup, stream, world):
+    """Capture step_fn in a CUDA graph; time exactly `steps` replays."""
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step_fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step_fn()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3, g
+
+
+# ---------------------------------------------------------------- workloads
+
+def bench_prefill_graph(M, wl, dev, calls, nsets, steps, warmup, world):
+    """Device-resident inputs, rotating sets, step = `calls` prefill calls."""
+    import ctypes
+    base = device_inputs(wl, dev)
+    sets = []
+    for s in range(nsets):
+        d = {n: (t.clone() if t is not None else None) for n, t in base.items()}
+        out = torch.empty_like(d["q"])
+        sets.append((d, out, make_args(M, d, out, wl)))
+    L = M.lib()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        h = stream.cuda_stream
+        for c in range(calls):
+            a = sets[c % nsets][2]
+            st = L.masked_gqa_attn_prefill(ctypes.byref(a), h)
+            if st != 0:
+                raise RuntimeError(f"prefill failed: {L.mgqa_last_error_detail()}")
+
+    secs, _ = time_graph(step, steps, warmup, stream, world)
+    return secs, sets
+
+
+def bench_prefill_e2e(M, wl, dev, calls, steps, warmup, world):
+    """Through the C ABI from pinned host buffers: per step H2D of q/k/v/mask,
+    `calls` prefill calls, D2H of the output."""
+    import ctypes
+    host = {n: (getattr(wl, n).pin_memory() if getattr(wl, n) is not None else None)
+            for n in ("q", "k", "v", "mask_bits", "kv_len", "seg_q", "seg_k")}
+    d = {n: (torch.empty_like(t, device=dev) if t is not None else None) for n, t in host.items()}
+    out = torch.empty_like(d["q"])
+    out_host = torch.empty_like(host["q"]).pin_memory()
+    a = make_args(M, d, out, wl)
+    L = M.lib()
+    stream = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for n, t in host.items():
+                if t is not None:
+                    d[n].copy_(t, non_blocking=True)
+            for _ in range(calls):
+                st = L.masked_gqa_attn_prefill(ctypes.byref(a), stream.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(L.mgqa_last_error_detail())
+            out_host.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
+
+
+def decode_needed_bytes(wl):
+    B, Hq, Hkv, Lq, Lk, D = wl.shape
+    es = wl.k.element_size()
+    filled = sum(int(x) for x in wl.allowed()[:, 0, :].sum(-1))
+    kv = filled * Hkv * D * 2 * es
+    qo = 2 * B * Hq * D * es
+    mask = 0 if wl.mask_bits is None else B * ((Lk + 31) // 32) * 4
+    return kv + qo + mask
+
+
+def bench_decode(M, wl, dev, steps, warmup, world, nsets=DECODE_SETS, calls=16):
+    import ctypes
+    base = device_inputs(wl, dev)
+    sets = []
+    for s in range(nsets):
+        d = {n: (t.clone() if t is not None else None) for n, t in base.items()}
+        out = torch.empty_like(d["q"])
+        a = make_args(M, d, out, wl)
+        masks = {n: d[n] for n in ("mask_bits", "kv_len", "seg_q", "seg_k")}
+        ws = M.new_decode_workspace(d["q"], d["k"], d["v"], **masks)
+        sets.append((d, out, a, ws))
+    L = M.lib()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        for c in range(calls):
+            d, out, a, ws = sets[c % nsets]
+            st = L.masked_gqa_attn_decode(ctypes.byref(a), ws.data_ptr(), ws.numel(),
+                                          stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(L.mgqa_last_error_detail())
+
+    secs, _ = time_graph(step, steps, warmup, stream, world)
+    return secs / (steps * calls)
+
+
+def bench_decode_e2e(M, wl, dev, steps, warmup, world):
+    """Per step: H2D of the new query and lengths, one decode call, D2H of the
+    output (the cache stays resident, as a static KV cache does)."""
+    import ctypes
+    d = device_inputs(wl, dev)
+    hq = wl.q.pin_memory()
+    hl = wl.kv_len.pin_memory() if wl.kv_len is not None else None
+    out = torch.empty_like(d["q"])
+    oh = torch.empty_like(hq).pin_memory()
+    a = make_args(M, d, out, wl)
+    masks = {n: d[n] for n in ("mask_bits", "kv_len", "seg_q", "seg_k")}
+    ws = M.new_decode_workspace(d["q"], d["k"], d["v"], **masks)
+    L = M.lib()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        with torch.cuda.stream(stream):
+            d["q"].copy_(hq, non_blocking=True)
+            if hl is not None:
+                d["kv_len"].copy_(hl, non_blocking=True)
+            st = L.masked_gqa_attn_decode(ctypes.byref(a), ws.data_ptr(), ws.numel(),
+                                          stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(L.mgqa_last_error_detail())
+            oh.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    h2d = hq.numel() * hq.element_size() + (hl.numel() * 4 if hl is not None else 0)
+    d2h = oh.numel() * oh.element_size()
+    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+
+
+def traffic_from_profiles(kernel_file: str):
+    """DRAM bytes per launch recorded by an ncu capture of the current kernel
+    source (profiles/*.md line 'traffic: <bytes> source-sha256: <hex>'), or None."""
+    import glob
+    import hashlib
+    src = os.path.join(ROOT, "masked_gqa_attention_gb300", "csrc", kernel_file)
+    if not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        for line in open(p):
+            if line.startswith("traffic:") and f"source-sha256: {sha}" in line and kernel_file in line:
+                try:
+                    return float(line.split()[1])
+                except ValueError:
+                    pass
+    return None
+
+
+# ---------------------------------------------------------------- arms
+
+def cpu_oracle_sample(wl, heads: int):
+    """Time the oracle on the first `heads` query heads of the workload (both rows)."""
+    import oracle
+    oracle.build()
+    n_rep = wl.q.shape[1] // wl.k.shape[1]
+    hk = max(1, math.ceil(heads / n_rep))
+    q = wl.q[:, :heads].contiguous()
+    k = wl.k[:, :hk].contiguous()
+    v = wl.v[:, :hk].contiguous()
+    t0 = time.perf_counter()
+    _, _, used = oracle.attention(q, k, v, scale=wl.scale, **wl.masks())
+    secs = time.perf_counter() - t0
+    flops = wl.flops() * heads / wl.q.shape[1]
+    return flops, secs, used
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = W.padded_cfg(variant="bits")
+    heads = 2
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, heads)
+    tot_f, tot_s, used = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        f, s, used = cpu_oracle_sample(wl, heads)
+        tot_f += f
+        tot_s += s
+    value = tot_f / tot_s / 1e12
+    sample = (f"{heads} of 16 query heads (both CFG rows) of one padded-CFG prefill call "
+              f"(2x1024 positions, head_dim 128) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "padded_cfg_bits (B=2, Hq=16, Hkv=8, D=128, L=1024; keys 1024/384)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_gpu(args):
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import masked_gqa_attention_gb300 as M
+    M.build_library()
+    M.lib()
+    pk, pk_kind = peaks()
+    hbm = peak_value(pk, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
+    bf16 = peak_value(pk, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
+
+    clocks = ClockSampler(local)
+    # ---- headline: padded CFG prefill, 32 calls per step
+    wl = W.padded_cfg(variant="bits")
+    flops_call = wl.flops()
+    clocks.start()
+    secs, _ = bench_prefill_graph(M, wl, dev, CALLS_PER_STEP, PREFILL_SETS, args.steps,
+                                  args.warmup, world)
+    clk = clocks.stop()
+    secs = max_over_ranks(secs, world)
+    calls = args.steps * CALLS_PER_STEP
+    per_call = secs / calls
+    value = world * calls * flops_call / secs / 1e12
+    achieved = flops_call / per_call / 1e12
+
+    e2e_secs, h2d, d2h = bench_prefill_e2e(M, wl, dev, CALLS_PER_STEP, max(3, args.steps // 10),
+                                           3, world)
+    e2e_steps = max(3, args.steps // 10)
+    e2e_secs = max_over_ranks(e2e_secs, world)
+    e2e_value = world * e2e_steps * CALLS_PER_STEP * flops_call / e2e_secs / 1e12
+
+    # ---- decode: static cache, full-cache bits and filled-span variants
+    dec = {}
+    for variant in ("full", "span"):
+        wd = W.static_cache_decode(variant=variant)
+        t = bench_decode(M, wd, dev, max(10, args.steps // 2), args.warmup, world)
+        nb = decode_needed_bytes(wd)
+        dec[variant] = {"us_per_call": t * 1e6, "needed_bytes": nb, "GB_s": nb / t / 1e9,
+                        "frac": nb / t / 1e9 / hbm}
+    wd = W.static_cache_decode(variant="span")
+    de2e, dh2d, dd2h = bench_decode_e2e(M, wd, dev, 200, 20, world)
+    nb = decode_needed_bytes(wd)
+
+    # ---- the other prefill workloads
+    others = {}
+    for name, maker, calls_o in (("packed_guidance", W.packed_guidance, 32),
+                                 ("dit_batch", W.dit_batch, 20)):
+        wo = maker()
+        nsets = 8 if name == "packed_guidance" else 1
+        so, _ = bench_prefill_graph(M, wo, dev, calls_o, nsets, 3, 2, world)
+        pc = so / (3 * calls_o)
+        others[name] = {"us_per_call": pc * 1e6, "allowed_TFLOP_s": wo.flops() / pc / 1e12,
+                        "nonempty_tile_TFLOP_s": wo.nonempty_tile_flops() / pc / 1e12,
+                        "frac_nonempty_of_peak": wo.nonempty_tile_flops() / pc / 1e12 / bf16}
+        del wo
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "padded_cfg_bits: B=2 CFG rows (keys 1024 / 384 valid), Hq=16, "
+                               "Hkv=8, D=128, L=1024, bf16, 4D key-padding mask as packed bits; "
+                               "32 calls per step",
+                   "l2": f"{PREFILL_SETS} rotating input sets (201 MB > L2)",
+                   "graph": "each step captured once in a CUDA graph", "parallelism": f"replicas x{world}"},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": calls,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": achieved / bf16, "traffic": traffic_from_profiles("prefill_tc.cu"),
+                     "peak_kind": f"bf16 burst, {pk_kind}",
+                     "flops_per_launch": flops_call, "kernel": "prefill_tc"},
+        "decode": {"workload": "static_cache_decode: B=8, Hq=16, Hkv=2, D=64, bf16, 8192 slots, "
+                               "filled 256..3100; 16 rotating cache sets (537 MB > L2)",
+                   "value": dec["span"]["GB_s"], "unit": "GB/s", "variants": dec,
+                   "roofline": {"bound": "hbm", "achieved": dec["span"]["GB_s"], "peak": hbm,
+                                "unit": "GB/s", "frac": dec["span"]["GB_s"] / hbm,
+                                "traffic": traffic_from_profiles("decode.cu"),
+                                "peak_kind": pk_kind, "bytes_per_launch": nb},
+                   "e2e": {"value": nb / de2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": dh2d,
+                           "d2h_bytes_per_step": dd2h}},
+        "other_workloads": others,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        heads = 4
+        f, s, used = cpu_oracle_sample(wl, heads)
+        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": used,
+                                "kind": "oracle",
+                                "sample": f"{heads} of 16 query heads (both CFG rows) of one "
+                                          f"padded-CFG prefill call, {s:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mgqa", choices=["mgqa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,142 @@
+/*
+ * masked_gqa_attn.h -- C ABI of the GB300 (sm_103a) masked grouped-query
+ * attention library.
+ *
+ * The operation (both entry points): scaled-dot-product attention with
+ * grouped KV heads under an explicit boolean mask, as the engine pages use it:
+ *   - VoxCPM page, "Upstream-identical practice", attention bullet: SDPA with
+ *     enable_gqa on contiguous tensors; bidirectional in the local DiT; cache
+ *     decode under an explicit boolean mask where slots past the current length
+ *     are masked and contribute exact zeros;
+ *   - OmniVoice page, "Upstream-identical practice", attention-mask bullet: a
+ *     full 4D boolean mask, not causal, with the KV heads repeated to the query
+ *     heads; the conditional and unconditional rows run as one batch;
+ *   - OmniVoice page, "Memory & speed", packed_guidance paragraph: both
+ *     sequences side by side in one row under a block-diagonal mask;
+ *   - VoxCPM page, "Memory & speed", attention_span paragraph: attend only to
+ *     the filled blocks of the 8192-slot static cache.
+ *
+ * For batch b, query head h, query row i, with KV head g = h / (Hq / Hkv):
+ *   s_j   = scale * <q[b,h,i,:], k[b,g,j,:]>   where allowed(b,i,j), else -inf
+ *   out   = sum_j softmax(s)_j * v[b,g,j,:]
+ *   lse   = log(sum_j exp(s_j))                 (natural log, optional output)
+ * A query row with no allowed key gets out = 0 and lse = -inf.
+ *
+ * allowed(b,i,j) is the AND of every mask form that is given (non-NULL):
+ *   mask_bits : bit (j % 32) of word mask_bits[b*mask_stride_b + i*mask_stride_q
+ *               + j/32] is 1 (least-significant bit first, 1 = may attend);
+ *               the same mask applies to every head;
+ *   kv_len    : j < kv_len[b]  (a per-row key length; for decode, the filled
+ *               length of the static cache);
+ *   seg_q/seg_k: seg_q[b*Lq + i] == seg_k[b*Lk + j] and that id is >= 0
+ *               (block-diagonal packing; negative ids attend nowhere).
+ * With no mask form given every key is allowed (dense bidirectional).
+ *
+ * Ownership: every pointer is device memory owned by the caller. The library
+ * allocates nothing, never synchronises, and enqueues its work on `stream`
+ * only. Errors found on the host return at once and enqueue nothing; errors
+ * found on the device are written to *dev_error (when given) as the first
+ * mgqa_status code seen, and the affected outputs are still written.
+ */
+#ifndef MASKED_GQA_ATTN_H
+#define MASKED_GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MGQA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define MGQA_API __attribute__((visibility("default")))
+#else
+#define MGQA_API
+#endif
+
+typedef enum {
+  MGQA_OK = 0,
+  MGQA_ERR_INVALID_ARG = 1,  /* bad pointer, shape, stride, alignment or scale;
+                                on the device: kv_len < 0 or kv_len > Lk */
+  MGQA_ERR_UNSUPPORTED = 2,  /* valid request this build has no kernel for */
+  MGQA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MGQA_ERR_TIMEOUT = 4       /* device: a bounded pipeline wait gave up */
+} mgqa_status;
+
+typedef enum {
+  MGQA_BF16 = 0,  /* q/k/v/out bf16, fp32 accumulation (tensor cores) */
+  MGQA_FP32 = 1   /* q/k/v/out fp32, fp32 arithmetic throughout */
+} mgqa_dtype;
+
+typedef struct mgqa_args {
+  mgqa_dtype dtype;
+  int32_t B;    /* batch rows */
+  int32_t Hq;   /* query heads */
+  int32_t Hkv;  /* KV heads; Hq % Hkv == 0 */
+  int32_t Lq;   /* query positions (decode: must be 1) */
+  int32_t Lk;   /* key positions (decode: static-cache capacity) */
+  int32_t D;    /* head dim: 64 or 128 */
+
+  /* q [B][Hq][Lq][D], k and v [B][Hkv][Lk][D], out [B][Hq][Lq][D]. The head-dim
+   * stride is 1; the three strides are (batch, head, position) in ELEMENTS.
+   * Every base pointer must be 16-byte aligned and every stride a multiple of
+   * 16 bytes (8 elements for bf16, 4 for fp32). */
+  const void *q, *k, *v;
+  void *out;
+  int64_t q_stride[3], k_stride[3], v_stride[3], o_stride[3];
+
+  /* optional mask forms, combined with AND (see above) */
+  const uint32_t *mask_bits;    /* words; row (b, i) starts at b*stride_b + i*stride_q */
+  int64_t mask_stride_b;        /* in 32-bit words */
+  int64_t mask_stride_q;        /* in 32-bit words, >= ceil(Lk/32) */
+  const int32_t *kv_len;        /* [B]; values outside [0, Lk] are a device error
+                                   (clamped; the static cache is full) */
+  const int32_t *seg_q;         /* [B][Lq] contiguous; given together with seg_k */
+  const int32_t *seg_k;         /* [B][Lk] contiguous */
+
+  float scale;                  /* finite softmax scale; SDPA's default is 1/sqrt(D) */
+  float *lse;                   /* optional out: [B][Hq][Lq] contiguous, natural log */
+  int32_t *dev_error;           /* optional: first device-side mgqa_status code */
+} mgqa_args;
+
+/* Full-sequence (prefill) attention: bidirectional, any of the mask forms.
+ * bf16 runs on the tensor cores (TMA-fed tcgen05 MMAs accumulating in tensor
+ * memory) and skips every 128x128 (query, key) tile the mask leaves empty;
+ * fp32 runs on the CUDA cores. Lq, Lk >= 1. Returns MGQA_OK once the kernel is
+ * enqueued. */
+MGQA_API mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream);
+
+/* Bytes of device workspace masked_gqa_attn_decode needs for these arguments
+ * (0 when the arguments are invalid). */
+MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
+
+/* One-query (Lq == 1) attention over a static KV cache of Lk slots, split
+ * over fixed 128-slot chunks of absolute cache positions; chunks the mask
+ * leaves empty are never read, and partial results are merged in ascending
+ * chunk order inside the same launch, so the full-cache (mask_bits) and
+ * filled-span (kv_len) forms of one mask give bit-identical outputs.
+ * `workspace` is caller-owned device memory of at least
+ * masked_gqa_attn_decode_workspace_size(args) bytes, 16-byte aligned, ZEROED
+ * ONCE before its first use; each call leaves it ready for the next call.
+ * Calls that share a workspace must be ordered on one stream. */
+MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
+                                            size_t workspace_bytes, cudaStream_t stream);
+
+/* Static description of a status code. */
+MGQA_API const char *mgqa_status_string(mgqa_status status);
+
+/* Human-readable reason for the last host-side error on the calling thread
+ * ("" when none). */
+MGQA_API const char *mgqa_last_error_detail(void);
+
+/* MGQA_ABI_VERSION of the loaded library. */
+MGQA_API int32_t mgqa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MASKED_GQA_ATTN_H */

@@ -1,0 +1,226 @@
+"""Python binding of the masked GQA attention library (libmgqa.so, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/masked_gqa_attn.h``. PyTorch
+is used for device memory and streams. There is no CPU path: calling into
+the library without the built extension or without a CUDA device raises.
+
+Entry points (same names as the C ABI):
+  * :func:`masked_gqa_attn_prefill` -- bidirectional full-sequence attention
+    under a packed-bit mask, per-row key lengths and/or segment ids;
+  * :func:`masked_gqa_attn_decode` -- one query per row over a static KV
+    cache, with a caller-owned workspace
+    (:func:`masked_gqa_attn_decode_workspace_size` bytes, zeroed once).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB as _LIB_PATH
+from .build import build as build_library
+
+__all__ = [
+    "MGQA_OK", "MGQA_ERR_INVALID_ARG", "MGQA_ERR_UNSUPPORTED", "MGQA_ERR_CUDA",
+    "MGQA_ERR_TIMEOUT", "MgqaError", "MgqaArgs", "lib", "make_args",
+    "masked_gqa_attn_prefill", "masked_gqa_attn_decode",
+    "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
+]
+
+MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT = range(5)
+MGQA_BF16, MGQA_FP32 = 0, 1
+
+EXPORTED_SYMBOLS = (
+    "masked_gqa_attn_prefill",
+    "masked_gqa_attn_decode_workspace_size",
+    "masked_gqa_attn_decode",
+    "mgqa_status_string",
+    "mgqa_last_error_detail",
+    "mgqa_abi_version",
+)
+
+
+class MgqaError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"mgqa status {status}: {detail}")
+        self.status = status
+        self.detail = detail
+
+
+class MgqaArgs(ctypes.Structure):
+    """Mirror of ``mgqa_args`` in include/masked_gqa_attn.h."""
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("B", ctypes.c_int32), ("Hq", ctypes.c_int32), ("Hkv", ctypes.c_int32),
+        ("Lq", ctypes.c_int32), ("Lk", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+        ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3),
+        ("mask_bits", ctypes.c_void_p),
+        ("mask_stride_b", ctypes.c_int64), ("mask_stride_q", ctypes.c_int64),
+        ("kv_len", ctypes.c_void_p),
+        ("seg_q", ctypes.c_void_p), ("seg_k", ctypes.c_void_p),
+        ("scale", ctypes.c_float),
+        ("lse", ctypes.c_void_p),
+        ("dev_error", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmgqa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libmgqa.so is not built ({_LIB_PATH}); run build_library()")
+        L = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        L.masked_gqa_attn_prefill.argtypes = [ctypes.POINTER(MgqaArgs), P]
+        L.masked_gqa_attn_prefill.restype = ctypes.c_int
+        L.masked_gqa_attn_decode_workspace_size.argtypes = [ctypes.POINTER(MgqaArgs)]
+        L.masked_gqa_attn_decode_workspace_size.restype = ctypes.c_size_t
+        L.masked_gqa_attn_decode.argtypes = [ctypes.POINTER(MgqaArgs), P, ctypes.c_size_t, P]
+        L.masked_gqa_attn_decode.restype = ctypes.c_int
+        L.mgqa_status_string.argtypes = [ctypes.c_int]
+        L.mgqa_status_string.restype = ctypes.c_char_p
+        L.mgqa_last_error_detail.argtypes = []
+        L.mgqa_last_error_detail.restype = ctypes.c_char_p
+        L.mgqa_abi_version.argtypes = []
+        L.mgqa_abi_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != MGQA_OK:
+        L = lib()
+        detail = L.mgqa_last_error_detail().decode() or L.mgqa_status_string(status).decode()
+        raise MgqaError(status, detail)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    return t
+
+
+def make_args(q, k, v, out, *, scale=None, mask_bits=None, kv_len=None, seg_q=None,
+              seg_k=None, lse=None, dev_error=None) -> MgqaArgs:
+    """Fill an MgqaArgs from tensors: q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D], out like q.
+
+    mask_bits: int32/uint32 words [B, Lq, W] (or [B, 1, W] / [1, Lq, W] with
+    stride 0 broadcast), W >= ceil(Lk/32); kv_len int32 [B]; seg_q int32 [B, Lq];
+    seg_k int32 [B, Lk]; lse fp32 [B, Hq, Lq] contiguous; dev_error int32 [1].
+    Tensors are passed by pointer; no copy is made.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _dev(t, name)
+        if t.dim() != 4 or t.stride(3) != 1:
+            raise ValueError(f"{name} must be 4-D with a unit-stride head dim")
+    if q.dtype == torch.bfloat16:
+        dt = MGQA_BF16
+    elif q.dtype == torch.float32:
+        dt = MGQA_FP32
+    else:
+        raise ValueError("q/k/v must be bfloat16 or float32")
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        if t.dtype != q.dtype:
+            raise ValueError(f"{name} dtype differs from q")
+    B, Hq, Lq, D = q.shape
+    Bk, Hkv, Lk, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape) or tuple(out.shape) != tuple(q.shape):
+        raise ValueError("shape mismatch among q, k, v, out")
+    a = MgqaArgs()
+    a.dtype = dt
+    a.B, a.Hq, a.Hkv, a.Lq, a.Lk, a.D = B, Hq, Hkv, Lq, Lk, D
+    a.q, a.k, a.v, a.out = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr()
+    for fld, t in (("q_stride", q), ("k_stride", k), ("v_stride", v), ("o_stride", out)):
+        getattr(a, fld)[:] = [t.stride(0), t.stride(1), t.stride(2)]
+    if mask_bits is not None:
+        _dev(mask_bits, "mask_bits")
+        if mask_bits.dtype not in (torch.int32, torch.uint32) or mask_bits.dim() != 3:
+            raise ValueError("mask_bits must be 3-D int32/uint32 words")
+        if mask_bits.stride(2) != 1:
+            raise ValueError("mask_bits words must be contiguous along keys")
+        a.mask_bits = mask_bits.data_ptr()
+        a.mask_stride_b = mask_bits.stride(0) if mask_bits.shape[0] > 1 else 0
+        a.mask_stride_q = mask_bits.stride(1) if mask_bits.shape[1] > 1 else 0
+    a.kv_len = _ptr(_dev(kv_len, "kv_len", torch.int32))
+    if (seg_q is None) != (seg_k is None):
+        raise ValueError("seg_q and seg_k go together")
+    if seg_q is not None:
+        for name, t, L in (("seg_q", seg_q, Lq), ("seg_k", seg_k, Lk)):
+            _dev(t, name, torch.int32)
+            if tuple(t.shape) != (B, L) or not t.is_contiguous():
+                raise ValueError(f"{name} must be contiguous int32 [B, {L}]")
+        a.seg_q, a.seg_k = seg_q.data_ptr(), seg_k.data_ptr()
+    a.scale = float(1.0 / math.sqrt(D) if scale is None else scale)
+    if lse is not None:
+        _dev(lse, "lse", torch.float32)
+        if tuple(lse.shape) != (B, Hq, Lq) or not lse.is_contiguous():
+            raise ValueError("lse must be contiguous fp32 [B, Hq, Lq]")
+        a.lse = lse.data_ptr()
+    a.dev_error = _ptr(_dev(dev_error, "dev_error", torch.int32))
+    return a
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def masked_gqa_attn_prefill(q, k, v, out=None, *, scale=None, mask_bits=None, kv_len=None,
+                            seg_q=None, seg_k=None, lse=None, dev_error=None, stream=None):
+    """Bidirectional masked GQA attention over full sequences; returns out."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
+                  seg_k=seg_k, lse=lse, dev_error=dev_error)
+    _check(lib().masked_gqa_attn_prefill(ctypes.byref(a), _stream_handle(stream)))
+    return out
+
+
+def masked_gqa_attn_decode_workspace_size(q, k, v, **masks) -> int:
+    out = q  # shape/dtype stand-in; the library only reads the sizes
+    a = make_args(q, k, v, out, **masks)
+    n = lib().masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
+    if n == 0:
+        _check(MGQA_ERR_INVALID_ARG)
+    return int(n)
+
+
+def new_decode_workspace(q, k, v, **masks) -> torch.Tensor:
+    """A zeroed workspace tensor (uint8) sized for these decode arguments."""
+    n = masked_gqa_attn_decode_workspace_size(q, k, v, **masks)
+    return torch.zeros(n, dtype=torch.uint8, device=q.device)
+
+
+def masked_gqa_attn_decode(q, k, v, out=None, *, workspace: torch.Tensor, scale=None,
+                           mask_bits=None, kv_len=None, seg_q=None, seg_k=None, lse=None,
+                           dev_error=None, stream=None):
+    """One query per row (q [B, Hq, 1, D]) over a static cache k/v [B, Hkv, Lk, D]."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
+                  seg_k=seg_k, lse=lse, dev_error=dev_error)
+    _dev(workspace, "workspace")
+    _check(lib().masked_gqa_attn_decode(ctypes.byref(a), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_handle(stream)))
+    return out

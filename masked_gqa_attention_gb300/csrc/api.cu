@@ -1,0 +1,122 @@
+// C ABI of the masked GQA attention library: argument validation and kernel
+// dispatch. Allocates nothing and never synchronises; all work is enqueued on
+// the caller's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/masked_gqa_attn.h"
+#include "internal.h"
+
+namespace mgqa {
+
+static thread_local char g_detail[256] = "";
+
+mgqa_status fail(mgqa_status code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+namespace {
+
+bool aligned(const void *p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+mgqa_status check_tensor(const char *name, const void *ptr, const int64_t *st, size_t esize) {
+  if (!ptr) return fail(MGQA_ERR_INVALID_ARG, "%s is null", name);
+  if (!aligned(ptr, 16)) return fail(MGQA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  for (int t = 0; t < 3; ++t) {
+    if (st[t] < 0) return fail(MGQA_ERR_INVALID_ARG, "%s stride %d is negative", name, t);
+    if ((st[t] * (int64_t)esize) % 16 != 0)
+      return fail(MGQA_ERR_INVALID_ARG, "%s stride %d is not a multiple of 16 bytes", name, t);
+  }
+  return MGQA_OK;
+}
+
+mgqa_status validate(const mgqa_args *a, bool decode) {
+  g_detail[0] = '\0';
+  if (!a) return fail(MGQA_ERR_INVALID_ARG, "args is null");
+  if (a->dtype != MGQA_BF16 && a->dtype != MGQA_FP32)
+    return fail(MGQA_ERR_INVALID_ARG, "unknown dtype %d", (int)a->dtype);
+  if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->Lq < 1 || a->Lk < 1)
+    return fail(MGQA_ERR_INVALID_ARG, "B, Hq, Hkv, Lq, Lk must be >= 1");
+  if (a->Hq % a->Hkv != 0) return fail(MGQA_ERR_INVALID_ARG, "Hq %% Hkv != 0");
+  if (a->D != 64 && a->D != 128) return fail(MGQA_ERR_UNSUPPORTED, "head dim %d (64 or 128)", a->D);
+  if (a->Lk > (1 << 24) || a->Lq > (1 << 24))
+    return fail(MGQA_ERR_UNSUPPORTED, "sequence longer than 2^24");
+  if ((int64_t)a->B * a->Hq * a->Lq > (int64_t)1 << 31)
+    return fail(MGQA_ERR_UNSUPPORTED, "B*Hq*Lq too large");
+  if (decode && a->Lq != 1) return fail(MGQA_ERR_INVALID_ARG, "decode needs Lq == 1");
+  if (!std::isfinite(a->scale)) return fail(MGQA_ERR_INVALID_ARG, "scale is not finite");
+  const size_t es = a->dtype == MGQA_BF16 ? 2 : 4;
+  mgqa_status st;
+  if ((st = check_tensor("q", a->q, a->q_stride, es)) != MGQA_OK) return st;
+  if ((st = check_tensor("k", a->k, a->k_stride, es)) != MGQA_OK) return st;
+  if ((st = check_tensor("v", a->v, a->v_stride, es)) != MGQA_OK) return st;
+  if ((st = check_tensor("out", a->out, a->o_stride, es)) != MGQA_OK) return st;
+  if (a->mask_bits) {
+    if (!aligned(a->mask_bits, 4)) return fail(MGQA_ERR_INVALID_ARG, "mask_bits misaligned");
+    const int64_t W = (a->Lk + 31) / 32;
+    if (a->mask_stride_q < W && a->Lq > 1)
+      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_q < ceil(Lk/32)");
+    if (a->mask_stride_b < 0 || a->mask_stride_q < 0)
+      return fail(MGQA_ERR_INVALID_ARG, "negative mask stride");
+    if (a->B > 1 && a->mask_stride_b < W && a->mask_stride_b != 0)
+      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_b too small");
+  }
+  if ((a->seg_q == nullptr) != (a->seg_k == nullptr))
+    return fail(MGQA_ERR_INVALID_ARG, "seg_q and seg_k must be given together");
+  if (a->seg_q && (!aligned(a->seg_q, 4) || !aligned(a->seg_k, 4)))
+    return fail(MGQA_ERR_INVALID_ARG, "segment ids misaligned");
+  if (a->kv_len && !aligned(a->kv_len, 4)) return fail(MGQA_ERR_INVALID_ARG, "kv_len misaligned");
+  if (a->lse && !aligned(a->lse, 4)) return fail(MGQA_ERR_INVALID_ARG, "lse misaligned");
+  if (a->dev_error && !aligned(a->dev_error, 4))
+    return fail(MGQA_ERR_INVALID_ARG, "dev_error misaligned");
+  return MGQA_OK;
+}
+
+}  // namespace
+}  // namespace mgqa
+
+extern "C" {
+
+mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream) {
+  mgqa_status st = mgqa::validate(args, false);
+  if (st != MGQA_OK) return st;
+  if (args->dtype == MGQA_BF16) return mgqa::launch_prefill_tc(*args, stream);
+  return mgqa::launch_prefill_simt(*args, stream);
+}
+
+size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args) {
+  if (mgqa::validate(args, true) != MGQA_OK) return 0;
+  return mgqa::decode_workspace_bytes(*args);
+}
+
+mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  mgqa_status st = mgqa::validate(args, true);
+  if (st != MGQA_OK) return st;
+  if (!workspace) return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace is null");
+  if ((reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  return mgqa::launch_decode(*args, workspace, workspace_bytes, stream);
+}
+
+const char *mgqa_status_string(mgqa_status s) {
+  switch (s) {
+    case MGQA_OK: return "ok";
+    case MGQA_ERR_INVALID_ARG: return "invalid argument";
+    case MGQA_ERR_UNSUPPORTED: return "unsupported";
+    case MGQA_ERR_CUDA: return "CUDA error";
+    case MGQA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char *mgqa_last_error_detail(void) { return mgqa::g_detail; }
+
+int32_t mgqa_abi_version(void) { return MGQA_ABI_VERSION; }
+
+}  // extern "C"

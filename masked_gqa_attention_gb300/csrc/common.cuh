@@ -1,0 +1,174 @@
+// Device helpers shared by the kernels of the masked GQA attention library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/masked_gqa_attn.h"
+
+#define MGQA_DEV __device__ __forceinline__
+
+namespace mgqa {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Record the first device-side error code (later ones are dropped).
+MGQA_DEV void report_error(int32_t *err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+MGQA_DEV float to_float(float x) { return x; }
+MGQA_DEV float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> MGQA_DEV T from_float(float x);
+template <> MGQA_DEV float from_float<float>(float x) { return x; }
+template <> MGQA_DEV __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// Unpack 16 bytes into float lanes: 8 bf16 or 4 fp32 values.
+MGQA_DEV void unpack16(const uint4 &u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+MGQA_DEV void unpack16(const uint4 &u, float (&f)[4]) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+
+// kv_len[b] clamped to [0, Lk]; out-of-range values are reported once.
+MGQA_DEV int load_kv_len(const int32_t *kv_len, int b, int Lk, int32_t *err, bool report) {
+  if (!kv_len) return Lk;
+  int n = __ldg(kv_len + b);
+  if (n < 0 || n > Lk) {
+    if (report) report_error(err, MGQA_ERR_INVALID_ARG);
+    n = n < 0 ? 0 : Lk;
+  }
+  return n;
+}
+
+// ---- mask forms -----------------------------------------------------------
+
+// The mask forms of one call; any pointer may be null (form absent).
+struct MaskView {
+  const uint32_t *bits;  // words, row (b, i) at b*sb + i*sq
+  int64_t sb, sq;
+  const int32_t *kv_len;  // [B]
+  const int32_t *seg_q;   // [B][Lq]
+  const int32_t *seg_k;   // [B][Lk]
+};
+
+// Bits t = 0..31 of the result: may query i of row b attend to key jbase + t?
+// jbase is a multiple of 32. kvl is the (clamped) kv_len of row b, segq the
+// query's segment id (ignored without segment ids). Keys >= Lk are never
+// allowed. Segment ids are read from global memory (cached).
+MGQA_DEV uint32_t mask_word(const MaskView &m, int b, int i, int jbase, int Lk, int Lq, int kvl,
+                            int segq) {
+  if (jbase >= Lk) return 0u;
+  const int lim = min(Lk, kvl) - jbase;
+  uint32_t w = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : ((1u << lim) - 1u));
+  if (m.bits && w) w &= __ldg(m.bits + (int64_t)b * m.sb + (int64_t)i * m.sq + (jbase >> 5));
+  if (m.seg_q && w) {
+    if (segq < 0) return 0u;
+    const int32_t *sk = m.seg_k + (int64_t)b * Lk + jbase;
+    uint32_t sw = 0u;
+    const int n = min(32, Lk - jbase);
+    for (int t = 0; t < n; ++t) sw |= (uint32_t)(__ldg(sk + t) == segq) << t;
+    w &= sw;
+  }
+  return w;
+}
+
+// ---- mbarrier / bulk-copy primitives (PTX) --------------------------------
+
+MGQA_DEV uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+MGQA_DEV void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+MGQA_DEV void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+MGQA_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+MGQA_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+MGQA_DEV void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+MGQA_DEV void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+MGQA_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+MGQA_DEV uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase: gives up after ~`limit_ns` of wall time
+// (measured with the global timer), records MGQA_ERR_TIMEOUT and returns
+// false. Never spins forever.
+MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
+                        uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 255u) == 0u) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        report_error(err, MGQA_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// Untiled bulk copy global -> shared (this CTA), completion counted in bytes
+// on `bar`. Both addresses 16-byte aligned, size a multiple of 16.
+MGQA_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace mgqa

@@ -1,0 +1,27 @@
+// Host-side interfaces between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/masked_gqa_attn.h"
+
+namespace mgqa {
+
+// Sets the thread-local detail string returned by mgqa_last_error_detail().
+mgqa_status fail(mgqa_status code, const char *fmt, ...);
+
+// Decode: fixed chunks of kDecodeChunk absolute cache slots per CTA.
+constexpr int kDecodeChunk = 128;
+// Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).
+int decode_heads_per_cta(int n_rep);
+size_t decode_workspace_bytes(const mgqa_args &a);
+mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// Prefill on the CUDA cores (fp32 I/O).
+mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s);
+
+// Prefill on the tensor cores (bf16 I/O): TMA + tcgen05 + TMEM.
+mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s);
+
+}  // namespace mgqa

@@ -1,0 +1,177 @@
+// Full-sequence masked GQA attention on the CUDA cores, fp32 arithmetic.
+// Serves fp32 inputs, where tensor-core tf32 (10-bit mantissa) cannot meet a
+// 1e-5 relative bound.
+//
+// Passages: VoxCPM page, "Upstream-identical practice", attention bullet
+// (SDPA with enable_gqa, bidirectional, explicit boolean mask); OmniVoice
+// page, "Upstream-identical practice", attention-mask bullet (4D boolean
+// mask, not causal, KV heads repeated) and "Memory & speed", packed_guidance
+// paragraph (block-diagonal mask).
+//
+// CTA = 64 query rows of one query head; two threads per row, each owning
+// half of the head dim. Keys advance in tiles of 64: a tile no row of the CTA
+// may attend to is skipped without reading K/V; otherwise K and V are staged
+// in shared memory, the 64 scores of a row are formed (the two halves summed
+// with one shuffle), masked to -inf, and folded into a running (max, sum, O)
+// with one rescale per tile.
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgqa {
+namespace {
+
+struct SimtParams {
+  const void *q, *k, *v;
+  void *out;
+  int64_t qs[3], ks[3], vs[3], os[3];
+  MaskView mask;
+  float scale_log2;
+  float *lse;
+  int32_t *err;
+  int B, Hq, Hkv, Lq, Lk, n_rep;
+};
+
+constexpr int kRows = 64;
+constexpr int kKeys = 64;
+constexpr int kThreads = 2 * kRows;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+prefill_simt_kernel(const __grid_constant__ SimtParams p) {
+  extern __shared__ __align__(16) float sh[];
+  float *ks = sh;                 // [kKeys][D]
+  float *vs = sh + kKeys * D;     // [kKeys][D]
+  constexpr int DH = D / 2;
+
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / p.n_rep;
+  const int tid = threadIdx.x;
+  const int row = tid >> 1, half = tid & 1;
+  const int i = qt * kRows + row;
+  const bool row_ok = i < p.Lq;
+  const int ic = row_ok ? i : p.Lq - 1;
+
+  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && h == 0 && tid == 0);
+  const int segq = p.mask.seg_q ? __ldg(p.mask.seg_q + (int64_t)b * p.Lq + ic) : 0;
+
+  float q[DH], o[DH];
+  const T *qrow = static_cast<const T *>(p.q) + b * p.qs[0] + h * p.qs[1] + (int64_t)ic * p.qs[2];
+#pragma unroll
+  for (int d = 0; d < DH; ++d) {
+    q[d] = to_float(qrow[half * DH + d]) * p.scale_log2;
+    o[d] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+
+  const T *kb = static_cast<const T *>(p.k) + b * p.ks[0] + g * p.ks[1];
+  const T *vb = static_cast<const T *>(p.v) + b * p.vs[0] + g * p.vs[1];
+
+  for (int j0 = 0; j0 < p.Lk; j0 += kKeys) {
+    uint32_t mw[kKeys / 32];
+#pragma unroll
+    for (int w = 0; w < kKeys / 32; ++w)
+      mw[w] = row_ok ? mask_word(p.mask, b, ic, j0 + 32 * w, p.Lk, p.Lq, kvl, segq) : 0u;
+    uint32_t any = 0;
+#pragma unroll
+    for (int w = 0; w < kKeys / 32; ++w) any |= mw[w];
+    if (!__syncthreads_or(any != 0u)) continue;  // empty tile: K/V never read
+
+    for (int e = tid; e < kKeys * D; e += kThreads) {
+      const int jj = e / D, d = e % D;
+      const int j = j0 + jj;
+      float kv = 0.f, vv = 0.f;
+      if (j < p.Lk) {
+        kv = to_float(kb[(int64_t)j * p.ks[2] + d]);
+        vv = to_float(vb[(int64_t)j * p.vs[2] + d]);
+      }
+      ks[e] = kv;
+      vs[e] = vv;
+    }
+    __syncthreads();
+
+    float s[kKeys];
+    float mt = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < kKeys; ++jj) {
+      const float *kr = ks + jj * D + half * DH;
+      float acc = 0.f;
+#pragma unroll
+      for (int d = 0; d < DH; ++d) acc = fmaf(q[d], kr[d], acc);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      const bool al = (mw[jj >> 5] >> (jj & 31)) & 1u;
+      s[jj] = al ? acc : -INFINITY;
+      mt = fmaxf(mt, s[jj]);
+    }
+    const float m_new = fmaxf(m, mt);
+    if (m_new != -INFINITY) {
+      const float corr = exp2f(m - m_new);  // m == -inf gives 0
+      l *= corr;
+#pragma unroll
+      for (int d = 0; d < DH; ++d) o[d] *= corr;
+#pragma unroll
+      for (int jj = 0; jj < kKeys; ++jj) {
+        const float pj = exp2f(s[jj] - m_new);  // masked: exp2(-inf) = 0
+        l += pj;
+        const float *vr = vs + jj * D + half * DH;
+#pragma unroll
+        for (int d = 0; d < DH; ++d) o[d] = fmaf(pj, vr[d], o[d]);
+      }
+      m = m_new;
+    }
+    __syncthreads();
+  }
+
+  if (row_ok) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    T *orow = static_cast<T *>(p.out) + b * p.os[0] + h * p.os[1] + (int64_t)i * p.os[2];
+#pragma unroll
+    for (int d = 0; d < DH; ++d) orow[half * DH + d] = from_float<T>(o[d] * inv);
+    if (p.lse && half == 0)
+      p.lse[((int64_t)b * p.Hq + h) * p.Lq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+  }
+}
+
+template <typename T, int D>
+mgqa_status launch_t(const SimtParams &p, cudaStream_t s) {
+  auto kern = prefill_simt_kernel<T, D>;
+  const size_t smem = 2 * kKeys * D * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+      return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the fp32 prefill kernel");
+    attr_set = true;
+  }
+  dim3 grid((p.Lq + kRows - 1) / kRows, p.Hq, p.B);
+  kern<<<grid, kThreads, smem, s>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+
+}  // namespace
+
+mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s) {
+  SimtParams p{};
+  p.q = a.q; p.k = a.k; p.v = a.v; p.out = a.out;
+  for (int t = 0; t < 3; ++t) {
+    p.qs[t] = a.q_stride[t]; p.ks[t] = a.k_stride[t];
+    p.vs[t] = a.v_stride[t]; p.os[t] = a.o_stride[t];
+  }
+  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k};
+  p.scale_log2 = a.scale * kLog2e;
+  p.lse = a.lse; p.err = a.dev_error;
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lq = a.Lq; p.Lk = a.Lk; p.n_rep = a.Hq / a.Hkv;
+  if (a.dtype == MGQA_FP32) {
+    if (a.D == 64) return launch_t<float, 64>(p, s);
+    if (a.D == 128) return launch_t<float, 128>(p, s);
+  } else {
+    if (a.D == 64) return launch_t<__nv_bfloat16, 64>(p, s);
+    if (a.D == 128) return launch_t<__nv_bfloat16, 128>(p, s);
+  }
+  return fail(MGQA_ERR_UNSUPPORTED, "prefill: head dim %d", a.D);
+}
+
+}  // namespace mgqa

@@ -1,0 +1,110 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every
+symbol the header declares, the ctypes mirror matches the C struct layout,
+and host-side validation rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import masked_gqa_attention_gb300 as M
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "masked_gqa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    M.build_library()
+    return M.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"MGQA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    assert set(syms) == set(M.EXPORTED_SYMBOLS), syms
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+    assert L.mgqa_abi_version() == 1
+    assert L.mgqa_status_string(M.MGQA_ERR_TIMEOUT) == b"device wait timed out"
+
+
+def test_struct_layout_matches_header(tmp_path):
+    fields = [f for f, _ in M.MgqaArgs._fields_]
+    src = tmp_path / "off.c"
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof(mgqa_args, {f}));' for f in fields)
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "masked_gqa_attn.h"\n'
+                   f'int main(void){{ {body} printf("size %zu\\n", sizeof(mgqa_args)); return 0; }}\n')
+    exe = tmp_path / "off"
+    cuda_inc = "/usr/local/cuda/include"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), "-I", cuda_inc, str(src), "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = dict(line.split() for line in out if line)
+    for f in fields:
+        assert int(got[f]) == getattr(M.MgqaArgs, f).offset, f
+    assert int(got["size"]) == ctypes.sizeof(M.MgqaArgs)
+
+
+def _valid_args():
+    a = M.MgqaArgs()
+    a.dtype = M.MGQA_BF16
+    a.B, a.Hq, a.Hkv, a.Lq, a.Lk, a.D = 2, 16, 8, 1024, 1024, 128
+    base = 1 << 20  # fake, never dereferenced: validation fails before any launch
+    a.q, a.k, a.v, a.out = base, base * 2, base * 3, base * 4
+    for fld, H in (("q_stride", 16), ("k_stride", 8), ("v_stride", 8), ("o_stride", 16)):
+        getattr(a, fld)[:] = [H * 1024 * 128, 1024 * 128, 128]
+    a.scale = 0.088
+    return a
+
+
+@pytest.mark.parametrize("mutate,code", [
+    (lambda a: setattr(a, "Hkv", 3), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "D", 96), M.MGQA_ERR_UNSUPPORTED),
+    (lambda a: setattr(a, "B", 0), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "Lk", 0), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "q", 0), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "k", (1 << 20) + 8), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: a.k_stride.__setitem__(2, 100), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: a.v_stride.__setitem__(1, -128), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "scale", float("nan")), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "scale", float("inf")), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "dtype", 7), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "seg_q", 1 << 22), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: (setattr(a, "mask_bits", 1 << 22), setattr(a, "mask_stride_q", 8)), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "mask_bits", (1 << 22) + 2), M.MGQA_ERR_INVALID_ARG),
+    (lambda a: setattr(a, "lse", (1 << 22) + 1), M.MGQA_ERR_INVALID_ARG),
+])
+def test_prefill_rejects_bad_arguments(L, mutate, code):
+    a = _valid_args()
+    mutate(a)
+    st = L.masked_gqa_attn_prefill(ctypes.byref(a), None)
+    assert st == code, L.mgqa_last_error_detail()
+    assert L.mgqa_last_error_detail() != b""
+
+
+def test_null_args_rejected(L):
+    assert L.masked_gqa_attn_prefill(None, None) == M.MGQA_ERR_INVALID_ARG
+    assert L.masked_gqa_attn_decode(None, None, 0, None) == M.MGQA_ERR_INVALID_ARG
+    assert L.masked_gqa_attn_decode_workspace_size(None) == 0
+
+
+def test_decode_validation(L):
+    a = _valid_args()
+    assert L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a)) == 0  # Lq != 1
+    assert L.masked_gqa_attn_decode(ctypes.byref(a), 1 << 20, 1 << 20, None) == M.MGQA_ERR_INVALID_ARG
+    a.Lq = 1
+    a.B, a.Hq, a.Hkv, a.Lk, a.D = 8, 16, 2, 8192, 64
+    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
+    # partial (m, l) and D floats per (b, head, 128-slot chunk) plus tickets
+    assert n >= 8 * 16 * 64 * (64 + 2) * 4
+    assert L.masked_gqa_attn_decode(ctypes.byref(a), None, n, None) == M.MGQA_ERR_INVALID_ARG
+    assert L.masked_gqa_attn_decode(ctypes.byref(a), (1 << 20) + 4, n, None) == M.MGQA_ERR_INVALID_ARG

@@ -1,0 +1,161 @@
+"""Parity of the prefill kernels against the fp64 oracle on the engine pages'
+workload shapes and on seeded ragged cases, plus the invariants the pages
+state: masked keys add exact zeros, a packed block-diagonal row equals each
+block run alone, grouped KV heads equal explicitly repeated heads."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from _util import assert_close_to_oracle, assert_lse_close, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    import masked_gqa_attention_gb300 as M
+    M.build_library()
+    return M
+
+
+def run_prefill(M, wl, lse=True, err=None, d=None):
+    d = d or to_device(wl)
+    out = torch.full_like(d["q"], float("nan"))
+    lse_t = torch.empty(d["q"].shape[:3], dtype=torch.float32, device="cuda") if lse else None
+    M.masked_gqa_attn_prefill(d["q"], d["k"], d["v"], out, scale=wl.scale, lse=lse_t,
+                              dev_error=err, mask_bits=d["mask_bits"], kv_len=d["kv_len"],
+                              seg_q=d["seg_q"], seg_k=d["seg_k"])
+    torch.cuda.synchronize()
+    return out, lse_t
+
+
+def oracle(oracle_mod, wl, rows=None):
+    q, k, v, masks = wl.q, wl.k, wl.v, wl.masks()
+    if rows is not None:
+        q, k, v = q[rows], k[rows], v[rows]
+        masks = {n: (t[rows] if t is not None else None) for n, t in masks.items()}
+    out, lse, _ = oracle_mod.attention(q, k, v, scale=wl.scale, **masks)
+    return out, lse
+
+
+def test_tiny_fp32_config(M, oracle_mod):
+    wl = W.tiny_fp32()
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.float32, "tiny fp32")
+    assert_lse_close(lse, ref_lse, 1e-5)
+
+
+@pytest.mark.parametrize("variant", ["bits", "kvlen"])
+def test_padded_cfg_config(M, oracle_mod, variant):
+    wl = W.padded_cfg(variant=variant)
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.bfloat16, f"padded cfg {variant}")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
+def test_padded_cfg_bits_equal_kvlen_bitwise(M):
+    o1, l1 = run_prefill(M, W.padded_cfg(variant="bits"))
+    o2, l2 = run_prefill(M, W.padded_cfg(variant="kvlen"))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_padded_cfg_masked_keys_refill(M):
+    wl = W.padded_cfg(variant="bits")
+    o1, l1 = run_prefill(M, wl)
+    g = torch.Generator().manual_seed(3)
+    wl.k[1, :, 384:] = (torch.randn(wl.k[1, :, 384:].shape, generator=g) * 50).to(torch.bfloat16)
+    wl.v[1, :, 384:] = (torch.randn(wl.v[1, :, 384:].shape, generator=g) * 1e4).to(torch.bfloat16)
+    o2, l2 = run_prefill(M, wl)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_packed_guidance_config_and_blocks_alone(M, oracle_mod):
+    wl = W.packed_guidance()
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.bfloat16, "packed")
+    assert_lse_close(lse, ref_lse, 2e-3)
+    for lo, hi in wl.info["segments"]:
+        alone = W.Workload("alone", wl.q[:, :, lo:hi].contiguous(), wl.k[:, :, lo:hi].contiguous(),
+                           wl.v[:, :, lo:hi].contiguous(), wl.scale)
+        o2, l2 = run_prefill(M, alone)
+        # block boundaries fall on 128-row tiles here, so the bits agree exactly
+        assert torch.equal(out[:, :, lo:hi], o2) and torch.equal(lse[:, :, lo:hi], l2)
+
+
+def test_dit_batch_config_sampled_rows(M, oracle_mod):
+    wl = W.dit_batch()
+    out, lse = run_prefill(M, wl)
+    rows = [0, 13, 31]
+    ref, ref_lse = oracle(oracle_mod, wl, rows=rows)
+    assert_close_to_oracle(out[rows], ref, torch.bfloat16, "dit rows")
+    assert_lse_close(lse[rows], ref_lse, 2e-3)
+    assert torch.isfinite(out).all()
+
+
+CASES = [
+    # B, Hq, Hkv, Lq, Lk, D
+    (2, 4, 2, 300, 300, 128),
+    (1, 2, 1, 129, 257, 64),
+    (3, 8, 8, 70, 500, 128),
+    (2, 6, 2, 256, 129, 64),
+    (1, 4, 4, 1, 700, 128),
+    (2, 16, 4, 384, 384, 128),
+]
+
+
+@pytest.mark.parametrize("mask", ["none", "bits", "kvlen", "segment", "bits+kvlen"])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_random_cases_bf16(M, oracle_mod, mask, case):
+    wl = W.random_case(sum(case) + len(mask), *case, dtype=torch.bfloat16, mask=mask)
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.bfloat16, f"{mask} {case}")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
+@pytest.mark.parametrize("mask", ["bits", "segment"])
+@pytest.mark.parametrize("case", [(2, 4, 2, 150, 200, 64), (1, 2, 2, 64, 1000, 128)],
+                         ids=lambda c: "x".join(map(str, c)))
+def test_random_cases_fp32(M, oracle_mod, mask, case):
+    wl = W.random_case(sum(case), *case, dtype=torch.float32, mask=mask)
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.float32, f"fp32 {mask} {case}")
+    assert_lse_close(lse, ref_lse, 1e-5)
+
+
+def test_gqa_equals_repeated_heads(M):
+    wl = W.random_case(5, 2, 8, 2, 200, 333, 128, dtype=torch.bfloat16, mask="bits")
+    o1, l1 = run_prefill(M, wl)
+    rep = W.Workload("rep", wl.q, wl.k.repeat_interleave(4, 1).contiguous(),
+                     wl.v.repeat_interleave(4, 1).contiguous(), wl.scale, mask_bits=wl.mask_bits)
+    o2, l2 = run_prefill(M, rep)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_fully_masked_rows_give_zero(M):
+    wl = W.random_case(9, 2, 4, 2, 200, 300, 128, dtype=torch.bfloat16, mask="kvlen")
+    wl.kv_len[:] = torch.tensor([0, 5], dtype=torch.int32)
+    out, lse = run_prefill(M, wl)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.isfinite(out[1]).all()
+
+
+def test_strided_views(M, oracle_mod):
+    """q/k/v/out as head-interleaved views ([B, L, H, D] storage)."""
+    B, Hq, Hkv, L, D = 2, 4, 2, 200, 128
+    g = torch.Generator().manual_seed(1)
+    qs = torch.randn((B, L, Hq, D), generator=g).to(torch.bfloat16)
+    ks = torch.randn((B, L, Hkv, D), generator=g).to(torch.bfloat16)
+    vs = torch.randn((B, L, Hkv, D), generator=g).to(torch.bfloat16)
+    qd, kd, vd = (t.cuda().transpose(1, 2) for t in (qs, ks, vs))
+    outd = torch.empty((B, L, Hq, D), dtype=torch.bfloat16, device="cuda").transpose(1, 2)
+    M.masked_gqa_attn_prefill(qd, kd, vd, outd, scale=0.1)
+    torch.cuda.synchronize()
+    ref, _, _ = oracle_mod.attention(qs.transpose(1, 2), ks.transpose(1, 2), vs.transpose(1, 2),
+                                     scale=0.1)
+    assert_close_to_oracle(outd, ref, torch.bfloat16, "strided")
