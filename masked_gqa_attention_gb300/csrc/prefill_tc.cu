@@ -1,7 +1,516 @@
-// Placeholder until the tensor-core prefill kernel lands: bf16 prefill runs
-// on the CUDA-core kernel.
+// Full-sequence masked GQA attention on the tensor cores (bf16 in, fp32
+// accumulation): TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating in tensor
+// memory, a warp-specialised load / MMA / softmax pipeline, and whole-tile
+// skipping wherever the mask leaves a 128x128 (query, key) tile empty.
+//
+// Passages: VoxCPM page, "Upstream-identical practice", attention bullet
+// (SDPA with enable_gqa, bidirectional in the local DiT, explicit boolean
+// mask whose masked positions add exact zeros); OmniVoice page,
+// "Upstream-identical practice", attention-mask bullet (4D boolean mask, not
+// causal, KV heads repeated; conditional and unconditional rows in one batch)
+// and "Memory & speed", packed_guidance paragraph (both sequences in one row
+// under a block-diagonal mask, so the padded half of the unconditional row is
+// never computed).
+//
+// CTA = one 128-row query tile of NT query heads that share one KV head
+// (NT = 2 when Hq/Hkv is even), so each K/V tile is fetched once for both.
+//   warp 0      : TMA producer (Q once, then K and V per key tile, STAGES-deep)
+//   warp 1      : allocates tensor memory; lane 0 issues every MMA
+//   warps 4..   : one softmax warpgroup per query head (thread = query row)
+// Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
+// P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
+// the P.V MMA straight from tensor memory.
+// Per key tile n and head t:
+//   MMA:     S_t = Q_t K_n^T              -> s_full[t]
+//   softmax: mask (partial tiles only), running max with lazy rescale of O_t
+//            (only when the max grows by more than 2^8), P = exp2(x - m)
+//            -> p_full[t]
+//   MMA:     O_t += P_t V_n               -> o_done[t]; both heads -> kv_empty
+// S_t(n+1) is issued only after o_done[t](n), since it overwrites P_t.
+// Before the pipeline, all warps classify the key tiles of this query tile
+// as empty / full / partial from the mask forms; only non-empty tiles enter
+// the pipeline and only partial tiles pay for per-element masking.
+// Every wait is bounded (about 2 s) and reports MGQA_ERR_TIMEOUT.
+#include <climits>
+#include <cmath>
+#include <cuda.h>
+
+#include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace mgqa {
-mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) { return launch_prefill_simt(a, s); }
+namespace {
+
+constexpr int BM = 128;       // query rows per tile
+constexpr int BN = 128;       // keys per tile
+constexpr int MAXKT = 2048;   // key tiles per row (Lk <= 262144)
+constexpr int BOX = 16384;    // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+
+struct TcParams {
+  MaskView mask;
+  int B, Hq, Hkv, Lq, Lk, n_rep, nkt;
+  float scale_log2;
+  void *out;
+  int64_t os[3];
+  float *lse;
+  int32_t *err;
+};
+
+template <int D, int NT, int STAGES>
+struct Layout {
+  static constexpr int KB = D / 64;  // TMA boxes per 128-row tile
+  static constexpr int q_off = 0;
+  static constexpr int k_off = q_off + NT * KB * BOX;
+  static constexpr int v_off = k_off + STAGES * KB * BOX;
+  static constexpr int bar_off = v_off + STAGES * KB * BOX;
+  // barriers: q, k_full[S], v_full[S], kv_empty[S], s_full[NT], p_full[NT], o_done[NT]
+  static constexpr int n_bars = 1 + 3 * STAGES + 3 * NT;
+  static constexpr int misc_off = bar_off + 8 * n_bars;
+  static constexpr int tmem_slot = misc_off;        // uint32
+  static constexpr int nk_slot = misc_off + 4;      // int32
+  static constexpr int seg_slot = misc_off + 8;     // int32 x2 (min, max of seg_q)
+  static constexpr int list_off = misc_off + 16;    // uint16[MAXKT]
+  static constexpr int cls_off = list_off + 2 * MAXKT;  // uint8[MAXKT]
+  static constexpr int total = cls_off + MAXKT;
+  static constexpr int smem_bytes = total + 1024;   // slack for 1024-B alignment
+  static constexpr int threads = 128 * (1 + NT);
+  static constexpr int tmem_cols_used = NT * (BN + D);
+  static constexpr uint32_t tmem_cols = tmem_cols_used <= 32 ? 32 : tmem_cols_used <= 64 ? 64
+                                        : tmem_cols_used <= 128 ? 128
+                                        : tmem_cols_used <= 256 ? 256 : 512;
+  static_assert(tmem_cols_used <= 512, "tensor memory");
+};
+
+template <int D, int NT, int STAGES>
+__global__ void __launch_bounds__(128 * (1 + NT), 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ TcParams p) {
+  using Lay = Layout<D, NT, STAGES>;
+  constexpr int KB = Lay::KB;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bar_off);
+  uint64_t *bar_q = bars;
+  uint64_t *bar_kfull = bars + 1;
+  uint64_t *bar_vfull = bars + 1 + STAGES;
+  uint64_t *bar_empty = bars + 1 + 2 * STAGES;
+  uint64_t *bar_sfull = bars + 1 + 3 * STAGES;
+  uint64_t *bar_pfull = bar_sfull + NT;
+  uint64_t *bar_odone = bar_pfull + NT;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
+  int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
+  int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
+  uint16_t *list = reinterpret_cast<uint16_t *>(smem + Lay::list_off);
+  uint8_t *cls = smem + Lay::cls_off;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int qt = blockIdx.x, hp = blockIdx.y, b = blockIdx.z;
+  const int h0 = hp * NT;
+  const int g = h0 / p.n_rep;
+  const int row0 = qt * BM;
+  const int rows = min(BM, p.Lq - row0);
+  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
+
+  // ---- set-up: barriers, tensor memory, segment range of the query tile ----
+  if (tid == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_kfull + s, 1);
+      mbar_init(bar_vfull + s, 1);
+      mbar_init(bar_empty + s, 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 128);
+      mbar_init(bar_odone + t, 1);
+    }
+    fence_mbarrier_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::tmem_cols);
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tensormap(&tm_q);
+      tc::prefetch_tensormap(&tm_k);
+      tc::prefetch_tensormap(&tm_v);
+    }
+    if (p.mask.seg_q) {
+      int mn = INT_MAX, mx = INT_MIN;
+      for (int r = lane; r < rows; r += 32) {
+        const int s = __ldg(p.mask.seg_q + (int64_t)b * p.Lq + row0 + r);
+        mn = min(mn, s);
+        mx = max(mx, s);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (lane == 0) {
+        seg_slot[0] = mn;
+        seg_slot[1] = mx;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- classify key tiles: 0 empty, 1 partial, 2 full ----------------------
+  for (int kt = warp; kt < p.nkt; kt += nwarps) {
+    const int k0 = kt * BN;
+    bool ne = k0 < p.Lk;
+    bool full = k0 + BN <= p.Lk;
+    if (p.mask.kv_len) {
+      ne = ne && k0 < kvl;
+      full = full && k0 + BN <= kvl;
+    }
+    if (p.mask.bits && ne) {
+      bool any = false, all = true;
+      for (int r = lane; r < rows; r += 32) {
+        const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
+#pragma unroll
+        for (int w = 0; w < BN / 32; ++w) {
+          const int j = k0 + 32 * w;
+          if (j < p.Lk) {
+            const int lim = p.Lk - j;
+            const uint32_t valid = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
+            const uint32_t word = __ldg(mrow + (j >> 5)) & valid;
+            any = any || word != 0u;
+            all = all && word == 0xffffffffu;
+          } else {
+            all = false;
+          }
+        }
+      }
+      ne = __any_sync(0xffffffffu, any);
+      full = full && __all_sync(0xffffffffu, all);
+    }
+    if (p.mask.seg_q && ne) {
+      int mn = INT_MAX, mx = INT_MIN;
+#pragma unroll
+      for (int i = 0; i < BN / 32; ++i) {
+        const int j = k0 + lane + 32 * i;
+        if (j < p.Lk) {
+          const int s = __ldg(p.mask.seg_k + (int64_t)b * p.Lk + j);
+          mn = min(mn, s);
+          mx = max(mx, s);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const int qmn = seg_slot[0], qmx = seg_slot[1];
+      if (qmx < 0 || mx < 0 || qmx < mn || mx < qmn) ne = false;
+      full = full && qmn == qmx && mn == mx && qmn == mn && qmn >= 0;
+    }
+    if (lane == 0) cls[kt] = ne ? (full ? 2 : 1) : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int count = 0;
+    for (int base = 0; base < p.nkt; base += 32) {
+      const int kt = base + lane;
+      const int c = kt < p.nkt ? cls[kt] : 0;
+      const uint32_t bal = __ballot_sync(0xffffffffu, c != 0);
+      const int pos = count + __popc(bal & ((1u << lane) - 1u));
+      if (c != 0) list[pos] = (uint16_t)(kt | (c == 1 ? 0x8000 : 0));
+      count += __popc(bal);
+    }
+    if (lane == 0) *nk_slot = count;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const int nk = *nk_slot;
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sm_base = smem_u32(smem);
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0 && nk > 0) {
+      mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
+      for (int t = 0; t < NT; ++t)
+        for (int c = 0; c < KB; ++c)
+          tc::tma_load_4d(smem + Lay::q_off + (t * KB + c) * BOX, &tm_q, c * 64, row0, h0 + t, b,
+                          bar_q);
+      for (int n = 0; n < nk && ok; ++n) {
+        const int st = n % STAGES, use = n / STAGES;
+        if (n >= STAGES) ok = mbar_wait(bar_empty + st, (use - 1) & 1, p.err);
+        if (!ok) break;
+        const int kt = list[n] & 0x7fff;
+        mbar_arrive_expect_tx(bar_kfull + st, KB * BOX);
+        for (int c = 0; c < KB; ++c)
+          tc::tma_load_4d(smem + Lay::k_off + (st * KB + c) * BOX, &tm_k, c * 64, kt * BN, g, b,
+                          bar_kfull + st);
+        mbar_arrive_expect_tx(bar_vfull + st, KB * BOX);
+        for (int c = 0; c < KB; ++c)
+          tc::tma_load_4d(smem + Lay::v_off + (st * KB + c) * BOX, &tm_v, c * 64, kt * BN, g, b,
+                          bar_vfull + st);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && nk > 0) {
+      constexpr uint32_t id_s = tc::idesc_bf16(BM, BN, 0, 0);
+      constexpr uint32_t id_pv = tc::idesc_bf16(BM, D, 0, 1);
+      ok = mbar_wait(bar_q, 0, p.err);
+      tc::fence_after_sync();
+      for (int n = 0; n < nk && ok; ++n) {
+        const int st = n % STAGES, use = n / STAGES;
+        if (!(ok = mbar_wait(bar_kfull + st, use & 1, p.err))) break;
+        tc::fence_after_sync();
+        for (int t = 0; t < NT && ok; ++t) {
+          if (n > 0 && !(ok = mbar_wait(bar_odone + t, (n - 1) & 1, p.err))) break;
+          tc::fence_after_sync();
+          const uint32_t d_s = tmem + t * BN;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t qa = sm_base + Lay::q_off + (t * KB + kk / 4) * BOX + (kk % 4) * 32;
+            const uint32_t ka = sm_base + Lay::k_off + (st * KB + kk / 4) * BOX + (kk % 4) * 32;
+            tc::mma_ss(d_s, tc::sw128_desc(qa, 16, 1024), tc::sw128_desc(ka, 16, 1024), id_s,
+                       kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar_sfull + t);
+        }
+        if (!ok) break;
+        if (!(ok = mbar_wait(bar_vfull + st, use & 1, p.err))) break;
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
+          tc::fence_after_sync();
+          const uint32_t d_o = tmem + NT * BN + t * D;
+          const uint32_t a_p = tmem + t * BN;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint32_t va = sm_base + Lay::v_off + st * KB * BOX + kk * 2048;
+            tc::mma_ts(d_o, a_p + kk * 8, tc::sw128_desc(va, BOX, 1024), id_pv,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(bar_odone + t);
+        }
+        tc::mma_commit(bar_empty + st);
+      }
+      // drain: the last release of every stage has landed before the CTA exits
+      for (int s = 0; s < STAGES && s < nk && ok; ++s) {
+        const int last_use = (nk - 1 - s) / STAGES;
+        ok = mbar_wait(bar_empty + s, last_use & 1, p.err);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax warpgroup t ----------------
+    const int t = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the tile
+    const int i = row0 + r;
+    const bool row_ok = r < rows;
+    const int ic = row_ok ? i : row0;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + t * BN;
+    const uint32_t t_o = tmem + lane_base + NT * BN + t * D;
+    const int segq = p.mask.seg_q ? __ldg(p.mask.seg_q + (int64_t)b * p.Lq + ic) : 0;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    for (int n = 0; n < nk; ++n) {
+      const int ent = list[n];
+      const int kt = ent & 0x7fff;
+      const bool partial = (ent & 0x8000) != 0;
+      uint32_t mw[BN / 32];
+      if (partial) {
+#pragma unroll
+        for (int w = 0; w < BN / 32; ++w)
+          mw[w] = row_ok ? mask_word(p.mask, b, ic, kt * BN + 32 * w, p.Lk, p.Lq, kvl, segq) : 0u;
+      }
+      if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
+      __syncwarp();
+      tc::fence_after_sync();
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t raw[32];
+        tc::tmem_ld32(t_s + c * 32, raw);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * sl2;
+      }
+      if (partial) {
+#pragma unroll
+        for (int j = 0; j < BN; ++j)
+          if (!((mw[j >> 5] >> (j & 31)) & 1u)) x[j] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < BN; ++j) mx = fmaxf(mx, x[j]);
+      const float m_new = fmaxf(m_used, mx);
+      bool rescale = false;
+      float factor = 1.f;
+      if (m_used == -INFINITY) {
+        m_used = m_new;
+      } else if (m_new - m_used > 8.f) {
+        rescale = true;
+        factor = tc::ex2(m_used - m_new);
+        m_used = m_new;
+        l *= factor;
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // O_t holds every P.V issued so far: s_full(n) was committed after
+        // o_done(n-1) completed.
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tc::tmem_ld32(t_o + c * 32, o);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+          tc::tmem_st32(t_o + c * 32, o);
+        }
+        tc::tmem_wait_st();
+      }
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = tc::ex2(x[c * 64 + 2 * j] - mb);
+          const float p1 = tc::ex2(x[c * 64 + 2 * j + 1] - mb);
+          ls += p0 + p1;
+          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          pk[j] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        tc::tmem_st32(t_s + c * 32, pk);
+      }
+      l += ls;
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(bar_pfull + t);
+    }
+    // epilogue
+    float o_scale = 0.f;
+    if (nk > 0) {
+      if (ok) ok = mbar_wait(bar_odone + t, (nk - 1) & 1, p.err);
+      __syncwarp();
+      tc::fence_after_sync();
+      o_scale = (l > 0.f) ? 1.f / l : 0.f;
+    }
+    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + (int64_t)b * p.os[0] +
+                          (int64_t)(h0 + t) * p.os[1] + (int64_t)ic * p.os[2];
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (nk > 0) {
+        tc::tmem_ld32(t_o + c * 32, o);
+        tc::tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[2 * j]) * o_scale,
+                                                 __uint_as_float(o[2 * j + 1]) * o_scale);
+        pk[j] = *reinterpret_cast<uint32_t *>(&h);
+      }
+      if (row_ok) {
+        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      }
+    }
+    if (row_ok && p.lse)
+      p.lse[((int64_t)b * p.Hq + h0 + t) * p.Lq + i] =
+          (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, Lay::tmem_cols);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// bf16 [B][H][L][D] view with element strides (b, h, l) -> 4-D map, box 64 x 128.
+bool make_map(CUtensorMap *m, const void *base, int B, int H, int L, int D, const int64_t *st) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int NT, int STAGES>
+mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                     const TcParams &p, cudaStream_t s) {
+  using Lay = Layout<D, NT, STAGES>;
+  auto kern = prefill_tc_kernel<D, NT, STAGES>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::smem_bytes) !=
+        cudaSuccess)
+      return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the tensor-core prefill");
+    attr_set = true;
+  }
+  dim3 grid((p.Lq + BM - 1) / BM, p.Hq / NT, p.B);
+  kern<<<grid, Lay::threads, Lay::smem_bytes, s>>>(mq, mk, mv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+
+}  // namespace
+
+mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
+  if (a.dtype != MGQA_BF16) return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill is bf16 only");
+  const int nkt = (a.Lk + BN - 1) / BN;
+  if (nkt > MAXKT) return fail(MGQA_ERR_UNSUPPORTED, "Lk > %d", MAXKT * BN);
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride) ||
+      !make_map(&mk, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride) ||
+      !make_map(&mv, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride))
+    return fail(MGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  TcParams p{};
+  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k};
+  p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lq = a.Lq; p.Lk = a.Lk;
+  p.n_rep = a.Hq / a.Hkv; p.nkt = nkt;
+  p.scale_log2 = a.scale * kLog2e;
+  p.out = a.out;
+  p.os[0] = a.o_stride[0]; p.os[1] = a.o_stride[1]; p.os[2] = a.o_stride[2];
+  p.lse = a.lse; p.err = a.dev_error;
+  const bool pair = (p.n_rep % 2) == 0;
+  if (a.D == 128) return pair ? launch_t<128, 2, 2>(mq, mk, mv, p, s) : launch_t<128, 1, 2>(mq, mk, mv, p, s);
+  if (a.D == 64) return pair ? launch_t<64, 2, 3>(mq, mk, mv, p, s) : launch_t<64, 1, 3>(mq, mk, mv, p, s);
+  return fail(MGQA_ERR_UNSUPPORTED, "head dim %d", a.D);
+}
+
 }  // namespace mgqa
