@@ -400,6 +400,18 @@ def run_gpu(args):
     hbm = peak_value(pk, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
     bf16 = peak_value(pk, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
 
+    if args.only == "prefill":
+        wl = W.padded_cfg(variant="bits")
+        secs, _ = bench_prefill_graph(M, wl, dev, CALLS_PER_STEP, PREFILL_SETS, args.steps,
+                                      args.warmup, world)
+        print(json.dumps({"leg": "prefill", "us_per_call": secs / (args.steps * CALLS_PER_STEP) * 1e6}))
+        return 0
+    if args.only == "decode":
+        wd = W.static_cache_decode(variant="span")
+        t = bench_decode(M, wd, dev, args.steps, args.warmup, world)
+        print(json.dumps({"leg": "decode", "us_per_call": t * 1e6}))
+        return 0
+
     clocks = ClockSampler(local)
     # ---- headline: padded CFG prefill, 32 calls per step
     wl = W.padded_cfg(variant="bits")
@@ -475,12 +487,16 @@ def run_gpu(args):
         "other_workloads": others,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        heads = 4
-        f, s, used = cpu_oracle_sample(wl, heads)
-        line["cpu_baseline"] = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": used,
+        tot_f, tot_s, reps = 0.0, 0.0, 0
+        while tot_s < 10.0 and reps < 100:
+            f, s, used = cpu_oracle_sample(wl, 16)
+            tot_f += f
+            tot_s += s
+            reps += 1
+        line["cpu_baseline"] = {"value": tot_f / tot_s / 1e12, "unit": "TFLOP/s", "cores": used,
                                 "kind": "oracle",
-                                "sample": f"{heads} of 16 query heads (both CFG rows) of one "
-                                          f"padded-CFG prefill call, {s:.1f} s"}
+                                "sample": f"{reps} whole padded-CFG prefill calls (2 rows x 16 heads "
+                                          f"x 1024 queries), {tot_s:.1f} s"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -496,6 +512,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mgqa", choices=["mgqa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="profiling aid: run only the headline prefill or only the decode leg "
+                         "and print its raw timings")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

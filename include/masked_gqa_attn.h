@@ -77,7 +77,7 @@ typedef struct mgqa_args {
   int32_t Hq;   /* query heads */
   int32_t Hkv;  /* KV heads; Hq % Hkv == 0 */
   int32_t Lq;   /* query positions (decode: must be 1) */
-  int32_t Lk;   /* key positions (decode: static-cache capacity) */
+  int32_t Lk;   /* key positions (decode: static-cache capacity, <= 32768) */
   int32_t D;    /* head dim: 64 or 128 */
 
   /* q [B][Hq][Lq][D], k and v [B][Hkv][Lk][D], out [B][Hq][Lq][D]. The head-dim

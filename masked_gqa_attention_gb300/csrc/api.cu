@@ -49,6 +49,8 @@ mgqa_status validate(const mgqa_args *a, bool decode) {
   if ((int64_t)a->B * a->Hq * a->Lq > (int64_t)1 << 31)
     return fail(MGQA_ERR_UNSUPPORTED, "B*Hq*Lq too large");
   if (decode && a->Lq != 1) return fail(MGQA_ERR_INVALID_ARG, "decode needs Lq == 1");
+  if (decode && a->Lk > kDecodeMaxLk)
+    return fail(MGQA_ERR_UNSUPPORTED, "decode cache longer than %d slots", kDecodeMaxLk);
   if (!std::isfinite(a->scale)) return fail(MGQA_ERR_INVALID_ARG, "scale is not finite");
   const size_t es = a->dtype == MGQA_BF16 ? 2 : 4;
   mgqa_status st;

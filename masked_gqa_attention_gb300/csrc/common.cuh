@@ -87,6 +87,14 @@ MGQA_DEV uint32_t mask_word(const MaskView &m, int b, int i, int jbase, int Lk, 
   return w;
 }
 
+// Named CTA barriers (ids 1..15; id 0 is __syncthreads).
+MGQA_DEV void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+MGQA_DEV void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---- mbarrier / bulk-copy primitives (PTX) --------------------------------
 
 MGQA_DEV uint32_t smem_u32(const void *p) {

@@ -18,9 +18,14 @@
 //   4. Per head: chunk max, exp2, sum (one warp per head).
 //   5. P.V: one thread per (head, pair of dims) walks the chunk's allowed
 //      slots in ascending order.
-//   6. The partial (m, l, o) goes to the workspace; the CTA that takes the
-//      last ticket of (b, hg) merges all chunks in ascending chunk order and
-//      resets the ticket. Empty chunks publish m = -inf and are skipped.
+//   6. The partial (m, l, o) goes to the workspace. Every non-empty CTA also
+//      knows which chunks of its row are non-empty (a bitmap built from the
+//      mask words or the length, one word per thread), so empty CTAs exit at
+//      once; the non-empty CTA that takes the last ticket of (b, hg) merges
+//      the non-empty chunks in ascending order (loads issued in parallel) and
+//      resets the ticket. With segment ids the bitmap would cost a scan of the
+//      whole row, so there every CTA takes a ticket and empty chunks publish
+//      m = -inf instead.
 // All sums run in a fixed order, so the bits depend only on which slots are
 // allowed: a full-cache bitmask and the equivalent filled length agree bit
 // for bit.
@@ -50,6 +55,7 @@ struct DecodeParams {
 };
 
 constexpr int kThreads = 256;
+constexpr int kMaxChunks = kDecodeMaxLk / kDecodeChunk;
 
 template <typename T, int D, int NREP, int C>
 struct DecodeSmem {
@@ -59,8 +65,14 @@ struct DecodeSmem {
   float s[NREP][C];
   uint32_t allowed[C / 32];
   float2 ml[NREP];
+  uint32_t chunk_ne[kMaxChunks / 32];  // non-empty chunks of this (b, head group)
+  float w[NREP][kMaxChunks];           // merge: per-chunk m, then weights 2^(m_c - M)
+  float lval[NREP][kMaxChunks];        // merge: per-chunk l
+  int nz[kMaxChunks];                  // merge: non-empty chunk indices, ascending
+  float inv_l[NREP];
   uint64_t bar;
   int n_allowed;
+  int n_ne;
   int is_last;
 };
 
@@ -97,7 +109,49 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     mbar_init(&sm.bar, 1);
     fence_mbarrier_init();
   }
+  const bool by_seg = p.seg_q != nullptr;
+  const bool mine_ne = __syncthreads_or(a);
+  // an empty chunk reads nothing and publishes nothing; chunk 0 stays to write
+  // the output of a row that has no allowed slot at all
+  if (!mine_ne && !by_seg && c != 0) return;
+
+  // which chunks of this row hold an allowed slot (identical in every CTA)
+  if (!by_seg) {
+    for (int base = 0; base < p.nch; base += kThreads) {
+      const int cc = base + tid;
+      const int jb = cc * C;
+      bool ne = cc < p.nch && jb < min(p.Lk, kvl);
+      if (ne && p.bits) {
+        uint32_t any = 0u;
+#pragma unroll
+        for (int w = 0; w < C / 32; ++w) {
+          const int jw = jb + 32 * w;
+          const int lim = min(p.Lk, kvl) - jw;
+          if (lim > 0) {
+            const uint32_t valid = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
+            any |= __ldg(p.bits + (int64_t)b * p.ms_b + (jw >> 5)) & valid;
+          }
+        }
+        ne = any != 0u;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, ne);
+      if (lane == 0 && base + warp * 32 < p.nch) sm.chunk_ne[cc >> 5] = bal;
+    }
+  }
   __syncthreads();
+  if (!mine_ne && !by_seg) {  // chunk 0, empty
+    bool row_empty = true;
+    for (int w = 0; w < (p.nch + 31) / 32; ++w) row_empty = row_empty && sm.chunk_ne[w] == 0u;
+    if (row_empty) {
+      for (int idx = tid; idx < NREP * D; idx += kThreads) {
+        const int r = idx / D, d = idx % D;
+        T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
+        orow[d] = from_float<T>(0.f);
+        if (d == 0 && p.lse) p.lse[(int64_t)b * p.Hq + h0 + r] = -INFINITY;
+      }
+    }
+    return;
+  }
   if (tid == 0) {
     int n = 0;
 #pragma unroll
@@ -218,41 +272,96 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     if (tid < NREP) p.ws_ml[row0 + (int64_t)tid * p.nch] = make_float2(-INFINITY, 0.f);
   }
 
-  // 6. ticket; the last CTA of (b, hg) merges every chunk
-  __threadfence();
+  // 6. ticket; the last non-empty CTA of (b, hg) merges the non-empty chunks
   __syncthreads();
   unsigned *tick = p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg;
   if (tid == 0) {
-    const unsigned t = atomicAdd(tick, 1u);
-    sm.is_last = (t == (unsigned)(gridDim.x - 1));
-    __threadfence();
+    int n_ne = p.nch;
+    if (!by_seg) {
+      n_ne = 0;
+      for (int w = 0; w < (p.nch + 31) / 32; ++w) n_ne += __popc(sm.chunk_ne[w]);
+    }
+    unsigned t;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(tick) : "memory");
+    sm.is_last = (t == (unsigned)(n_ne - 1));
   }
   __syncthreads();
   if (!sm.is_last) return;
 
+  // non-empty chunk list, ascending
+  if (warp == 0) {
+    int count = 0;
+    for (int base = 0; base < p.nch; base += 32) {
+      const int cc = base + lane;
+      bool ne = false;
+      if (cc < p.nch) {
+        if (by_seg) ne = __ldcg(&p.ws_ml[((int64_t)b * p.Hq + h0) * p.nch + cc]).x != -INFINITY;
+        else ne = (sm.chunk_ne[cc >> 5] >> (cc & 31)) & 1u;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, ne);
+      if (ne) sm.nz[count + __popc(bal & ((1u << lane) - 1u))] = cc;
+      count += __popc(bal);
+    }
+    if (lane == 0) sm.n_ne = count;
+  }
+  __syncthreads();
+  const int nnz = sm.n_ne;
+  for (int idx = tid; idx < NREP * nnz; idx += kThreads) {
+    const int r = idx / nnz, k = idx % nnz;
+    const float2 ml = __ldcg(&p.ws_ml[((int64_t)b * p.Hq + h0 + r) * p.nch + sm.nz[k]]);
+    sm.w[r][k] = ml.x;
+    sm.lval[r][k] = ml.y;
+  }
+  __syncthreads();
+  for (int r = warp; r < NREP; r += kThreads / 32) {
+    float M = -INFINITY;
+    for (int k = lane; k < nnz; k += 32) M = fmaxf(M, sm.w[r][k]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int k = lane; k < nnz; k += 32) {
+      const float m = sm.w[r][k];
+      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      L = fmaf(sm.lval[r][k], wgt, L);
+      sm.w[r][k] = wgt;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      sm.inv_l[r] = (L > 0.f) ? 1.f / L : 0.f;
+      sm.ml[r] = make_float2(M, L);
+    }
+  }
+  __syncthreads();
   for (int idx = tid; idx < NREP * D / 2; idx += kThreads) {
     const int r = idx / (D / 2), dp = idx % (D / 2);
     const int64_t hrow = ((int64_t)b * p.Hq + h0 + r) * p.nch;
-    float M = -INFINITY;
-    for (int cc = 0; cc < p.nch; ++cc) M = fmaxf(M, __ldcg(&p.ws_ml[hrow + cc]).x);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-    if (M != -INFINITY) {
-      for (int cc = 0; cc < p.nch; ++cc) {
-        const float2 ml = __ldcg(&p.ws_ml[hrow + cc]);
-        if (ml.x == -INFINITY) continue;
-        const float w = exp2f(ml.x - M);
-        const float2 o = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hrow + cc) * D) + dp);
-        L = fmaf(ml.y, w, L);
-        o0 = fmaf(o.x, w, o0);
-        o1 = fmaf(o.y, w, o1);
+    float o0 = 0.f, o1 = 0.f;
+    int k = 0;
+    for (; k + 4 <= nnz; k += 4) {
+      float2 o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        o[u] = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hrow + sm.nz[k + u]) * D) + dp);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        o0 = fmaf(o[u].x, sm.w[r][k + u], o0);
+        o1 = fmaf(o[u].y, sm.w[r][k + u], o1);
       }
     }
-    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    for (; k < nnz; ++k) {
+      const float2 o = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hrow + sm.nz[k]) * D) + dp);
+      o0 = fmaf(o.x, sm.w[r][k], o0);
+      o1 = fmaf(o.y, sm.w[r][k], o1);
+    }
+    const float inv = sm.inv_l[r];
     T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
     orow[2 * dp] = from_float<T>(o0 * inv);
     orow[2 * dp + 1] = from_float<T>(o1 * inv);
-    if (dp == 0 && p.lse)
-      p.lse[(int64_t)b * p.Hq + h0 + r] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
+    if (dp == 0 && p.lse) {
+      const float2 ML = sm.ml[r];
+      p.lse[(int64_t)b * p.Hq + h0 + r] = (ML.y > 0.f) ? (ML.x + log2f(ML.y)) * kLn2 : -INFINITY;
+    }
   }
   if (tid == 0) *tick = 0u;
 }

@@ -13,6 +13,8 @@ mgqa_status fail(mgqa_status code, const char *fmt, ...);
 
 // Decode: fixed chunks of kDecodeChunk absolute cache slots per CTA.
 constexpr int kDecodeChunk = 128;
+// Longest static cache the decode kernel accepts (bounds its merge tables).
+constexpr int kDecodeMaxLk = 32768;
 // Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).
 int decode_heads_per_cta(int n_rep);
 size_t decode_workspace_bytes(const mgqa_args &a);

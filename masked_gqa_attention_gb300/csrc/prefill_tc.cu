@@ -26,7 +26,9 @@
 //            (only when the max grows by more than 2^8), P = exp2(x - m)
 //            -> p_full[t]
 //   MMA:     O_t += P_t V_n               -> o_done[t]; both heads -> kv_empty
-// S_t(n+1) is issued only after o_done[t](n), since it overwrites P_t.
+// S_t(n+1) is issued right behind O_t += P_t(n) V(n) (same issuing thread,
+// executed in order), so the tensor pipe never idles waiting for a
+// completion round trip.
 // Before the pipeline, all warps classify the key tiles of this query tile
 // as empty / full / partial from the mask forms; only non-empty tiles enter
 // the pipeline and only partial tiles pay for per-element masking.
@@ -46,6 +48,7 @@ constexpr int BM = 128;       // query rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int MAXKT = 2048;   // key tiles per row (Lk <= 262144)
 constexpr int BOX = 16384;    // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+constexpr int kPrefetch = 4;  // key tiles prefetched into L2 ahead of their load
 
 struct TcParams {
   MaskView mask;
@@ -64,13 +67,16 @@ struct Layout {
   static constexpr int k_off = q_off + NT * KB * BOX;
   static constexpr int v_off = k_off + STAGES * KB * BOX;
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
-  // barriers: q, k_full[S], v_full[S], kv_empty[S], s_full[NT], p_full[NT], o_done[NT]
-  static constexpr int n_bars = 1 + 3 * STAGES + 3 * NT;
+  // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
+  // o_done[NT], tok[2] (softmax turn hand-over between the two heads)
+  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32
   static constexpr int seg_slot = misc_off + 8;     // int32 x2 (min, max of seg_q)
-  static constexpr int list_off = misc_off + 16;    // uint16[MAXKT]
+  static constexpr int any_off = misc_off + 16;     // uint32[MAXKT/32]: tile has an allowed bit
+  static constexpr int all_off = any_off + MAXKT / 8;  // uint32[MAXKT/32]: tile all allowed
+  static constexpr int list_off = all_off + MAXKT / 8;  // uint16[MAXKT]
   static constexpr int cls_off = list_off + 2 * MAXKT;  // uint8[MAXKT]
   static constexpr int total = cls_off + MAXKT;
   static constexpr int smem_bytes = total + 1024;   // slack for 1024-B alignment
@@ -81,6 +87,172 @@ struct Layout {
                                         : tmem_cols_used <= 256 ? 256 : 512;
   static_assert(tmem_cols_used <= 512, "tensor memory");
 };
+
+// Allowed-key words of one query row for a partial key tile (keys k0..k0+127).
+// Segment ids: each lane loads 4 of the tile's key ids (coalesced) and the
+// warp builds each row's words with ballots, one round per distinct query
+// segment among its 32 rows (usually one or two).
+MGQA_DEV void tile_mask_words(const TcParams &p, int b, int i, bool row_ok, int k0, int kvl,
+                              int segq, int lane, uint32_t (&mw)[BN / 32]) {
+#pragma unroll
+  for (int w = 0; w < BN / 32; ++w) {
+    const int jw = k0 + 32 * w;
+    const int lim = min(p.Lk, kvl) - jw;
+    mw[w] = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : ((1u << lim) - 1u));
+  }
+  if (p.mask.bits) {
+    const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)i * p.mask.sq;
+    uint32_t v[BN / 32];
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) v[w] = (mw[w] != 0u) ? __ldg(mrow + ((k0 >> 5) + w)) : 0u;
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) mw[w] &= v[w];
+  }
+  if (p.mask.seg_q) {
+    int sk[BN / 32];
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) {
+      const int j = k0 + 32 * w + lane;
+      sk[w] = j < p.Lk ? __ldg(p.mask.seg_k + (int64_t)b * p.Lk + j) : -1;
+    }
+    const int mine = (row_ok && segq >= 0) ? segq : -1;
+    uint32_t sw[BN / 32] = {0u, 0u, 0u, 0u};
+    uint32_t pending = __ballot_sync(0xffffffffu, mine >= 0);
+    while (pending) {
+      const int x = __shfl_sync(0xffffffffu, mine, __ffs(pending) - 1);
+#pragma unroll
+      for (int w = 0; w < BN / 32; ++w) {
+        const uint32_t bw = __ballot_sync(0xffffffffu, sk[w] == x);
+        if (mine == x) sw[w] = bw;
+      }
+      pending &= ~__ballot_sync(0xffffffffu, mine == x);
+    }
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) mw[w] &= sw[w];
+  }
+  if (!row_ok) {
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) mw[w] = 0u;
+  }
+}
+
+// 2^x for x <= 8 on the FMA pipe: x = n + f with n = round(x) (magic-number
+// rounding, 1.5 * 2^23), f in [-1/2, 1/2]; 2^f from a degree-3 polynomial
+// fitted by Remez exchange for minimax relative error on that interval
+// (max relative error 7.5e-5, far below bf16's 2^-9); n is added into the
+// exponent field. Inputs below -126 are clamped (result ~1e-38).
+MGQA_DEV float exp2_poly(float x) {
+  x = fmaxf(x, -126.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  float q = fmaf(f, 0.0551716685f, 0.2426111251f);
+  q = fmaf(q, f, 0.6932609677f);
+  q = fmaf(q, f, 0.9999280572f);
+  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+}
+
+// Every kPolyEvery-th exponential pair of a row goes to exp2_poly, the rest to
+// the MUFU ex2 unit, so both pipes share the softmax's exponentials.
+constexpr int kPolyEvery = 4;
+
+// One 128-key tile of one softmax row (thread = row): running max with lazy
+// rescale, P = exp2(s*scale*log2e - m) as bf16 pairs over the S columns, and
+// the row sum. NEG: the scale is negative (the max of scaled scores is the
+// min of raw ones). PARTIAL: mw holds the row's allowed-key bits.
+template <int D, bool NEG, bool PARTIAL>
+MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
+                           float &m_used, float &l) {
+  constexpr float MV = NEG ? INFINITY : -INFINITY;
+  // pass 1: row extreme of the raw scores; 8 independent accumulators
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = MV;
+#pragma unroll
+  for (int c = 0; c < BN / 32; c += 2) {
+    uint32_t r0[32], r1[32];
+    tc::tmem_ld32(t_s + c * 32, r0);
+    tc::tmem_ld32(t_s + (c + 1) * 32, r1);
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float a0 = __uint_as_float(r0[j]), a1 = __uint_as_float(r1[j]);
+      if (PARTIAL) {
+        if (!((mw[c] >> j) & 1u)) a0 = MV;
+        if (!((mw[c + 1] >> j) & 1u)) a1 = MV;
+      }
+      mx[j & 7] = NEG ? fminf(mx[j & 7], fminf(a0, a1)) : fmaxf(mx[j & 7], fmaxf(a0, a1));
+    }
+  }
+#pragma unroll
+  for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+    for (int u = 0; u < k; ++u) mx[u] = NEG ? fminf(mx[u], mx[u + k]) : fmaxf(mx[u], mx[u + k]);
+  const float mr = mx[0];
+  const float m_tile = (PARTIAL && mr == MV) ? -INFINITY : mr * sl2;
+  const float m_new = fmaxf(m_used, m_tile);
+  bool rescale = false;
+  float factor = 1.f;
+  if (m_used == -INFINITY) {
+    m_used = m_new;
+  } else if (m_new - m_used > 8.f) {
+    rescale = true;
+    factor = tc::ex2(m_used - m_new);
+    m_used = m_new;
+    l *= factor;
+  }
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O holds every P.V issued so far: this tile's S MMA was issued after the
+    // previous tile's P.V, and its completion covers that MMA.
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tc::tmem_ld32(t_o + c * 32, o);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
+      tc::tmem_st32(t_o + c * 32, o);
+    }
+    tc::tmem_wait_st();
+  }
+  const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+  // pass 2: 16-column chunk c+1 loads while chunk c is exponentiated/packed
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  uint32_t rb[2][16];
+  tc::tmem_ld16(t_s, rb[0]);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < BN / 16; ++c) {
+    if (c + 1 < BN / 16) tc::tmem_ld16(t_s + (c + 1) * 16, rb[(c + 1) & 1]);
+    const uint32_t(&raw)[16] = rb[c & 1];
+    const uint32_t bits = PARTIAL ? (mw[c >> 1] >> ((c & 1) * 16)) : 0u;
+    uint32_t pk[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float y0 = fmaf(__uint_as_float(raw[2 * j]), sl2, -mb);
+      const float y1 = fmaf(__uint_as_float(raw[2 * j + 1]), sl2, -mb);
+      const bool poly = kPolyEvery > 0 && ((c * 8 + j) % kPolyEvery) == kPolyEvery - 1;
+      float p0 = poly ? exp2_poly(y0) : tc::ex2(y0);
+      float p1 = poly ? exp2_poly(y1) : tc::ex2(y1);
+      if (PARTIAL) {
+        if (!((bits >> (2 * j)) & 1u)) p0 = 0.f;
+        if (!((bits >> (2 * j + 1)) & 1u)) p1 = 0.f;
+      }
+      acc[j] += p0 + p1;
+      __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+      pk[j] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    tc::tmem_st8(t_s + c * 8, pk);
+    tc::tmem_wait_ld();
+  }
+#pragma unroll
+  for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+    for (int u = 0; u < k; ++u) acc[u] += acc[u + k];
+  l += acc[0];
+  tc::tmem_wait_st();
+}
 
 template <int D, int NT, int STAGES>
 __global__ void __launch_bounds__(128 * (1 + NT), 1)
@@ -95,14 +267,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_q = bars;
   uint64_t *bar_kfull = bars + 1;
   uint64_t *bar_vfull = bars + 1 + STAGES;
-  uint64_t *bar_empty = bars + 1 + 2 * STAGES;
-  uint64_t *bar_sfull = bars + 1 + 3 * STAGES;
+  uint64_t *bar_kempty = bars + 1 + 2 * STAGES;
+  uint64_t *bar_vempty = bars + 1 + 3 * STAGES;
+  uint64_t *bar_sfull = bars + 1 + 4 * STAGES;
   uint64_t *bar_pfull = bar_sfull + NT;
   uint64_t *bar_odone = bar_pfull + NT;
+  uint64_t *bar_tok = bar_odone + NT;  // [0]: head 0 -> head 1, [1]: head 1 -> head 0
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
   uint16_t *list = reinterpret_cast<uint16_t *>(smem + Lay::list_off);
+  uint32_t *any_bits = reinterpret_cast<uint32_t *>(smem + Lay::any_off);
+  uint32_t *all_bits = reinterpret_cast<uint32_t *>(smem + Lay::all_off);
   uint8_t *cls = smem + Lay::cls_off;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -120,16 +296,32 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_empty + s, 1);
+      mbar_init(bar_kempty + s, 1);
+      mbar_init(bar_vempty + s, 1);
     }
     for (int t = 0; t < NT; ++t) {
       mbar_init(bar_sfull + t, 1);
       mbar_init(bar_pfull + t, 128);
       mbar_init(bar_odone + t, 1);
     }
+    mbar_init(bar_tok, 128);
+    mbar_init(bar_tok + 1, 128);
     fence_mbarrier_init();
+    // Q does not depend on the mask: start its load before classifying
+    if (row0 < p.Lq) {
+      mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
+      for (int t = 0; t < NT; ++t)
+        for (int c = 0; c < KB; ++c)
+          tc::tma_load_4d(smem + Lay::q_off + (t * KB + c) * BOX, &tm_q, c * 64, row0, h0 + t, b,
+                          bar_q);
+    }
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::tmem_cols);
+  if (p.mask.bits)
+    for (int w = tid; w < (p.nkt + 31) / 32; w += blockDim.x) {
+      any_bits[w] = 0u;
+      all_bits[w] = 0xffffffffu;
+    }
   if (warp == 0) {
     if (lane == 0) {
       tc::prefetch_tensormap(&tm_q);
@@ -156,6 +348,45 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   __syncthreads();
 
+  // ---- packed-bit mask: per-tile "some key allowed" / "all keys allowed" ---
+  // Each warp reads whole mask rows (32 consecutive words per load), folds
+  // its rows per word, reduces the 4 words of a tile across lanes and merges
+  // into the CTA's bitsets.
+  if (p.mask.bits) {
+    const int W = (p.Lk + 31) >> 5;
+    for (int wb = 0; wb < W; wb += 32) {
+      const int w = wb + lane;
+      const int lim = p.Lk - 32 * w;
+      const uint32_t valid = w >= W ? 0u : (lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u));
+      uint32_t o = 0u, a = 0xffffffffu;
+#pragma unroll 4
+      for (int r = warp; r < rows; r += nwarps) {
+        const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
+        const uint32_t word = (w < W) ? (__ldg(mrow + w) & valid) : 0u;
+        o |= word;
+        a &= (word == valid && valid == 0xffffffffu) ? 0xffffffffu : 0u;
+      }
+      // a word slot past Lk (or a ragged last word) can never make a tile full
+      if (w >= W || valid != 0xffffffffu) a = 0u;
+      // 4 words per tile: lanes 4m..4m+3 -> tile (wb + 4m) / 4
+      // (every lane runs every shuffle: no short-circuit around a sync op)
+      uint32_t t_any = o != 0u ? 1u : 0u, t_all = a != 0u ? 1u : 0u;
+#pragma unroll
+      for (int off = 1; off < 4; off <<= 1) {
+        const uint32_t o_any = __shfl_xor_sync(0xffffffffu, t_any, off);
+        const uint32_t o_all = __shfl_xor_sync(0xffffffffu, t_all, off);
+        t_any |= o_any;
+        t_all &= o_all;
+      }
+      const int kt = w >> 2;
+      if ((lane & 3) == 0 && w < W) {
+        if (t_any) atomicOr(&any_bits[kt >> 5], 1u << (kt & 31));
+        if (!t_all) atomicAnd(&all_bits[kt >> 5], ~(1u << (kt & 31)));
+      }
+    }
+    __syncthreads();
+  }
+
   // ---- classify key tiles: 0 empty, 1 partial, 2 full ----------------------
   for (int kt = warp; kt < p.nkt; kt += nwarps) {
     const int k0 = kt * BN;
@@ -166,25 +397,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       full = full && k0 + BN <= kvl;
     }
     if (p.mask.bits && ne) {
-      bool any = false, all = true;
-      for (int r = lane; r < rows; r += 32) {
-        const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
-#pragma unroll
-        for (int w = 0; w < BN / 32; ++w) {
-          const int j = k0 + 32 * w;
-          if (j < p.Lk) {
-            const int lim = p.Lk - j;
-            const uint32_t valid = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
-            const uint32_t word = __ldg(mrow + (j >> 5)) & valid;
-            any = any || word != 0u;
-            all = all && word == 0xffffffffu;
-          } else {
-            all = false;
-          }
-        }
-      }
-      ne = __any_sync(0xffffffffu, any);
-      full = full && __all_sync(0xffffffffu, all);
+      ne = (any_bits[kt >> 5] >> (kt & 31)) & 1u;  // ne was true here
+      full = full && ((all_bits[kt >> 5] >> (kt & 31)) & 1u);
     }
     if (p.mask.seg_q && ne) {
       int mn = INT_MAX, mx = INT_MIN;
@@ -231,21 +445,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
+    if (lane == 0 && nk == 0) ok = mbar_wait(bar_q, 0, p.err);  // Q landed before exit
     if (lane == 0 && nk > 0) {
-      mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
-      for (int t = 0; t < NT; ++t)
-        for (int c = 0; c < KB; ++c)
-          tc::tma_load_4d(smem + Lay::q_off + (t * KB + c) * BOX, &tm_q, c * 64, row0, h0 + t, b,
-                          bar_q);
+      // L2 prefetch runs kPrefetch tiles ahead of the loads
+      auto prefetch = [&](int n) {
+        const int kt = list[n] & 0x7fff;
+        for (int c = 0; c < KB; ++c) {
+          tc::tma_prefetch_4d(&tm_k, c * 64, kt * BN, g, b);
+          tc::tma_prefetch_4d(&tm_v, c * 64, kt * BN, g, b);
+        }
+      };
+      for (int n = 0; n < nk && n < kPrefetch; ++n) prefetch(n);
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
-        if (n >= STAGES) ok = mbar_wait(bar_empty + st, (use - 1) & 1, p.err);
-        if (!ok) break;
         const int kt = list[n] & 0x7fff;
+        if (n + kPrefetch < nk) prefetch(n + kPrefetch);
+        // K(n) reuses the stage K(n-STAGES) held; it is free once the S MMAs
+        // that read it completed (V is released later, after P.V)
+        if (n >= STAGES && !(ok = mbar_wait(bar_kempty + st, (use - 1) & 1, p.err))) break;
         mbar_arrive_expect_tx(bar_kfull + st, KB * BOX);
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::k_off + (st * KB + c) * BOX, &tm_k, c * 64, kt * BN, g, b,
                           bar_kfull + st);
+        if (n >= STAGES && !(ok = mbar_wait(bar_vempty + st, (use - 1) & 1, p.err))) break;
         mbar_arrive_expect_tx(bar_vfull + st, KB * BOX);
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::v_off + (st * KB + c) * BOX, &tm_v, c * 64, kt * BN, g, b,
@@ -254,30 +476,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // Issue order: S_t(0) for every head, then per key tile n and head t:
+    // O_t += P_t(n) V(n) followed at once by S_t(n+1) = Q_t K(n+1)^T. The
+    // tensor pipe executes one thread's MMAs in issue order, so S_t(n+1)
+    // overwrites P_t(n) only after the P.V MMA has consumed it; completion of
+    // S_t(n+1) (s_full) therefore also implies O_t holds P.V up to tile n.
     if (lane == 0 && nk > 0) {
       constexpr uint32_t id_s = tc::idesc_bf16(BM, BN, 0, 0);
       constexpr uint32_t id_pv = tc::idesc_bf16(BM, D, 0, 1);
-      ok = mbar_wait(bar_q, 0, p.err);
+      auto issue_s = [&](int t, int st) {
+        const uint32_t d_s = tmem + t * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t qa = sm_base + Lay::q_off + (t * KB + kk / 4) * BOX + (kk % 4) * 32;
+          const uint32_t ka = sm_base + Lay::k_off + (st * KB + kk / 4) * BOX + (kk % 4) * 32;
+          tc::mma_ss(d_s, tc::sw128_desc(qa, 16, 1024), tc::sw128_desc(ka, 16, 1024), id_s,
+                     kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(bar_sfull + t);
+        if (t == NT - 1) tc::mma_commit(bar_kempty + st);
+      };
+      ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, 0, p.err);
       tc::fence_after_sync();
+      if (ok)
+        for (int t = 0; t < NT; ++t) issue_s(t, 0);
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
-        if (!(ok = mbar_wait(bar_kfull + st, use & 1, p.err))) break;
-        tc::fence_after_sync();
-        for (int t = 0; t < NT && ok; ++t) {
-          if (n > 0 && !(ok = mbar_wait(bar_odone + t, (n - 1) & 1, p.err))) break;
-          tc::fence_after_sync();
-          const uint32_t d_s = tmem + t * BN;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qa = sm_base + Lay::q_off + (t * KB + kk / 4) * BOX + (kk % 4) * 32;
-            const uint32_t ka = sm_base + Lay::k_off + (st * KB + kk / 4) * BOX + (kk % 4) * 32;
-            tc::mma_ss(d_s, tc::sw128_desc(qa, 16, 1024), tc::sw128_desc(ka, 16, 1024), id_s,
-                       kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar_sfull + t);
-        }
-        if (!ok) break;
+        const bool has_next = n + 1 < nk;
+        const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
         if (!(ok = mbar_wait(bar_vfull + st, use & 1, p.err))) break;
+        if (has_next && !(ok = mbar_wait(bar_kfull + st1, use1 & 1, p.err))) break;
         for (int t = 0; t < NT && ok; ++t) {
           if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
           tc::fence_after_sync();
@@ -290,13 +518,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                        (n > 0 || kk > 0) ? 1u : 0u);
           }
           tc::mma_commit(bar_odone + t);
+          if (t == NT - 1) tc::mma_commit(bar_vempty + st);
+          if (has_next) issue_s(t, st1);
         }
-        tc::mma_commit(bar_empty + st);
       }
       // drain: the last release of every stage has landed before the CTA exits
       for (int s = 0; s < STAGES && s < nk && ok; ++s) {
         const int last_use = (nk - 1 - s) / STAGES;
-        ok = mbar_wait(bar_empty + s, last_use & 1, p.err);
+        ok = mbar_wait(bar_kempty + s, last_use & 1, p.err) &&
+             mbar_wait(bar_vempty + s, last_use & 1, p.err);
       }
     }
   } else if (warp >= 4) {
@@ -311,82 +541,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t t_s = tmem + lane_base + t * BN;
     const uint32_t t_o = tmem + lane_base + NT * BN + t * D;
     const int segq = p.mask.seg_q ? __ldg(p.mask.seg_q + (int64_t)b * p.Lq + ic) : 0;
+    const bool neg = p.scale_log2 < 0.f;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     for (int n = 0; n < nk; ++n) {
       const int ent = list[n];
       const int kt = ent & 0x7fff;
       const bool partial = (ent & 0x8000) != 0;
-      uint32_t mw[BN / 32];
-      if (partial) {
-#pragma unroll
-        for (int w = 0; w < BN / 32; ++w)
-          mw[w] = row_ok ? mask_word(p.mask, b, ic, kt * BN + 32 * w, p.Lk, p.Lq, kvl, segq) : 0u;
+      uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
+      if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
+      // two heads: their softmax passes alternate (head 1 waits for head 0's
+      // pass n, head 0 for head 1's pass n-1), so each one runs while the
+      // tensor core works on the other head
+      if (NT == 2 && ok) {
+        if (t == 1) ok = mbar_wait(bar_tok, n & 1, p.err);
+        else if (n > 0) ok = mbar_wait(bar_tok + 1, (n - 1) & 1, p.err);
       }
       if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
-      float x[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t raw[32];
-        tc::tmem_ld32(t_s + c * 32, raw);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[j]) * sl2;
+      if (neg) {
+        if (partial) softmax_tile<D, true, true>(t_s, t_o, mw, sl2, m_used, l);
+        else softmax_tile<D, true, false>(t_s, t_o, mw, sl2, m_used, l);
+      } else {
+        if (partial) softmax_tile<D, false, true>(t_s, t_o, mw, sl2, m_used, l);
+        else softmax_tile<D, false, false>(t_s, t_o, mw, sl2, m_used, l);
       }
-      if (partial) {
-#pragma unroll
-        for (int j = 0; j < BN; ++j)
-          if (!((mw[j >> 5] >> (j & 31)) & 1u)) x[j] = -INFINITY;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < BN; ++j) mx = fmaxf(mx, x[j]);
-      const float m_new = fmaxf(m_used, mx);
-      bool rescale = false;
-      float factor = 1.f;
-      if (m_used == -INFINITY) {
-        m_used = m_new;
-      } else if (m_new - m_used > 8.f) {
-        rescale = true;
-        factor = tc::ex2(m_used - m_new);
-        m_used = m_new;
-        l *= factor;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O_t holds every P.V issued so far: s_full(n) was committed after
-        // o_done(n-1) completed.
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(t_o + c * 32, o);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * factor);
-          tc::tmem_st32(t_o + c * 32, o);
-        }
-        tc::tmem_wait_st();
-      }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-      float ls = 0.f;
-#pragma unroll
-      for (int c = 0; c < BN / 64; ++c) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = tc::ex2(x[c * 64 + 2 * j] - mb);
-          const float p1 = tc::ex2(x[c * 64 + 2 * j + 1] - mb);
-          ls += p0 + p1;
-          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          pk[j] = *reinterpret_cast<uint32_t *>(&h);
-        }
-        tc::tmem_st32(t_s + c * 32, pk);
-      }
-      l += ls;
-      tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(bar_pfull + t);
+      if (NT == 2) mbar_arrive(bar_tok + t);
     }
     // epilogue
     float o_scale = 0.f;
