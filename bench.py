@@ -125,12 +125,20 @@ def dist_env():
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, max_secs: float) -> float:
+    """Replicas: every rank processes the same units; the job rate is all
+    ranks' units over the slowest rank's time."""
+    return world * units_per_rank / max_secs
 
 
 def barrier(world):
@@ -423,14 +431,14 @@ def run_gpu(args):
     secs = max_over_ranks(secs, world)
     calls = args.steps * CALLS_PER_STEP
     per_call = secs / calls
-    value = world * calls * flops_call / secs / 1e12
+    value = whole_job_rate(calls * flops_call, world, secs) / 1e12
     achieved = flops_call / per_call / 1e12
 
     e2e_secs, h2d, d2h = bench_prefill_e2e(M, wl, dev, CALLS_PER_STEP, max(3, args.steps // 10),
                                            3, world)
     e2e_steps = max(3, args.steps // 10)
     e2e_secs = max_over_ranks(e2e_secs, world)
-    e2e_value = world * e2e_steps * CALLS_PER_STEP * flops_call / e2e_secs / 1e12
+    e2e_value = whole_job_rate(e2e_steps * CALLS_PER_STEP * flops_call, world, e2e_secs) / 1e12
 
     # ---- decode: static cache, full-cache bits and filled-span variants
     dec = {}
