@@ -125,6 +125,28 @@ MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
                                             size_t workspace_bytes, cudaStream_t stream);
 
+/* Bytes of the fixed device scratch array behind masked_gqa_attn_decode_static
+ * (one per GPU that loads the library, kept until the process exits). */
+#define MGQA_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
+
+/* masked_gqa_attn_decode without a caller-supplied workspace. No passage of
+ * the engine pages has a counterpart: this entry point exists for callers that
+ * cannot allocate device memory for the library, such as code running inside
+ * a host framework that owns every device buffer and hands an extension only
+ * its inputs and outputs, or a latency-critical per-token loop that must not
+ * call the allocator. The caller still passes q/k/v, out and the mask forms.
+ * Scratch comes from a fixed array of MGQA_DECODE_STATIC_SCRATCH_BYTES in the
+ * library; a call whose masked_gqa_attn_decode_workspace_size exceeds it
+ * returns MGQA_ERR_UNSUPPORTED. Nothing is allocated or freed: no cudaMalloc,
+ * cudaFree or allocating library routine is called.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture. Every call
+ * on a device shares the one array (the previous call's contents stay in it;
+ * the merge tickets are cleared on `stream` before each launch), so calls whose
+ * executions overlap on the GPU -- different streams, or different host
+ * threads -- race and corrupt each other's results: order them on one stream. */
+MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream);
+
 /* Static description of a status code. */
 MGQA_API const char *mgqa_status_string(mgqa_status status);
 

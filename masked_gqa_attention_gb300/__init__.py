@@ -29,10 +29,13 @@ __all__ = [
     "MGQA_ERR_TIMEOUT", "MgqaError", "MgqaArgs", "lib", "make_args",
     "masked_gqa_attn_prefill", "masked_gqa_attn_decode",
     "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
+    "masked_gqa_attn_decode_static", "DECODE_STATIC_SCRATCH_BYTES",
 ]
 
 MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT = range(5)
 MGQA_BF16, MGQA_FP32 = 0, 1
+# size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
+DECODE_STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTED_SYMBOLS = (
     "masked_gqa_attn_prefill",
@@ -41,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "mgqa_status_string",
     "mgqa_last_error_detail",
     "mgqa_abi_version",
+    "masked_gqa_attn_decode_static",
 )
 
 
@@ -92,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.mgqa_status_string.restype = ctypes.c_char_p
         L.mgqa_last_error_detail.argtypes = []
         L.mgqa_last_error_detail.restype = ctypes.c_char_p
+        L.masked_gqa_attn_decode_static.argtypes = [ctypes.POINTER(MgqaArgs), P]
+        L.masked_gqa_attn_decode_static.restype = ctypes.c_int
         L.mgqa_abi_version.argtypes = []
         L.mgqa_abi_version.restype = ctypes.c_int32
         _lib = L
@@ -223,4 +229,17 @@ def masked_gqa_attn_decode(q, k, v, out=None, *, workspace: torch.Tensor, scale=
     _check(lib().masked_gqa_attn_decode(ctypes.byref(a), workspace.data_ptr(),
                                         workspace.numel() * workspace.element_size(),
                                         _stream_handle(stream)))
+    return out
+
+
+def masked_gqa_attn_decode_static(q, k, v, out=None, *, scale=None, mask_bits=None, kv_len=None,
+                                  seg_q=None, seg_k=None, lse=None, dev_error=None, stream=None):
+    """masked_gqa_attn_decode with the library's fixed scratch instead of a
+    workspace, for callers that may not allocate device memory. Calls on one
+    device share that scratch: keep them ordered on one stream."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
+                  seg_k=seg_k, lse=lse, dev_error=dev_error)
+    _check(lib().masked_gqa_attn_decode_static(ctypes.byref(a), _stream_handle(stream)))
     return out

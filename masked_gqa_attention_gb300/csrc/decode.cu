@@ -31,6 +31,7 @@
 // for bit.
 #include <cfloat>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -453,3 +454,61 @@ mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStr
 }
 
 }  // namespace mgqa
+
+// ---- decode with library-owned scratch -------------------------------------
+// For callers that cannot hand the library any device memory of its own: the
+// partial results and merge tickets of a call live in one fixed array that
+// every GPU loading this library keeps until the process exits.
+
+namespace mgqa {
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)MGQA_DECODE_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device
+
+// Device address of the scratch array on the current device. The first call
+// on a device looks it up (with that device current) and caches it.
+mgqa_status static_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(MGQA_ERR_CUDA, "no usable current CUDA device");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void *addr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_scratch);
+    if (e != cudaSuccess || addr == nullptr)
+      return fail(MGQA_ERR_CUDA, "cudaGetSymbolAddress of the decode scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_scratch_addr[dev] = addr;
+  }
+  *out = g_scratch_addr[dev];
+  return MGQA_OK;
+}
+
+}  // namespace
+}  // namespace mgqa
+
+extern "C" mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream) {
+  const size_t need = masked_gqa_attn_decode_workspace_size(args);
+  if (need == 0) return masked_gqa_attn_decode(args, nullptr, 0, stream);  // reports the bad argument
+  if (need > mgqa::kStaticScratchBytes)
+    return mgqa::fail(MGQA_ERR_UNSUPPORTED,
+                      "this decode needs %zu bytes of scratch; the library's fixed scratch holds %zu "
+                      "(pass a workspace to masked_gqa_attn_decode instead)",
+                      need, mgqa::kStaticScratchBytes);
+  void *ws = nullptr;
+  const mgqa_status st = mgqa::static_scratch(&ws);
+  if (st != MGQA_OK) return st;
+  // The merge tickets must start at zero. Their place in the array depends on
+  // the shape, so a call after one of another shape could find leftovers
+  // there: clear them on the caller's stream before every launch.
+  const mgqa::WsLayout lay = mgqa::ws_layout(*args);
+  if (cudaMemsetAsync(static_cast<char *>(ws) + lay.tick, 0, lay.total - lay.tick, stream) !=
+      cudaSuccess)
+    return mgqa::fail(MGQA_ERR_CUDA, "clearing the decode scratch tickets failed");
+  return masked_gqa_attn_decode(args, ws, mgqa::kStaticScratchBytes, stream);
+}
