@@ -113,11 +113,12 @@ MGQA_API mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t
  * (0 when the arguments are invalid). */
 MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 
-/* One-query (Lq == 1) attention over a static KV cache of Lk slots, split
- * over fixed 128-slot chunks of absolute cache positions; chunks the mask
- * leaves empty are never read, and partial results are merged in ascending
- * chunk order inside the same launch, so the full-cache (mask_bits) and
- * filled-span (kv_len) forms of one mask give bit-identical outputs.
+/* One-query (Lq == 1) attention over a static KV cache of Lk slots. The
+ * cache is cut into 128-slot chunks of absolute positions, dealt round-robin
+ * to a fixed set of 16 CTAs per (request, KV-head group); masked slots are
+ * never read, and the partial results are merged in a fixed order inside the
+ * same launch, so the full-cache (mask_bits) and filled-span (kv_len) forms
+ * of one mask give bit-identical outputs.
  * `workspace` is caller-owned device memory of at least
  * masked_gqa_attn_decode_workspace_size(args) bytes, 16-byte aligned, ZEROED
  * ONCE before its first use; each call leaves it ready for the next call.

@@ -169,6 +169,35 @@ MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
   return true;
 }
 
+// 16-byte asynchronous copy global -> shared through the L1-bypassing path;
+// both addresses 16-byte aligned. Completion: cp_async_wait_all().
+MGQA_DEV void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+MGQA_DEV void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col): register
+// fragments of the warp-wide mma.sync shape m16n8k16.
+MGQA_DEV void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two transposed 8x8 bf16 tiles from shared memory; lane i (0..15) gives the
+// address of row i (rows 8..15 form the second tile).
+MGQA_DEV void ldmatrix_x2_trans(uint32_t &b0, uint32_t &b1, const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(b0), "=r"(b1)
+               : "r"(smem_u32(row)));
+}
+
 // Untiled bulk copy global -> shared (this CTA), completion counted in bytes
 // on `bar`. Both addresses 16-byte aligned, size a multiple of 16.
 MGQA_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {

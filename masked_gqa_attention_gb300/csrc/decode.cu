@@ -1,5 +1,5 @@
-// One-query attention over a static KV cache (split over fixed chunks of
-// absolute cache slots, merged by log-sum-exp in the same launch).
+// One-query attention over a static KV cache, split over a fixed set of CTAs
+// per (request, KV-head group) and merged by log-sum-exp in the same launch.
 //
 // Passages: VoxCPM page, "Upstream-identical practice", attention bullet
 // (decode against the static cache under an explicit boolean mask; slots past
@@ -7,28 +7,25 @@
 // attention_span paragraph (attend only to the filled blocks of the 8192-slot
 // cache instead of all of it).
 //
-// Design: CTA (chunk c, head group hg, batch b) owns cache slots
-// [c*C, c*C + C) for the NREP query heads of one KV head.
-//   1. Each thread tests one slot against every mask form; a warp ballot
-//      gives the chunk's allowed-slot bitmap. An empty chunk reads no K/V.
-//   2. Every allowed slot's K row and V row is fetched with one untiled bulk
-//      copy each (TMA engine) into shared memory; masked slots are never read.
-//   3. Scores: D/8 (bf16) lanes share a slot, each holding 16 bytes of the
-//      row; NREP dot products per lane, butterfly-summed across the lanes.
-//   4. Per head: chunk max, exp2, sum (one warp per head).
-//   5. P.V: one thread per (head, pair of dims) walks the chunk's allowed
-//      slots in ascending order.
-//   6. The partial (m, l, o) goes to the workspace. Every non-empty CTA also
-//      knows which chunks of its row are non-empty (a bitmap built from the
-//      mask words or the length, one word per thread), so empty CTAs exit at
-//      once; the non-empty CTA that takes the last ticket of (b, hg) merges
-//      the non-empty chunks in ascending order (loads issued in parallel) and
-//      resets the ticket. With segment ids the bitmap would cost a scan of the
-//      whole row, so there every CTA takes a ticket and empty chunks publish
-//      m = -inf instead.
-// All sums run in a fixed order, so the bits depend only on which slots are
-// allowed: a full-cache bitmask and the equivalent filled length agree bit
-// for bit.
+// Design: kDecodeSplits CTAs serve one (request b, head group hg) -- the NREP
+// query heads of one KV head. The cache is cut into 128-slot chunks of
+// absolute positions; CTA x owns chunks x, x+S, x+2S, ... (S = kDecodeSplits).
+//   1. One thread per slot tests every mask form; warp ballots give the CTA's
+//      allowed-slot bitmap, which is compacted into a dense list. Masked slots
+//      are never read, empty chunks cost nothing.
+//   2. The allowed K and V rows are gathered with 16-byte asynchronous copies
+//      (consecutive threads on one row, so each row is one coalesced read)
+//      into dense shared-memory rows, up to CAP rows per batch.
+//   3. Scores: D/8 (bf16) lanes share a row, 16 bytes each, NREP dot products
+//      per lane, butterfly-summed; per-head batch softmax (one warp a head);
+//      P.V by one thread per (head, pair of dims) over the dense rows; batches
+//      fold into a running (m, l, o) in ascending slot order.
+//   4. Every CTA writes its partial (m, l, o) to the workspace and takes a
+//      ticket; the last of the S CTAs merges the S partials in ascending x and
+//      resets the ticket.
+// The chunk-to-CTA assignment and every summation order depend only on the
+// set of allowed slots, so a full-cache bitmask and the equivalent filled
+// length give bit-identical outputs.
 #include <cfloat>
 #include <cmath>
 #include <mutex>
@@ -50,318 +47,443 @@ struct DecodeParams {
   float *lse;
   int32_t *err;
   int B, Hq, Hkv, Lk, n_rep, nch;
-  float2 *ws_ml;      // [B][Hq][nch]   (m in log2 units, l)
-  float *ws_o;        // [B][Hq][nch][D] unnormalised partial outputs
-  unsigned *ws_tick;  // [B][Hq/NREP]
+  float2 *ws_ml;      // [B][Hq][S]    (m in log2 units, l)
+  float *ws_o;        // [B][Hq][S][D] unnormalised partial outputs
+  unsigned *ws_tick;  // [B][Hq]
 };
 
 constexpr int kThreads = 256;
-constexpr int kMaxChunks = kDecodeMaxLk / kDecodeChunk;
+constexpr int C = kDecodeChunk;
+constexpr int S = kDecodeSplits;
+constexpr int kMaxCI = (kDecodeMaxLk / kDecodeChunk + S - 1) / S;  // chunks per CTA
 
-template <typename T, int D, int NREP, int C>
+template <typename T, int D>
+constexpr int cap_rows() {  // dense K/V rows per batch: K and V <= 32 KB each
+  return (32768 / (D * (int)sizeof(T))) < 256 ? (32768 / (D * (int)sizeof(T))) : 256;
+}
+
+// bf16 runs the two products on the tensor cores (mma.sync m16n8k16, the
+// NREP query heads padded to 16 rows); fp32 stays on the CUDA cores.
+template <typename T>
+constexpr bool use_mma() {
+  return sizeof(T) == 2;
+}
+
+template <typename T, int D, int NREP>
 struct DecodeSmem {
-  alignas(128) T k[C][D];
-  alignas(128) T v[C][D];
+  static constexpr int CAP = cap_rows<T, D>();
+  static constexpr int RS = use_mma<T>() ? D + 8 : D;  // padded rows: conflict-free fragments
+  static constexpr int SROWS = use_mma<T>() ? 1 : CAP;
+  static constexpr int WG = use_mma<T>() ? kThreads / 32 : 1;
+  alignas(128) T k[CAP][RS];
+  alignas(128) T v[CAP][RS];
   float q[NREP][D];
-  float s[NREP][C];
-  uint32_t allowed[C / 32];
-  float2 ml[NREP];
-  uint32_t chunk_ne[kMaxChunks / 32];  // non-empty chunks of this (b, head group)
-  float w[NREP][kMaxChunks];           // merge: per-chunk m, then weights 2^(m_c - M)
-  float lval[NREP][kMaxChunks];        // merge: per-chunk l
-  int nz[kMaxChunks];                  // merge: non-empty chunk indices, ascending
-  float inv_l[NREP];
-  uint64_t bar;
-  int n_allowed;
-  int n_ne;
+  float s[NREP][SROWS];
+  float wm[WG][NREP], wl[WG][NREP];  // per-warp (m, l) for the final in-CTA merge
+  float wo[WG][NREP][D];             // per-warp unnormalised O
+  uint32_t words[kMaxCI][C / 32];
+  uint16_t slot[kMaxCI * C];
+  int chunk_base[kMaxCI];
+  float fo[NREP], fb[NREP];
+  int n_all;
   int is_last;
 };
 
-template <typename T, int D, int NREP, int C>
+template <typename T, int D, int NREP>
 __global__ void __launch_bounds__(kThreads)
 decode_kernel(const __grid_constant__ DecodeParams p) {
-  static_assert(C % 32 == 0 && C <= kThreads, "chunk size");
+  using Sm = DecodeSmem<T, D, NREP>;
+  constexpr int CAP = Sm::CAP;
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<DecodeSmem<T, D, NREP, C> *>(smem_raw);
+  auto &sm = *reinterpret_cast<Sm *>(smem_raw);
 
-  const int c = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
-  const int j0 = c * C;
-  const int64_t row0 = ((int64_t)b * p.Hq + h0) * p.nch + c;  // ws row of head h0
+  const int nci = x < p.nch ? (p.nch - x + S - 1) / S : 0;
+  // q does not depend on the mask: its loads fly together with kv_len's
+  const T *qb = static_cast<const T *>(p.q) + (int64_t)b * p.qs_b;
+  constexpr int QPT = (NREP * D + kThreads - 1) / kThreads;
+  float qv[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int i = tid + u * kThreads;
+    qv[u] = i < NREP * D ? to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]) : 0.f;
+  }
+  const int kvl = load_kv_len(p.kv_len, b, p.Lk, p.err, x == 0 && hg == 0 && tid == 0);
+  const int segq = p.seg_q ? __ldg(p.seg_q + b) : 0;
 
-  // 1. allowed-slot bitmap of this chunk
-  const int kvl = load_kv_len(p.kv_len, b, p.Lk, p.err, c == 0 && hg == 0 && tid == 0);
-  bool a = false;
-  const int j = j0 + tid;
-  if (tid < C && j < p.Lk) {
-    a = true;
-    if (p.bits) a = (__ldg(p.bits + (int64_t)b * p.ms_b + (j >> 5)) >> (j & 31)) & 1u;
-    if (p.kv_len) a = a && (j < kvl);
-    if (p.seg_q) {
-      const int sq = __ldg(p.seg_q + b);
-      a = a && sq >= 0 && __ldg(p.seg_k + (int64_t)b * p.Lk + j) == sq;
+  // 1. allowed-slot bitmap of this CTA's chunks (two chunks per pass)
+  auto allowed = [&](int i, int t) {
+    const int j = (x + S * i) * C + t;
+    bool a = i < nci && j < p.Lk && j < kvl;
+    if (a && p.bits) a = (__ldg(p.bits + (int64_t)b * p.ms_b + (j >> 5)) >> (j & 31)) & 1u;
+    if (a && p.seg_q) a = segq >= 0 && __ldg(p.seg_k + (int64_t)b * p.Lk + j) == segq;
+    return a;
+  };
+  for (int i0 = 0; i0 < nci; i0 += kThreads / C) {
+    const int i = i0 + tid / C, t = tid % C;
+    const uint32_t word = __ballot_sync(0xffffffffu, allowed(i, t));
+    if (lane == 0 && i < nci) sm.words[i][t >> 5] = word;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int base = 0;
+    for (int i = 0; i < nci; ++i) {
+      sm.chunk_base[i] = base;
+#pragma unroll
+      for (int w = 0; w < C / 32; ++w) base += __popc(sm.words[i][w]);
+    }
+    sm.n_all = base;
+  }
+  __syncthreads();
+  // dense list of allowed slots, ascending
+  for (int i0 = 0; i0 < nci; i0 += kThreads / C) {
+    const int i = i0 + tid / C, t = tid % C;
+    if (i < nci) {
+      const uint32_t wd = sm.words[i][t >> 5];
+      if ((wd >> (t & 31)) & 1u) {
+        int rank = sm.chunk_base[i] + __popc(wd & ((1u << (t & 31)) - 1u));
+        for (int w = 0; w < (t >> 5); ++w) rank += __popc(sm.words[i][w]);
+        sm.slot[rank] = (uint16_t)(i * C + t);
+      }
     }
   }
-  const uint32_t word = __ballot_sync(0xffffffffu, a);
-  if (lane == 0 && warp < C / 32) sm.allowed[warp] = word;
-  if (tid == 0) {
-    mbar_init(&sm.bar, 1);
-    fence_mbarrier_init();
-  }
-  const bool by_seg = p.seg_q != nullptr;
-  const bool mine_ne = __syncthreads_or(a);
-  // an empty chunk reads nothing and publishes nothing; chunk 0 stays to write
-  // the output of a row that has no allowed slot at all
-  if (!mine_ne && !by_seg && c != 0) return;
-
-  // which chunks of this row hold an allowed slot (identical in every CTA)
-  if (!by_seg) {
-    for (int base = 0; base < p.nch; base += kThreads) {
-      const int cc = base + tid;
-      const int jb = cc * C;
-      bool ne = cc < p.nch && jb < min(p.Lk, kvl);
-      if (ne && p.bits) {
-        uint32_t any = 0u;
 #pragma unroll
-        for (int w = 0; w < C / 32; ++w) {
-          const int jw = jb + 32 * w;
-          const int lim = min(p.Lk, kvl) - jw;
-          if (lim > 0) {
-            const uint32_t valid = lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u);
-            any |= __ldg(p.bits + (int64_t)b * p.ms_b + (jw >> 5)) & valid;
+  for (int u = 0; u < QPT; ++u) {
+    const int i = tid + u * kThreads;
+    if (i < NREP * D) sm.q[i / D][i % D] = qv[u];
+  }
+  __syncthreads();
+  const int n_all = sm.n_all;
+
+  // 2-3. batches of dense rows
+  constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte lane load
+  constexpr int G = D / EPL;           // lanes per row
+  constexpr int SPW = 32 / G;          // rows per warp pass
+  constexpr int ROWS_W = CAP / (kThreads / 32);
+  static_assert(G <= 32 && ROWS_W % SPW == 0, "lane layout");
+  constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, dim pair) per thread
+  float o[ITEMS][2];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) o[u][0] = o[u][1] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;  // meaningful in warp r < NREP
+  const bool ok = true;
+  const int e = lane % G, sub = lane / G;
+  // tensor-core path: Q as the A fragment (heads gq < NREP; rows gq+8 are padding)
+  constexpr int RW = CAP / (kThreads / 32);  // dense rows per warp per batch
+  constexpr int NT8 = RW / 8;
+  const int gq = lane >> 2, tq = lane & 3;
+  uint32_t qa[use_mma<T>() ? D / 16 : 1][2];
+  float ow[use_mma<T>() ? D / 8 : 1][4];
+  float wm_run = -INFINITY, wl_run = 0.f;
+  if constexpr (use_mma<T>()) {
+    static_assert(RW % 16 == 0, "rows per warp");
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(0.f, 0.f), hi = lo;
+      if (gq < NREP) {
+        lo = __floats2bfloat162_rn(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
+        hi = __floats2bfloat162_rn(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
+      }
+      qa[kk][0] = *reinterpret_cast<uint32_t *>(&lo);
+      qa[kk][1] = *reinterpret_cast<uint32_t *>(&hi);
+    }
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) ow[dt][0] = ow[dt][1] = ow[dt][2] = ow[dt][3] = 0.f;
+  }
+  const T *kg = static_cast<const T *>(p.k) + (int64_t)b * p.ks_b + (int64_t)g * p.ks_h;
+  const T *vg = static_cast<const T *>(p.v) + (int64_t)b * p.vs_b + (int64_t)g * p.vs_h;
+  for (int bs = 0; bs < n_all; bs += CAP) {
+    const int nb = min(CAP, n_all - bs);
+    // gather the allowed rows: 16-byte pieces, consecutive threads on one row
+    constexpr int PPR = D * sizeof(T) / 16;  // pieces per row
+    for (int idx = tid; idx < nb * PPR; idx += kThreads) {
+      const int kk = idx / PPR, part = idx % PPR;
+      const int loc = sm.slot[bs + kk];
+      const int64_t j = (int64_t)(x + S * (loc / C)) * C + loc % C;
+      cp_async16(reinterpret_cast<char *>(&sm.k[kk][0]) + part * 16,
+                 reinterpret_cast<const char *>(kg + j * p.ks_l) + part * 16);
+      cp_async16(reinterpret_cast<char *>(&sm.v[kk][0]) + part * 16,
+                 reinterpret_cast<const char *>(vg + j * p.vs_l) + part * 16);
+    }
+    if constexpr (use_mma<T>()) {
+      // rows past nb in the last 16-row group feed the P.V MMA with P = 0:
+      // keep them finite
+      const int tail = min(CAP, (nb + 15) & ~15) - nb;
+      for (int idx = tid; idx < tail * (D / 8); idx += kThreads)
+        *reinterpret_cast<uint4 *>(&sm.v[nb + idx / (D / 8)][(idx % (D / 8)) * 8]) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    if constexpr (use_mma<T>()) {
+      // warp w owns dense rows [w*RW, w*RW + RW) of the batch and keeps its
+      // own running (m, l, O) for head gq; warps merge after the last batch
+      const int r0 = warp * RW;
+      if (r0 < nb) {
+        const int n8 = min(NT8, (nb - r0 + 7) / 8);    // row tiles holding a valid row
+        const int n16 = min(RW / 16, (nb - r0 + 15) / 16);
+        float c[NT8][4];
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+          c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+          if (nt >= n8) continue;  // warp-uniform
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const T *kr = &sm.k[r0 + nt * 8 + gq][kk * 16 + 2 * tq];
+            mma_bf16_16816(c[nt], qa[kk][0], 0u, qa[kk][1], 0u,
+                           *reinterpret_cast<const uint32_t *>(kr),
+                           *reinterpret_cast<const uint32_t *>(kr + 8));
           }
         }
-        ne = any != 0u;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = r0 + nt * 8 + 2 * tq + h;
+            c[nt][h] = row < nb ? c[nt][h] * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, c[nt][h]);
+          }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(wm_run, mx);
+        const float f = (wm_run == -INFINITY) ? 0.f : exp2f(wm_run - m_new);
+        float ps = 0.f;
+        uint32_t pa[NT8];
+#pragma unroll
+        for (int nt = 0; nt < NT8; ++nt) {
+          const float p0 = exp2f(c[nt][0] - m_new), p1 = exp2f(c[nt][1] - m_new);
+          ps += p0 + p1;
+          __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
+          pa[nt] = *reinterpret_cast<uint32_t *>(&hp);
+        }
+        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+        wl_run = wl_run * f + ps;
+        wm_run = m_new;
+#pragma unroll
+        for (int dt = 0; dt < D / 8; ++dt) {
+          ow[dt][0] *= f;
+          ow[dt][1] *= f;
+        }
+#pragma unroll
+        for (int ks = 0; ks < RW / 16; ++ks) {
+          if (ks >= n16) break;  // warp-uniform; rows up to the next 16 are zero-filled
+#pragma unroll
+          for (int dt = 0; dt < D / 8; ++dt) {
+            uint32_t b0, b1;
+            ldmatrix_x2_trans(b0, b1, &sm.v[r0 + ks * 16 + (lane & 15)][dt * 8]);
+            mma_bf16_16816(ow[dt], pa[2 * ks], 0u, pa[2 * ks + 1], 0u, b0, b1);
+          }
+        }
       }
-      const uint32_t bal = __ballot_sync(0xffffffffu, ne);
-      if (lane == 0 && base + warp * 32 < p.nch) sm.chunk_ne[cc >> 5] = bal;
-    }
-  }
-  __syncthreads();
-  if (!mine_ne && !by_seg) {  // chunk 0, empty
-    bool row_empty = true;
-    for (int w = 0; w < (p.nch + 31) / 32; ++w) row_empty = row_empty && sm.chunk_ne[w] == 0u;
-    if (row_empty) {
-      for (int idx = tid; idx < NREP * D; idx += kThreads) {
-        const int r = idx / D, d = idx % D;
-        T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
-        orow[d] = from_float<T>(0.f);
-        if (d == 0 && p.lse) p.lse[(int64_t)b * p.Hq + h0 + r] = -INFINITY;
-      }
-    }
-    return;
-  }
-  if (tid == 0) {
-    int n = 0;
-#pragma unroll
-    for (int w = 0; w < C / 32; ++w) n += __popc(sm.allowed[w]);
-    sm.n_allowed = n;
-    if (n > 0) mbar_arrive_expect_tx(&sm.bar, (uint32_t)(n * 2 * D * sizeof(T)));
-  }
-  __syncthreads();
-  const int n_allowed = sm.n_allowed;
-
-  if (n_allowed > 0) {
-    // 2. fetch exactly the allowed K/V rows
-    if (a) {
-      const T *kr = static_cast<const T *>(p.k) + (int64_t)b * p.ks_b + (int64_t)g * p.ks_h +
-                    (int64_t)j * p.ks_l;
-      const T *vr = static_cast<const T *>(p.v) + (int64_t)b * p.vs_b + (int64_t)g * p.vs_h +
-                    (int64_t)j * p.vs_l;
-      bulk_g2s(&sm.k[tid][0], kr, D * sizeof(T), &sm.bar);
-      bulk_g2s(&sm.v[tid][0], vr, D * sizeof(T), &sm.bar);
-    }
-    const T *qb = static_cast<const T *>(p.q) + (int64_t)b * p.qs_b;
-    for (int i = tid; i < NREP * D; i += kThreads) {
-      const int r = i / D, d = i % D;
-      sm.q[r][d] = to_float(qb[(int64_t)(h0 + r) * p.qs_h + d]);
-    }
-    __syncthreads();
-    const bool ok = mbar_wait(&sm.bar, 0, p.err);
-
-    // 3. scores (log2 units)
-    constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte lane load
-    constexpr int G = D / EPL;           // lanes per slot
-    constexpr int SPW = 32 / G;          // slots per warp pass
-    constexpr int SLOTS_W = C / (kThreads / 32);
-    static_assert(G <= 32 && SLOTS_W % SPW == 0, "lane layout");
-    const int e = lane % G, sub = lane / G;
-    float qr[NREP][EPL];
-#pragma unroll
-    for (int r = 0; r < NREP; ++r)
-#pragma unroll
-      for (int i = 0; i < EPL; ++i) qr[r][i] = sm.q[r][e * EPL + i];
-#pragma unroll 2
-    for (int it = 0; it < SLOTS_W / SPW; ++it) {
-      const int sl = warp * SLOTS_W + it * SPW + sub;
-      const bool al = ok && ((sm.allowed[sl >> 5] >> (sl & 31)) & 1u);
-      float acc[NREP];
-#pragma unroll
-      for (int r = 0; r < NREP; ++r) acc[r] = 0.f;
-      if (al) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(&sm.k[sl][e * EPL]);
-        float kf[EPL];
-        unpack16(u, kf);
-#pragma unroll
+    } else {
+    // scores (log2 units)
+      {
+        float qr[NREP][EPL];
+  #pragma unroll
         for (int r = 0; r < NREP; ++r)
-#pragma unroll
-          for (int i = 0; i < EPL; ++i) acc[r] = fmaf(qr[r][i], kf[i], acc[r]);
-      }
-#pragma unroll
-      for (int off = G / 2; off > 0; off >>= 1)
-#pragma unroll
-        for (int r = 0; r < NREP; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
-      if (e == 0) {
-#pragma unroll
-        for (int r = 0; r < NREP; ++r) sm.s[r][sl] = al ? acc[r] * p.scale_log2 : -INFINITY;
-      }
-    }
-    __syncthreads();
-
-    // 4. per-head chunk max and sum
-    for (int r = warp; r < NREP; r += kThreads / 32) {
-      float m = -INFINITY;
-#pragma unroll
-      for (int i = lane; i < C; i += 32) m = fmaxf(m, sm.s[r][i]);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      float l = 0.f;
-#pragma unroll
-      for (int i = lane; i < C; i += 32) {
-        const float x = sm.s[r][i];
-        const float pr = (x == -INFINITY) ? 0.f : exp2f(x - m);
-        sm.s[r][i] = pr;
-        l += pr;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (lane == 0) sm.ml[r] = make_float2(m, l);
-    }
-    __syncthreads();
-
-    // 5. P.V over the allowed slots, ascending
-    for (int idx = tid; idx < NREP * D / 2; idx += kThreads) {
-      const int r = idx / (D / 2), dp = idx % (D / 2);
-      float o0 = 0.f, o1 = 0.f;
-      for (int w = 0; w < C / 32; ++w) {
-        uint32_t bitsw = ok ? sm.allowed[w] : 0u;
-        while (bitsw) {
-          const int sl = w * 32 + __ffs(bitsw) - 1;
-          bitsw &= bitsw - 1;
-          const float pr = sm.s[r][sl];
-          float v0, v1;
-          if constexpr (sizeof(T) == 2) {
-            const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162 *>(&sm.v[sl][2 * dp]);
-            v0 = __low2float(vv);
-            v1 = __high2float(vv);
-          } else {
-            const float2 vv = *reinterpret_cast<const float2 *>(&sm.v[sl][2 * dp]);
-            v0 = vv.x;
-            v1 = vv.y;
+  #pragma unroll
+          for (int i = 0; i < EPL; ++i) qr[r][i] = sm.q[r][e * EPL + i];
+        for (int it = 0; it < ROWS_W / SPW; ++it) {
+          const int row_first = warp * ROWS_W + it * SPW;
+          if (row_first >= nb) break;  // warp-uniform
+          const int row = row_first + sub;
+          const bool valid = row < nb;
+          float acc[NREP];
+  #pragma unroll
+          for (int r = 0; r < NREP; ++r) acc[r] = 0.f;
+          if (valid) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(&sm.k[row][e * EPL]);
+            float kf[EPL];
+            unpack16(u, kf);
+  #pragma unroll
+            for (int r = 0; r < NREP; ++r)
+  #pragma unroll
+              for (int i = 0; i < EPL; ++i) acc[r] = fmaf(qr[r][i], kf[i], acc[r]);
           }
-          o0 = fmaf(pr, v0, o0);
-          o1 = fmaf(pr, v1, o1);
+  #pragma unroll
+          for (int off = G / 2; off > 0; off >>= 1)
+  #pragma unroll
+            for (int r = 0; r < NREP; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+          if (e == 0 && valid) {
+  #pragma unroll
+            for (int r = 0; r < NREP; ++r) sm.s[r][row] = acc[r] * p.scale_log2;
+          }
         }
       }
-      reinterpret_cast<float2 *>(p.ws_o + (row0 + (int64_t)r * p.nch) * D)[dp] =
-          make_float2(o0, o1);
+      __syncthreads();
+      // per-head batch softmax, folded into the running (m, l)
+      if (warp < NREP) {
+        const int r = warp;
+        float mb = -INFINITY;
+        for (int i = lane; i < nb; i += 32) mb = fmaxf(mb, sm.s[r][i]);
+  #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+        float lb = 0.f;
+        for (int i = lane; i < nb; i += 32) {
+          const float pr = exp2f(sm.s[r][i] - mb);
+          sm.s[r][i] = pr;
+          lb += pr;
+        }
+  #pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, off);
+        const float m_new = fmaxf(m_run, mb);
+        const float f_old = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+        const float f_b = exp2f(mb - m_new);
+        l_run = l_run * f_old + lb * f_b;
+        m_run = m_new;
+        if (lane == 0) {
+          sm.fo[r] = f_old;
+          sm.fb[r] = f_b;
+        }
+      }
+      __syncthreads();
+      // P.V over the dense rows, ascending
+  #pragma unroll
+      for (int u = 0; u < ITEMS; ++u) {
+        const int idx = tid + u * kThreads;
+        if (idx < NREP * D / 2) {
+          const int r = idx / (D / 2), dp = idx % (D / 2);
+          float a0 = 0.f, a1 = 0.f;
+  #pragma unroll 4
+          for (int kk = 0; kk < nb; ++kk) {
+            const float pr = sm.s[r][kk];
+            float v0, v1;
+            if constexpr (sizeof(T) == 2) {
+              const __nv_bfloat162 vv = *reinterpret_cast<const __nv_bfloat162 *>(&sm.v[kk][2 * dp]);
+              v0 = __low2float(vv);
+              v1 = __high2float(vv);
+            } else {
+              const float2 vv = *reinterpret_cast<const float2 *>(&sm.v[kk][2 * dp]);
+              v0 = vv.x;
+              v1 = vv.y;
+            }
+            a0 = fmaf(pr, v0, a0);
+            a1 = fmaf(pr, v1, a1);
+          }
+          o[u][0] = o[u][0] * sm.fo[r] + a0 * sm.fb[r];
+          o[u][1] = o[u][1] * sm.fo[r] + a1 * sm.fb[r];
+        }
+      }
     }
-    if (tid < NREP) p.ws_ml[row0 + (int64_t)tid * p.nch] = ok ? sm.ml[tid] : make_float2(-INFINITY, 0.f);
-  } else {
-    if (tid < NREP) p.ws_ml[row0 + (int64_t)tid * p.nch] = make_float2(-INFINITY, 0.f);
+    __syncthreads();  // the next batch overwrites k, v and s
   }
 
-  // 6. ticket; the last non-empty CTA of (b, hg) merges the non-empty chunks
-  __syncthreads();
-  unsigned *tick = p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg;
-  if (tid == 0) {
-    int n_ne = p.nch;
-    if (!by_seg) {
-      n_ne = 0;
-      for (int w = 0; w < (p.nch + 31) / 32; ++w) n_ne += __popc(sm.chunk_ne[w]);
+  if constexpr (use_mma<T>()) {
+    // in-CTA merge of the warps' (m, l, O), ascending warp order
+    if (gq < NREP) {
+      if (tq == 0) {
+        sm.wm[warp][gq] = wm_run;
+        sm.wl[warp][gq] = wl_run;
+      }
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) {
+        sm.wo[warp][gq][dt * 8 + 2 * tq] = ow[dt][0];
+        sm.wo[warp][gq][dt * 8 + 2 * tq + 1] = ow[dt][1];
+      }
     }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < ITEMS; ++u) {
+      const int idx = tid + u * kThreads;
+      if (idx < NREP * D / 2) {
+        const int r = idx / (D / 2), dp = idx % (D / 2);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, sm.wm[w][r]);
+        float a0 = 0.f, a1 = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int w = 0; w < kThreads / 32; ++w) {
+            if (sm.wm[w][r] == -INFINITY) continue;
+            const float wt = exp2f(sm.wm[w][r] - M);
+            a0 = fmaf(sm.wo[w][r][2 * dp], wt, a0);
+            a1 = fmaf(sm.wo[w][r][2 * dp + 1], wt, a1);
+          }
+        }
+        o[u][0] = a0;
+        o[u][1] = a1;
+      }
+    }
+    if (warp < NREP) {
+      const int r = warp;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) M = fmaxf(M, sm.wm[w][r]);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w)
+          if (sm.wm[w][r] != -INFINITY) L = fmaf(sm.wl[w][r], exp2f(sm.wm[w][r] - M), L);
+      }
+      m_run = M;
+      l_run = L;
+    }
+  }
+
+  // 4. partial of this CTA; the last of the S CTAs merges all of them
+  const int64_t hrow0 = ((int64_t)b * p.Hq + h0) * S;  // ws row of (head h0, split 0)
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int idx = tid + u * kThreads;
+    if (idx < NREP * D / 2) {
+      const int r = idx / (D / 2), dp = idx % (D / 2);
+      reinterpret_cast<float2 *>(p.ws_o + (hrow0 + (int64_t)r * S + x) * D)[dp] =
+          make_float2(o[u][0], o[u][1]);
+    }
+  }
+  if (warp < NREP && lane == 0)
+    p.ws_ml[hrow0 + (int64_t)warp * S + x] =
+        (ok && m_run != -INFINITY) ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+  __syncthreads();
+  unsigned *tick = p.ws_tick + (int64_t)b * p.Hq + h0;
+  if (tid == 0) {
     unsigned t;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(tick) : "memory");
-    sm.is_last = (t == (unsigned)(n_ne - 1));
+    sm.is_last = (t == (unsigned)(S - 1));
   }
   __syncthreads();
   if (!sm.is_last) return;
 
-  // non-empty chunk list, ascending
-  if (warp == 0) {
-    int count = 0;
-    for (int base = 0; base < p.nch; base += 32) {
-      const int cc = base + lane;
-      bool ne = false;
-      if (cc < p.nch) {
-        if (by_seg) ne = __ldcg(&p.ws_ml[((int64_t)b * p.Hq + h0) * p.nch + cc]).x != -INFINITY;
-        else ne = (sm.chunk_ne[cc >> 5] >> (cc & 31)) & 1u;
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int idx = tid + u * kThreads;
+    if (idx < NREP * D / 2) {
+      const int r = idx / (D / 2), dp = idx % (D / 2);
+      const int64_t hr = hrow0 + (int64_t)r * S;
+      // every split wrote its partial this call (empty ones: m = -inf, zeros),
+      // so all loads go out in one round
+      float2 ml[S], ov[S];
+#pragma unroll
+      for (int xx = 0; xx < S; ++xx) {
+        ml[xx] = __ldcg(&p.ws_ml[hr + xx]);
+        ov[xx] = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hr + xx) * D) + dp);
       }
-      const uint32_t bal = __ballot_sync(0xffffffffu, ne);
-      if (ne) sm.nz[count + __popc(bal & ((1u << lane) - 1u))] = cc;
-      count += __popc(bal);
-    }
-    if (lane == 0) sm.n_ne = count;
-  }
-  __syncthreads();
-  const int nnz = sm.n_ne;
-  for (int idx = tid; idx < NREP * nnz; idx += kThreads) {
-    const int r = idx / nnz, k = idx % nnz;
-    const float2 ml = __ldcg(&p.ws_ml[((int64_t)b * p.Hq + h0 + r) * p.nch + sm.nz[k]]);
-    sm.w[r][k] = ml.x;
-    sm.lval[r][k] = ml.y;
-  }
-  __syncthreads();
-  for (int r = warp; r < NREP; r += kThreads / 32) {
-    float M = -INFINITY;
-    for (int k = lane; k < nnz; k += 32) M = fmaxf(M, sm.w[r][k]);
+      float M = -INFINITY;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float L = 0.f;
-    for (int k = lane; k < nnz; k += 32) {
-      const float m = sm.w[r][k];
-      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
-      L = fmaf(sm.lval[r][k], wgt, L);
-      sm.w[r][k] = wgt;
-    }
+      for (int xx = 0; xx < S; ++xx) M = fmaxf(M, ml[xx].x);
+      float L = 0.f, o0 = 0.f, o1 = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) {
-      sm.inv_l[r] = (L > 0.f) ? 1.f / L : 0.f;
-      sm.ml[r] = make_float2(M, L);
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < NREP * D / 2; idx += kThreads) {
-    const int r = idx / (D / 2), dp = idx % (D / 2);
-    const int64_t hrow = ((int64_t)b * p.Hq + h0 + r) * p.nch;
-    float o0 = 0.f, o1 = 0.f;
-    int k = 0;
-    for (; k + 4 <= nnz; k += 4) {
-      float2 o[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        o[u] = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hrow + sm.nz[k + u]) * D) + dp);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        o0 = fmaf(o[u].x, sm.w[r][k + u], o0);
-        o1 = fmaf(o[u].y, sm.w[r][k + u], o1);
+        for (int xx = 0; xx < S; ++xx) {
+          if (ml[xx].x == -INFINITY) continue;
+          const float w = exp2f(ml[xx].x - M);
+          L = fmaf(ml[xx].y, w, L);
+          o0 = fmaf(ov[xx].x, w, o0);
+          o1 = fmaf(ov[xx].y, w, o1);
+        }
       }
-    }
-    for (; k < nnz; ++k) {
-      const float2 o = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hrow + sm.nz[k]) * D) + dp);
-      o0 = fmaf(o.x, sm.w[r][k], o0);
-      o1 = fmaf(o.y, sm.w[r][k], o1);
-    }
-    const float inv = sm.inv_l[r];
-    T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
-    orow[2 * dp] = from_float<T>(o0 * inv);
-    orow[2 * dp + 1] = from_float<T>(o1 * inv);
-    if (dp == 0 && p.lse) {
-      const float2 ML = sm.ml[r];
-      p.lse[(int64_t)b * p.Hq + h0 + r] = (ML.y > 0.f) ? (ML.x + log2f(ML.y)) * kLn2 : -INFINITY;
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
+      orow[2 * dp] = from_float<T>(o0 * inv);
+      orow[2 * dp + 1] = from_float<T>(o1 * inv);
+      if (dp == 0 && p.lse)
+        p.lse[(int64_t)b * p.Hq + h0 + r] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
     }
   }
   if (tid == 0) *tick = 0u;
@@ -369,9 +491,8 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 
 template <typename T, int D, int NREP>
 mgqa_status launch_t(const DecodeParams &p, cudaStream_t s) {
-  constexpr int C = kDecodeChunk;
-  auto kern = decode_kernel<T, D, NREP, C>;
-  const size_t smem = sizeof(DecodeSmem<T, D, NREP, C>);
+  auto kern = decode_kernel<T, D, NREP>;
+  const size_t smem = sizeof(DecodeSmem<T, D, NREP>);
   static bool attr_set = false;  // per process; the attribute is per function
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -379,7 +500,7 @@ mgqa_status launch_t(const DecodeParams &p, cudaStream_t s) {
       return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the decode kernel");
     attr_set = true;
   }
-  dim3 grid(p.nch, p.Hq / NREP, p.B);
+  dim3 grid(S, p.Hq / NREP, p.B);
   kern<<<grid, kThreads, smem, s>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
@@ -402,8 +523,7 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(const mgqa_args &a) {
-  const int nch = (a.Lk + kDecodeChunk - 1) / kDecodeChunk;
-  const size_t rows = (size_t)a.B * a.Hq * nch;
+  const size_t rows = (size_t)a.B * a.Hq * S;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   WsLayout w;
   w.ml = 0;

@@ -11,8 +11,10 @@ namespace mgqa {
 // Sets the thread-local detail string returned by mgqa_last_error_detail().
 mgqa_status fail(mgqa_status code, const char *fmt, ...);
 
-// Decode: fixed chunks of kDecodeChunk absolute cache slots per CTA.
+// Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
+// kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.
 constexpr int kDecodeChunk = 128;
+constexpr int kDecodeSplits = 16;
 // Longest static cache the decode kernel accepts (bounds its merge tables).
 constexpr int kDecodeMaxLk = 32768;
 // Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).

@@ -17,6 +17,10 @@
 //   warp 0      : TMA producer (Q once, then K and V per key tile, STAGES-deep)
 //   warp 1      : allocates tensor memory; lane 0 issues every MMA
 //   warps 4..   : one softmax warpgroup per query head (thread = query row)
+// With two heads (384 threads, 168 registers each at launch) the first
+// warpgroup gives registers away (88) and the softmax warpgroups take them
+// (208; 88 + 2 x 208 = 3 x 168 per scheduler), enough to hold a whole
+// 128-column score row per thread.
 // Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
 // P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
 // the P.V MMA straight from tensor memory.
@@ -136,52 +140,60 @@ MGQA_DEV void tile_mask_words(const TcParams &p, int b, int i, bool row_ok, int 
   }
 }
 
-// 2^x for x <= 8 on the FMA pipe: x = n + f with n = round(x) (magic-number
-// rounding, 1.5 * 2^23), f in [-1/2, 1/2]; 2^f from a degree-3 polynomial
-// fitted by Remez exchange for minimax relative error on that interval
-// (max relative error 7.5e-5, far below bf16's 2^-9); n is added into the
-// exponent field. Inputs below -126 are clamped (result ~1e-38).
-MGQA_DEV float exp2_poly(float x) {
-  x = fmaxf(x, -126.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  float q = fmaf(f, 0.0551716685f, 0.2426111251f);
-  q = fmaf(q, f, 0.6932609677f);
-  q = fmaf(q, f, 0.9999280572f);
-  return __int_as_float(__float_as_int(q) + (__float_as_int(t) << 23));
+// 2^x for a pair of x <= 8 on the FMA pipe, packed f32x2 arithmetic:
+// x = n + f with n = round(x) (magic-number rounding, 1.5 * 2^23),
+// f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted by Remez exchange
+// for minimax relative error on that interval (max relative error 7.5e-5, far
+// below bf16's 2^-9); n is added into the exponent field. Inputs below -126
+// are clamped (result ~1e-38 instead of 0).
+MGQA_DEV void exp2_poly2(uint64_t y, float &p0, float &p1) {
+  float y0, y1;
+  tc::upk2(y, y0, y1);
+  const uint64_t yc = tc::pk2(fmaxf(y0, -126.f), fmaxf(y1, -126.f));
+  const uint64_t magic = tc::pk2(12582912.f, 12582912.f);
+  const uint64_t t = tc::add2(yc, magic);
+  const uint64_t nn = tc::add2(t, tc::pk2(-12582912.f, -12582912.f));
+  const uint64_t f = tc::fma2(nn, tc::pk2(-1.f, -1.f), yc);
+  uint64_t q = tc::fma2(f, tc::pk2(0.0551716685f, 0.0551716685f),
+                        tc::pk2(0.2426111251f, 0.2426111251f));
+  q = tc::fma2(q, f, tc::pk2(0.6932609677f, 0.6932609677f));
+  q = tc::fma2(q, f, tc::pk2(0.9999280572f, 0.9999280572f));
+  float q0, q1, t0, t1;
+  tc::upk2(q, q0, q1);
+  tc::upk2(t, t0, t1);
+  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
+  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
 }
 
-// Every kPolyEvery-th exponential pair of a row goes to exp2_poly, the rest to
-// the MUFU ex2 unit, so both pipes share the softmax's exponentials.
+// Every kPolyEvery-th exponential pair of a row goes to exp2_poly2 (FMA
+// pipe), the rest to the MUFU ex2 unit, so both pipes share the work.
 constexpr int kPolyEvery = 4;
 
-// One 128-key tile of one softmax row (thread = row): running max with lazy
-// rescale, P = exp2(s*scale*log2e - m) as bf16 pairs over the S columns, and
-// the row sum. NEG: the scale is negative (the max of scaled scores is the
-// min of raw ones). PARTIAL: mw holds the row's allowed-key bits.
-template <int D, bool NEG, bool PARTIAL>
+// One 128-key tile of one softmax row (thread = row): the whole score row is
+// read from tensor memory once (four 32-column loads, one wait); its extreme
+// (8 independent accumulators) updates the running max with lazy rescale of O
+// (only when it grows by more than 2^8); P = exp2(s*scale*log2e - m) goes
+// back as bf16 pairs over the first 64 S columns; the row sum is added to l.
+// NEG: negative scale (the max of scaled scores is the min of raw ones).
+// PARTIAL: mw holds the row's allowed-key bits. The optional hand-over wait
+// (two heads) sits between the load and the exponentials.
+template <int D, bool NEG, bool PARTIAL, typename Turn>
 MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
-                           float &m_used, float &l) {
+                           float &m_used, float &l, Turn &&take_turn) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
-  // pass 1: row extreme of the raw scores; 8 independent accumulators
+  uint32_t sr[BN];
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c)
+    tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+  tc::tmem_wait_ld();
   float mx[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) mx[k] = MV;
 #pragma unroll
-  for (int c = 0; c < BN / 32; c += 2) {
-    uint32_t r0[32], r1[32];
-    tc::tmem_ld32(t_s + c * 32, r0);
-    tc::tmem_ld32(t_s + (c + 1) * 32, r1);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float a0 = __uint_as_float(r0[j]), a1 = __uint_as_float(r1[j]);
-      if (PARTIAL) {
-        if (!((mw[c] >> j) & 1u)) a0 = MV;
-        if (!((mw[c + 1] >> j) & 1u)) a1 = MV;
-      }
-      mx[j & 7] = NEG ? fminf(mx[j & 7], fminf(a0, a1)) : fmaxf(mx[j & 7], fmaxf(a0, a1));
-    }
+  for (int j = 0; j < BN; ++j) {
+    float a = __uint_as_float(sr[j]);
+    if (PARTIAL && !((mw[j >> 5] >> (j & 31)) & 1u)) a = MV;
+    mx[j & 7] = NEG ? fminf(mx[j & 7], a) : fmaxf(mx[j & 7], a);
   }
 #pragma unroll
   for (int k = 4; k > 0; k >>= 1)
@@ -215,49 +227,52 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
     tc::tmem_wait_st();
   }
   const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-  // pass 2: 16-column chunk c+1 loads while chunk c is exponentiated/packed
-  float acc[8];
+  take_turn();
+  const uint64_t sl2x2 = tc::pk2(sl2, sl2), nmb2 = tc::pk2(-mb, -mb);
+  uint64_t acc[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-  uint32_t rb[2][16];
-  tc::tmem_ld16(t_s, rb[0]);
-  tc::tmem_wait_ld();
+  for (int k = 0; k < 4; ++k) acc[k] = tc::pk2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < BN / 16; ++c) {
-    if (c + 1 < BN / 16) tc::tmem_ld16(t_s + (c + 1) * 16, rb[(c + 1) & 1]);
-    const uint32_t(&raw)[16] = rb[c & 1];
-    const uint32_t bits = PARTIAL ? (mw[c >> 1] >> ((c & 1) * 16)) : 0u;
-    uint32_t pk[8];
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t pk[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float y0 = fmaf(__uint_as_float(raw[2 * j]), sl2, -mb);
-      const float y1 = fmaf(__uint_as_float(raw[2 * j + 1]), sl2, -mb);
-      const bool poly = kPolyEvery > 0 && ((c * 8 + j) % kPolyEvery) == kPolyEvery - 1;
-      float p0 = poly ? exp2_poly(y0) : tc::ex2(y0);
-      float p1 = poly ? exp2_poly(y1) : tc::ex2(y1);
-      if (PARTIAL) {
-        if (!((bits >> (2 * j)) & 1u)) p0 = 0.f;
-        if (!((bits >> (2 * j + 1)) & 1u)) p1 = 0.f;
+    for (int j = 0; j < 16; ++j) {
+      const int col = c * 32 + 2 * j;
+      const uint64_t y =
+          tc::fma2(tc::pk2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sl2x2, nmb2);
+      float p0, p1;
+      if (kPolyEvery > 0 && ((c * 16 + j) % kPolyEvery) == kPolyEvery - 1) {
+        exp2_poly2(y, p0, p1);
+      } else {
+        float y0, y1;
+        tc::upk2(y, y0, y1);
+        p0 = tc::ex2(y0);
+        p1 = tc::ex2(y1);
       }
-      acc[j] += p0 + p1;
+      if (PARTIAL) {
+        if (!((mw[c] >> (2 * j)) & 1u)) p0 = 0.f;
+        if (!((mw[c] >> (2 * j + 1)) & 1u)) p1 = 0.f;
+      }
+      acc[j & 3] = tc::add2(acc[j & 3], tc::pk2(p0, p1));
       __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
       pk[j] = *reinterpret_cast<uint32_t *>(&h);
     }
-    tc::tmem_st8(t_s + c * 8, pk);
-    tc::tmem_wait_ld();
+    tc::tmem_st16(t_s + c * 16, pk);
   }
-#pragma unroll
-  for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-    for (int u = 0; u < k; ++u) acc[u] += acc[u + k];
-  l += acc[0];
+  acc[0] = tc::add2(acc[0], acc[1]);
+  acc[2] = tc::add2(acc[2], acc[3]);
+  acc[0] = tc::add2(acc[0], acc[2]);
+  float s0, s1;
+  tc::upk2(acc[0], s0, s1);
+  l += s0 + s1;
   tc::tmem_wait_st();
 }
 
 template <int D, int NT, int STAGES>
 __global__ void __launch_bounds__(128 * (1 + NT), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ TcParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const __grid_constant__ TcParams p) {
   using Lay = Layout<D, NT, STAGES>;
   constexpr int KB = Lay::KB;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -359,12 +374,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int lim = p.Lk - 32 * w;
       const uint32_t valid = w >= W ? 0u : (lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u));
       uint32_t o = 0u, a = 0xffffffffu;
-#pragma unroll 4
-      for (int r = warp; r < rows; r += nwarps) {
+      // at most 16 rows per warp (128 rows, >= 8 warps): every load in flight
+      uint32_t wv[BM / 8];
+#pragma unroll
+      for (int k = 0; k < BM / 8; ++k) {
+        const int r = warp + k * nwarps;
         const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
-        const uint32_t word = (w < W) ? (__ldg(mrow + w) & valid) : 0u;
-        o |= word;
-        a &= (word == valid && valid == 0xffffffffu) ? 0xffffffffu : 0u;
+        wv[k] = (r < rows && w < W) ? (__ldg(mrow + w) & valid) : valid;
+      }
+#pragma unroll
+      for (int k = 0; k < BM / 8; ++k) {
+        o |= (warp + k * nwarps < rows) ? wv[k] : 0u;
+        a &= (wv[k] == valid && valid == 0xffffffffu) ? 0xffffffffu : 0u;
       }
       // a word slot past Lk (or a ragged last word) can never make a tile full
       if (w >= W || valid != 0xffffffffu) a = 0u;
@@ -443,7 +464,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t sm_base = smem_u32(smem);
   bool ok = true;
 
+  // Each role ends in role_end(): all threads meet on named barrier 1 (the
+  // register split keeps the roles' code paths apart), then warp 1 frees the
+  // tensor memory.
+  auto role_end = [&]() {
+    tc::fence_before_sync();
+    named_sync(1, Lay::threads);
+  };
   if (warp == 0) {
+    if constexpr (NT == 2) tc::regs_dec<88>();
     // ---------------- TMA producer ----------------
     if (lane == 0 && nk == 0) ok = mbar_wait(bar_q, 0, p.err);  // Q landed before exit
     if (lane == 0 && nk > 0) {
@@ -474,7 +503,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                           bar_vfull + st);
       }
     }
+    __syncwarp();
+    role_end();
   } else if (warp == 1) {
+    if constexpr (NT == 2) tc::regs_dec<88>();
     // ---------------- MMA issuer ----------------
     // Issue order: S_t(0) for every head, then per key tile n and head t:
     // O_t += P_t(n) V(n) followed at once by S_t(n+1) = Q_t K(n+1)^T. The
@@ -529,7 +561,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
              mbar_wait(bar_vempty + s, last_use & 1, p.err);
       }
     }
-  } else if (warp >= 4) {
+    __syncwarp();
+    role_end();
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, Lay::tmem_cols);
+  } else if (warp < 4) {
+    if constexpr (NT == 2) tc::regs_dec<88>();
+    role_end();
+  } else {
+    if constexpr (NT == 2) tc::regs_inc<208>();
     // ---------------- softmax warpgroup t ----------------
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -550,72 +590,75 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool partial = (ent & 0x8000) != 0;
       uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
       if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
-      // two heads: their softmax passes alternate (head 1 waits for head 0's
-      // pass n, head 0 for head 1's pass n-1), so each one runs while the
-      // tensor core works on the other head
-      if (NT == 2 && ok) {
-        if (t == 1) ok = mbar_wait(bar_tok, n & 1, p.err);
-        else if (n > 0) ok = mbar_wait(bar_tok + 1, (n - 1) & 1, p.err);
-      }
       if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
+      // two heads: their exponential passes alternate (head 1 waits for head
+      // 0's pass n, head 0 for head 1's pass n-1), so each one runs while the
+      // tensor core works on the other head
+      auto take_turn = [&]() {
+        if (NT == 2 && ok) {
+          if (t == 1) ok = mbar_wait(bar_tok, n & 1, p.err);
+          else if (n > 0) ok = mbar_wait(bar_tok + 1, (n - 1) & 1, p.err);
+        }
+      };
       if (neg) {
-        if (partial) softmax_tile<D, true, true>(t_s, t_o, mw, sl2, m_used, l);
-        else softmax_tile<D, true, false>(t_s, t_o, mw, sl2, m_used, l);
+        if (partial) softmax_tile<D, true, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        else softmax_tile<D, true, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
       } else {
-        if (partial) softmax_tile<D, false, true>(t_s, t_o, mw, sl2, m_used, l);
-        else softmax_tile<D, false, false>(t_s, t_o, mw, sl2, m_used, l);
+        if (partial) softmax_tile<D, false, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        else softmax_tile<D, false, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
       }
       tc::fence_before_sync();
       mbar_arrive(bar_pfull + t);
       if (NT == 2) mbar_arrive(bar_tok + t);
     }
-    // epilogue
+    // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
+    // last S MMA completed) in the 128-byte-swizzled box layout, then written
+    // by TMA tensor stores (rows past Lq are clipped by the store)
     float o_scale = 0.f;
     if (nk > 0) {
       if (ok) ok = mbar_wait(bar_odone + t, (nk - 1) & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;
+    } else if (ok) {
+      ok = mbar_wait(bar_q, 0, p.err);  // the Q load must land before the buffer is reused
     }
-    __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + (int64_t)b * p.os[0] +
-                          (int64_t)(h0 + t) * p.os[1] + (int64_t)ic * p.os[2];
-#pragma unroll 1
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      if (nk > 0) {
-        tc::tmem_ld32(t_o + c * 32, o);
-        tc::tmem_wait_ld();
-      } else {
+    uint32_t orow[D];
+    if (nk > 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = 0u;
-      }
-      uint32_t pk[16];
+      for (int c = 0; c < D / 32; ++c)
+        tc::tmem_ld32(t_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&orow[c * 32]));
+      tc::tmem_wait_ld();
+    } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[2 * j]) * o_scale,
-                                                 __uint_as_float(o[2 * j + 1]) * o_scale);
-        pk[j] = *reinterpret_cast<uint32_t *>(&h);
-      }
-      if (row_ok) {
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+      for (int j = 0; j < D; ++j) orow[j] = 0u;
+    }
+    unsigned char *ob = smem + Lay::q_off + t * KB * BOX;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    for (int cc = 0; cc < D / 8; ++cc) {  // 16-byte chunks of the row
+      uint32_t w4[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(orow[cc * 8 + 2 * h]) * o_scale,
+                                                  __uint_as_float(orow[cc * 8 + 2 * h + 1]) * o_scale);
+        w4[h] = *reinterpret_cast<uint32_t *>(&hv);
       }
+      const int box = cc >> 3, ch = cc & 7;
+      *reinterpret_cast<uint4 *>(ob + box * BOX + r * 128 + ((ch ^ (r & 7)) << 4)) =
+          make_uint4(w4[0], w4[1], w4[2], w4[3]);
+    }
+    fence_proxy_async_smem();
+    named_sync(2 + t, 128);
+    if (warp == 4 + 4 * t && lane == 0) {
+      for (int c = 0; c < KB; ++c) tc::tma_store_4d(&tm_o, ob + c * BOX, c * 64, row0, h0 + t, b);
+      tc::tma_store_commit_and_wait_read();
     }
     if (row_ok && p.lse)
       p.lse[((int64_t)b * p.Hq + h0 + t) * p.Lq + i] =
           (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
-  }
-
-  // ---- teardown -------------------------------------------------------------
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, Lay::tmem_cols);
+    role_end();
   }
 }
 
@@ -654,7 +697,7 @@ bool make_map(CUtensorMap *m, const void *base, int B, int H, int L, int D, cons
 
 template <int D, int NT, int STAGES>
 mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                     const TcParams &p, cudaStream_t s) {
+                     const CUtensorMap &mo, const TcParams &p, cudaStream_t s) {
   using Lay = Layout<D, NT, STAGES>;
   auto kern = prefill_tc_kernel<D, NT, STAGES>;
   static bool attr_set = false;
@@ -665,7 +708,7 @@ mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
     attr_set = true;
   }
   dim3 grid((p.Lq + BM - 1) / BM, p.Hq / NT, p.B);
-  kern<<<grid, Lay::threads, Lay::smem_bytes, s>>>(mq, mk, mv, p);
+  kern<<<grid, Lay::threads, Lay::smem_bytes, s>>>(mq, mk, mv, mo, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
@@ -677,10 +720,11 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
   if (a.dtype != MGQA_BF16) return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill is bf16 only");
   const int nkt = (a.Lk + BN - 1) / BN;
   if (nkt > MAXKT) return fail(MGQA_ERR_UNSUPPORTED, "Lk > %d", MAXKT * BN);
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   if (!make_map(&mq, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride) ||
       !make_map(&mk, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride) ||
-      !make_map(&mv, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride))
+      !make_map(&mv, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride) ||
+      !make_map(&mo, a.out, a.B, a.Hq, a.Lq, a.D, a.o_stride))
     return fail(MGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   TcParams p{};
   p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k};
@@ -691,8 +735,8 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
   p.os[0] = a.o_stride[0]; p.os[1] = a.o_stride[1]; p.os[2] = a.o_stride[2];
   p.lse = a.lse; p.err = a.dev_error;
   const bool pair = (p.n_rep % 2) == 0;
-  if (a.D == 128) return pair ? launch_t<128, 2, 2>(mq, mk, mv, p, s) : launch_t<128, 1, 2>(mq, mk, mv, p, s);
-  if (a.D == 64) return pair ? launch_t<64, 2, 3>(mq, mk, mv, p, s) : launch_t<64, 1, 3>(mq, mk, mv, p, s);
+  if (a.D == 128) return pair ? launch_t<128, 2, 2>(mq, mk, mv, mo, p, s) : launch_t<128, 1, 2>(mq, mk, mv, mo, p, s);
+  if (a.D == 64) return pair ? launch_t<64, 2, 3>(mq, mk, mv, mo, p, s) : launch_t<64, 1, 3>(mq, mk, mv, mo, p, s);
   return fail(MGQA_ERR_UNSUPPORTED, "head dim %d", a.D);
 }
 

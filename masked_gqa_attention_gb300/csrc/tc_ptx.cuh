@@ -24,6 +24,21 @@ MGQA_DEV void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z
       : "memory");
 }
 
+// 4-D tiled tensor store from this CTA's shared memory (bulk-group tracked);
+// coordinates are non-negative, x a multiple of 16 bytes of elements.
+MGQA_DEV void tma_store_4d(const CUtensorMap *map, const void *src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(src))
+      : "memory");
+}
+// Commit this thread's bulk stores and wait until their shared-memory reads
+// are done (the buffer may then be reused or the CTA may exit).
+MGQA_DEV void tma_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // L2 prefetch of the same 4-D tile (no shared-memory destination).
 MGQA_DEV void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w) {
   asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
@@ -180,6 +195,26 @@ template <uint32_t N> MGQA_DEV void regs_dec() {
 }
 template <uint32_t N> MGQA_DEV void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packed pairs of fp32 (one 64-bit register, .f32x2 arithmetic).
+MGQA_DEV uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+MGQA_DEV void upk2(uint64_t r, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+MGQA_DEV uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+MGQA_DEV uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 MGQA_DEV float ex2(float x) {

@@ -104,7 +104,7 @@ def test_decode_validation(L):
     a.Lq = 1
     a.B, a.Hq, a.Hkv, a.Lk, a.D = 8, 16, 2, 8192, 64
     n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
-    # partial (m, l) and D floats per (b, head, 128-slot chunk) plus tickets
-    assert n >= 8 * 16 * 64 * (64 + 2) * 4
+    # partial (m, l) and D floats per (b, head, split) plus tickets
+    assert n >= 8 * 16 * 16 * (64 + 2) * 4
     assert L.masked_gqa_attn_decode(ctypes.byref(a), None, n, None) == M.MGQA_ERR_INVALID_ARG
     assert L.masked_gqa_attn_decode(ctypes.byref(a), (1 << 20) + 4, n, None) == M.MGQA_ERR_INVALID_ARG
