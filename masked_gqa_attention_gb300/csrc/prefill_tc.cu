@@ -182,24 +182,37 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
                            float &m_used, float &l, Turn &&take_turn) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
   uint32_t sr[BN];
+  float mr;
+  if constexpr (!PARTIAL) {
+    // full tile: the loads also reduce each 32-column piece of the row
+    float red[BN / 32];
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c)
-    tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-  tc::tmem_wait_ld();
-  float mx[8];
+    for (int c = 0; c < BN / 32; ++c)
+      tc::tmem_ld32_red<!NEG>(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]),
+                              red[c]);
+    tc::tmem_wait_ld();
+    mr = NEG ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
+             : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  } else {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) mx[k] = MV;
+    for (int c = 0; c < BN / 32; ++c)
+      tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+    tc::tmem_wait_ld();
+    float mx[8];
 #pragma unroll
-  for (int j = 0; j < BN; ++j) {
-    float a = __uint_as_float(sr[j]);
-    if (PARTIAL && !((mw[j >> 5] >> (j & 31)) & 1u)) a = MV;
-    mx[j & 7] = NEG ? fminf(mx[j & 7], a) : fmaxf(mx[j & 7], a);
+    for (int k = 0; k < 8; ++k) mx[k] = MV;
+#pragma unroll
+    for (int j = 0; j < BN; ++j) {
+      float a = __uint_as_float(sr[j]);
+      if (!((mw[j >> 5] >> (j & 31)) & 1u)) a = MV;
+      mx[j & 7] = NEG ? fminf(mx[j & 7], a) : fmaxf(mx[j & 7], a);
+    }
+#pragma unroll
+    for (int k = 4; k > 0; k >>= 1)
+#pragma unroll
+      for (int u = 0; u < k; ++u) mx[u] = NEG ? fminf(mx[u], mx[u + k]) : fmaxf(mx[u], mx[u + k]);
+    mr = mx[0];
   }
-#pragma unroll
-  for (int k = 4; k > 0; k >>= 1)
-#pragma unroll
-    for (int u = 0; u < k; ++u) mx[u] = NEG ? fminf(mx[u], mx[u + k]) : fmaxf(mx[u], mx[u + k]);
-  const float mr = mx[0];
   const float m_tile = (PARTIAL && mr == MV) ? -INFINITY : mr * sl2;
   const float m_new = fmaxf(m_used, m_tile);
   bool rescale = false;
@@ -537,7 +550,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
         if (!(ok = mbar_wait(bar_vfull + st, use & 1, p.err))) break;
-        if (has_next && !(ok = mbar_wait(bar_kfull + st1, use1 & 1, p.err))) break;
         for (int t = 0; t < NT && ok; ++t) {
           if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
           tc::fence_after_sync();
@@ -551,7 +563,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
           tc::mma_commit(bar_odone + t);
           if (t == NT - 1) tc::mma_commit(bar_vempty + st);
-          if (has_next) issue_s(t, st1);
+          if (has_next) {
+            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, use1 & 1, p.err))) break;
+            tc::fence_after_sync();
+            issue_s(t, st1);
+          }
         }
       }
       // drain: the last release of every stage has landed before the CTA exits
