@@ -95,6 +95,15 @@ MGQA_DEV void named_arrive(int id, int nthreads) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel in the stream is still
+// running. Everything before grid_dependency_wait() must not touch global
+// memory the previous kernel writes or reads; after it, that kernel has
+// completed and its writes are visible. allow_dependents() lets the next
+// kernel in the stream start its own set-up early.
+MGQA_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MGQA_DEV void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- mbarrier / bulk-copy primitives (PTX) --------------------------------
 
 MGQA_DEV uint32_t smem_u32(const void *p) {

@@ -99,6 +99,8 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 
   const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) allow_dependents();
+  grid_dependency_wait();  // everything below may read what the previous kernel wrote
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
   const int nci = x < p.nch ? (p.nch - x + S - 1) / S : 0;
@@ -501,8 +503,7 @@ mgqa_status launch_t(const DecodeParams &p, cudaStream_t s) {
     attr_set = true;
   }
   dim3 grid(S, p.Hq / NREP, p.B);
-  kern<<<grid, kThreads, smem, s>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_runtime.h>
 
 #include "../../include/masked_gqa_attn.h"
 
@@ -10,6 +11,24 @@ namespace mgqa {
 
 // Sets the thread-local detail string returned by mgqa_last_error_detail().
 mgqa_status fail(mgqa_status code, const char *fmt, ...);
+
+// Launch with programmatic stream serialisation (the kernel itself calls
+// grid_dependency_wait() before touching global memory).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 // Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
 // kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.

@@ -316,9 +316,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int g = h0 / p.n_rep;
   const int row0 = qt * BM;
   const int rows = min(BM, p.Lq - row0);
-  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
 
-  // ---- set-up: barriers, tensor memory, segment range of the query tile ----
+  // ---- set-up that touches no global memory (may overlap the previous kernel)
   if (tid == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < STAGES; ++s) {
@@ -335,6 +334,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mbar_init(bar_tok, 128);
     mbar_init(bar_tok + 1, 128);
     fence_mbarrier_init();
+    tc::prefetch_tensormap(&tm_q);
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_v);
+    tc::prefetch_tensormap(&tm_o);
+    allow_dependents();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::tmem_cols);
+  if (p.mask.bits)
+    for (int w = tid; w < (p.nkt + 31) / 32; w += blockDim.x) {
+      any_bits[w] = 0u;
+      all_bits[w] = 0xffffffffu;
+    }
+  grid_dependency_wait();
+  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
+
+  // ---- Q load, segment range of the query tile ----------------------------
+  if (tid == 0) {
     // Q does not depend on the mask: start its load before classifying
     if (row0 < p.Lq) {
       mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
@@ -344,18 +360,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                           bar_q);
     }
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::tmem_cols);
-  if (p.mask.bits)
-    for (int w = tid; w < (p.nkt + 31) / 32; w += blockDim.x) {
-      any_bits[w] = 0u;
-      all_bits[w] = 0xffffffffu;
-    }
   if (warp == 0) {
-    if (lane == 0) {
-      tc::prefetch_tensormap(&tm_q);
-      tc::prefetch_tensormap(&tm_k);
-      tc::prefetch_tensormap(&tm_v);
-    }
     if (p.mask.seg_q) {
       int mn = INT_MAX, mx = INT_MIN;
       for (int r = lane; r < rows; r += 32) {
@@ -724,8 +729,8 @@ mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
     attr_set = true;
   }
   dim3 grid((p.Lq + BM - 1) / BM, p.Hq / NT, p.B);
-  kern<<<grid, Lay::threads, Lay::smem_bytes, s>>>(mq, mk, mv, mo, p);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_pdl(kern, grid, dim3(Lay::threads), Lay::smem_bytes, s, mq, mk, mv,
+                                   mo, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
