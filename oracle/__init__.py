@@ -14,7 +14,9 @@ arrays. What it computes, with the passages it follows:
 * OmniVoice page, "Upstream-identical practice", attention-mask bullet: a
   full 4D boolean mask, not causal, KV heads repeated to the query heads;
 * OmniVoice page, "Memory & speed", packed_guidance paragraph: a
-  block-diagonal mask, each block equal to its run alone.
+  block-diagonal mask, each block equal to its run alone;
+* VoxCPM page, "Upstream-identical practice", attention bullet: causal
+  attention at prefill (query rows = the last Lq of the Lk positions).
 
 Readings where the pages are silent (each also listed in the design notes):
 query head h reads KV head ``h // (Hq // Hkv)``; mask ``True`` means "may
@@ -59,7 +61,7 @@ def _load():
             f = lib.mgqa_oracle_attention
             P = ctypes.c_void_p
             I = ctypes.c_int
-            f.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P,
+            f.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P, I,
                           ctypes.c_double, P, P, I]
             f.restype = I
             _lib = lib
@@ -94,12 +96,13 @@ def _u32(x):
 
 
 def attention(q, k, v, *, scale: float, mask_bits=None, kv_len=None,
-              seg_q=None, seg_k=None, threads: int = 0):
+              seg_q=None, seg_k=None, causal: bool = False, threads: int = 0):
     """Masked GQA attention in fp64.
 
     q: [B, Hq, Lq, D]; k, v: [B, Hkv, Lk, D]; mask_bits: uint32
     [B, Lq, ceil(Lk/32)] (LSB-first, 1 = attend); kv_len: int32 [B];
-    seg_q: int32 [B, Lq]; seg_k: int32 [B, Lk]. Returns (out [B,Hq,Lq,D],
+    seg_q: int32 [B, Lq]; seg_k: int32 [B, Lk]; causal: key j only for query
+    i with j <= i + Lk - Lq. Returns (out [B,Hq,Lq,D],
     lse [B,Hq,Lq], threads_used), all fp64 except the count.
     """
     q64, k64, v64 = _f64(q), _f64(k), _f64(v)
@@ -125,7 +128,7 @@ def attention(q, k, v, *, scale: float, mask_bits=None, kv_len=None,
 
     used = _load().mgqa_oracle_attention(
         ptr(q64), ptr(k64), ptr(v64), B, Hq, Hkv, Lq, Lk, D,
-        ptr(bits), ptr(kvl), ptr(sq), ptr(sk), float(scale),
+        ptr(bits), ptr(kvl), ptr(sq), ptr(sk), int(bool(causal)), float(scale),
         ptr(out), ptr(lse), int(threads))
     if used < 0:
         raise ValueError("oracle rejected the shapes")

@@ -30,7 +30,11 @@
  *   bits   : bit (j % 32) of word bits[(b*Lq + i)*W + j/32], W = ceil(Lk/32),
  *            least-significant bit first; 1 = may attend (SDPA bool polarity);
  *   kv_len : j < kv_len[b];
- *   seg    : seg_q[b*Lq + i] == seg_k[b*Lk + j] and that id is >= 0.
+ *   seg    : seg_q[b*Lq + i] == seg_k[b*Lk + j] and that id is >= 0;
+ *   causal : j <= i + (Lk - Lq)  (VoxCPM page, "Upstream-identical practice",
+ *            attention bullet: causal attention at prefill; the query rows
+ *            are taken to be the last Lq of the Lk positions, which for
+ *            Lq == Lk is the usual lower triangle).
  * With no mask form given every key is allowed.
  *
  * Layout: q [B][Hq][Lq][D], k and v [B][Hkv][Lk][D], out [B][Hq][Lq][D],
@@ -45,7 +49,8 @@
 
 static int key_allowed(int b, int i, int j, int Lq, int Lk,
                        const uint32_t *bits, const int32_t *kv_len,
-                       const int32_t *seg_q, const int32_t *seg_k) {
+                       const int32_t *seg_q, const int32_t *seg_k, int causal) {
+    if (causal && j > i + (Lk - Lq)) return 0;
     if (bits) {
         long W = (Lk + 31) / 32;
         uint32_t word = bits[((long)b * Lq + i) * W + j / 32];
@@ -68,7 +73,7 @@ int mgqa_oracle_attention(const double *q, const double *k, const double *v,
                           int B, int Hq, int Hkv, int Lq, int Lk, int D,
                           const uint32_t *bits, const int32_t *kv_len,
                           const int32_t *seg_q, const int32_t *seg_k,
-                          double scale, double *out, double *lse, int nthreads) {
+                          int causal, double scale, double *out, double *lse, int nthreads) {
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Lq < 0 || Lk < 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
     if ((seg_q == NULL) != (seg_k == NULL)) return -1;
@@ -98,7 +103,7 @@ int mgqa_oracle_attention(const double *q, const double *k, const double *v,
 
             double m = -INFINITY;
             for (int j = 0; j < Lk; ++j) {
-                if (key_allowed(b, i, j, Lq, Lk, bits, kv_len, seg_q, seg_k)) {
+                if (key_allowed(b, i, j, Lq, Lk, bits, kv_len, seg_q, seg_k, causal)) {
                     double dot = 0.0;
                     for (int d = 0; d < D; ++d) dot += qi[d] * kg[(long)j * D + d];
                     s[j] = scale * dot;

@@ -246,3 +246,38 @@ def test_pack_unpack_roundtrip():
     one[0, 0, 33] = True
     w = W.pack_bool_mask(one)
     assert int(w[0, 0, 0]) == 1 and int(w[0, 0, 1]) == 2
+
+
+# --- causal form (VoxCPM page, "Upstream-identical practice": causal prefill)
+
+@pytest.mark.parametrize("shape", [(2, 4, 2, 33, 33, 16), (1, 6, 3, 70, 70, 8)])
+@pytest.mark.parametrize("mask", ["none", "bits"])
+def test_causal_matches_torch_sdpa_fp64(oracle_mod, shape, mask):
+    B, Hq, Hkv, Lq, Lk, D = shape
+    wl = W.random_case(7 + Lq, B, Hq, Hkv, Lq, Lk, D, torch.float64, mask=mask)
+    out, lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, causal=True,
+                                       mask_bits=wl.mask_bits)
+    tril = torch.ones((Lq, Lk), dtype=torch.bool).tril()
+    allowed = tril[None].expand(B, Lq, Lk).clone()
+    if wl.mask_bits is not None:
+        allowed &= W.unpack_bits(wl.mask_bits, Lk)
+    if mask == "none":  # library causal flag itself
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            wl.q, wl.k, wl.v, is_causal=True, scale=wl.scale, enable_gqa=True)
+    else:
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            wl.q, wl.k, wl.v, attn_mask=allowed[:, None], scale=wl.scale, enable_gqa=True)
+    sel = allowed.any(-1)[:, None, :].expand(B, Hq, Lq).numpy()
+    np.testing.assert_allclose(out[sel], ref.numpy()[sel], rtol=1e-12, atol=1e-12)
+
+
+def test_causal_first_row_and_single_query(oracle_mod):
+    g, q, k, v = W.random_qkv(2, 1, 2, 1, 9, 9, 4, torch.float64)
+    out, lse, _ = oracle_mod.attention(q, k, v, scale=0.7, causal=True)
+    # row 0 sees key 0 only: its value, exactly
+    assert np.array_equal(out[0, 0, 0], v[0, 0, 0].numpy())
+    assert np.array_equal(out[0, 1, 0], v[0, 0, 0].numpy())
+    # one query over a 9-slot cache is the last position: every key allowed
+    o1, l1, _ = oracle_mod.attention(q[:, :, -1:], k, v, scale=0.7, causal=True)
+    o2, l2, _ = oracle_mod.attention(q[:, :, -1:], k, v, scale=0.7)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

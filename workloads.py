@@ -68,6 +68,7 @@ class Workload:
     kv_len: Optional[torch.Tensor] = None
     seg_q: Optional[torch.Tensor] = None
     seg_k: Optional[torch.Tensor] = None
+    causal: bool = False
     seed: int = 0
     info: dict = field(default_factory=dict)
 
@@ -89,11 +90,18 @@ class Workload:
             sq = self.seg_q.cpu()[:, :, None]
             sk = self.seg_k.cpu()[:, None, :]
             a &= (sq == sk) & (sq >= 0)
+        if self.causal:
+            i = torch.arange(Lq)[:, None]
+            j = torch.arange(Lk)[None, :]
+            a &= (j <= i + (Lk - Lq))[None]
         return a
 
     def masks(self) -> dict:
-        return dict(mask_bits=self.mask_bits, kv_len=self.kv_len,
-                    seg_q=self.seg_q, seg_k=self.seg_k)
+        d = dict(mask_bits=self.mask_bits, kv_len=self.kv_len,
+                 seg_q=self.seg_q, seg_k=self.seg_k)
+        if self.causal:
+            d["causal"] = True
+        return d
 
     def allowed_pairs(self) -> int:
         return int(self.allowed().sum())
@@ -238,7 +246,7 @@ def random_case(seed: int, B, Hq, Hkv, Lq, Lk, D, dtype=torch.bfloat16,
                 mask: str = "bits", density: float = 0.7) -> Workload:
     """A generic seeded case for parity tests. mask is one of "none", "bits"
     (random key-padding and random per-element holes), "kvlen", "segment",
-    "bits+kvlen"."""
+    "bits+kvlen", "causal"."""
     g, q, k, v = random_qkv(seed, B, Hq, Hkv, Lq, Lk, D, dtype)
     w = Workload(f"random_{mask}", q, k, v, 1.0 / math.sqrt(D), seed=seed,
                  info=dict(dtype=str(dtype).replace("torch.", "")))
@@ -268,7 +276,9 @@ def random_case(seed: int, B, Hq, Hkv, Lq, Lk, D, dtype=torch.bfloat16,
                 seg[b, : max(1, L // 16)] = -1
         w.seg_q = seg[:, :Lq].contiguous()
         w.seg_k = seg[:, :Lk].contiguous()
-    if mask not in ("none", "bits", "kvlen", "segment", "bits+kvlen"):
+    if mask == "causal":
+        w.causal = True
+    if mask not in ("none", "bits", "kvlen", "segment", "bits+kvlen", "causal"):
         raise ValueError(mask)
     return w
 
