@@ -29,7 +29,10 @@
  *   kv_len    : j < kv_len[b]  (a per-row key length; for decode, the filled
  *               length of the static cache);
  *   seg_q/seg_k: seg_q[b*Lq + i] == seg_k[b*Lk + j] and that id is >= 0
- *               (block-diagonal packing; negative ids attend nowhere).
+ *               (block-diagonal packing; negative ids attend nowhere);
+ *   causal    : j <= i + (Lk - Lq) when nonzero (the query rows are the last
+ *               Lq of the Lk positions; for Lq == Lk the lower triangle) --
+ *               VoxCPM page, "Upstream-identical practice": causal prefill.
  * With no mask form given every key is allowed (dense bidirectional).
  *
  * Ownership: every pointer is device memory owned by the caller. The library
@@ -49,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MGQA_ABI_VERSION 1
+#define MGQA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MGQA_API __attribute__((visibility("default")))
@@ -68,7 +71,8 @@ typedef enum {
 
 typedef enum {
   MGQA_BF16 = 0,  /* q/k/v/out bf16, fp32 accumulation (tensor cores) */
-  MGQA_FP32 = 1   /* q/k/v/out fp32, fp32 arithmetic throughout */
+  MGQA_FP32 = 1,  /* q/k/v/out fp32, fp32 arithmetic throughout */
+  MGQA_FP16 = 2   /* q/k/v/out fp16, fp32 accumulation (tensor cores) */
 } mgqa_dtype;
 
 typedef struct mgqa_args {
@@ -100,6 +104,7 @@ typedef struct mgqa_args {
   float scale;                  /* finite softmax scale; SDPA's default is 1/sqrt(D) */
   float *lse;                   /* optional out: [B][Hq][Lq] contiguous, natural log */
   int32_t *dev_error;           /* optional: first device-side mgqa_status code */
+  int32_t causal;               /* nonzero: add the causal form to the mask */
 } mgqa_args;
 
 /* Full-sequence (prefill) attention: bidirectional, any of the mask forms.

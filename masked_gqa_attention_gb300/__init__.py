@@ -33,7 +33,7 @@ __all__ = [
 ]
 
 MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT = range(5)
-MGQA_BF16, MGQA_FP32 = 0, 1
+MGQA_BF16, MGQA_FP32, MGQA_FP16 = 0, 1, 2
 # size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
 DECODE_STATIC_SCRATCH_BYTES = 4 << 20
 
@@ -72,6 +72,7 @@ class MgqaArgs(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("lse", ctypes.c_void_p),
         ("dev_error", ctypes.c_void_p),
+        ("causal", ctypes.c_int32),
     ]
 
 
@@ -126,12 +127,13 @@ def _dev(t: Optional[torch.Tensor], name: str, dtype=None):
 
 
 def make_args(q, k, v, out, *, scale=None, mask_bits=None, kv_len=None, seg_q=None,
-              seg_k=None, lse=None, dev_error=None) -> MgqaArgs:
+              seg_k=None, lse=None, dev_error=None, causal=False) -> MgqaArgs:
     """Fill an MgqaArgs from tensors: q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D], out like q.
 
     mask_bits: int32/uint32 words [B, Lq, W] (or [B, 1, W] / [1, Lq, W] with
     stride 0 broadcast), W >= ceil(Lk/32); kv_len int32 [B]; seg_q int32 [B, Lq];
-    seg_k int32 [B, Lk]; lse fp32 [B, Hq, Lq] contiguous; dev_error int32 [1].
+    seg_k int32 [B, Lk]; lse fp32 [B, Hq, Lq] contiguous; dev_error int32 [1];
+    causal: key j only for query i with j <= i + Lk - Lq.
     Tensors are passed by pointer; no copy is made.
     """
     for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
@@ -142,8 +144,10 @@ def make_args(q, k, v, out, *, scale=None, mask_bits=None, kv_len=None, seg_q=No
         dt = MGQA_BF16
     elif q.dtype == torch.float32:
         dt = MGQA_FP32
+    elif q.dtype == torch.float16:
+        dt = MGQA_FP16
     else:
-        raise ValueError("q/k/v must be bfloat16 or float32")
+        raise ValueError("q/k/v must be bfloat16, float16 or float32")
     for name, t in (("k", k), ("v", v), ("out", out)):
         if t.dtype != q.dtype:
             raise ValueError(f"{name} dtype differs from q")
@@ -182,6 +186,7 @@ def make_args(q, k, v, out, *, scale=None, mask_bits=None, kv_len=None, seg_q=No
             raise ValueError("lse must be contiguous fp32 [B, Hq, Lq]")
         a.lse = lse.data_ptr()
     a.dev_error = _ptr(_dev(dev_error, "dev_error", torch.int32))
+    a.causal = 1 if causal else 0
     return a
 
 
@@ -192,12 +197,13 @@ def _stream_handle(stream) -> int:
 
 
 def masked_gqa_attn_prefill(q, k, v, out=None, *, scale=None, mask_bits=None, kv_len=None,
-                            seg_q=None, seg_k=None, lse=None, dev_error=None, stream=None):
-    """Bidirectional masked GQA attention over full sequences; returns out."""
+                            seg_q=None, seg_k=None, lse=None, dev_error=None, causal=False,
+                            stream=None):
+    """Masked GQA attention over full sequences (bidirectional unless causal); returns out."""
     if out is None:
         out = torch.empty_like(q)
     a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
-                  seg_k=seg_k, lse=lse, dev_error=dev_error)
+                  seg_k=seg_k, lse=lse, dev_error=dev_error, causal=causal)
     _check(lib().masked_gqa_attn_prefill(ctypes.byref(a), _stream_handle(stream)))
     return out
 

@@ -38,7 +38,7 @@ mgqa_status check_tensor(const char *name, const void *ptr, const int64_t *st, s
 mgqa_status validate(const mgqa_args *a, bool decode) {
   g_detail[0] = '\0';
   if (!a) return fail(MGQA_ERR_INVALID_ARG, "args is null");
-  if (a->dtype != MGQA_BF16 && a->dtype != MGQA_FP32)
+  if (a->dtype != MGQA_BF16 && a->dtype != MGQA_FP32 && a->dtype != MGQA_FP16)
     return fail(MGQA_ERR_INVALID_ARG, "unknown dtype %d", (int)a->dtype);
   if (a->B < 1 || a->Hq < 1 || a->Hkv < 1 || a->Lq < 1 || a->Lk < 1)
     return fail(MGQA_ERR_INVALID_ARG, "B, Hq, Hkv, Lq, Lk must be >= 1");
@@ -52,7 +52,7 @@ mgqa_status validate(const mgqa_args *a, bool decode) {
   if (decode && a->Lk > kDecodeMaxLk)
     return fail(MGQA_ERR_UNSUPPORTED, "decode cache longer than %d slots", kDecodeMaxLk);
   if (!std::isfinite(a->scale)) return fail(MGQA_ERR_INVALID_ARG, "scale is not finite");
-  const size_t es = a->dtype == MGQA_BF16 ? 2 : 4;
+  const size_t es = a->dtype == MGQA_FP32 ? 4 : 2;
   mgqa_status st;
   if ((st = check_tensor("q", a->q, a->q_stride, es)) != MGQA_OK) return st;
   if ((st = check_tensor("k", a->k, a->k_stride, es)) != MGQA_OK) return st;
@@ -87,7 +87,7 @@ extern "C" {
 mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream) {
   mgqa_status st = mgqa::validate(args, false);
   if (st != MGQA_OK) return st;
-  if (args->dtype == MGQA_BF16) return mgqa::launch_prefill_tc(*args, stream);
+  if (args->dtype != MGQA_FP32) return mgqa::launch_prefill_tc(*args, stream);
   return mgqa::launch_prefill_simt(*args, stream);
 }
 

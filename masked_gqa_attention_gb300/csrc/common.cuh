@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/masked_gqa_attn.h"
@@ -21,14 +22,27 @@ MGQA_DEV void report_error(int32_t *err, int32_t code) {
 
 MGQA_DEV float to_float(float x) { return x; }
 MGQA_DEV float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+MGQA_DEV float to_float(__half x) { return __half2float(x); }
 
 template <typename T> MGQA_DEV T from_float(float x);
 template <> MGQA_DEV float from_float<float>(float x) { return x; }
 template <> MGQA_DEV __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
   return __float2bfloat16_rn(x);
 }
+template <> MGQA_DEV __half from_float<__half>(float x) { return __float2half_rn(x); }
 
-// Unpack 16 bytes into float lanes: 8 bf16 or 4 fp32 values.
+// Two floats rounded to a packed pair of 16-bit values (low half = lo).
+template <typename T> MGQA_DEV uint32_t pack2(float lo, float hi);
+template <> MGQA_DEV uint32_t pack2<__nv_bfloat16>(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+template <> MGQA_DEV uint32_t pack2<__half>(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Unpack 16 bytes into float lanes: 8 bf16 / 8 fp16 or 4 fp32 values.
 MGQA_DEV void unpack16(const uint4 &u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -36,6 +50,24 @@ MGQA_DEV void unpack16(const uint4 &u, float (&f)[8]) {
     f[2 * i] = __uint_as_float(w[i] << 16);
     f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
+}
+template <typename T> MGQA_DEV void unpack16_t(const uint4 &u, float (&f)[8]);
+template <> MGQA_DEV void unpack16_t<__nv_bfloat16>(const uint4 &u, float (&f)[8]) { unpack16(u, f); }
+template <> MGQA_DEV void unpack16_t<__half>(const uint4 &u, float (&f)[8]) {
+  const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(h[i]);
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+template <typename T> MGQA_DEV void unpack16_t(const uint4 &u, float (&f)[4]);
+template <> MGQA_DEV void unpack16_t<float>(const uint4 &u, float (&f)[4]) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
 }
 MGQA_DEV void unpack16(const uint4 &u, float (&f)[4]) {
   f[0] = __uint_as_float(u.x);
@@ -64,6 +96,8 @@ struct MaskView {
   const int32_t *kv_len;  // [B]
   const int32_t *seg_q;   // [B][Lq]
   const int32_t *seg_k;   // [B][Lk]
+  int causal;             // key j only for query i with j <= i + coff
+  int coff;               // Lk - Lq
 };
 
 // Bits t = 0..31 of the result: may query i of row b attend to key jbase + t?
@@ -73,7 +107,8 @@ struct MaskView {
 MGQA_DEV uint32_t mask_word(const MaskView &m, int b, int i, int jbase, int Lk, int Lq, int kvl,
                             int segq) {
   if (jbase >= Lk) return 0u;
-  const int lim = min(Lk, kvl) - jbase;
+  int lim = min(Lk, kvl) - jbase;
+  if (m.causal) lim = min(lim, i + m.coff + 1 - jbase);
   uint32_t w = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : ((1u << lim) - 1u));
   if (m.bits && w) w &= __ldg(m.bits + (int64_t)b * m.sb + (int64_t)i * m.sq + (jbase >> 5));
   if (m.seg_q && w) {
@@ -188,15 +223,24 @@ MGQA_DEV void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col): register
-// fragments of the warp-wide mma.sync shape m16n8k16.
-MGQA_DEV void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                             uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// D (16x8 fp32) += A (16x16, row) * B (16x8, col), both bf16 or both fp16:
+// register fragments of the warp-wide mma.sync shape m16n8k16.
+template <typename T>
+MGQA_DEV void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                        uint32_t b0, uint32_t b1) {
+  if constexpr (sizeof(T) == 2 && __is_same(T, __half)) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
 }
 
 // Two transposed 8x8 bf16 tiles from shared memory; lane i (0..15) gives the

@@ -62,8 +62,9 @@ constexpr int cap_rows() {  // dense K/V rows per batch: K and V <= 32 KB each
   return (32768 / (D * (int)sizeof(T))) < 256 ? (32768 / (D * (int)sizeof(T))) : 256;
 }
 
-// bf16 runs the two products on the tensor cores (mma.sync m16n8k16, the
-// NREP query heads padded to 16 rows); fp32 stays on the CUDA cores.
+// bf16 and fp16 run the two products on the tensor cores (mma.sync m16n8k16,
+// the NREP query heads padded to 16 rows); fp32 stays on the CUDA cores.
+// (A causal mask needs nothing here: the single query is the last position.)
 template <typename T>
 constexpr bool use_mma() {
   return sizeof(T) == 2;
@@ -184,13 +185,11 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     static_assert(RW % 16 == 0, "rows per warp");
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      __nv_bfloat162 lo = __floats2bfloat162_rn(0.f, 0.f), hi = lo;
+      qa[kk][0] = qa[kk][1] = 0u;
       if (gq < NREP) {
-        lo = __floats2bfloat162_rn(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
-        hi = __floats2bfloat162_rn(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
+        qa[kk][0] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
+        qa[kk][1] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
       }
-      qa[kk][0] = *reinterpret_cast<uint32_t *>(&lo);
-      qa[kk][1] = *reinterpret_cast<uint32_t *>(&hi);
     }
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) ow[dt][0] = ow[dt][1] = ow[dt][2] = ow[dt][3] = 0.f;
@@ -236,7 +235,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const T *kr = &sm.k[r0 + nt * 8 + gq][kk * 16 + 2 * tq];
-            mma_bf16_16816(c[nt], qa[kk][0], 0u, qa[kk][1], 0u,
+            mma_16816<T>(c[nt], qa[kk][0], 0u, qa[kk][1], 0u,
                            *reinterpret_cast<const uint32_t *>(kr),
                            *reinterpret_cast<const uint32_t *>(kr + 8));
           }
@@ -260,8 +259,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
         for (int nt = 0; nt < NT8; ++nt) {
           const float p0 = exp2f(c[nt][0] - m_new), p1 = exp2f(c[nt][1] - m_new);
           ps += p0 + p1;
-          __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
-          pa[nt] = *reinterpret_cast<uint32_t *>(&hp);
+          pa[nt] = pack2<T>(p0, p1);
         }
         ps += __shfl_xor_sync(0xffffffffu, ps, 1);
         ps += __shfl_xor_sync(0xffffffffu, ps, 2);
@@ -279,7 +277,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
           for (int dt = 0; dt < D / 8; ++dt) {
             uint32_t b0, b1;
             ldmatrix_x2_trans(b0, b1, &sm.v[r0 + ks * 16 + (lane & 15)][dt * 8]);
-            mma_bf16_16816(ow[dt], pa[2 * ks], 0u, pa[2 * ks + 1], 0u, b0, b1);
+            mma_16816<T>(ow[dt], pa[2 * ks], 0u, pa[2 * ks + 1], 0u, b0, b1);
           }
         }
       }
@@ -302,7 +300,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
           if (valid) {
             const uint4 u = *reinterpret_cast<const uint4 *>(&sm.k[row][e * EPL]);
             float kf[EPL];
-            unpack16(u, kf);
+            unpack16_t<T>(u, kf);
   #pragma unroll
             for (int r = 0; r < NREP; ++r)
   #pragma unroll
@@ -567,6 +565,9 @@ mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStr
   if (a.dtype == MGQA_BF16) {
     if (a.D == 64) return launch_nrep<__nv_bfloat16, 64>(p, hpc, s);
     if (a.D == 128) return launch_nrep<__nv_bfloat16, 128>(p, hpc, s);
+  } else if (a.dtype == MGQA_FP16) {
+    if (a.D == 64) return launch_nrep<__half, 64>(p, hpc, s);
+    if (a.D == 128) return launch_nrep<__half, 128>(p, hpc, s);
   } else {
     if (a.D == 64) return launch_nrep<float, 64>(p, hpc, s);
     if (a.D == 128) return launch_nrep<float, 128>(p, hpc, s);

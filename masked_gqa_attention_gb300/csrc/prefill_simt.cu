@@ -160,16 +160,14 @@ mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s) {
     p.qs[t] = a.q_stride[t]; p.ks[t] = a.k_stride[t];
     p.vs[t] = a.v_stride[t]; p.os[t] = a.o_stride[t];
   }
-  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k};
+  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k,
+                    a.causal != 0, a.Lk - a.Lq};
   p.scale_log2 = a.scale * kLog2e;
   p.lse = a.lse; p.err = a.dev_error;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lq = a.Lq; p.Lk = a.Lk; p.n_rep = a.Hq / a.Hkv;
   if (a.dtype == MGQA_FP32) {
     if (a.D == 64) return launch_t<float, 64>(p, s);
     if (a.D == 128) return launch_t<float, 128>(p, s);
-  } else {
-    if (a.D == 64) return launch_t<__nv_bfloat16, 64>(p, s);
-    if (a.D == 128) return launch_t<__nv_bfloat16, 128>(p, s);
   }
   return fail(MGQA_ERR_UNSUPPORTED, "prefill: head dim %d", a.D);
 }

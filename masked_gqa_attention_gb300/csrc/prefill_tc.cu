@@ -101,7 +101,8 @@ MGQA_DEV void tile_mask_words(const TcParams &p, int b, int i, bool row_ok, int 
 #pragma unroll
   for (int w = 0; w < BN / 32; ++w) {
     const int jw = k0 + 32 * w;
-    const int lim = min(p.Lk, kvl) - jw;
+    int lim = min(p.Lk, kvl) - jw;
+    if (p.mask.causal) lim = min(lim, i + p.mask.coff + 1 - jw);
     mw[w] = lim >= 32 ? 0xffffffffu : (lim <= 0 ? 0u : ((1u << lim) - 1u));
   }
   if (p.mask.bits) {
@@ -177,7 +178,7 @@ constexpr int kPolyEvery = 4;
 // NEG: negative scale (the max of scaled scores is the min of raw ones).
 // PARTIAL: mw holds the row's allowed-key bits. The optional hand-over wait
 // (two heads) sits between the load and the exponentials.
-template <int D, bool NEG, bool PARTIAL, typename Turn>
+template <typename T, int D, bool NEG, bool PARTIAL, typename Turn>
 MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
                            float &m_used, float &l, Turn &&take_turn) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
@@ -267,8 +268,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
         if (!((mw[c] >> (2 * j + 1)) & 1u)) p1 = 0.f;
       }
       acc[j & 3] = tc::add2(acc[j & 3], tc::pk2(p0, p1));
-      __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-      pk[j] = *reinterpret_cast<uint32_t *>(&h);
+      pk[j] = pack2<T>(p0, p1);
     }
     tc::tmem_st16(t_s + c * 16, pk);
   }
@@ -281,7 +281,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
   tc::tmem_wait_st();
 }
 
-template <int D, int NT, int STAGES>
+template <typename T, int D, int NT, int STAGES>
 __global__ void __launch_bounds__(128 * (1 + NT), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -435,6 +435,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ne = ne && k0 < kvl;
       full = full && k0 + BN <= kvl;
     }
+    if (p.mask.causal) {  // key j for query i when j <= i + coff
+      ne = ne && k0 <= row0 + rows - 1 + p.mask.coff;
+      full = full && k0 + BN - 1 <= row0 + p.mask.coff;
+    }
     if (p.mask.bits && ne) {
       ne = (any_bits[kt >> 5] >> (kt & 31)) & 1u;  // ne was true here
       full = full && ((all_bits[kt >> 5] >> (kt & 31)) & 1u);
@@ -532,8 +536,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // overwrites P_t(n) only after the P.V MMA has consumed it; completion of
     // S_t(n+1) (s_full) therefore also implies O_t holds P.V up to tile n.
     if (lane == 0 && nk > 0) {
-      constexpr uint32_t id_s = tc::idesc_bf16(BM, BN, 0, 0);
-      constexpr uint32_t id_pv = tc::idesc_bf16(BM, D, 0, 1);
+      constexpr bool kBf16 = !__is_same(T, __half);
+      constexpr uint32_t id_s = tc::idesc_16bit(BM, BN, 0, 0, kBf16);
+      constexpr uint32_t id_pv = tc::idesc_16bit(BM, D, 0, 1, kBf16);
       auto issue_s = [&](int t, int st) {
         const uint32_t d_s = tmem + t * BN;
 #pragma unroll
@@ -624,11 +629,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       };
       if (neg) {
-        if (partial) softmax_tile<D, true, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
-        else softmax_tile<D, true, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
       } else {
-        if (partial) softmax_tile<D, false, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
-        else softmax_tile<D, false, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
       }
       tc::fence_before_sync();
       mbar_arrive(bar_pfull + t);
@@ -661,11 +666,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int cc = 0; cc < D / 8; ++cc) {  // 16-byte chunks of the row
       uint32_t w4[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(orow[cc * 8 + 2 * h]) * o_scale,
-                                                  __uint_as_float(orow[cc * 8 + 2 * h + 1]) * o_scale);
-        w4[h] = *reinterpret_cast<uint32_t *>(&hv);
-      }
+      for (int h = 0; h < 4; ++h)
+        w4[h] = pack2<T>(__uint_as_float(orow[cc * 8 + 2 * h]) * o_scale,
+                         __uint_as_float(orow[cc * 8 + 2 * h + 1]) * o_scale);
       const int box = cc >> 3, ch = cc & 7;
       *reinterpret_cast<uint4 *>(ob + box * BOX + r * 128 + ((ch ^ (r & 7)) << 4)) =
           make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -703,24 +706,25 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 [B][H][L][D] view with element strides (b, h, l) -> 4-D map, box 64 x 128.
-bool make_map(CUtensorMap *m, const void *base, int B, int H, int L, int D, const int64_t *st) {
+// 16-bit [B][H][L][D] view with element strides (b, h, l) -> 4-D map, box 64 x 128.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int B, int H, int L, int D,
+              const int64_t *st) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
   const cuuint32_t box[4] = {64, 128, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+  return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int NT, int STAGES>
+template <typename T, int D, int NT, int STAGES>
 mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                      const CUtensorMap &mo, const TcParams &p, cudaStream_t s) {
   using Lay = Layout<D, NT, STAGES>;
-  auto kern = prefill_tc_kernel<D, NT, STAGES>;
+  auto kern = prefill_tc_kernel<T, D, NT, STAGES>;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::smem_bytes) !=
@@ -735,20 +739,35 @@ mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
   return MGQA_OK;
 }
 
+template <typename T>
+mgqa_status dispatch_d(int D, bool pair, const CUtensorMap &mq, const CUtensorMap &mk,
+                       const CUtensorMap &mv, const CUtensorMap &mo, const TcParams &p,
+                       cudaStream_t s) {
+  if (D == 128)
+    return pair ? launch_t<T, 128, 2, 2>(mq, mk, mv, mo, p, s) : launch_t<T, 128, 1, 2>(mq, mk, mv, mo, p, s);
+  if (D == 64)
+    return pair ? launch_t<T, 64, 2, 3>(mq, mk, mv, mo, p, s) : launch_t<T, 64, 1, 3>(mq, mk, mv, mo, p, s);
+  return fail(MGQA_ERR_UNSUPPORTED, "head dim %d", D);
+}
+
 }  // namespace
 
 mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
-  if (a.dtype != MGQA_BF16) return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill is bf16 only");
+  if (a.dtype != MGQA_BF16 && a.dtype != MGQA_FP16)
+    return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill takes bf16 or fp16");
   const int nkt = (a.Lk + BN - 1) / BN;
   if (nkt > MAXKT) return fail(MGQA_ERR_UNSUPPORTED, "Lk > %d", MAXKT * BN);
+  const CUtensorMapDataType dt =
+      a.dtype == MGQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride) ||
-      !make_map(&mk, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride) ||
-      !make_map(&mv, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride) ||
-      !make_map(&mo, a.out, a.B, a.Hq, a.Lq, a.D, a.o_stride))
+  if (!make_map(&mq, dt, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride) ||
+      !make_map(&mk, dt, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride) ||
+      !make_map(&mv, dt, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride) ||
+      !make_map(&mo, dt, a.out, a.B, a.Hq, a.Lq, a.D, a.o_stride))
     return fail(MGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   TcParams p{};
-  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k};
+  p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k,
+                    a.causal != 0, a.Lk - a.Lq};
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lq = a.Lq; p.Lk = a.Lk;
   p.n_rep = a.Hq / a.Hkv; p.nkt = nkt;
   p.scale_log2 = a.scale * kLog2e;
@@ -756,9 +775,8 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
   p.os[0] = a.o_stride[0]; p.os[1] = a.o_stride[1]; p.os[2] = a.o_stride[2];
   p.lse = a.lse; p.err = a.dev_error;
   const bool pair = (p.n_rep % 2) == 0;
-  if (a.D == 128) return pair ? launch_t<128, 2, 2>(mq, mk, mv, mo, p, s) : launch_t<128, 1, 2>(mq, mk, mv, mo, p, s);
-  if (a.D == 64) return pair ? launch_t<64, 2, 3>(mq, mk, mv, mo, p, s) : launch_t<64, 1, 3>(mq, mk, mv, mo, p, s);
-  return fail(MGQA_ERR_UNSUPPORTED, "head dim %d", a.D);
+  if (a.dtype == MGQA_BF16) return dispatch_d<__nv_bfloat16>(a.D, pair, mq, mk, mv, mo, p, s);
+  return dispatch_d<__half>(a.D, pair, mq, mk, mv, mo, p, s);
 }
 
 }  // namespace mgqa

@@ -180,12 +180,13 @@ MGQA_DEV uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator.
-// a_mn / b_mn: operand is MN-major (1) or K-major (0).
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4)                      // D format: f32
-         | (1u << 7)                    // A format: bf16
-         | (1u << 10)                   // B format: bf16
+// Instruction descriptor, kind::f16 with an fp32 accumulator; A and B both
+// bf16 (bf16 = true) or both fp16. a_mn / b_mn: operand is MN-major (1) or
+// K-major (0).
+__host__ __device__ constexpr uint32_t idesc_16bit(int M, int N, int a_mn, int b_mn, bool bf16) {
+  return (1u << 4)                          // D format: f32
+         | ((bf16 ? 1u : 0u) << 7)          // A format: bf16 (1) or f16 (0)
+         | ((bf16 ? 1u : 0u) << 10)         // B format: the same
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
          | ((uint32_t)(N >> 3) << 17)   // N / 8
          | ((uint32_t)(M >> 4) << 24);  // M / 16

@@ -25,7 +25,7 @@ def run_prefill(M, wl, lse=True, err=None, d=None):
     lse_t = torch.empty(d["q"].shape[:3], dtype=torch.float32, device="cuda") if lse else None
     M.masked_gqa_attn_prefill(d["q"], d["k"], d["v"], out, scale=wl.scale, lse=lse_t,
                               dev_error=err, mask_bits=d["mask_bits"], kv_len=d["kv_len"],
-                              seg_q=d["seg_q"], seg_k=d["seg_k"])
+                              seg_q=d["seg_q"], seg_k=d["seg_k"], causal=wl.causal)
     torch.cuda.synchronize()
     return out, lse_t
 
@@ -107,7 +107,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("mask", ["none", "bits", "kvlen", "segment", "bits+kvlen"])
+@pytest.mark.parametrize("mask", ["none", "bits", "kvlen", "segment", "bits+kvlen", "causal"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
 def test_random_cases_bf16(M, oracle_mod, mask, case):
     wl = W.random_case(sum(case) + len(mask), *case, dtype=torch.bfloat16, mask=mask)
@@ -117,7 +117,27 @@ def test_random_cases_bf16(M, oracle_mod, mask, case):
     assert_lse_close(lse, ref_lse, 2e-3)
 
 
-@pytest.mark.parametrize("mask", ["bits", "segment"])
+@pytest.mark.parametrize("mask", ["none", "bits", "segment", "causal"])
+@pytest.mark.parametrize("case", [(2, 8, 2, 300, 300, 128), (1, 2, 1, 129, 257, 64),
+                                  (2, 4, 4, 200, 700, 128)], ids=lambda c: "x".join(map(str, c)))
+def test_random_cases_fp16(M, oracle_mod, mask, case):
+    wl = W.random_case(sum(case) + 3 * len(mask), *case, dtype=torch.float16, mask=mask)
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.float16, f"fp16 {mask} {case}")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
+def test_causal_lq_shorter_than_lk(M, oracle_mod):
+    """Causal queries as the last Lq of the Lk positions (a prefill chunk after a cache)."""
+    wl = W.random_case(44, 2, 4, 2, 200, 640, 128, dtype=torch.bfloat16, mask="causal")
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.bfloat16, "causal chunk")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
+@pytest.mark.parametrize("mask", ["bits", "segment", "causal"])
 @pytest.mark.parametrize("case", [(2, 4, 2, 150, 200, 64), (1, 2, 2, 64, 1000, 128)],
                          ids=lambda c: "x".join(map(str, c)))
 def test_random_cases_fp32(M, oracle_mod, mask, case):
