@@ -131,6 +131,47 @@ MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
                                             size_t workspace_bytes, cudaStream_t stream);
 
+/* One decode step fused with its cache append (VoxCPM page, "Memory & speed":
+ * each patch advances the language model by one position against its static
+ * cache, inside one CUDA graph per patch; when the cache is full, the step
+ * errors where upstream errors). For each request b this writes the step's
+ * key/value rows k_new[b][g][:], v_new[b][g][:] (element strides
+ * k_new_stride = {batch, head}, same for v_new; head dim contiguous, 16-byte
+ * aligned) into cache slot kv_len[b] of args->k / args->v, then attends the
+ * query over slots 0 .. kv_len[b] (the new one included), and writes
+ * kv_len[b] + 1 to kv_len_out[b] when kv_len_out is given (it must not alias
+ * kv_len, so a captured graph can ping-pong two length buffers). args->kv_len
+ * is required; packed bits and segment ids are not accepted here. A request
+ * whose cache is already full (kv_len[b] == Lk) appends nothing, attends over
+ * the whole cache, and sets *dev_error to MGQA_ERR_INVALID_ARG. Workspace as
+ * for masked_gqa_attn_decode. */
+MGQA_API mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_new,
+                                                   const void *v_new, const int64_t *k_new_stride,
+                                                   const int64_t *v_new_stride,
+                                                   int32_t *kv_len_out, void *workspace,
+                                                   size_t workspace_bytes, cudaStream_t stream);
+
+/* Packed-guidance helpers (OmniVoice page, "Memory & speed", packed_guidance:
+ * the conditional sequence and the target part of the unconditional one side
+ * by side in one row under a block-diagonal mask, positions of each starting
+ * at 0). pack: packed[:, :, 0:La] = a, packed[:, :, La:La+Lb] = b for every
+ * batch row and head, and, when seg is given, seg[b][0:La] = 0 and
+ * seg[b][La:La+Lb] = 1 (int32 [B][La+Lb], usable as seg_q and seg_k of the
+ * packed call). unpack: the inverse split of a packed output. Views are
+ * [B][H][L][D] with element strides (batch, head, position), head dim
+ * contiguous, 16-byte aligned; D * element size a multiple of 16 bytes.
+ * Positional encodings are the caller's (applied per sequence before packing). */
+MGQA_API mgqa_status masked_gqa_pack_pair(mgqa_dtype dtype, int32_t B, int32_t H, int32_t D,
+                                          const void *a, const int64_t *a_stride, int32_t La,
+                                          const void *b, const int64_t *b_stride, int32_t Lb,
+                                          void *packed, const int64_t *packed_stride,
+                                          int32_t *seg, cudaStream_t stream);
+MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t H, int32_t D,
+                                            const void *packed, const int64_t *packed_stride,
+                                            void *a, const int64_t *a_stride, int32_t La,
+                                            void *b, const int64_t *b_stride, int32_t Lb,
+                                            cudaStream_t stream);
+
 /* Bytes of the fixed device scratch array behind masked_gqa_attn_decode_static
  * (one per GPU that loads the library, kept until the process exits). */
 #define MGQA_DECODE_STATIC_SCRATCH_BYTES (4u << 20)

@@ -30,6 +30,7 @@ __all__ = [
     "masked_gqa_attn_prefill", "masked_gqa_attn_decode",
     "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
     "masked_gqa_attn_decode_static", "DECODE_STATIC_SCRATCH_BYTES",
+    "masked_gqa_attn_decode_append", "masked_gqa_pack_pair", "masked_gqa_unpack_pair",
 ]
 
 MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT = range(5)
@@ -45,6 +46,9 @@ EXPORTED_SYMBOLS = (
     "mgqa_last_error_detail",
     "mgqa_abi_version",
     "masked_gqa_attn_decode_static",
+    "masked_gqa_attn_decode_append",
+    "masked_gqa_pack_pair",
+    "masked_gqa_unpack_pair",
 )
 
 
@@ -97,6 +101,19 @@ def lib() -> ctypes.CDLL:
         L.mgqa_status_string.restype = ctypes.c_char_p
         L.mgqa_last_error_detail.argtypes = []
         L.mgqa_last_error_detail.restype = ctypes.c_char_p
+        L.masked_gqa_attn_decode_append.argtypes = [ctypes.POINTER(MgqaArgs), P, P,
+                                                    ctypes.POINTER(ctypes.c_int64),
+                                                    ctypes.POINTER(ctypes.c_int64), P, P,
+                                                    ctypes.c_size_t, P]
+        L.masked_gqa_attn_decode_append.restype = ctypes.c_int
+        I64P = ctypes.POINTER(ctypes.c_int64)
+        I32 = ctypes.c_int32
+        L.masked_gqa_pack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, I32, P, I64P, I32,
+                                           P, I64P, P, P]
+        L.masked_gqa_pack_pair.restype = ctypes.c_int
+        L.masked_gqa_unpack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, P, I64P, I32,
+                                             P, I64P, I32, P]
+        L.masked_gqa_unpack_pair.restype = ctypes.c_int
         L.masked_gqa_attn_decode_static.argtypes = [ctypes.POINTER(MgqaArgs), P]
         L.masked_gqa_attn_decode_static.restype = ctypes.c_int
         L.mgqa_abi_version.argtypes = []
@@ -249,3 +266,64 @@ def masked_gqa_attn_decode_static(q, k, v, out=None, *, scale=None, mask_bits=No
                   seg_k=seg_k, lse=lse, dev_error=dev_error)
     _check(lib().masked_gqa_attn_decode_static(ctypes.byref(a), _stream_handle(stream)))
     return out
+
+
+def masked_gqa_attn_decode_append(q, k_cache, v_cache, k_new, v_new, kv_len, out=None, *,
+                                  workspace: torch.Tensor, kv_len_out=None, scale=None, lse=None,
+                                  dev_error=None, stream=None):
+    """One decode step fused with its cache append: k_new/v_new [B, Hkv, 1, D]
+    go to slot kv_len[b] of k_cache/v_cache [B, Hkv, Lk, D] (written in place),
+    then q [B, Hq, 1, D] attends over slots 0..kv_len[b]; kv_len_out (int32 [B],
+    optional, not kv_len itself) receives kv_len + 1."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k_cache, v_cache, out, scale=scale, kv_len=kv_len, lse=lse,
+                  dev_error=dev_error)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _dev(t, name, q.dtype)
+        if t.dim() != 4 or t.shape[2] != 1 or t.stride(3) != 1:
+            raise ValueError(f"{name} must be [B, Hkv, 1, D] with a unit-stride head dim")
+    ks = (ctypes.c_int64 * 2)(k_new.stride(0), k_new.stride(1))
+    vs = (ctypes.c_int64 * 2)(v_new.stride(0), v_new.stride(1))
+    _dev(workspace, "workspace")
+    _check(lib().masked_gqa_attn_decode_append(
+        ctypes.byref(a), k_new.data_ptr(), v_new.data_ptr(), ks, vs,
+        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return out
+
+
+def _dtype_code(t):
+    return {torch.bfloat16: MGQA_BF16, torch.float16: MGQA_FP16, torch.float32: MGQA_FP32}[t.dtype]
+
+
+def _st3(t):
+    return (ctypes.c_int64 * 3)(t.stride(0), t.stride(1), t.stride(2))
+
+
+def masked_gqa_pack_pair(a, b, *, stream=None):
+    """Pack two sequences [B, H, La, D] and [B, H, Lb, D] into one block-diagonal
+    row [B, H, La + Lb, D]; returns (packed, seg) with seg int32 [B, La + Lb]
+    (0 for a's positions, 1 for b's) for seg_q / seg_k."""
+    for name, t in (("a", a), ("b", b)):
+        _dev(t, name, a.dtype)
+    B, H, La, D = a.shape
+    Lb = b.shape[2]
+    packed = torch.empty((B, H, La + Lb, D), dtype=a.dtype, device=a.device)
+    seg = torch.empty((B, La + Lb), dtype=torch.int32, device=a.device)
+    _check(lib().masked_gqa_pack_pair(_dtype_code(a), B, H, D, a.data_ptr(), _st3(a), La,
+                                      b.data_ptr(), _st3(b), Lb, packed.data_ptr(),
+                                      _st3(packed), seg.data_ptr(), _stream_handle(stream)))
+    return packed, seg
+
+
+def masked_gqa_unpack_pair(packed, La, *, stream=None):
+    """Split a packed [B, H, La + Lb, D] output into ([B, H, La, D], [B, H, Lb, D])."""
+    _dev(packed, "packed")
+    B, H, L, D = packed.shape
+    a = torch.empty((B, H, La, D), dtype=packed.dtype, device=packed.device)
+    b = torch.empty((B, H, L - La, D), dtype=packed.dtype, device=packed.device)
+    _check(lib().masked_gqa_unpack_pair(_dtype_code(packed), B, H, D, packed.data_ptr(),
+                                        _st3(packed), a.data_ptr(), _st3(a), La, b.data_ptr(),
+                                        _st3(b), L - La, _stream_handle(stream)))
+    return a, b

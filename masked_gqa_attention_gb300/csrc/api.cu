@@ -106,6 +106,35 @@ mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace, size_
   return mgqa::launch_decode(*args, workspace, workspace_bytes, stream);
 }
 
+mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_new,
+                                          const void *v_new, const int64_t *k_new_stride,
+                                          const int64_t *v_new_stride, int32_t *kv_len_out,
+                                          void *workspace, size_t workspace_bytes,
+                                          cudaStream_t stream) {
+  mgqa_status st = mgqa::validate(args, true);
+  if (st != MGQA_OK) return st;
+  if (!args->kv_len) return mgqa::fail(MGQA_ERR_INVALID_ARG, "append needs kv_len");
+  if (args->mask_bits || args->seg_q)
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "append takes the kv_len form only");
+  if (!k_new || !v_new || !k_new_stride || !v_new_stride)
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "append needs k_new, v_new and their strides");
+  const size_t es = args->dtype == MGQA_FP32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
+  for (int t = 0; t < 2; ++t)
+    if (k_new_stride[t] < 0 || v_new_stride[t] < 0 || (k_new_stride[t] * (int64_t)es) % 16 ||
+        (v_new_stride[t] * (int64_t)es) % 16)
+      return mgqa::fail(MGQA_ERR_INVALID_ARG, "k_new / v_new strides must be multiples of 16 bytes");
+  if (kv_len_out && kv_len_out == args->kv_len)
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "kv_len_out must not alias kv_len");
+  if (kv_len_out && (reinterpret_cast<uintptr_t>(kv_len_out) % 4))
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "kv_len_out misaligned");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+    return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
+  return mgqa::launch_decode_append(*args, k_new, v_new, k_new_stride, v_new_stride, kv_len_out,
+                                    workspace, workspace_bytes, stream);
+}
+
 const char *mgqa_status_string(mgqa_status s) {
   switch (s) {
     case MGQA_OK: return "ok";

@@ -43,6 +43,11 @@ struct DecodeParams {
   const uint32_t *bits;
   int64_t ms_b;
   const int32_t *kv_len, *seg_q, *seg_k;
+  // fused append: this step's K/V rows go to slot kv_len[b] first
+  const void *k_new, *v_new;
+  int64_t kn_b, kn_h, vn_b, vn_h;
+  int32_t *kv_len_out;
+  int append;
   float scale_log2;
   float *lse;
   int32_t *err;
@@ -114,7 +119,19 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     const int i = tid + u * kThreads;
     qv[u] = i < NREP * D ? to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]) : 0.f;
   }
-  const int kvl = load_kv_len(p.kv_len, b, p.Lk, p.err, x == 0 && hg == 0 && tid == 0);
+  int kvl = load_kv_len(p.kv_len, b, p.Lk, p.err, x == 0 && hg == 0 && tid == 0);
+  // append: the new row sits at slot `pos`, and the step attends to it too;
+  // a full cache (kv_len == Lk) is an error and appends nothing
+  int pos = -1;
+  if (p.append) {
+    if (kvl < p.Lk) {
+      pos = kvl;
+      kvl += 1;
+    } else if (x == 0 && hg == 0 && tid == 0) {
+      report_error(p.err, MGQA_ERR_INVALID_ARG);
+    }
+    if (p.kv_len_out && x == 0 && hg == 0 && tid == 0) p.kv_len_out[b] = kvl;
+  }
   const int segq = p.seg_q ? __ldg(p.seg_q + b) : 0;
 
   // 1. allowed-slot bitmap of this CTA's chunks (two chunks per pass)
@@ -204,10 +221,15 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       const int kk = idx / PPR, part = idx % PPR;
       const int loc = sm.slot[bs + kk];
       const int64_t j = (int64_t)(x + S * (loc / C)) * C + loc % C;
+      const T *ksrc = kg + j * p.ks_l, *vsrc = vg + j * p.vs_l;
+      if (j == pos) {  // the appended row: read it from the step's input
+        ksrc = static_cast<const T *>(p.k_new) + (int64_t)b * p.kn_b + (int64_t)g * p.kn_h;
+        vsrc = static_cast<const T *>(p.v_new) + (int64_t)b * p.vn_b + (int64_t)g * p.vn_h;
+      }
       cp_async16(reinterpret_cast<char *>(&sm.k[kk][0]) + part * 16,
-                 reinterpret_cast<const char *>(kg + j * p.ks_l) + part * 16);
+                 reinterpret_cast<const char *>(ksrc) + part * 16);
       cp_async16(reinterpret_cast<char *>(&sm.v[kk][0]) + part * 16,
-                 reinterpret_cast<const char *>(vg + j * p.vs_l) + part * 16);
+                 reinterpret_cast<const char *>(vsrc) + part * 16);
     }
     if constexpr (use_mma<T>()) {
       // rows past nb in the last 16-row group feed the P.V MMA with P = 0:
@@ -426,6 +448,25 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     }
   }
 
+  // append: the CTA owning slot pos stores the new row into the cache (once
+  // per KV head: only its first head group); no other CTA of this step reads
+  // that slot from the cache
+  if (pos >= 0 && (pos / C) % S == x && h0 % p.n_rep == 0) {
+    constexpr int PPR = D * sizeof(T) / 16;
+    const char *kn = static_cast<const char *>(p.k_new) +
+                     ((int64_t)b * p.kn_b + (int64_t)g * p.kn_h) * sizeof(T);
+    const char *vn = static_cast<const char *>(p.v_new) +
+                     ((int64_t)b * p.vn_b + (int64_t)g * p.vn_h) * sizeof(T);
+    char *kd = const_cast<char *>(reinterpret_cast<const char *>(kg + (int64_t)pos * p.ks_l));
+    char *vd = const_cast<char *>(reinterpret_cast<const char *>(vg + (int64_t)pos * p.vs_l));
+    for (int part = tid; part < 2 * PPR; part += kThreads) {
+      if (part < PPR)
+        reinterpret_cast<uint4 *>(kd)[part] = reinterpret_cast<const uint4 *>(kn)[part];
+      else
+        reinterpret_cast<uint4 *>(vd)[part - PPR] = reinterpret_cast<const uint4 *>(vn)[part - PPR];
+    }
+  }
+
   // 4. partial of this CTA; the last of the S CTAs merges all of them
   const int64_t hrow0 = ((int64_t)b * p.Hq + h0) * S;  // ws row of (head h0, split 0)
 #pragma unroll
@@ -543,6 +584,12 @@ int decode_heads_per_cta(int n_rep) {
 size_t decode_workspace_bytes(const mgqa_args &a) { return ws_layout(a).total; }
 
 mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s) {
+  return launch_decode_append(a, nullptr, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, s);
+}
+
+mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
+                                 const int64_t *k_new_stride, const int64_t *v_new_stride,
+                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s) {
   const WsLayout L = ws_layout(a);
   if (ws_bytes < L.total) return fail(MGQA_ERR_INVALID_ARG, "decode workspace too small");
   DecodeParams p{};
@@ -561,6 +608,14 @@ mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStr
   p.ws_ml = reinterpret_cast<float2 *>(base + L.ml);
   p.ws_o = reinterpret_cast<float *>(base + L.o);
   p.ws_tick = reinterpret_cast<unsigned *>(base + L.tick);
+  p.append = k_new != nullptr;
+  if (p.append) {
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.kn_b = k_new_stride[0]; p.kn_h = k_new_stride[1];
+    p.vn_b = v_new_stride[0]; p.vn_h = v_new_stride[1];
+    p.kv_len_out = kv_len_out;
+  }
   const int hpc = decode_heads_per_cta(p.n_rep);
   if (a.dtype == MGQA_BF16) {
     if (a.D == 64) return launch_nrep<__nv_bfloat16, 64>(p, hpc, s);

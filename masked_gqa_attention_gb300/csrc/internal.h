@@ -40,6 +40,14 @@ constexpr int kDecodeMaxLk = 32768;
 int decode_heads_per_cta(int n_rep);
 size_t decode_workspace_bytes(const mgqa_args &a);
 mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
+mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
+                                 const int64_t *k_new_stride, const int64_t *v_new_stride,
+                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s);
+
+// Packed-guidance row copies (pack or unpack one pair of sequences).
+mgqa_status pack_pair(bool unpack, mgqa_dtype dt, int B, int H, int D, const void *a,
+                      const int64_t *as, int La, const void *b, const int64_t *bs, int Lb,
+                      const void *packed, const int64_t *ps, int32_t *seg, cudaStream_t s);
 
 // Prefill on the CUDA cores (fp32 I/O).
 mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s);
