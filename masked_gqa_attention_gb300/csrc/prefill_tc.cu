@@ -494,7 +494,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     named_sync(1, Lay::threads);
   };
   if (warp == 0) {
-    if constexpr (NT == 2) tc::regs_dec<88>();
+    if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- TMA producer ----------------
     if (lane == 0 && nk == 0) ok = mbar_wait(bar_q, 0, p.err);  // Q landed before exit
     if (lane == 0 && nk > 0) {
@@ -528,7 +528,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncwarp();
     role_end();
   } else if (warp == 1) {
-    if constexpr (NT == 2) tc::regs_dec<88>();
+    if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- MMA issuer ----------------
     // Issue order: S_t(0) for every head, then per key tile n and head t:
     // O_t += P_t(n) V(n) followed at once by S_t(n+1) = Q_t K(n+1)^T. The
@@ -539,14 +539,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       constexpr bool kBf16 = !__is_same(T, __half);
       constexpr uint32_t id_s = tc::idesc_16bit(BM, BN, 0, 0, kBf16);
       constexpr uint32_t id_pv = tc::idesc_16bit(BM, D, 0, 1, kBf16);
+      // The issuing lane shares its scheduler with two busy softmax warps, so
+      // each MMA costs one descriptor add: a descriptor's address field is
+      // (shared address >> 4) and every buffer lies below 256 KB, so moving
+      // within a buffer is adding (byte offset >> 4) to a base descriptor.
+      const uint64_t qd0 = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024);
+      const uint64_t kd0 = tc::sw128_desc(sm_base + Lay::k_off, 16, 1024);
+      const uint64_t vd0 = tc::sw128_desc(sm_base + Lay::v_off, BOX, 1024);
+      constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
       auto issue_s = [&](int t, int st) {
         const uint32_t d_s = tmem + t * BN;
+        const uint64_t qd = qd0 + (uint64_t)t * kTileStep, kd = kd0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t qa = sm_base + Lay::q_off + (t * KB + kk / 4) * BOX + (kk % 4) * 32;
-          const uint32_t ka = sm_base + Lay::k_off + (st * KB + kk / 4) * BOX + (kk % 4) * 32;
-          tc::mma_ss(d_s, tc::sw128_desc(qa, 16, 1024), tc::sw128_desc(ka, 16, 1024), id_s,
-                     kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
+          tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(bar_sfull + t);
         if (t == NT - 1) tc::mma_commit(bar_kempty + st);
@@ -565,12 +572,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc::fence_after_sync();
           const uint32_t d_o = tmem + NT * BN + t * D;
           const uint32_t a_p = tmem + t * BN;
+          const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint32_t va = sm_base + Lay::v_off + st * KB * BOX + kk * 2048;
-            tc::mma_ts(d_o, a_p + kk * 8, tc::sw128_desc(va, BOX, 1024), id_pv,
+          for (int kk = 0; kk < BN / 16; ++kk)
+            tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
                        (n > 0 || kk > 0) ? 1u : 0u);
-          }
           tc::mma_commit(bar_odone + t);
           if (t == NT - 1) tc::mma_commit(bar_vempty + st);
           if (has_next) {
@@ -592,10 +598,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Lay::tmem_cols);
   } else if (warp < 4) {
-    if constexpr (NT == 2) tc::regs_dec<88>();
+    if constexpr (NT == 2) tc::regs_dec<104>();
     role_end();
   } else {
-    if constexpr (NT == 2) tc::regs_inc<208>();
+    if constexpr (NT == 2) tc::regs_inc<200>();
     // ---------------- softmax warpgroup t ----------------
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
