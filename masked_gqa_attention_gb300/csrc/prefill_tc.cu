@@ -18,8 +18,8 @@
 //   warp 1      : allocates tensor memory; lane 0 issues every MMA
 //   warps 4..   : one softmax warpgroup per query head (thread = query row)
 // With two heads (384 threads, 168 registers each at launch) the first
-// warpgroup gives registers away (88) and the softmax warpgroups take them
-// (208; 88 + 2 x 208 = 3 x 168 per scheduler), enough to hold a whole
+// warpgroup gives registers away (104) and the softmax warpgroups take them
+// (200; 104 + 2 x 200 = 3 x 168 per scheduler), enough to hold a whole
 // 128-column score row per thread.
 // Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
 // P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
@@ -35,7 +35,11 @@
 // completion round trip.
 // Before the pipeline, all warps classify the key tiles of this query tile
 // as empty / full / partial from the mask forms; only non-empty tiles enter
-// the pipeline and only partial tiles pay for per-element masking.
+// the pipeline and only partial tiles pay for per-element masking. Key tile
+// 0 is loaded speculatively together with Q while the classification runs;
+// when the first non-empty tile is another one, the producer lets that load
+// land and reloads stage 0 (the MMA warp then waits for stage 0's second
+// phase).
 // Every wait is bounded (about 2 s) and reports MGQA_ERR_TIMEOUT.
 #include <climits>
 #include <cmath>
@@ -76,7 +80,7 @@ struct Layout {
   static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
-  static constexpr int nk_slot = misc_off + 4;      // int32
+  static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
   static constexpr int seg_slot = misc_off + 8;     // int32 x2 (min, max of seg_q)
   static constexpr int any_off = misc_off + 16;     // uint32[MAXKT/32]: tile has an allowed bit
   static constexpr int all_off = any_off + MAXKT / 8;  // uint32[MAXKT/32]: tile all allowed
@@ -351,7 +355,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   // ---- Q load, segment range of the query tile ----------------------------
   if (tid == 0) {
-    // Q does not depend on the mask: start its load before classifying
+    // Q does not depend on the mask: start its load before classifying, and
+    // key tile 0 with it (most masks keep it; checked after classifying)
     if (row0 < p.Lq) {
       mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
       for (int t = 0; t < NT; ++t)
@@ -359,6 +364,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc::tma_load_4d(smem + Lay::q_off + (t * KB + c) * BOX, &tm_q, c * 64, row0, h0 + t, b,
                           bar_q);
     }
+    mbar_arrive_expect_tx(bar_kfull, KB * BOX);
+    for (int c = 0; c < KB; ++c)
+      tc::tma_load_4d(smem + Lay::k_off + c * BOX, &tm_k, c * 64, 0, g, b, bar_kfull);
+    mbar_arrive_expect_tx(bar_vfull, KB * BOX);
+    for (int c = 0; c < KB; ++c)
+      tc::tma_load_4d(smem + Lay::v_off + c * BOX, &tm_v, c * 64, 0, g, b, bar_vfull);
   }
   if (warp == 0) {
     if (p.mask.seg_q) {
@@ -476,12 +487,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (c != 0) list[pos] = (uint16_t)(kt | (c == 1 ? 0x8000 : 0));
       count += __popc(bal);
     }
-    if (lane == 0) *nk_slot = count;
+    // speculation missed when the first non-empty tile is not tile 0
+    const bool miss = count == 0 || (list[0] & 0x7fff) != 0;
+    if (lane == 0) *nk_slot = count | (miss ? (int)0x80000000 : 0);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const int nk = *nk_slot;
+  const int nk = *nk_slot & 0x7fffffff;
+  const uint32_t spec_miss = (*nk_slot < 0) ? 1u : 0u;  // stage 0 holds a stale tile 0
   const uint32_t tmem = *tmem_slot;
   const uint32_t sm_base = smem_u32(smem);
   bool ok = true;
@@ -496,7 +510,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (warp == 0) {
     if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- TMA producer ----------------
-    if (lane == 0 && nk == 0) ok = mbar_wait(bar_q, 0, p.err);  // Q landed before exit
+    if (lane == 0 && (nk == 0 || spec_miss)) {
+      // every speculative load lands before its stage is reused or the CTA exits
+      ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, 0, p.err) &&
+           mbar_wait(bar_vfull, 0, p.err);
+    }
     if (lane == 0 && nk > 0) {
       // L2 prefetch runs kPrefetch tiles ahead of the loads
       auto prefetch = [&](int n) {
@@ -511,6 +529,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int st = n % STAGES, use = n / STAGES;
         const int kt = list[n] & 0x7fff;
         if (n + kPrefetch < nk) prefetch(n + kPrefetch);
+        if (n == 0 && !spec_miss) continue;  // tile 0 is already on its way
         // K(n) reuses the stage K(n-STAGES) held; it is free once the S MMAs
         // that read it completed (V is released later, after P.V)
         if (n >= STAGES && !(ok = mbar_wait(bar_kempty + st, (use - 1) & 1, p.err))) break;
@@ -558,7 +577,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc::mma_commit(bar_sfull + t);
         if (t == NT - 1) tc::mma_commit(bar_kempty + st);
       };
-      ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, 0, p.err);
+      // After a missed speculation stage 0's first real fill is its phase 1.
+      // A parity wait cannot tell phase 1 done from phase 0 pending, so the
+      // speculative phase 0 is waited for first.
+      auto par = [&](int st, int use) { return (uint32_t)(use + (st == 0 ? spec_miss : 0u)) & 1u; };
+      if (spec_miss) ok = mbar_wait(bar_kfull, 0, p.err) && mbar_wait(bar_vfull, 0, p.err);
+      ok = ok && mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, par(0, 0), p.err);
       tc::fence_after_sync();
       if (ok)
         for (int t = 0; t < NT; ++t) issue_s(t, 0);
@@ -566,7 +590,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int st = n % STAGES, use = n / STAGES;
         const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
-        if (!(ok = mbar_wait(bar_vfull + st, use & 1, p.err))) break;
+        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err))) break;
         for (int t = 0; t < NT && ok; ++t) {
           if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
           tc::fence_after_sync();
@@ -580,7 +604,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tc::mma_commit(bar_odone + t);
           if (t == NT - 1) tc::mma_commit(bar_vempty + st);
           if (has_next) {
-            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, use1 & 1, p.err))) break;
+            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
             tc::fence_after_sync();
             issue_s(t, st1);
           }
