@@ -15,12 +15,13 @@
 // CTA = one 128-row query tile of NT query heads that share one KV head
 // (NT = 2 when Hq/Hkv is even), so each K/V tile is fetched once for both.
 //   warp 0      : TMA producer (Q once, then K and V per key tile, STAGES-deep)
-//   warp 1      : allocates tensor memory; lane 0 issues every MMA
+//   warp 1      : allocates tensor memory; lane 0 issues head 0's MMAs
+//   warp 2      : lane 0 issues head 1's MMAs (NT = 2)
 //   warps 4..   : one softmax warpgroup per query head (thread = query row)
 // With two heads (384 threads, 168 registers each at launch) the first
-// warpgroup gives registers away (104) and the softmax warpgroups take them
-// (200; 104 + 2 x 200 = 3 x 168 per scheduler), enough to hold a whole
-// 128-column score row per thread.
+// warpgroup gives registers away (120) and the softmax warpgroups take them
+// (192; 120 + 2 x 192 = 3 x 168 per scheduler), enough to hold a 64-column
+// half row of scores per thread with room to spare.
 // Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
 // P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
 // the P.V MMA straight from tensor memory.
@@ -31,8 +32,8 @@
 //            -> p_full[t]
 //   MMA:     O_t += P_t V_n               -> o_done[t]; both heads -> kv_empty
 // S_t(n+1) is issued right behind O_t += P_t(n) V(n) (same issuing thread,
-// executed in order), so the tensor pipe never idles waiting for a
-// completion round trip.
+// executed in order), so head t needs no completion round trip between them,
+// and the other head's issuer keeps the tensor pipe fed meanwhile.
 // Before the pipeline, all warps classify the key tiles of this query tile
 // as empty / full / partial from the mask forms; only non-empty tiles enter
 // the pipeline and only partial tiles pay for per-element masking. Key tile
@@ -75,9 +76,9 @@ struct Layout {
   static constexpr int k_off = q_off + NT * KB * BOX;
   static constexpr int v_off = k_off + STAGES * KB * BOX;
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
-  // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
-  // o_done[NT], tok[2] (softmax turn hand-over between the two heads)
-  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2;
+  // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], then per head
+  // and key half: s_full[NT][2], p_full[NT][2], o_done[NT][2]
+  static constexpr int n_bars = 1 + 4 * STAGES + 6 * NT;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
@@ -174,40 +175,41 @@ MGQA_DEV void exp2_poly2(uint64_t y, float &p0, float &p1) {
 // pipe), the rest to the MUFU ex2 unit, so both pipes share the work.
 constexpr int kPolyEvery = 4;
 
-// One 128-key tile of one softmax row (thread = row): the whole score row is
-// read from tensor memory once (four 32-column loads, one wait); its extreme
-// (8 independent accumulators) updates the running max with lazy rescale of O
-// (only when it grows by more than 2^8); P = exp2(s*scale*log2e - m) goes
-// back as bf16 pairs over the first 64 S columns; the row sum is added to l.
+// One 64-key half tile of one softmax row (thread = row): the half row of
+// scores is read from tensor memory once (two 32-column loads, one wait); its
+// extreme updates the running max with lazy rescale of O (only when it grows
+// by more than 2^8; rescale_wait() first waits until every P.V issued before
+// has completed); P = exp2(s*scale*log2e - m) goes back as bf16 pairs over
+// the first 32 columns of the half; the row sum is added to l.
 // NEG: negative scale (the max of scaled scores is the min of raw ones).
-// PARTIAL: mw holds the row's allowed-key bits. The optional hand-over wait
-// (two heads) sits between the load and the exponentials.
-template <typename T, int D, bool NEG, bool PARTIAL, typename Turn>
-MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
-                           float &m_used, float &l, Turn &&take_turn) {
+// PARTIAL: mw0/mw1 hold the row's allowed-key bits for the 64 keys.
+template <typename T, int D, bool NEG, bool PARTIAL, typename Wait>
+MGQA_DEV void softmax_half(uint32_t t_s, uint32_t t_o, uint32_t mw0, uint32_t mw1, float sl2,
+                           float &m_used, float &l, Wait &&rescale_wait) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
-  uint32_t sr[BN];
+  constexpr int HN = BN / 2;
+  const uint32_t mw[2] = {mw0, mw1};
+  uint32_t sr[HN];
   float mr;
   if constexpr (!PARTIAL) {
-    // full tile: the loads also reduce each 32-column piece of the row
-    float red[BN / 32];
+    // full half: the loads also reduce each 32-column piece of the row
+    float red[2];
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c)
+    for (int c = 0; c < 2; ++c)
       tc::tmem_ld32_red<!NEG>(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]),
                               red[c]);
     tc::tmem_wait_ld();
-    mr = NEG ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
-             : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    mr = NEG ? fminf(red[0], red[1]) : fmaxf(red[0], red[1]);
   } else {
 #pragma unroll
-    for (int c = 0; c < BN / 32; ++c)
+    for (int c = 0; c < 2; ++c)
       tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
     tc::tmem_wait_ld();
     float mx[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = MV;
 #pragma unroll
-    for (int j = 0; j < BN; ++j) {
+    for (int j = 0; j < HN; ++j) {
       float a = __uint_as_float(sr[j]);
       if (!((mw[j >> 5] >> (j & 31)) & 1u)) a = MV;
       mx[j & 7] = NEG ? fminf(mx[j & 7], a) : fmaxf(mx[j & 7], a);
@@ -223,7 +225,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
   bool rescale = false;
   float factor = 1.f;
   if (m_used == -INFINITY) {
-    m_used = m_new;
+    m_used = m_new;  // O is still zero (or about to be written afresh)
   } else if (m_new - m_used > 8.f) {
     rescale = true;
     factor = tc::ex2(m_used - m_new);
@@ -231,8 +233,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
     l *= factor;
   }
   if (__any_sync(0xffffffffu, rescale)) {
-    // O holds every P.V issued so far: this tile's S MMA was issued after the
-    // previous tile's P.V, and its completion covers that MMA.
+    rescale_wait();
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -245,13 +246,12 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
     tc::tmem_wait_st();
   }
   const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-  take_turn();
   const uint64_t sl2x2 = tc::pk2(sl2, sl2), nmb2 = tc::pk2(-mb, -mb);
   uint64_t acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = tc::pk2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = 0; c < 2; ++c) {
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -301,10 +301,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_vfull = bars + 1 + STAGES;
   uint64_t *bar_kempty = bars + 1 + 2 * STAGES;
   uint64_t *bar_vempty = bars + 1 + 3 * STAGES;
-  uint64_t *bar_sfull = bars + 1 + 4 * STAGES;
-  uint64_t *bar_pfull = bar_sfull + NT;
-  uint64_t *bar_odone = bar_pfull + NT;
-  uint64_t *bar_tok = bar_odone + NT;  // [0]: head 0 -> head 1, [1]: head 1 -> head 0
+  uint64_t *bar_sfull = bars + 1 + 4 * STAGES;  // [2 t + half]
+  uint64_t *bar_pfull = bar_sfull + 2 * NT;
+  uint64_t *bar_odone = bar_pfull + 2 * NT;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
@@ -327,16 +326,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_kempty + s, 1);
-      mbar_init(bar_vempty + s, 1);
+      mbar_init(bar_kempty + s, NT);  // one commit per MMA issuer
+      mbar_init(bar_vempty + s, NT);
     }
-    for (int t = 0; t < NT; ++t) {
-      mbar_init(bar_sfull + t, 1);
-      mbar_init(bar_pfull + t, 128);
-      mbar_init(bar_odone + t, 1);
+    for (int x = 0; x < 2 * NT; ++x) {
+      mbar_init(bar_sfull + x, 1);
+      mbar_init(bar_pfull + x, 128);
+      mbar_init(bar_odone + x, 1);
     }
-    mbar_init(bar_tok, 128);
-    mbar_init(bar_tok + 1, 128);
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_q);
     tc::prefetch_tensormap(&tm_k);
@@ -508,7 +505,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     named_sync(1, Lay::threads);
   };
   if (warp == 0) {
-    if constexpr (NT == 2) tc::regs_dec<104>();
+    if constexpr (NT == 2) tc::regs_dec<120>();
     // ---------------- TMA producer ----------------
     if (lane == 0 && (nk == 0 || spec_miss)) {
       // every speculative load lands before its stage is reused or the CTA exits
@@ -546,36 +543,52 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncwarp();
     role_end();
-  } else if (warp == 1) {
-    if constexpr (NT == 2) tc::regs_dec<104>();
-    // ---------------- MMA issuer ----------------
-    // Issue order: S_t(0) for every head, then per key tile n and head t:
-    // O_t += P_t(n) V(n) followed at once by S_t(n+1) = Q_t K(n+1)^T. The
-    // tensor pipe executes one thread's MMAs in issue order, so S_t(n+1)
-    // overwrites P_t(n) only after the P.V MMA has consumed it; completion of
-    // S_t(n+1) (s_full) therefore also implies O_t holds P.V up to tile n.
+  } else if (warp == 1 || (NT == 2 && warp == 2)) {
+    if constexpr (NT == 2) tc::regs_dec<120>();
+    // ---------------- MMA issuers: one thread per head ----------------
+    // Lane 0 of warp 1 + t issues head t's MMAs. S_t is computed as two
+    // 64-key halves a and b (separate tensor memory, separate barriers):
+    //   S_t^a(0), S_t^b(0), then per key tile n:
+    //   O_t += P_t^a(n) V^a(n), S_t^a(n+1), O_t += P_t^b(n) V^b(n), S_t^b(n+1)
+    // The tensor pipe executes one thread's MMAs in issue order, so S^x(n+1)
+    // overwrites P^x(n) only after the P.V MMA that reads it. While the
+    // softmax works on one half, the MMAs that refill the other half run,
+    // so neither side waits for a completion round trip of the other.
+    // Stage releases (k_empty, v_empty) count one commit per issuer.
+    const int t = warp - 1;
     if (lane == 0 && nk > 0) {
       constexpr bool kBf16 = !__is_same(T, __half);
-      constexpr uint32_t id_s = tc::idesc_16bit(BM, BN, 0, 0, kBf16);
+      constexpr uint32_t id_s = tc::idesc_16bit(BM, BN / 2, 0, 0, kBf16);
       constexpr uint32_t id_pv = tc::idesc_16bit(BM, D, 0, 1, kBf16);
-      // The issuing lane shares its scheduler with two busy softmax warps, so
-      // each MMA costs one descriptor add: a descriptor's address field is
+      // Each MMA costs one descriptor add: a descriptor's address field is
       // (shared address >> 4) and every buffer lies below 256 KB, so moving
       // within a buffer is adding (byte offset >> 4) to a base descriptor.
-      const uint64_t qd0 = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024);
+      constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
+      constexpr uint64_t kHalfKeys = (uint64_t)(BN / 2 * 128) >> 4;  // 64 key rows of a box
+      const uint64_t qd = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024) + (uint64_t)t * kTileStep;
       const uint64_t kd0 = tc::sw128_desc(sm_base + Lay::k_off, 16, 1024);
       const uint64_t vd0 = tc::sw128_desc(sm_base + Lay::v_off, BOX, 1024);
-      constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
-      auto issue_s = [&](int t, int st) {
-        const uint32_t d_s = tmem + t * BN;
-        const uint64_t qd = qd0 + (uint64_t)t * kTileStep, kd = kd0 + (uint64_t)st * kTileStep;
+      const uint32_t d_s = tmem + t * BN;           // S_t^a | S_t^b; P^x over each half's start
+      const uint32_t d_o = tmem + NT * BN + t * D;  // O_t
+      auto issue_s = [&](int st, int h) {
+        const uint64_t kd = kd0 + (uint64_t)st * kTileStep + (uint64_t)h * kHalfKeys;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
-          tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+          tc::mma_ss(d_s + h * (BN / 2), qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar_sfull + t);
-        if (t == NT - 1) tc::mma_commit(bar_kempty + st);
+        tc::mma_commit(bar_sfull + 2 * t + h);
+        if (h == 1) tc::mma_commit(bar_kempty + st);
+      };
+      auto issue_pv = [&](int st, int h, bool acc0) {
+        const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
+#pragma unroll
+        for (int kk = 0; kk < BN / 32; ++kk)
+          tc::mma_ts(d_o, d_s + h * (BN / 2) + kk * 8,
+                     vd + (uint64_t)((h * (BN / 32) + kk) * 2048 >> 4), id_pv,
+                     (acc0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(bar_odone + 2 * t + h);
+        if (h == 1) tc::mma_commit(bar_vempty + st);
       };
       // After a missed speculation stage 0's first real fill is its phase 1.
       // A parity wait cannot tell phase 1 done from phase 0 pending, so the
@@ -584,31 +597,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (spec_miss) ok = mbar_wait(bar_kfull, 0, p.err) && mbar_wait(bar_vfull, 0, p.err);
       ok = ok && mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, par(0, 0), p.err);
       tc::fence_after_sync();
-      if (ok)
-        for (int t = 0; t < NT; ++t) issue_s(t, 0);
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
-        const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
-        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err))) break;
-        for (int t = 0; t < NT && ok; ++t) {
-          if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
+        const bool has_next = n + 1 < nk;
+        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err) &&
+                   mbar_wait(bar_pfull + 2 * t, n & 1, p.err)))
+          break;
+        tc::fence_after_sync();
+        issue_pv(st, 0, n > 0);
+        if (has_next) {
+          if (!(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
           tc::fence_after_sync();
-          const uint32_t d_o = tmem + NT * BN + t * D;
-          const uint32_t a_p = tmem + t * BN;
-          const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
-                       (n > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(bar_odone + t);
-          if (t == NT - 1) tc::mma_commit(bar_vempty + st);
-          if (has_next) {
-            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
-            tc::fence_after_sync();
-            issue_s(t, st1);
-          }
+          issue_s(st1, 0);
         }
+        if (!(ok = mbar_wait(bar_pfull + 2 * t + 1, n & 1, p.err))) break;
+        tc::fence_after_sync();
+        issue_pv(st, 1, true);
+        if (has_next) issue_s(st1, 1);
       }
       // drain: the last release of every stage has landed before the CTA exits
       for (int s = 0; s < STAGES && s < nk && ok; ++s) {
@@ -619,13 +629,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncwarp();
     role_end();
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, Lay::tmem_cols);
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, Lay::tmem_cols);
+    }
   } else if (warp < 4) {
-    if constexpr (NT == 2) tc::regs_dec<104>();
+    if constexpr (NT == 2) tc::regs_dec<120>();
     role_end();
   } else {
-    if constexpr (NT == 2) tc::regs_inc<200>();
+    if constexpr (NT == 2) tc::regs_inc<192>();
     // ---------------- softmax warpgroup t ----------------
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -646,35 +658,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool partial = (ent & 0x8000) != 0;
       uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
       if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
-      if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
-      __syncwarp();
-      tc::fence_after_sync();
-      // two heads: their exponential passes alternate (head 1 waits for head
-      // 0's pass n, head 0 for head 1's pass n-1), so each one runs while the
-      // tensor core works on the other head
-      auto take_turn = [&]() {
-        if (NT == 2 && ok) {
-          if (t == 1) ok = mbar_wait(bar_tok, n & 1, p.err);
-          else if (n > 0) ok = mbar_wait(bar_tok + 1, (n - 1) & 1, p.err);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        if (ok) ok = mbar_wait(bar_sfull + 2 * t + h, n & 1, p.err);
+        __syncwarp();
+        tc::fence_after_sync();
+        // before O is rescaled every P.V issued so far has completed: for
+        // half a that is O += P^b(n-1) V (and all before it), for half b it
+        // is O += P^a(n) V
+        auto rescale_wait = [&]() {
+          if (h == 0) {
+            if (n > 0 && ok) ok = mbar_wait(bar_odone + 2 * t + 1, (n - 1) & 1, p.err);
+          } else if (ok) {
+            ok = mbar_wait(bar_odone + 2 * t, n & 1, p.err);
+          }
+          __syncwarp();
+          tc::fence_after_sync();
+        };
+        const uint32_t ts = t_s + h * (BN / 2);
+        const uint32_t w0 = h ? mw[2] : mw[0], w1 = h ? mw[3] : mw[1];
+        if (neg) {
+          if (partial) softmax_half<T, D, true, true>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
+          else softmax_half<T, D, true, false>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
+        } else {
+          if (partial) softmax_half<T, D, false, true>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
+          else softmax_half<T, D, false, false>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
         }
-      };
-      if (neg) {
-        if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
-        else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
-      } else {
-        if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l, take_turn);
-        else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l, take_turn);
+        tc::fence_before_sync();
+        mbar_arrive(bar_pfull + 2 * t + h);
       }
-      tc::fence_before_sync();
-      mbar_arrive(bar_pfull + t);
-      if (NT == 2) mbar_arrive(bar_tok + t);
     }
     // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
     // last S MMA completed) in the 128-byte-swizzled box layout, then written
     // by TMA tensor stores (rows past Lq are clipped by the store)
     float o_scale = 0.f;
     if (nk > 0) {
-      if (ok) ok = mbar_wait(bar_odone + t, (nk - 1) & 1, p.err);
+      if (ok) ok = mbar_wait(bar_odone + 2 * t + 1, (nk - 1) & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;
