@@ -15,13 +15,12 @@
 // CTA = one 128-row query tile of NT query heads that share one KV head
 // (NT = 2 when Hq/Hkv is even), so each K/V tile is fetched once for both.
 //   warp 0      : TMA producer (Q once, then K and V per key tile, STAGES-deep)
-//   warp 1      : allocates tensor memory; lane 0 issues head 0's MMAs
-//   warp 2      : lane 0 issues head 1's MMAs (NT = 2)
+//   warp 1      : allocates tensor memory; lane 0 issues every MMA
 //   warps 4..   : one softmax warpgroup per query head (thread = query row)
 // With two heads (384 threads, 168 registers each at launch) the first
-// warpgroup gives registers away (120) and the softmax warpgroups take them
-// (192; 120 + 2 x 192 = 3 x 168 per scheduler), enough to hold a 64-column
-// half row of scores per thread with room to spare.
+// warpgroup gives registers away (104) and the softmax warpgroups take them
+// (200; 104 + 2 x 200 = 3 x 168 per scheduler), enough to hold a whole
+// 128-column score row per thread.
 // Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
 // P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
 // the P.V MMA straight from tensor memory.
@@ -29,11 +28,13 @@
 //   MMA:     S_t = Q_t K_n^T              -> s_full[t]
 //   softmax: mask (partial tiles only), running max with lazy rescale of O_t
 //            (only when the max grows by more than 2^8), P = exp2(x - m)
-//            -> p_full[t]
+//            -> p_full[t]; every exponential is one MUFU ex2 (measured: the
+//            MUFU pass beats moving part of them to an FMA-pipe polynomial,
+//            whose extra instructions cost more issue slots than they save)
 //   MMA:     O_t += P_t V_n               -> o_done[t]; both heads -> kv_empty
 // S_t(n+1) is issued right behind O_t += P_t(n) V(n) (same issuing thread,
-// executed in order), so head t needs no completion round trip between them,
-// and the other head's issuer keeps the tensor pipe fed meanwhile.
+// executed in order), so the tensor pipe never idles waiting for a
+// completion round trip.
 // Before the pipeline, all warps classify the key tiles of this query tile
 // as empty / full / partial from the mask forms; only non-empty tiles enter
 // the pipeline and only partial tiles pay for per-element masking. Key tile
@@ -76,9 +77,9 @@ struct Layout {
   static constexpr int k_off = q_off + NT * KB * BOX;
   static constexpr int v_off = k_off + STAGES * KB * BOX;
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
-  // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], then per head
-  // and key half: s_full[NT][2], p_full[NT][2], o_done[NT][2]
-  static constexpr int n_bars = 1 + 4 * STAGES + 6 * NT;
+  // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
+  // o_done[NT]
+  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
@@ -146,70 +147,39 @@ MGQA_DEV void tile_mask_words(const TcParams &p, int b, int i, bool row_ok, int 
   }
 }
 
-// 2^x for a pair of x <= 8 on the FMA pipe, packed f32x2 arithmetic:
-// x = n + f with n = round(x) (magic-number rounding, 1.5 * 2^23),
-// f in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted by Remez exchange
-// for minimax relative error on that interval (max relative error 7.5e-5, far
-// below bf16's 2^-9); n is added into the exponent field. Inputs below -126
-// are clamped (result ~1e-38 instead of 0).
-MGQA_DEV void exp2_poly2(uint64_t y, float &p0, float &p1) {
-  float y0, y1;
-  tc::upk2(y, y0, y1);
-  const uint64_t yc = tc::pk2(fmaxf(y0, -126.f), fmaxf(y1, -126.f));
-  const uint64_t magic = tc::pk2(12582912.f, 12582912.f);
-  const uint64_t t = tc::add2(yc, magic);
-  const uint64_t nn = tc::add2(t, tc::pk2(-12582912.f, -12582912.f));
-  const uint64_t f = tc::fma2(nn, tc::pk2(-1.f, -1.f), yc);
-  uint64_t q = tc::fma2(f, tc::pk2(0.0551716685f, 0.0551716685f),
-                        tc::pk2(0.2426111251f, 0.2426111251f));
-  q = tc::fma2(q, f, tc::pk2(0.6932609677f, 0.6932609677f));
-  q = tc::fma2(q, f, tc::pk2(0.9999280572f, 0.9999280572f));
-  float q0, q1, t0, t1;
-  tc::upk2(q, q0, q1);
-  tc::upk2(t, t0, t1);
-  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-}
-
-// Every kPolyEvery-th exponential pair of a row goes to exp2_poly2 (FMA
-// pipe), the rest to the MUFU ex2 unit, so both pipes share the work.
-constexpr int kPolyEvery = 4;
-
-// One 64-key half tile of one softmax row (thread = row): the half row of
-// scores is read from tensor memory once (two 32-column loads, one wait); its
-// extreme updates the running max with lazy rescale of O (only when it grows
-// by more than 2^8; rescale_wait() first waits until every P.V issued before
-// has completed); P = exp2(s*scale*log2e - m) goes back as bf16 pairs over
-// the first 32 columns of the half; the row sum is added to l.
+// One 128-key tile of one softmax row (thread = row): the whole score row is
+// read from tensor memory once (four 32-column loads, one wait); its extreme
+// (8 independent accumulators) updates the running max with lazy rescale of O
+// (only when it grows by more than 2^8); P = exp2(s*scale*log2e - m) goes
+// back as bf16 pairs over the first 64 S columns; the row sum is added to l.
 // NEG: negative scale (the max of scaled scores is the min of raw ones).
-// PARTIAL: mw0/mw1 hold the row's allowed-key bits for the 64 keys.
-template <typename T, int D, bool NEG, bool PARTIAL, typename Wait>
-MGQA_DEV void softmax_half(uint32_t t_s, uint32_t t_o, uint32_t mw0, uint32_t mw1, float sl2,
-                           float &m_used, float &l, Wait &&rescale_wait) {
+// PARTIAL: mw holds the row's allowed-key bits.
+template <typename T, int D, bool NEG, bool PARTIAL>
+MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
+                           float &m_used, float &l) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
-  constexpr int HN = BN / 2;
-  const uint32_t mw[2] = {mw0, mw1};
-  uint32_t sr[HN];
+  uint32_t sr[BN];
   float mr;
   if constexpr (!PARTIAL) {
-    // full half: the loads also reduce each 32-column piece of the row
-    float red[2];
+    // full tile: the loads also reduce each 32-column piece of the row
+    float red[BN / 32];
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < BN / 32; ++c)
       tc::tmem_ld32_red<!NEG>(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]),
                               red[c]);
     tc::tmem_wait_ld();
-    mr = NEG ? fminf(red[0], red[1]) : fmaxf(red[0], red[1]);
+    mr = NEG ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
+             : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   } else {
 #pragma unroll
-    for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < BN / 32; ++c)
       tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
     tc::tmem_wait_ld();
     float mx[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = MV;
 #pragma unroll
-    for (int j = 0; j < HN; ++j) {
+    for (int j = 0; j < BN; ++j) {
       float a = __uint_as_float(sr[j]);
       if (!((mw[j >> 5] >> (j & 31)) & 1u)) a = MV;
       mx[j & 7] = NEG ? fminf(mx[j & 7], a) : fmaxf(mx[j & 7], a);
@@ -225,7 +195,7 @@ MGQA_DEV void softmax_half(uint32_t t_s, uint32_t t_o, uint32_t mw0, uint32_t mw
   bool rescale = false;
   float factor = 1.f;
   if (m_used == -INFINITY) {
-    m_used = m_new;  // O is still zero (or about to be written afresh)
+    m_used = m_new;
   } else if (m_new - m_used > 8.f) {
     rescale = true;
     factor = tc::ex2(m_used - m_new);
@@ -233,7 +203,8 @@ MGQA_DEV void softmax_half(uint32_t t_s, uint32_t t_o, uint32_t mw0, uint32_t mw
     l *= factor;
   }
   if (__any_sync(0xffffffffu, rescale)) {
-    rescale_wait();
+    // O holds every P.V issued so far: this tile's S MMA was issued after the
+    // previous tile's P.V, and its completion covers that MMA.
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -251,22 +222,16 @@ MGQA_DEV void softmax_half(uint32_t t_s, uint32_t t_o, uint32_t mw0, uint32_t mw
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = tc::pk2(0.f, 0.f);
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < BN / 32; ++c) {
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int col = c * 32 + 2 * j;
       const uint64_t y =
           tc::fma2(tc::pk2(__uint_as_float(sr[col]), __uint_as_float(sr[col + 1])), sl2x2, nmb2);
-      float p0, p1;
-      if (kPolyEvery > 0 && ((c * 16 + j) % kPolyEvery) == kPolyEvery - 1) {
-        exp2_poly2(y, p0, p1);
-      } else {
-        float y0, y1;
-        tc::upk2(y, y0, y1);
-        p0 = tc::ex2(y0);
-        p1 = tc::ex2(y1);
-      }
+      float y0, y1;
+      tc::upk2(y, y0, y1);
+      float p0 = tc::ex2(y0), p1 = tc::ex2(y1);
       if (PARTIAL) {
         if (!((mw[c] >> (2 * j)) & 1u)) p0 = 0.f;
         if (!((mw[c] >> (2 * j + 1)) & 1u)) p1 = 0.f;
@@ -301,9 +266,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_vfull = bars + 1 + STAGES;
   uint64_t *bar_kempty = bars + 1 + 2 * STAGES;
   uint64_t *bar_vempty = bars + 1 + 3 * STAGES;
-  uint64_t *bar_sfull = bars + 1 + 4 * STAGES;  // [2 t + half]
-  uint64_t *bar_pfull = bar_sfull + 2 * NT;
-  uint64_t *bar_odone = bar_pfull + 2 * NT;
+  uint64_t *bar_sfull = bars + 1 + 4 * STAGES;
+  uint64_t *bar_pfull = bar_sfull + NT;
+  uint64_t *bar_odone = bar_pfull + NT;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
@@ -326,13 +291,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar_kfull + s, 1);
       mbar_init(bar_vfull + s, 1);
-      mbar_init(bar_kempty + s, NT);  // one commit per MMA issuer
-      mbar_init(bar_vempty + s, NT);
+      mbar_init(bar_kempty + s, 1);
+      mbar_init(bar_vempty + s, 1);
     }
-    for (int x = 0; x < 2 * NT; ++x) {
-      mbar_init(bar_sfull + x, 1);
-      mbar_init(bar_pfull + x, 128);
-      mbar_init(bar_odone + x, 1);
+    for (int t = 0; t < NT; ++t) {
+      mbar_init(bar_sfull + t, 1);
+      mbar_init(bar_pfull + t, 128);
+      mbar_init(bar_odone + t, 1);
     }
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_q);
@@ -505,7 +470,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     named_sync(1, Lay::threads);
   };
   if (warp == 0) {
-    if constexpr (NT == 2) tc::regs_dec<120>();
+    if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- TMA producer ----------------
     if (lane == 0 && (nk == 0 || spec_miss)) {
       // every speculative load lands before its stage is reused or the CTA exits
@@ -543,52 +508,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncwarp();
     role_end();
-  } else if (warp == 1 || (NT == 2 && warp == 2)) {
-    if constexpr (NT == 2) tc::regs_dec<120>();
-    // ---------------- MMA issuers: one thread per head ----------------
-    // Lane 0 of warp 1 + t issues head t's MMAs. S_t is computed as two
-    // 64-key halves a and b (separate tensor memory, separate barriers):
-    //   S_t^a(0), S_t^b(0), then per key tile n:
-    //   O_t += P_t^a(n) V^a(n), S_t^a(n+1), O_t += P_t^b(n) V^b(n), S_t^b(n+1)
-    // The tensor pipe executes one thread's MMAs in issue order, so S^x(n+1)
-    // overwrites P^x(n) only after the P.V MMA that reads it. While the
-    // softmax works on one half, the MMAs that refill the other half run,
-    // so neither side waits for a completion round trip of the other.
-    // Stage releases (k_empty, v_empty) count one commit per issuer.
-    const int t = warp - 1;
+  } else if (warp == 1) {
+    if constexpr (NT == 2) tc::regs_dec<104>();
+    // ---------------- MMA issuer ----------------
+    // Issue order: S_t(0) for every head, then per key tile n and head t:
+    // O_t += P_t(n) V(n) followed at once by S_t(n+1) = Q_t K(n+1)^T. The
+    // tensor pipe executes one thread's MMAs in issue order, so S_t(n+1)
+    // overwrites P_t(n) only after the P.V MMA has consumed it; completion of
+    // S_t(n+1) (s_full) therefore also implies O_t holds P.V up to tile n.
     if (lane == 0 && nk > 0) {
       constexpr bool kBf16 = !__is_same(T, __half);
-      constexpr uint32_t id_s = tc::idesc_16bit(BM, BN / 2, 0, 0, kBf16);
+      constexpr uint32_t id_s = tc::idesc_16bit(BM, BN, 0, 0, kBf16);
       constexpr uint32_t id_pv = tc::idesc_16bit(BM, D, 0, 1, kBf16);
-      // Each MMA costs one descriptor add: a descriptor's address field is
+      // The issuing lane shares its scheduler with two busy softmax warps, so
+      // each MMA costs one descriptor add: a descriptor's address field is
       // (shared address >> 4) and every buffer lies below 256 KB, so moving
       // within a buffer is adding (byte offset >> 4) to a base descriptor.
-      constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
-      constexpr uint64_t kHalfKeys = (uint64_t)(BN / 2 * 128) >> 4;  // 64 key rows of a box
-      const uint64_t qd = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024) + (uint64_t)t * kTileStep;
+      const uint64_t qd0 = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024);
       const uint64_t kd0 = tc::sw128_desc(sm_base + Lay::k_off, 16, 1024);
       const uint64_t vd0 = tc::sw128_desc(sm_base + Lay::v_off, BOX, 1024);
-      const uint32_t d_s = tmem + t * BN;           // S_t^a | S_t^b; P^x over each half's start
-      const uint32_t d_o = tmem + NT * BN + t * D;  // O_t
-      auto issue_s = [&](int st, int h) {
-        const uint64_t kd = kd0 + (uint64_t)st * kTileStep + (uint64_t)h * kHalfKeys;
+      constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
+      auto issue_s = [&](int t, int st) {
+        const uint32_t d_s = tmem + t * BN;
+        const uint64_t qd = qd0 + (uint64_t)t * kTileStep, kd = kd0 + (uint64_t)st * kTileStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
-          tc::mma_ss(d_s + h * (BN / 2), qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+          tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar_sfull + 2 * t + h);
-        if (h == 1) tc::mma_commit(bar_kempty + st);
-      };
-      auto issue_pv = [&](int st, int h, bool acc0) {
-        const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
-#pragma unroll
-        for (int kk = 0; kk < BN / 32; ++kk)
-          tc::mma_ts(d_o, d_s + h * (BN / 2) + kk * 8,
-                     vd + (uint64_t)((h * (BN / 32) + kk) * 2048 >> 4), id_pv,
-                     (acc0 || kk > 0) ? 1u : 0u);
-        tc::mma_commit(bar_odone + 2 * t + h);
-        if (h == 1) tc::mma_commit(bar_vempty + st);
+        tc::mma_commit(bar_sfull + t);
+        if (t == NT - 1) tc::mma_commit(bar_kempty + st);
       };
       // After a missed speculation stage 0's first real fill is its phase 1.
       // A parity wait cannot tell phase 1 done from phase 0 pending, so the
@@ -597,28 +546,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (spec_miss) ok = mbar_wait(bar_kfull, 0, p.err) && mbar_wait(bar_vfull, 0, p.err);
       ok = ok && mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, par(0, 0), p.err);
       tc::fence_after_sync();
-      if (ok) {
-        issue_s(0, 0);
-        issue_s(0, 1);
-      }
+      if (ok)
+        for (int t = 0; t < NT; ++t) issue_s(t, 0);
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
-        const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
         const bool has_next = n + 1 < nk;
-        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err) &&
-                   mbar_wait(bar_pfull + 2 * t, n & 1, p.err)))
-          break;
-        tc::fence_after_sync();
-        issue_pv(st, 0, n > 0);
-        if (has_next) {
-          if (!(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
+        const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
+        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err))) break;
+        for (int t = 0; t < NT && ok; ++t) {
+          if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
           tc::fence_after_sync();
-          issue_s(st1, 0);
+          const uint32_t d_o = tmem + NT * BN + t * D;
+          const uint32_t a_p = tmem + t * BN;
+          const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(bar_odone + t);
+          if (t == NT - 1) tc::mma_commit(bar_vempty + st);
+          if (has_next) {
+            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
+            tc::fence_after_sync();
+            issue_s(t, st1);
+          }
         }
-        if (!(ok = mbar_wait(bar_pfull + 2 * t + 1, n & 1, p.err))) break;
-        tc::fence_after_sync();
-        issue_pv(st, 1, true);
-        if (has_next) issue_s(st1, 1);
       }
       // drain: the last release of every stage has landed before the CTA exits
       for (int s = 0; s < STAGES && s < nk && ok; ++s) {
@@ -629,15 +581,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncwarp();
     role_end();
-    if (warp == 1) {
-      tc::fence_after_sync();
-      tc::tmem_dealloc(tmem, Lay::tmem_cols);
-    }
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, Lay::tmem_cols);
   } else if (warp < 4) {
-    if constexpr (NT == 2) tc::regs_dec<120>();
+    if constexpr (NT == 2) tc::regs_dec<104>();
     role_end();
   } else {
-    if constexpr (NT == 2) tc::regs_inc<192>();
+    if constexpr (NT == 2) tc::regs_inc<200>();
     // ---------------- softmax warpgroup t ----------------
     const int t = (warp - 4) >> 2;
     const int quarter = warp & 3;
@@ -658,42 +608,25 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool partial = (ent & 0x8000) != 0;
       uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
       if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (ok) ok = mbar_wait(bar_sfull + 2 * t + h, n & 1, p.err);
-        __syncwarp();
-        tc::fence_after_sync();
-        // before O is rescaled every P.V issued so far has completed: for
-        // half a that is O += P^b(n-1) V (and all before it), for half b it
-        // is O += P^a(n) V
-        auto rescale_wait = [&]() {
-          if (h == 0) {
-            if (n > 0 && ok) ok = mbar_wait(bar_odone + 2 * t + 1, (n - 1) & 1, p.err);
-          } else if (ok) {
-            ok = mbar_wait(bar_odone + 2 * t, n & 1, p.err);
-          }
-          __syncwarp();
-          tc::fence_after_sync();
-        };
-        const uint32_t ts = t_s + h * (BN / 2);
-        const uint32_t w0 = h ? mw[2] : mw[0], w1 = h ? mw[3] : mw[1];
-        if (neg) {
-          if (partial) softmax_half<T, D, true, true>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
-          else softmax_half<T, D, true, false>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
-        } else {
-          if (partial) softmax_half<T, D, false, true>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
-          else softmax_half<T, D, false, false>(ts, t_o, w0, w1, sl2, m_used, l, rescale_wait);
-        }
-        tc::fence_before_sync();
-        mbar_arrive(bar_pfull + 2 * t + h);
+      if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
+      __syncwarp();
+      tc::fence_after_sync();
+      if (neg) {
+        if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l);
+        else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l);
+      } else {
+        if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l);
+        else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l);
       }
+      tc::fence_before_sync();
+      mbar_arrive(bar_pfull + t);
     }
     // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
     // last S MMA completed) in the 128-byte-swizzled box layout, then written
     // by TMA tensor stores (rows past Lq are clipped by the store)
     float o_scale = 0.f;
     if (nk > 0) {
-      if (ok) ok = mbar_wait(bar_odone + 2 * t + 1, (nk - 1) & 1, p.err);
+      if (ok) ok = mbar_wait(bar_odone + t, (nk - 1) & 1, p.err);
       __syncwarp();
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;
