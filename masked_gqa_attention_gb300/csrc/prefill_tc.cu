@@ -516,35 +516,46 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // tensor pipe executes one thread's MMAs in issue order, so S_t(n+1)
     // overwrites P_t(n) only after the P.V MMA has consumed it; completion of
     // S_t(n+1) (s_full) therefore also implies O_t holds P.V up to tile n.
-    if (lane == 0 && nk > 0) {
+    // The whole warp runs the loop (waits, descriptor arithmetic) so every
+    // operand is warp-uniform; one elected lane issues the MMAs and commits.
+    if (nk > 0) {
+      const bool leader = tc::elect_one();
       constexpr bool kBf16 = !__is_same(T, __half);
       constexpr uint32_t id_s = tc::idesc_16bit(BM, BN, 0, 0, kBf16);
       constexpr uint32_t id_pv = tc::idesc_16bit(BM, D, 0, 1, kBf16);
-      // The issuing lane shares its scheduler with two busy softmax warps, so
-      // each MMA costs one descriptor add: a descriptor's address field is
+      // Each MMA costs one descriptor add: a descriptor's address field is
       // (shared address >> 4) and every buffer lies below 256 KB, so moving
       // within a buffer is adding (byte offset >> 4) to a base descriptor.
       const uint64_t qd0 = tc::sw128_desc(sm_base + Lay::q_off, 16, 1024);
       const uint64_t kd0 = tc::sw128_desc(sm_base + Lay::k_off, 16, 1024);
       const uint64_t vd0 = tc::sw128_desc(sm_base + Lay::v_off, BOX, 1024);
       constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
+      // every lane waits; the outcome is made warp-uniform
+      auto wait = [&](uint64_t *bar, uint32_t parity) {
+        const bool r = ok && mbar_wait(bar, parity, p.err);
+        ok = __all_sync(0xffffffffu, r);
+        return ok;
+      };
       auto issue_s = [&](int t, int st) {
         const uint32_t d_s = tmem + t * BN;
         const uint64_t qd = qd0 + (uint64_t)t * kTileStep, kd = kd0 + (uint64_t)st * kTileStep;
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
-          tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
+            tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar_sfull + t);
+          if (t == NT - 1) tc::mma_commit(bar_kempty + st);
         }
-        tc::mma_commit(bar_sfull + t);
-        if (t == NT - 1) tc::mma_commit(bar_kempty + st);
+        __syncwarp();
       };
       // After a missed speculation stage 0's first real fill is its phase 1.
       // A parity wait cannot tell phase 1 done from phase 0 pending, so the
       // speculative phase 0 is waited for first.
       auto par = [&](int st, int use) { return (uint32_t)(use + (st == 0 ? spec_miss : 0u)) & 1u; };
-      if (spec_miss) ok = mbar_wait(bar_kfull, 0, p.err) && mbar_wait(bar_vfull, 0, p.err);
-      ok = ok && mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, par(0, 0), p.err);
+      if (spec_miss) wait(bar_kfull, 0) && wait(bar_vfull, 0);
+      wait(bar_q, 0) && wait(bar_kfull, par(0, 0));
       tc::fence_after_sync();
       if (ok)
         for (int t = 0; t < NT; ++t) issue_s(t, 0);
@@ -552,21 +563,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int st = n % STAGES, use = n / STAGES;
         const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
-        if (!(ok = mbar_wait(bar_vfull + st, par(st, use), p.err))) break;
+        if (!wait(bar_vfull + st, par(st, use))) break;
         for (int t = 0; t < NT && ok; ++t) {
-          if (!(ok = mbar_wait(bar_pfull + t, n & 1, p.err))) break;
+          if (!wait(bar_pfull + t, n & 1)) break;
           tc::fence_after_sync();
           const uint32_t d_o = tmem + NT * BN + t * D;
           const uint32_t a_p = tmem + t * BN;
           const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
-                       (n > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(bar_odone + t);
-          if (t == NT - 1) tc::mma_commit(bar_vempty + st);
+            for (int kk = 0; kk < BN / 16; ++kk)
+              tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
+                         (n > 0 || kk > 0) ? 1u : 0u);
+            if (n == nk - 1) tc::mma_commit(bar_odone + t);  // read by the epilogue only
+            if (t == NT - 1) tc::mma_commit(bar_vempty + st);
+          }
+          __syncwarp();
           if (has_next) {
-            if (t == 0 && !(ok = mbar_wait(bar_kfull + st1, par(st1, use1), p.err))) break;
+            if (t == 0 && !wait(bar_kfull + st1, par(st1, use1))) break;
             tc::fence_after_sync();
             issue_s(t, st1);
           }
@@ -575,8 +589,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // drain: the last release of every stage has landed before the CTA exits
       for (int s = 0; s < STAGES && s < nk && ok; ++s) {
         const int last_use = (nk - 1 - s) / STAGES;
-        ok = mbar_wait(bar_kempty + s, last_use & 1, p.err) &&
-             mbar_wait(bar_vempty + s, last_use & 1, p.err);
+        wait(bar_kempty + s, last_use & 1) && wait(bar_vempty + s, last_use & 1);
       }
     }
     __syncwarp();
@@ -626,7 +639,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // by TMA tensor stores (rows past Lq are clipped by the store)
     float o_scale = 0.f;
     if (nk > 0) {
-      if (ok) ok = mbar_wait(bar_odone + t, (nk - 1) & 1, p.err);
+      if (ok) ok = mbar_wait(bar_odone + t, 0, p.err);  // committed once, after the last P.V
       __syncwarp();
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;

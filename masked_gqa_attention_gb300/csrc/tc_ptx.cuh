@@ -221,6 +221,15 @@ MGQA_DEV void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// One lane of the (fully active) warp, chosen by the hardware.
+MGQA_DEV bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Register reconfiguration for a whole warpgroup (all four warps execute it).
 template <uint32_t N> MGQA_DEV void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
