@@ -58,7 +58,6 @@ constexpr int BM = 128;       // query rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int MAXKT = 2048;   // key tiles per row (Lk <= 262144)
 constexpr int BOX = 16384;    // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
-constexpr int kPrefetch = 4;  // key tiles prefetched into L2 ahead of their load
 
 struct TcParams {
   MaskView mask;
@@ -78,8 +77,8 @@ struct Layout {
   static constexpr int v_off = k_off + STAGES * KB * BOX;
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
   // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
-  // o_done[NT]
-  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT;
+  // o_done[NT], spec (the speculative tile-0 loads have landed)
+  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 1;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
@@ -269,6 +268,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_sfull = bars + 1 + 4 * STAGES;
   uint64_t *bar_pfull = bar_sfull + NT;
   uint64_t *bar_odone = bar_pfull + NT;
+  uint64_t *bar_spec = bar_odone + NT;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
@@ -299,6 +299,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bar_pfull + t, 128);
       mbar_init(bar_odone + t, 1);
     }
+    mbar_init(bar_spec, 1);
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_q);
     tc::prefetch_tensormap(&tm_k);
@@ -476,21 +477,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // every speculative load lands before its stage is reused or the CTA exits
       ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, 0, p.err) &&
            mbar_wait(bar_vfull, 0, p.err);
+      mbar_arrive(bar_spec);  // tells the MMA warp that stage 0 is at its phase 1
     }
     if (lane == 0 && nk > 0) {
-      // L2 prefetch runs kPrefetch tiles ahead of the loads
-      auto prefetch = [&](int n) {
-        const int kt = list[n] & 0x7fff;
-        for (int c = 0; c < KB; ++c) {
-          tc::tma_prefetch_4d(&tm_k, c * 64, kt * BN, g, b);
-          tc::tma_prefetch_4d(&tm_v, c * 64, kt * BN, g, b);
-        }
-      };
-      for (int n = 0; n < nk && n < kPrefetch; ++n) prefetch(n);
+      // (an L2 prefetch of the tiles ahead of their loads measured no faster)
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
         const int kt = list[n] & 0x7fff;
-        if (n + kPrefetch < nk) prefetch(n + kPrefetch);
         if (n == 0 && !spec_miss) continue;  // tile 0 is already on its way
         // K(n) reuses the stage K(n-STAGES) held; it is free once the S MMAs
         // that read it completed (V is released later, after P.V)
@@ -551,10 +544,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
       };
       // After a missed speculation stage 0's first real fill is its phase 1.
-      // A parity wait cannot tell phase 1 done from phase 0 pending, so the
-      // speculative phase 0 is waited for first.
+      // A parity wait cannot tell phase 1 done from phase 0 pending, nor
+      // (waiting late) phase 0 done from phase 2 pending, so the producer's
+      // one-shot spec barrier, raised once it saw phase 0 land, is waited
+      // for first; phase 2 needs this warp's first MMAs, so it cannot pass.
       auto par = [&](int st, int use) { return (uint32_t)(use + (st == 0 ? spec_miss : 0u)) & 1u; };
-      if (spec_miss) wait(bar_kfull, 0) && wait(bar_vfull, 0);
+      if (spec_miss) wait(bar_spec, 0);
       wait(bar_q, 0) && wait(bar_kfull, par(0, 0));
       tc::fence_after_sync();
       if (ok)

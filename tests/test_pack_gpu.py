@@ -40,9 +40,12 @@ def test_packed_guidance_end_to_end(M, oracle_mod):
     qp, seg = M.masked_gqa_pack_pair(qc.cuda(), qu.cuda())
     kp, _ = M.masked_gqa_pack_pair(kc.cuda(), ku.cuda())
     vp, _ = M.masked_gqa_pack_pair(vc.cuda(), vu.cuda())
-    out = M.masked_gqa_attn_prefill(qp, kp, vp, scale=D ** -0.5, seg_q=seg, seg_k=seg)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = M.masked_gqa_attn_prefill(qp, kp, vp, scale=D ** -0.5, seg_q=seg, seg_k=seg,
+                                    dev_error=err)
     oc, ou = M.masked_gqa_unpack_pair(out, 1024)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0, "a bounded wait gave up"
     rc, _, _ = oracle_mod.attention(qc, kc, vc, scale=D ** -0.5)
     ru, _, _ = oracle_mod.attention(qu, ku, vu, scale=D ** -0.5)
     assert_close_to_oracle(oc, rc, torch.bfloat16, "cond block")

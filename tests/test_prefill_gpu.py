@@ -20,13 +20,20 @@ def M():
 
 
 def run_prefill(M, wl, lse=True, err=None, d=None):
+    """Every call carries a device error flag, so a bounded wait that gave up
+    (which would leave stale output behind) fails the test by itself."""
     d = d or to_device(wl)
     out = torch.full_like(d["q"], float("nan"))
     lse_t = torch.empty(d["q"].shape[:3], dtype=torch.float32, device="cuda") if lse else None
+    own = err is None
+    if own:
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
     M.masked_gqa_attn_prefill(d["q"], d["k"], d["v"], out, scale=wl.scale, lse=lse_t,
                               dev_error=err, mask_bits=d["mask_bits"], kv_len=d["kv_len"],
                               seg_q=d["seg_q"], seg_k=d["seg_k"], causal=wl.causal)
     torch.cuda.synchronize()
+    if own:
+        assert int(err.item()) == 0, f"device error {int(err.item())}"
     return out, lse_t
 
 
@@ -84,6 +91,28 @@ def test_packed_guidance_config_and_blocks_alone(M, oracle_mod):
         o2, l2 = run_prefill(M, alone)
         # block boundaries fall on 128-row tiles here, so the bits agree exactly
         assert torch.equal(out[:, :, lo:hi], o2) and torch.equal(lse[:, :, lo:hi], l2)
+
+
+def test_missed_speculation_repeated(M):
+    """Query tiles of the second packed block find key tile 0 empty, so the
+    speculative first load misses and stage 0 runs one phase late. Repeated
+    back-to-back launches (no host sync in between) vary the timing between
+    the producer and the MMA warp: no wait may give up and every run must
+    give the same bits as a run after a full synchronisation."""
+    wl = W.packed_guidance()
+    d = to_device(wl)
+    ref, _ = run_prefill(M, wl, lse=False, d=d)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for _ in range(24):
+        o = torch.empty_like(d["q"])
+        M.masked_gqa_attn_prefill(d["q"], d["k"], d["v"], o, scale=wl.scale, dev_error=err,
+                                  seg_q=d["seg_q"], seg_k=d["seg_k"])
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for o in outs:
+        assert torch.equal(o, ref)
 
 
 def test_dit_batch_config_sampled_rows(M, oracle_mod):
