@@ -197,9 +197,23 @@ MGQA_DEV uint64_t globaltimer_ns() {
 // Bounded wait on an mbarrier phase: gives up after ~`limit_ns` of wall time
 // (measured with the global timer), records MGQA_ERR_TIMEOUT and returns
 // false. Never spins forever.
+// Non-blocking probe of the same phase (cheaper than try_wait when the phase
+// has already completed, the common case on a pipeline's fast path).
+MGQA_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
                         uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
