@@ -126,9 +126,6 @@ MGQA_DEV uint32_t mask_word(const MaskView &m, int b, int i, int jbase, int Lk, 
 MGQA_DEV void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-MGQA_DEV void named_arrive(int id, int nthreads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel in the stream is still
@@ -165,11 +162,6 @@ MGQA_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-MGQA_DEV void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
 
 MGQA_DEV void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
@@ -263,16 +255,6 @@ MGQA_DEV void ldmatrix_x2_trans(uint32_t &b0, uint32_t &b1, const void *row) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
                : "=r"(b0), "=r"(b1)
                : "r"(smem_u32(row)));
-}
-
-// Untiled bulk copy global -> shared (this CTA), completion counted in bytes
-// on `bar`. Both addresses 16-byte aligned, size a multiple of 16.
-MGQA_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
 }
 
 }  // namespace mgqa

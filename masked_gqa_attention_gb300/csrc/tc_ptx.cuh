@@ -39,14 +39,6 @@ MGQA_DEV void tma_store_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-// L2 prefetch of the same 4-D tile (no shared-memory destination).
-MGQA_DEV void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z), "r"(w)
-               : "memory");
-}
-
 MGQA_DEV void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
