@@ -529,17 +529,36 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ok = __all_sync(0xffffffffu, r);
         return ok;
       };
-      auto issue_s = [&](int t, int st) {
+      // S_t = Q_t K(st)^T, k-steps [k0, k1); the commits follow the last one
+      auto issue_s = [&](int t, int st, int k0, int k1) {
         const uint32_t d_s = tmem + t * BN;
         const uint64_t qd = qd0 + (uint64_t)t * kTileStep, kd = kd0 + (uint64_t)st * kTileStep;
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
+            if (kk < k0 || kk >= k1) continue;
             const uint64_t off = (uint64_t)((kk / 4) * BOX + (kk % 4) * 32) >> 4;
             tc::mma_ss(d_s, qd + off, kd + off, id_s, kk > 0 ? 1u : 0u);
           }
-          tc::mma_commit(bar_sfull + t);
-          if (t == NT - 1) tc::mma_commit(bar_kempty + st);
+          if (k1 == D / 16) {
+            tc::mma_commit(bar_sfull + t);
+            if (t == NT - 1) tc::mma_commit(bar_kempty + st);
+          }
+        }
+        __syncwarp();
+      };
+      // O_t += P_t V(st), k-steps [k0, k1)
+      auto issue_pv = [&](int t, int st, int k0, int k1, bool first) {
+        const uint32_t d_o = tmem + NT * BN + t * D;
+        const uint32_t a_p = tmem + t * BN;
+        const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk) {
+            if (kk < k0 || kk >= k1) continue;
+            tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
+                       (!first || kk > 0) ? 1u : 0u);
+          }
         }
         __syncwarp();
       };
@@ -550,34 +569,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // for first; phase 2 needs this warp's first MMAs, so it cannot pass.
       auto par = [&](int st, int use) { return (uint32_t)(use + (st == 0 ? spec_miss : 0u)) & 1u; };
       if (spec_miss) wait(bar_spec, 0);
-      wait(bar_q, 0) && wait(bar_kfull, par(0, 0));
+      wait(bar_q, 0) && wait(bar_kfull, par(0, 0)) && wait(bar_vfull, par(0, 0));
       tc::fence_after_sync();
       if (ok)
-        for (int t = 0; t < NT; ++t) issue_s(t, 0);
+        for (int t = 0; t < NT; ++t) issue_s(t, 0, 0, D / 16);
+      // The MMA queue is shallow: an issuing thread stalls in it until the
+      // pipe has nearly drained, so any wait between two groups of MMAs
+      // leaves the pipe idle. The waits for the next tile's K and V therefore
+      // sit in the middle of a P.V group (its first half still queued), and
+      // head 0's next P is probed in the middle of head 1's S group; only the
+      // P waits that cannot be known early stay between groups.
+      constexpr int kHalfPV = BN / 32, kLateS = D / 16 - 1;
+      bool p0_seen = false;  // P_0(n) already observed complete
       for (int n = 0; n < nk && ok; ++n) {
-        const int st = n % STAGES, use = n / STAGES;
+        const int st = n % STAGES;
         const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
-        if (!wait(bar_vfull + st, par(st, use))) break;
         for (int t = 0; t < NT && ok; ++t) {
-          if (!wait(bar_pfull + t, n & 1)) break;
+          if (!(t == 0 && p0_seen) && !wait(bar_pfull + t, n & 1)) break;
           tc::fence_after_sync();
-          const uint32_t d_o = tmem + NT * BN + t * D;
-          const uint32_t a_p = tmem + t * BN;
-          const uint64_t vd = vd0 + (uint64_t)st * kTileStep;
+          issue_pv(t, st, 0, kHalfPV, n == 0);
+          if (has_next) {  // K(n+1) before head 0's S(n+1), V(n+1) before the next P.V
+            if (t == 0 && !wait(bar_kfull + st1, par(st1, use1))) break;
+            if (t == NT - 1 && !wait(bar_vfull + st1, par(st1, use1))) break;
+            tc::fence_after_sync();
+          }
+          issue_pv(t, st, kHalfPV, BN / 16, n == 0);
           if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              tc::mma_ts(d_o, a_p + kk * 8, vd + (uint64_t)(kk * 2048 >> 4), id_pv,
-                         (n > 0 || kk > 0) ? 1u : 0u);
             if (n == nk - 1) tc::mma_commit(bar_odone + t);  // read by the epilogue only
             if (t == NT - 1) tc::mma_commit(bar_vempty + st);
           }
           __syncwarp();
           if (has_next) {
-            if (t == 0 && !wait(bar_kfull + st1, par(st1, use1))) break;
-            tc::fence_after_sync();
-            issue_s(t, st1);
+            if (NT > 1 && t == NT - 1) {
+              issue_s(t, st1, 0, kLateS);
+              // a probe, not a wait: P_0(n+1) needs the softmax of head 0,
+              // which may still be running
+              p0_seen = __all_sync(0xffffffffu, mbar_test_wait(bar_pfull, (n + 1) & 1));
+              issue_s(t, st1, kLateS, D / 16);
+            } else {
+              issue_s(t, st1, 0, D / 16);
+            }
           }
         }
       }
