@@ -578,15 +578,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // leaves the pipe idle. The waits for the next tile's K and V therefore
       // sit in the middle of a P.V group (its first half still queued), and
       // head 0's next P is probed in the middle of head 1's S group; only the
-      // P waits that cannot be known early stay between groups.
+      // P waits that cannot be known early stay between groups; head 1's P is
+      // likewise probed before the last MMA of head 0's S group.
       constexpr int kHalfPV = BN / 32, kLateS = D / 16 - 1;
       bool p0_seen = false;  // P_0(n) already observed complete
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES;
         const bool has_next = n + 1 < nk;
         const int st1 = (n + 1) % STAGES, use1 = (n + 1) / STAGES;
+        bool p1_seen = false;  // P_1(n) already observed complete
         for (int t = 0; t < NT && ok; ++t) {
-          if (!(t == 0 && p0_seen) && !wait(bar_pfull + t, n & 1)) break;
+          if (!(t == 0 ? p0_seen : p1_seen) && !wait(bar_pfull + t, n & 1)) break;
           tc::fence_after_sync();
           issue_pv(t, st, 0, kHalfPV, n == 0);
           if (has_next) {  // K(n+1) before head 0's S(n+1), V(n+1) before the next P.V
@@ -606,6 +608,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               // a probe, not a wait: P_0(n+1) needs the softmax of head 0,
               // which may still be running
               p0_seen = __all_sync(0xffffffffu, mbar_test_wait(bar_pfull, (n + 1) & 1));
+              issue_s(t, st1, kLateS, D / 16);
+            } else if (NT > 1) {
+              issue_s(t, st1, 0, kLateS);
+              p1_seen = __all_sync(0xffffffffu, mbar_test_wait(bar_pfull + 1, n & 1));
               issue_s(t, st1, kLateS, D / 16);
             } else {
               issue_s(t, st1, 0, D / 16);
