@@ -1,5 +1,5 @@
-// Full-sequence masked GQA attention on the tensor cores (bf16 in, fp32
-// accumulation): TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating in tensor
+// Full-sequence masked GQA attention on the tensor cores (bf16 or fp16 in,
+// fp32 accumulation): TMA-staged Q/K/V tiles, tcgen05 MMAs accumulating in tensor
 // memory, a warp-specialised load / MMA / softmax pipeline, and whole-tile
 // skipping wherever the mask leaves a 128x128 (query, key) tile empty.
 //
@@ -15,14 +15,15 @@
 // CTA = one 128-row query tile of NT query heads that share one KV head
 // (NT = 2 when Hq/Hkv is even), so each K/V tile is fetched once for both.
 //   warp 0      : TMA producer (Q once, then K and V per key tile, STAGES-deep)
-//   warp 1      : allocates tensor memory; lane 0 issues every MMA
+//   warp 1      : allocates tensor memory and runs the MMA loop; one elected
+//                 lane issues every MMA
 //   warps 4..   : one softmax warpgroup per query head (thread = query row)
 // With two heads (384 threads, 168 registers each at launch) the first
 // warpgroup gives registers away (104) and the softmax warpgroups take them
 // (200; 104 + 2 x 200 = 3 x 168 per scheduler), enough to hold a whole
 // 128-column score row per thread.
 // Tensor memory: S_t (128 fp32 columns) and O_t (D fp32 columns) per head;
-// P_t (bf16) overwrites the first 64 columns of S_t and is the A operand of
+// P_t (16-bit) overwrites the first 64 columns of S_t and is the A operand of
 // the P.V MMA straight from tensor memory.
 // Per key tile n and head t:
 //   MMA:     S_t = Q_t K_n^T              -> s_full[t]
@@ -31,17 +32,19 @@
 //            -> p_full[t]; every exponential is one MUFU ex2 (measured: the
 //            MUFU pass beats moving part of them to an FMA-pipe polynomial,
 //            whose extra instructions cost more issue slots than they save)
-//   MMA:     O_t += P_t V_n               -> o_done[t]; both heads -> kv_empty
+//   MMA:     O_t += P_t V_n               -> v_empty after both heads;
+//                                             o_done[t] after the last tile
 // S_t(n+1) is issued right behind O_t += P_t(n) V(n) (same issuing thread,
-// executed in order), so the tensor pipe never idles waiting for a
-// completion round trip.
+// executed in order), so head t needs no completion round trip between
+// them; the waits for the next tile's K and V sit inside P.V groups and the
+// P waits are probed ahead, so few waits fall between groups of MMAs.
 // Before the pipeline, all warps classify the key tiles of this query tile
 // as empty / full / partial from the mask forms; only non-empty tiles enter
 // the pipeline and only partial tiles pay for per-element masking. Key tile
 // 0 is loaded speculatively together with Q while the classification runs;
 // when the first non-empty tile is another one, the producer lets that load
-// land and reloads stage 0 (the MMA warp then waits for stage 0's second
-// phase).
+// land, raises a one-shot barrier and reloads stage 0 (the MMA warp waits
+// for that barrier, then for stage 0's second phase).
 // Every wait is bounded (about 2 s) and reports MGQA_ERR_TIMEOUT.
 #include <climits>
 #include <cmath>
