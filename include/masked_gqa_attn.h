@@ -107,11 +107,11 @@ typedef struct mgqa_args {
   int32_t causal;               /* nonzero: add the causal form to the mask */
 } mgqa_args;
 
-/* Full-sequence (prefill) attention: bidirectional, any of the mask forms.
- * bf16 runs on the tensor cores (TMA-fed tcgen05 MMAs accumulating in tensor
- * memory) and skips every 128x128 (query, key) tile the mask leaves empty;
- * fp32 runs on the CUDA cores. Lq, Lk >= 1. Returns MGQA_OK once the kernel is
- * enqueued. */
+/* Full-sequence (prefill) attention: bidirectional unless `causal` is set,
+ * any of the mask forms. bf16 and fp16 run on the tensor cores (TMA-fed
+ * tcgen05 MMAs accumulating in tensor memory) and skip every 128x128 (query,
+ * key) tile the mask leaves empty; fp32 runs on the CUDA cores. Lq, Lk >= 1.
+ * Returns MGQA_OK once the kernel is enqueued. */
 MGQA_API mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream);
 
 /* Bytes of device workspace masked_gqa_attn_decode needs for these arguments
