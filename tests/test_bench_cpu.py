@@ -1,0 +1,97 @@
+"""Host-side pieces of the benchmark and the workload generators, checked
+without a GPU: the algorithmic work each metric divides by, the seeded
+inputs, the peak fallback and the profile lookup that feeds `traffic`."""
+import hashlib
+import importlib.util
+import os
+
+import pytest
+import torch
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_padded_cfg_flops_closed_form():
+    # rows of 1024 and 384 valid keys, every query row attends to all of them:
+    # 4 * D * Hq * Lq * (1024 + 384)
+    wl = W.padded_cfg(variant="bits")
+    assert wl.flops() == 4.0 * 128 * 16 * 1024 * (1024 + 384)
+    # 384 = 3 x 128: the non-empty 128 x 128 tiles hold exactly the allowed pairs
+    assert wl.nonempty_tile_flops() == wl.flops()
+    assert W.padded_cfg(variant="kvlen").flops() == wl.flops()
+
+
+def test_packed_guidance_flops_closed_form():
+    wl = W.packed_guidance()
+    assert wl.flops() == 4.0 * 128 * 16 * (1024 * 1024 + 384 * 384)
+
+
+def test_seeded_inputs_are_reproducible():
+    a, b = W.padded_cfg(variant="bits"), W.padded_cfg(variant="bits")
+    for n in ("q", "k", "v", "mask_bits"):
+        assert torch.equal(getattr(a, n), getattr(b, n))
+    c = W.padded_cfg(seed=7, variant="bits")
+    assert not torch.equal(a.q, c.q)
+
+
+def test_decode_needed_bytes_counts_filled_rows_only(bench):
+    wl = W.static_cache_decode(variant="span")
+    B, Hq, Hkv, Lq, Lk, D = wl.shape
+    filled = int(wl.kv_len.sum())
+    expect = filled * Hkv * D * 2 * 2 + 2 * B * Hq * D * 2
+    assert bench.decode_needed_bytes(wl) == expect
+    full = W.static_cache_decode(variant="full")
+    # the bitmask form also reads one bit per cache slot
+    assert bench.decode_needed_bytes(full) == expect + B * (Lk // 32) * 4
+
+
+def test_peak_fallback_when_not_measured(bench, tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    d, kind = bench.peaks()
+    assert kind == "fallback"
+    assert d["hbm_gbs"] == 6800.0 and d["bf16_tflops"] == 1900.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"gpu": {"hbm_gbs": 7000.5, "bf16_tflops": 1888}}')
+    d, kind = bench.peaks()
+    assert kind == "measured"
+    assert bench.peak_value(d, "hbm_gbs") == 7000.5
+    assert bench.peak_value(d, "bf16_tflops") == 1888.0
+
+
+def test_traffic_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
+    src_dir = tmp_path / "masked_gqa_attention_gb300" / "csrc"
+    src_dir.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = src_dir / "k.cu"
+    src.write_text("// kernel v1\n")
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    (tmp_path / "profiles" / "k.md").write_text(f"notes\n\ntraffic: 123456 source-sha256: {sha} k.cu\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_from_profiles("k.cu") == 123456.0
+    src.write_text("// kernel v2\n")  # the kernel changed since the capture
+    assert bench.traffic_from_profiles("k.cu") is None
+    assert bench.traffic_from_profiles("missing.cu") is None
+
+
+def test_committed_profiles_name_their_sources():
+    # every traffic line names a kernel file that exists and a 16-hex hash
+    lines = []
+    for f in os.listdir(os.path.join(ROOT, "profiles")):
+        for line in open(os.path.join(ROOT, "profiles", f)):
+            if line.startswith("traffic:"):
+                lines.append(line.split())
+    assert lines, "no traffic line in profiles/"
+    for parts in lines:
+        assert float(parts[1]) > 0
+        assert parts[2] == "source-sha256:" and len(parts[3]) == 16
+        int(parts[3], 16)
+        assert os.path.exists(os.path.join(ROOT, "masked_gqa_attention_gb300", "csrc", parts[4]))
