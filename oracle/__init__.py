@@ -16,7 +16,11 @@ arrays. What it computes, with the passages it follows:
 * OmniVoice page, "Memory & speed", packed_guidance paragraph: a
   block-diagonal mask, each block equal to its run alone;
 * VoxCPM page, "Upstream-identical practice", attention bullet: causal
-  attention at prefill (query rows = the last Lq of the Lk positions).
+  attention at prefill (query rows = the last Lq of the Lk positions);
+* rotary position embedding (``rope``): F5-TTS page (interleaved pairs, on
+  the first pe_attn_head heads), Qwen3-TTS and VoxCPM pages (fp32 inverse
+  frequencies, LongRoPE tables built in fp32), OmniVoice page, packed_guidance
+  paragraph (positions restart per packed sequence).
 
 Readings where the pages are silent (each also listed in the design notes):
 query head h reads KV head ``h // (Hq // Hkv)``; mask ``True`` means "may
@@ -64,6 +68,9 @@ def _load():
             f.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, P, I,
                           ctypes.c_double, P, P, I]
             f.restype = I
+            g = lib.mgqa_oracle_rope
+            g.argtypes = [P, I, I, I, I, P, P, I, I, I]
+            g.restype = I
             _lib = lib
     return _lib
 
@@ -133,3 +140,31 @@ def attention(q, k, v, *, scale: float, mask_bits=None, kv_len=None,
     if used < 0:
         raise ValueError("oracle rejected the shapes")
     return out, lse, used
+
+
+def rope(x, *, inv_freq, positions=None, rot_dim=None, heads=None, interleaved=False):
+    """Rotary position embedding in fp64 (see mgqa_oracle_rope in the C file).
+
+    x: [B, H, L, D] (any float type, widened exactly); inv_freq: [rot_dim/2]
+    fp32; positions: int32 [B, L] or None (position = row index); rot_dim:
+    rotated features per head (default D); heads: rotated heads (default H).
+    Returns the rotated copy as fp64.
+    """
+    x64 = _f64(x).copy()
+    B, H, L, D = x64.shape
+    rot_dim = D if rot_dim is None else int(rot_dim)
+    heads = H if heads is None else int(heads)
+    f = inv_freq.detach().cpu().numpy() if hasattr(inv_freq, "detach") else inv_freq
+    f = np.ascontiguousarray(np.asarray(f), dtype=np.float32)
+    if f.shape != (rot_dim // 2,):
+        raise ValueError(f"inv_freq must be [{rot_dim // 2}] fp32")
+    pos = _i32(positions)
+    if pos is not None and pos.shape != (B, L):
+        raise ValueError("positions must be [B, L] int32")
+    rc = _load().mgqa_oracle_rope(
+        x64.ctypes.data_as(ctypes.c_void_p), B, H, L, D,
+        None if pos is None else pos.ctypes.data_as(ctypes.c_void_p),
+        f.ctypes.data_as(ctypes.c_void_p), rot_dim, heads, int(bool(interleaved)))
+    if rc != 0:
+        raise ValueError("oracle rejected the rope arguments")
+    return x64

@@ -39,6 +39,9 @@
  *
  * Layout: q [B][Hq][Lq][D], k and v [B][Hkv][Lk][D], out [B][Hq][Lq][D],
  * lse [B][Hq][Lq], all contiguous fp64.
+ *
+ * The file also holds mgqa_oracle_rope (rotary position embedding), defined
+ * and cited where it is written, below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -132,4 +135,48 @@ int mgqa_oracle_attention(const double *q, const double *k, const double *v,
         free(acc);
     }
     return used;
+}
+
+/*
+ * Rotary position embedding (RoPE), in place on x [B][H][L][D] (fp64 values
+ * of the 16- or 32-bit input):
+ *   - F5-TTS page, module table and "Upstream-identical practice": the DiT
+ *     rotates interleaved feature pairs, on its first pe_attn_head heads only;
+ *   - Qwen3-TTS / VoxCPM pages: the language models rotate with an fp32
+ *     inverse-frequency table (LongRoPE: a table built in fp32);
+ *   - OmniVoice page, "Memory & speed", packed_guidance paragraph: under
+ *     packing every sequence's positions start at 0 (so positions are an
+ *     input, not the row index).
+ * For batch b, head h < heads, position index l, pair i < rot_dim/2:
+ *   theta = fl32( (float)pos[b,l] * inv_freq[i] )      (one fp32 product)
+ *   (a, c) = (x[.., e0], x[.., e1]) with (e0, e1) = (2i, 2i+1) if interleaved,
+ *                                                   (i, i + rot_dim/2) otherwise
+ *   x[.., e0] = a cos(theta) - c sin(theta);  x[.., e1] = a sin(theta) + c cos(theta)
+ * cos and sin of theta in fp64. Features >= rot_dim and heads >= `heads` are
+ * untouched. positions == NULL means pos[b,l] = l. Returns 0, or -1 on bad
+ * sizes.
+ */
+int mgqa_oracle_rope(double *x, int B, int H, int L, int D, const int32_t *positions,
+                     const float *inv_freq, int rot_dim, int heads, int interleaved) {
+    if (B < 0 || H <= 0 || L < 0 || D <= 0 || rot_dim < 0 || rot_dim > D || (rot_dim & 1) ||
+        heads < 0 || heads > H)
+        return -1;
+    const int half = rot_dim / 2;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < heads; ++h)
+            for (int l = 0; l < L; ++l) {
+                const int32_t p = positions ? positions[(long)b * L + l] : l;
+                double *row = x + (((long)b * H + h) * L + l) * D;
+                for (int i = 0; i < half; ++i) {
+                    volatile float theta = (float)p * inv_freq[i];
+                    const double t = (double)theta;
+                    const double cs = cos(t), sn = sin(t);
+                    const int e0 = interleaved ? 2 * i : i;
+                    const int e1 = interleaved ? 2 * i + 1 : i + half;
+                    const double a = row[e0], c = row[e1];
+                    row[e0] = a * cs - c * sn;
+                    row[e1] = a * sn + c * cs;
+                }
+            }
+    return 0;
 }

@@ -281,3 +281,107 @@ def test_causal_first_row_and_single_query(oracle_mod):
     o1, l1, _ = oracle_mod.attention(q[:, :, -1:], k, v, scale=0.7, causal=True)
     o2, l2, _ = oracle_mod.attention(q[:, :, -1:], k, v, scale=0.7)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ---- rotary position embedding (F5-TTS page: interleaved pairs on the first
+# pe_attn_head heads; Qwen3-TTS / VoxCPM pages: fp32 inverse frequencies;
+# OmniVoice page, packed_guidance: positions restart per packed sequence) ----
+
+def _rope_inputs(seed, B=2, H=3, L=5, D=8):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(B, H, L, D, generator=g, dtype=torch.float64).numpy()
+
+
+def test_rope_hand_worked_pairs(oracle_mod):
+    # interleaved: (x0, x1) rotates by pos * f0, (x2, x3) by pos * f1
+    x = np.array([[[[1.0, 0.0, 0.0, 1.0]]]])
+    f = np.array([1.0, 0.5], np.float32)
+    y = oracle_mod.rope(x, inv_freq=f, positions=np.array([[1]], np.int32), interleaved=True)
+    assert np.allclose(y[0, 0, 0], [math.cos(1), math.sin(1), -math.sin(0.5), math.cos(0.5)],
+                       rtol=0, atol=1e-15)
+    # half-split: (x0, x2) rotates by f0, (x1, x3) by f1
+    y = oracle_mod.rope(x, inv_freq=f, positions=np.array([[1]], np.int32), interleaved=False)
+    assert np.allclose(y[0, 0, 0], [math.cos(1), -math.sin(0.5), math.sin(1), math.cos(0.5)],
+                       rtol=0, atol=1e-15)
+
+
+def test_rope_position_zero_is_identity(oracle_mod):
+    x = _rope_inputs(1)
+    f = (10000.0 ** (-np.arange(0, 8, 2) / 8)).astype(np.float32)
+    y = oracle_mod.rope(x, inv_freq=f, positions=np.zeros((2, 5), np.int32))
+    assert np.array_equal(y, x)
+
+
+def test_rope_quarter_turn(oracle_mod):
+    # angle fl32(pi/2): (a, c) -> (-c, a) up to the 4.4e-8 rounding of pi/2
+    x = _rope_inputs(2, D=2)
+    y = oracle_mod.rope(x, inv_freq=np.array([np.float32(math.pi / 2)]),
+                        positions=np.ones((2, 5), np.int32), interleaved=True)
+    assert np.allclose(y[..., 0], -x[..., 1], atol=1e-7) and np.allclose(y[..., 1], x[..., 0], atol=1e-7)
+
+
+@pytest.mark.parametrize("interleaved", [True, False])
+def test_rope_keeps_pair_norms(oracle_mod, interleaved):
+    x = _rope_inputs(3)
+    f = (10000.0 ** (-np.arange(0, 8, 2) / 8)).astype(np.float32)
+    pos = np.array([[0, 7, 100, 4095, 8191], [3, 1, 2, 5, 9]], np.int32)
+    y = oracle_mod.rope(x, inv_freq=f, positions=pos, interleaved=interleaved)
+    if interleaved:
+        n0, n1 = x[..., 0::2] ** 2 + x[..., 1::2] ** 2, y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    else:
+        n0, n1 = x[..., :4] ** 2 + x[..., 4:] ** 2, y[..., :4] ** 2 + y[..., 4:] ** 2
+    assert np.allclose(n1, n0, rtol=1e-13, atol=0)
+    assert not np.allclose(y, x)
+
+
+def test_rope_layouts_are_one_permutation(oracle_mod):
+    # interleaved pairs (2i, 2i+1) are half-split pairs (i, i + r/2) of the
+    # feature-permuted vector
+    x = _rope_inputs(4)
+    f = np.array([0.9, 0.3, 0.05, 0.001], np.float32)
+    pos = np.array([[0, 1, 2, 30, 500], [5, 4, 3, 2, 1]], np.int32)
+    perm = np.array([0, 2, 4, 6, 1, 3, 5, 7])  # interleaved index of half-split slot
+    yi = oracle_mod.rope(x, inv_freq=f, positions=pos, interleaved=True)
+    yh = oracle_mod.rope(np.ascontiguousarray(x[..., perm]), inv_freq=f, positions=pos,
+                         interleaved=False)
+    assert np.array_equal(yi[..., perm], yh)
+
+
+def test_rope_partial_dims_and_heads(oracle_mod):
+    x = _rope_inputs(5, H=4, D=8)
+    f = np.array([0.5, 0.25], np.float32)
+    y = oracle_mod.rope(x, inv_freq=f, rot_dim=4, heads=1, interleaved=True)
+    assert np.array_equal(y[:, 1:], x[:, 1:])           # heads past `heads` untouched
+    assert np.array_equal(y[:, :1, :, 4:], x[:, :1, :, 4:])  # features past rot_dim untouched
+    assert not np.array_equal(y[:, :1, 1:, :4], x[:, :1, 1:, :4])
+    # positions default to the row index
+    pos = np.tile(np.arange(5, dtype=np.int32), (2, 1))
+    y2 = oracle_mod.rope(x, inv_freq=f, rot_dim=4, heads=1, interleaved=True, positions=pos)
+    assert np.array_equal(y, y2)
+
+
+def test_rope_angles_add_and_scores_see_only_offsets(oracle_mod):
+    # power-of-two frequencies make every fp32 angle exact, so rotations
+    # compose (R(p) R(q) = R(p + q)) and q.k after rotation depends only on
+    # the position difference
+    x = _rope_inputs(6, B=1, H=1, L=1, D=8)
+    k = _rope_inputs(7, B=1, H=1, L=1, D=8)
+    f = np.array([1.0, 0.5, 0.125, 2 ** -10], np.float32)
+
+    def rot(v, p):
+        return oracle_mod.rope(v, inv_freq=f, positions=np.array([[p]], np.int32), interleaved=False)
+    assert np.allclose(rot(rot(x, 37), 1000), rot(x, 1037), rtol=0, atol=1e-12)
+    s1 = float((rot(x, 50) * rot(k, 20)).sum())
+    s2 = float((rot(x, 1050) * rot(k, 1020)).sum())
+    assert abs(s1 - s2) < 1e-12 and abs(s1 - float((x * k).sum())) > 1e-3
+
+
+def test_rope_angle_is_the_fp32_product(oracle_mod):
+    # theta = fl32(pos * f): with f = fl32(0.1) and pos = 3 the product rounds
+    # to a different float than 3 * 0.1 in fp64
+    f = np.float32(0.1)
+    theta32 = float(np.float32(np.float32(3) * f))
+    assert theta32 != 3 * float(f)
+    x = np.array([[[[1.0, 0.0]]]])
+    y = oracle_mod.rope(x, inv_freq=np.array([f]), positions=np.array([[3]], np.int32))
+    assert y[0, 0, 0, 0] == math.cos(theta32) and y[0, 0, 0, 1] == math.sin(theta32)
