@@ -13,8 +13,9 @@ captured once in a CUDA graph and replayed.
 Also measured in the same run and reported under "decode" and
 "other_workloads": static-cache decode (8 requests, 16/2 heads, dim 64,
 8192-slot cache, filled 256..3100, 16 rotating cache sets of 33.5 MB),
-packed-guidance prefill (one 1408-position row, segments 1024 + 384), and the
-DiT batch (32 rows x 4096 positions, 1..6 segments per row).
+packed-guidance prefill (one 1408-position row, segments 1024 + 384), the
+DiT batch (32 rows x 4096 positions, 1..6 segments per row), and the rotary
+position embedding of the headline's q and k (12 rotating sets, 144 MB).
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of the same workload (the baseline arm).
@@ -251,6 +252,45 @@ def bench_prefill_e2e(M, wl, dev, calls, steps, warmup, world):
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
+def bench_rope(M, dev, reps=20, warmup=3, nsets=12):
+    """Rotary embedding of the headline shapes' q [2,16,1024,128] and
+    k [2,8,1024,128] (bf16, full rotary dim, positions = row index); one call =
+    q then k of one of `nsets` rotating sets. One pass over the sets is
+    captured in a CUDA graph (no host launch cost in the timed region) and
+    replayed. Returns (seconds per call, algorithmic bytes per call: every
+    rotated element read and written, plus the frequency table)."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(1006)
+    sets = [(torch.randn(2, 16, 1024, 128, generator=g).to(torch.bfloat16).to(dev),
+             torch.randn(2, 8, 1024, 128, generator=g).to(torch.bfloat16).to(dev)) for _ in range(nsets)]
+    f = (10000.0 ** (-torch.arange(0, 128, 2, dtype=torch.float64) / 128)).to(torch.float32).to(dev)
+
+    def one_pass():
+        for q, k in sets:
+            M.masked_gqa_rope(q, f)
+            M.masked_gqa_rope(k, f)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        one_pass()  # warm-up and lazy set-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        one_pass()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    q, k = sets[0]
+    nbytes = 2 * (q.numel() + k.numel()) * q.element_size() + f.numel() * 4
+    return e0.elapsed_time(e1) / 1e3 / (reps * nsets), nbytes
+
+
 def decode_needed_bytes(wl):
     B, Hq, Hkv, Lq, Lk, D = wl.shape
     es = wl.k.element_size()
@@ -464,6 +504,11 @@ def run_gpu(args):
                         "nonempty_tile_TFLOP_s": wo.nonempty_tile_flops() / pc / 1e12,
                         "frac_nonempty_of_peak": wo.nonempty_tile_flops() / pc / 1e12 / bf16}
         del wo
+    t_rope, b_rope = bench_rope(M, dev)
+    others["rope"] = {"workload": "rotary embedding of q [2,16,1024,128] and k [2,8,1024,128], "
+                                  "bf16, 12 rotating sets (144 MB > L2)",
+                      "us_per_call": t_rope * 1e6, "bytes_per_call": b_rope,
+                      "GB_s": b_rope / t_rope / 1e9, "frac_of_hbm": b_rope / t_rope / 1e9 / hbm}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,

@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MGQA_ABI_VERSION 2
+#define MGQA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define MGQA_API __attribute__((visibility("default")))
@@ -193,6 +193,41 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
  * executions overlap on the GPU -- different streams, or different host
  * threads -- race and corrupt each other's results: order them on one stream. */
 MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream);
+
+/* Rotary position embedding, in place, on q or k before attention (the
+ * attention passages above take q and k already rotated):
+ *   - F5-TTS page, module table and "Upstream-identical practice": the DiT
+ *     rotates interleaved feature pairs (x-transformers), on its first
+ *     pe_attn_head heads only -> `interleaved`, `heads`;
+ *   - Qwen3-TTS page: the inverse-frequency table stays fp32; VoxCPM page,
+ *     "Upstream-identical practice", precision bullet: the LongRoPE table is
+ *     built in fp32 -> `inv_freq` is a caller-built fp32 table (plain, scaled
+ *     or LongRoPE-rescaled frequencies alike);
+ *   - OmniVoice page, "Memory & speed", packed_guidance paragraph: under
+ *     packing each sequence's positions start at 0 -> `positions`.
+ * For b < B, h < heads, l < L, pair i < rot_dim/2:
+ *   theta = fl32((float)positions[b][l] * inv_freq[i])      (one fp32 product)
+ *   (e0, e1) = (2i, 2i+1) if interleaved, else (i, i + rot_dim/2)
+ *   x[e0], x[e1] <- x[e0] cos(theta) - x[e1] sin(theta),
+ *                   x[e0] sin(theta) + x[e1] cos(theta)     (fp32, rounded to dtype)
+ * Features >= rot_dim and heads >= `heads` are left as they are. */
+typedef struct {
+  mgqa_dtype dtype;             /* MGQA_BF16, MGQA_FP16 or MGQA_FP32 */
+  int32_t B, H, L, D;           /* x is [B][H][L][D] */
+  void *x;                      /* device, rotated in place, element-aligned */
+  int64_t x_stride[3];          /* batch, head, position strides in elements; head dim contiguous */
+  const int32_t *positions;     /* device [B][L] contiguous, or NULL for positions[b][l] = l */
+  const float *inv_freq;        /* device [rot_dim / 2] fp32 angular frequencies */
+  int32_t rot_dim;              /* even, 2 <= rot_dim <= D */
+  int32_t heads;                /* 1 <= heads <= H */
+  int32_t interleaved;          /* nonzero: pairs (2i, 2i+1); zero: pairs (i, i + rot_dim/2) */
+} mgqa_rope_args;
+
+/* Host-detectable argument errors return MGQA_ERR_INVALID_ARG (detail in
+ * mgqa_last_error_detail); a failed launch returns MGQA_ERR_CUDA. Allocates
+ * nothing, never synchronises; MGQA_OK once the kernel is enqueued. All
+ * pointers are caller-owned device memory. */
+MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *args, cudaStream_t stream);
 
 /* Static description of a status code. */
 MGQA_API const char *mgqa_status_string(mgqa_status status);

@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "masked_gqa_attn_decode_append",
     "masked_gqa_pack_pair",
     "masked_gqa_unpack_pair",
+    "masked_gqa_rope",
 )
 
 
@@ -77,6 +78,19 @@ class MgqaArgs(ctypes.Structure):
         ("lse", ctypes.c_void_p),
         ("dev_error", ctypes.c_void_p),
         ("causal", ctypes.c_int32),
+    ]
+
+
+class MgqaRopeArgs(ctypes.Structure):
+    """Mirror of ``mgqa_rope_args`` in include/masked_gqa_attn.h."""
+    _fields_ = [
+        ("dtype", ctypes.c_int),
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("L", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("x", ctypes.c_void_p),
+        ("x_stride", ctypes.c_int64 * 3),
+        ("positions", ctypes.c_void_p),
+        ("inv_freq", ctypes.c_void_p),
+        ("rot_dim", ctypes.c_int32), ("heads", ctypes.c_int32), ("interleaved", ctypes.c_int32),
     ]
 
 
@@ -116,6 +130,8 @@ def lib() -> ctypes.CDLL:
         L.masked_gqa_unpack_pair.restype = ctypes.c_int
         L.masked_gqa_attn_decode_static.argtypes = [ctypes.POINTER(MgqaArgs), P]
         L.masked_gqa_attn_decode_static.restype = ctypes.c_int
+        L.masked_gqa_rope.argtypes = [ctypes.POINTER(MgqaRopeArgs), P]
+        L.masked_gqa_rope.restype = ctypes.c_int
         L.mgqa_abi_version.argtypes = []
         L.mgqa_abi_version.restype = ctypes.c_int32
         _lib = L
@@ -327,3 +343,36 @@ def masked_gqa_unpack_pair(packed, La, *, stream=None):
                                         _st3(packed), a.data_ptr(), _st3(a), La, b.data_ptr(),
                                         _st3(b), L - La, _stream_handle(stream)))
     return a, b
+
+
+def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, interleaved=False,
+                    stream=None):
+    """Rotate x [B, H, L, D] (bf16, fp16 or fp32, head dim contiguous) in place by
+    rotary position embedding and return it: theta = fl32(position * inv_freq[i])
+    for pair i of the first rot_dim features (default D) of the first `heads`
+    heads (default H); positions int32 [B, L] (default: the row index);
+    inv_freq fp32 [rot_dim / 2]; interleaved pairs (2i, 2i+1) or half-split
+    pairs (i, i + rot_dim/2)."""
+    _dev(x, "x")
+    B, H, L, D = x.shape
+    if x.stride(3) != 1:
+        raise ValueError("x must have a contiguous head dimension")
+    rot_dim = D if rot_dim is None else int(rot_dim)
+    heads = H if heads is None else int(heads)
+    _dev(inv_freq, "inv_freq", torch.float32)
+    if not inv_freq.is_contiguous() or inv_freq.numel() != rot_dim // 2:
+        raise ValueError(f"inv_freq must be a contiguous fp32 tensor of {rot_dim // 2} values")
+    if positions is not None:
+        _dev(positions, "positions", torch.int32)
+        if tuple(positions.shape) != (B, L) or not positions.is_contiguous():
+            raise ValueError("positions must be a contiguous int32 [B, L] tensor")
+    a = MgqaRopeArgs()
+    a.dtype = _dtype_code(x)
+    a.B, a.H, a.L, a.D = B, H, L, D
+    a.x = x.data_ptr()
+    a.x_stride = _st3(x)
+    a.positions = _ptr(positions)
+    a.inv_freq = inv_freq.data_ptr()
+    a.rot_dim, a.heads, a.interleaved = rot_dim, heads, int(bool(interleaved))
+    _check(lib().masked_gqa_rope(ctypes.byref(a), _stream_handle(stream)))
+    return x

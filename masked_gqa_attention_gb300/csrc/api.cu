@@ -12,6 +12,8 @@ namespace mgqa {
 
 static thread_local char g_detail[256] = "";
 
+void clear_error_detail() { g_detail[0] = '\0'; }
+
 mgqa_status fail(mgqa_status code, const char *fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

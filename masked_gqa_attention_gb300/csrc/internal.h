@@ -11,6 +11,8 @@ namespace mgqa {
 
 // Sets the thread-local detail string returned by mgqa_last_error_detail().
 mgqa_status fail(mgqa_status code, const char *fmt, ...);
+// Empties the calling thread's error detail (entry points call it first).
+void clear_error_detail();
 
 // Launch with programmatic stream serialisation (the kernel itself calls
 // grid_dependency_wait() before touching global memory).

@@ -1,0 +1,102 @@
+// Rotary position embedding, in place, on q or k.
+//
+// Passages: F5-TTS page, module table and "Upstream-identical practice"
+// (interleaved feature pairs, x-transformers; only the first pe_attn_head
+// heads rotate); Qwen3-TTS page (the inverse-frequency table stays fp32) and
+// VoxCPM page, "Upstream-identical practice", precision bullet (LongRoPE table
+// built in fp32); OmniVoice page, "Memory & speed", packed_guidance paragraph
+// (positions restart at 0 for each packed sequence).
+//
+// One thread per (row b, position l, pair i): it forms theta = fl32(pos * f_i)
+// once, takes its sine and cosine (accurate sincosf: positions reach several
+// thousand radians) and rotates pair i of every rotated head at (b, l).
+// Consecutive threads take consecutive pairs, so each warp reads and writes
+// whole runs of a row (interleaved: one contiguous run; half-split: two).
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgqa {
+namespace {
+
+struct RopeParams {
+  void *x;
+  int64_t s_b, s_h, s_l;
+  const int32_t *positions;
+  const float *inv_freq;
+  int B, L, half, heads, interleaved;
+};
+
+constexpr int kRopeThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeParams p) {
+  const int64_t idx = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x;
+  const int64_t total = (int64_t)p.B * p.L * p.half;
+  if (idx >= total) return;
+  const int i = (int)(idx % p.half);
+  const int64_t bl = idx / p.half;
+  const int l = (int)(bl % p.L), b = (int)(bl / p.L);
+  const int pos = p.positions ? __ldg(p.positions + bl) : l;
+  const float theta = __fmul_rn((float)pos, __ldg(p.inv_freq + i));
+  float sn, cs;
+  sincosf(theta, &sn, &cs);
+  const int e0 = p.interleaved ? 2 * i : i;
+  const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
+  T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
+  for (int h = 0; h < p.heads; ++h) {
+    T *r = row + (int64_t)h * p.s_h;
+    const float a = to_float(r[e0]), c = to_float(r[e1]);
+    r[e0] = from_float<T>(a * cs - c * sn);
+    r[e1] = from_float<T>(a * sn + c * cs);
+  }
+}
+
+template <typename T>
+mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
+  const int64_t total = (int64_t)p.B * p.L * p.half;
+  const int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
+  if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
+  rope_kernel<T><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+
+}  // namespace
+}  // namespace mgqa
+
+extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStream_t stream) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (!a) return fail(MGQA_ERR_INVALID_ARG, "args is null");
+  if (a->dtype != MGQA_BF16 && a->dtype != MGQA_FP16 && a->dtype != MGQA_FP32)
+    return fail(MGQA_ERR_INVALID_ARG, "rope: unknown dtype");
+  if (a->B < 1 || a->H < 1 || a->L < 1 || a->D < 2)
+    return fail(MGQA_ERR_INVALID_ARG, "rope: B, H, L must be >= 1 and D >= 2");
+  if (a->rot_dim < 2 || a->rot_dim > a->D || (a->rot_dim & 1))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: rot_dim must be even and in [2, D]");
+  if (a->heads < 1 || a->heads > a->H)
+    return fail(MGQA_ERR_INVALID_ARG, "rope: heads must be in [1, H]");
+  if (!a->x || !a->inv_freq) return fail(MGQA_ERR_INVALID_ARG, "rope: x or inv_freq is null");
+  const size_t es = a->dtype == MGQA_FP32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(a->x) % es != 0 ||
+      reinterpret_cast<uintptr_t>(a->inv_freq) % 4 != 0 ||
+      (a->positions && reinterpret_cast<uintptr_t>(a->positions) % 4 != 0))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: misaligned pointer");
+  // a zero stride over a dimension of extent > 1 would rotate shared elements
+  // more than once (or from two threads at once)
+  const int ext[3] = {a->B, a->H, a->L};
+  for (int t = 0; t < 3; ++t)
+    if (a->x_stride[t] < 0 || (a->x_stride[t] == 0 && ext[t] > 1))
+      return fail(MGQA_ERR_INVALID_ARG, "rope: stride %d must be positive", t);
+  RopeParams p{};
+  p.x = a->x;
+  p.s_b = a->x_stride[0]; p.s_h = a->x_stride[1]; p.s_l = a->x_stride[2];
+  p.positions = a->positions;
+  p.inv_freq = a->inv_freq;
+  p.B = a->B; p.L = a->L; p.half = a->rot_dim / 2; p.heads = a->heads;
+  p.interleaved = a->interleaved != 0;
+  if (a->dtype == MGQA_BF16) return launch_t<__nv_bfloat16>(p, stream);
+  if (a->dtype == MGQA_FP16) return launch_t<__half>(p, stream);
+  return launch_t<float>(p, stream);
+}

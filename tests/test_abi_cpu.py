@@ -33,16 +33,17 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(L):
     for name in declared_symbols():
         assert hasattr(L, name), name
-    assert L.mgqa_abi_version() == 2
+    assert L.mgqa_abi_version() == 3
     assert L.mgqa_status_string(M.MGQA_ERR_TIMEOUT) == b"device wait timed out"
 
 
-def test_struct_layout_matches_header(tmp_path):
-    fields = [f for f, _ in M.MgqaArgs._fields_]
+@pytest.mark.parametrize("cname,py", [("mgqa_args", M.MgqaArgs), ("mgqa_rope_args", M.MgqaRopeArgs)])
+def test_struct_layout_matches_header(tmp_path, cname, py):
+    fields = [f for f, _ in py._fields_]
     src = tmp_path / "off.c"
-    body = "\n".join(f'printf("{f} %zu\\n", offsetof(mgqa_args, {f}));' for f in fields)
+    body = "\n".join(f'printf("{f} %zu\\n", offsetof({cname}, {f}));' for f in fields)
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "masked_gqa_attn.h"\n'
-                   f'int main(void){{ {body} printf("size %zu\\n", sizeof(mgqa_args)); return 0; }}\n')
+                   f'int main(void){{ {body} printf("size %zu\\n", sizeof({cname})); return 0; }}\n')
     exe = tmp_path / "off"
     cuda_inc = "/usr/local/cuda/include"
     subprocess.run(["gcc", "-I", os.path.dirname(HEADER), "-I", cuda_inc, str(src), "-o", str(exe)],
@@ -50,8 +51,8 @@ def test_struct_layout_matches_header(tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     got = dict(line.split() for line in out if line)
     for f in fields:
-        assert int(got[f]) == getattr(M.MgqaArgs, f).offset, f
-    assert int(got["size"]) == ctypes.sizeof(M.MgqaArgs)
+        assert int(got[f]) == getattr(py, f).offset, f
+    assert int(got["size"]) == ctypes.sizeof(py)
 
 
 def _valid_args():
@@ -108,3 +109,38 @@ def test_decode_validation(L):
     assert n >= 8 * 16 * 16 * (64 + 2) * 4
     assert L.masked_gqa_attn_decode(ctypes.byref(a), None, n, None) == M.MGQA_ERR_INVALID_ARG
     assert L.masked_gqa_attn_decode(ctypes.byref(a), (1 << 20) + 4, n, None) == M.MGQA_ERR_INVALID_ARG
+
+
+def _valid_rope():
+    a = M.MgqaRopeArgs()
+    a.dtype = M.MGQA_BF16
+    a.B, a.H, a.L, a.D = 2, 16, 1024, 128
+    a.x = 1 << 20  # fake, never dereferenced: validation fails before any launch
+    a.x_stride[:] = [16 * 1024 * 128, 1024 * 128, 128]
+    a.inv_freq = 1 << 22
+    a.rot_dim, a.heads, a.interleaved = 64, 1, 1
+    return a
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda a: setattr(a, "rot_dim", 63),
+    lambda a: setattr(a, "rot_dim", 0),
+    lambda a: setattr(a, "rot_dim", 130),
+    lambda a: setattr(a, "heads", 0),
+    lambda a: setattr(a, "heads", 17),
+    lambda a: setattr(a, "L", 0),
+    lambda a: setattr(a, "dtype", 5),
+    lambda a: setattr(a, "x", 0),
+    lambda a: setattr(a, "inv_freq", 0),
+    lambda a: setattr(a, "x", (1 << 20) + 1),
+    lambda a: setattr(a, "inv_freq", (1 << 22) + 2),
+    lambda a: setattr(a, "positions", (1 << 23) + 2),
+    lambda a: a.x_stride.__setitem__(1, -1),
+    lambda a: a.x_stride.__setitem__(2, 0),  # rows would share elements
+])
+def test_rope_rejects_bad_arguments(L, mutate):
+    a = _valid_rope()
+    mutate(a)
+    assert L.masked_gqa_rope(ctypes.byref(a), None) == M.MGQA_ERR_INVALID_ARG
+    assert L.mgqa_last_error_detail() != b""
+    assert L.masked_gqa_rope(None, None) == M.MGQA_ERR_INVALID_ARG

@@ -1,0 +1,109 @@
+"""Parity of the rotary-position-embedding kernel against the fp64 oracle, and
+the properties the pages fix: only the first `heads` heads and `rot_dim`
+features rotate (F5-TTS page, pe_attn_head), and under packing each
+sequence's positions restart at 0 (OmniVoice page, packed_guidance), so a
+packed row rotates exactly like its sequences alone."""
+import numpy as np
+import pytest
+import torch
+
+from _util import assert_close_to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    import masked_gqa_attention_gb300 as M
+    M.build_library()
+    return M
+
+
+def inv_freq_table(rot_dim, base=10000.0):
+    # the usual table, built in fp32 (Qwen3-TTS page: it stays fp32)
+    return (base ** (-torch.arange(0, rot_dim, 2, dtype=torch.float64) / rot_dim)).to(torch.float32)
+
+
+def make_x(seed, B, H, L, D, dtype):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(B, H, L, D, generator=g, dtype=torch.float32).to(dtype)
+
+
+CASES = [  # B, H, L, D, rot_dim, heads
+    (2, 16, 1024, 128, 128, 16),   # language-model q at the padded-CFG shape
+    (2, 8, 1024, 128, 64, 8),      # partial rotary dim
+    (1, 3, 77, 64, 32, 1),         # F5 DiT: one rotated head (pe_attn_head = 1)
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
+def test_rope_matches_oracle(M, oracle_mod, dtype, interleaved, case):
+    B, H, L, D, rot, heads = case
+    x = make_x(11 + L, B, H, L, D, dtype)
+    f = inv_freq_table(rot)
+    g = torch.Generator().manual_seed(5)
+    pos = torch.randint(0, 8192, (B, L), generator=g, dtype=torch.int32)
+    ref = oracle_mod.rope(x, inv_freq=f, positions=pos, rot_dim=rot, heads=heads,
+                          interleaved=interleaved)
+    xd = x.cuda()
+    M.masked_gqa_rope(xd, f.cuda(), positions=pos.cuda(), rot_dim=rot, heads=heads,
+                      interleaved=interleaved)
+    torch.cuda.synchronize()
+    assert_close_to_oracle(xd, ref, dtype, f"rope {case}")
+    got = xd.cpu()
+    if dtype != torch.float32:
+        # per element: rounding the fp32 result to the output type (unit
+        # roundoff 2^-8 for bf16, 2^-11 for fp16) plus the fp32 arithmetic
+        # (a few ulp of |a| + |c| <= 1e-5 here) and fp16's subnormal spacing
+        u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -11
+        err = np.abs(got.double().numpy() - ref)
+        assert np.all(err <= u * np.abs(ref) + 4e-6), float((err - u * np.abs(ref)).max())
+    # what must not rotate is bit-for-bit the input
+    assert torch.equal(got[:, heads:], x[:, heads:])
+    assert torch.equal(got[..., rot:], x[..., rot:])
+
+
+def test_rope_default_positions_are_row_index(M):
+    x = make_x(3, 2, 4, 300, 64, torch.bfloat16).cuda()
+    f = inv_freq_table(64).cuda()
+    a = M.masked_gqa_rope(x.clone(), f)
+    pos = torch.arange(300, dtype=torch.int32, device="cuda").repeat(2, 1).contiguous()
+    b = M.masked_gqa_rope(x.clone(), f, positions=pos)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_rope_packed_row_equals_sequences_alone(M):
+    # cond (1024) and uncond target (384) packed in one row, positions 0.. per sequence
+    B, H, D = 1, 8, 128
+    xc, xu = make_x(21, B, H, 1024, D, torch.bfloat16).cuda(), make_x(22, B, H, 384, D, torch.bfloat16).cuda()
+    f = inv_freq_table(D).cuda()
+    packed, _ = M.masked_gqa_pack_pair(xc, xu)
+    pos = torch.cat([torch.arange(1024), torch.arange(384)]).to(torch.int32)[None].cuda().contiguous()
+    M.masked_gqa_rope(packed, f, positions=pos)
+    M.masked_gqa_rope(xc, f)
+    M.masked_gqa_rope(xu, f)
+    torch.cuda.synchronize()
+    assert torch.equal(packed[:, :, :1024], xc) and torch.equal(packed[:, :, 1024:], xu)
+
+
+def test_rope_strided_view(M):
+    # q laid out [B, L, H, D] and viewed as [B, H, L, D]: same bits as contiguous
+    base = make_x(31, 2, 200, 16, 128, torch.bfloat16).cuda()  # [B, L, H, D]
+    view = base.transpose(1, 2)
+    cont = view.contiguous()
+    f = inv_freq_table(128).cuda()
+    M.masked_gqa_rope(view, f, interleaved=False)
+    M.masked_gqa_rope(cont, f, interleaved=False)
+    torch.cuda.synchronize()
+    assert torch.equal(view, cont)
+
+
+def test_rope_rejects_host_tensors_and_bad_tables(M):
+    x = make_x(1, 1, 2, 8, 64, torch.bfloat16)
+    with pytest.raises(ValueError):
+        M.masked_gqa_rope(x, inv_freq_table(64))
+    with pytest.raises(ValueError):
+        M.masked_gqa_rope(x.cuda(), inv_freq_table(32).cuda())
