@@ -12,6 +12,10 @@
 // thousand radians) and rotates pair i of every rotated head at (b, l).
 // Consecutive threads take consecutive pairs, so each warp reads and writes
 // whole runs of a row (interleaved: one contiguous run; half-split: two).
+// The pairs of kHeadBatch heads are loaded before any is stored, so their
+// loads are in flight together (a store could alias a later head's load, so
+// the compiler would not hoist the loads by itself); interleaved 16-bit pairs
+// move as one 32-bit word when the rows allow it.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,8 +31,32 @@ struct RopeParams {
 };
 
 constexpr int kRopeThreads = 256;
+constexpr int kHeadBatch = 8;
 
-template <typename T>
+// the pair (x[e0], x[e1]) of one row as floats, and back
+template <typename T, bool PAIRED>
+MGQA_DEV void load_pair(const T *r, int e0, int e1, float &a, float &c) {
+  if constexpr (PAIRED) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(r + e0);  // e1 == e0 + 1
+    const T *t = reinterpret_cast<const T *>(&w);
+    a = to_float(t[0]);
+    c = to_float(t[1]);
+  } else {
+    a = to_float(r[e0]);
+    c = to_float(r[e1]);
+  }
+}
+template <typename T, bool PAIRED>
+MGQA_DEV void store_pair(T *r, int e0, int e1, float a, float c) {
+  if constexpr (PAIRED) {
+    *reinterpret_cast<uint32_t *>(r + e0) = pack2<T>(a, c);
+  } else {
+    r[e0] = from_float<T>(a);
+    r[e1] = from_float<T>(c);
+  }
+}
+
+template <typename T, bool PAIRED>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeParams p) {
   const int64_t idx = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x;
   const int64_t total = (int64_t)p.B * p.L * p.half;
@@ -43,11 +71,17 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   const int e0 = p.interleaved ? 2 * i : i;
   const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
   T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
-  for (int h = 0; h < p.heads; ++h) {
-    T *r = row + (int64_t)h * p.s_h;
-    const float a = to_float(r[e0]), c = to_float(r[e1]);
-    r[e0] = from_float<T>(a * cs - c * sn);
-    r[e1] = from_float<T>(a * sn + c * cs);
+  for (int h0 = 0; h0 < p.heads; h0 += kHeadBatch) {
+    float a[kHeadBatch], c[kHeadBatch];
+#pragma unroll
+    for (int u = 0; u < kHeadBatch; ++u)
+      if (h0 + u < p.heads)
+        load_pair<T, PAIRED>(row + (int64_t)(h0 + u) * p.s_h, e0, e1, a[u], c[u]);
+#pragma unroll
+    for (int u = 0; u < kHeadBatch; ++u)
+      if (h0 + u < p.heads)
+        store_pair<T, PAIRED>(row + (int64_t)(h0 + u) * p.s_h, e0, e1, a[u] * cs - c[u] * sn,
+                              a[u] * sn + c[u] * cs);
   }
 }
 
@@ -56,7 +90,14 @@ mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
   const int64_t total = (int64_t)p.B * p.L * p.half;
   const int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
   if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
-  rope_kernel<T><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
+  // interleaved 16-bit pairs as 32-bit words: every row start 4-byte aligned
+  const bool paired = sizeof(T) == 2 && p.interleaved &&
+                      (reinterpret_cast<uintptr_t>(p.x) % 4) == 0 && p.s_b % 2 == 0 &&
+                      p.s_h % 2 == 0 && p.s_l % 2 == 0;
+  if (paired)
+    rope_kernel<T, sizeof(T) == 2><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
+  else
+    rope_kernel<T, false><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
