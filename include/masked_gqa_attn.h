@@ -2,8 +2,10 @@
  * masked_gqa_attn.h -- C ABI of the GB300 (sm_103a) masked grouped-query
  * attention library.
  *
- * The operation (both entry points): scaled-dot-product attention with
- * grouped KV heads under an explicit boolean mask, as the engine pages use it:
+ * The attention operation (the prefill and decode entry points): scaled-
+ * dot-product attention with grouped KV heads under an explicit boolean mask,
+ * as the engine pages use it (the rotary embedding and the packing helpers
+ * further down are the steps around it):
  *   - VoxCPM page, "Upstream-identical practice", attention bullet: SDPA with
  *     enable_gqa on contiguous tensors; bidirectional in the local DiT; cache
  *     decode under an explicit boolean mask where slots past the current length
