@@ -95,3 +95,41 @@ def test_committed_profiles_name_their_sources():
         assert parts[2] == "source-sha256:" and len(parts[3]) == 16
         int(parts[3], 16)
         assert os.path.exists(os.path.join(ROOT, "masked_gqa_attention_gb300", "csrc", parts[4]))
+
+
+# ---- the input recipe: the structure every parity and invariance test relies on
+
+def test_padded_cfg_mask_encodes_the_two_row_lengths():
+    wl = W.padded_cfg(variant="bits")
+    a = W.unpack_bits(wl.mask_bits, 1024)          # [B, Lq, Lk] bool
+    assert a.shape == (2, 1024, 1024)
+    assert bool(a[0].all())
+    assert bool(a[1, :, :384].all()) and not bool(a[1, :, 384:].any())
+    kv = W.padded_cfg(variant="kvlen")
+    assert kv.kv_len.tolist() == [1024, 384]
+    assert torch.equal(kv.allowed(), wl.allowed())
+
+
+def test_static_cache_garbage_past_the_filled_length():
+    wl = W.static_cache_decode(variant="span")
+    filled = wl.kv_len.tolist()
+    assert all(256 <= f <= 3100 for f in filled)
+    for b, f in enumerate(filled):
+        tail_k, tail_v = wl.k[b, :, f:].float(), wl.v[b, :, f:].float()
+        # large finite values: if masked slots leaked into a result, it would show
+        assert bool(torch.isfinite(tail_k).all()) and float(tail_k.abs().max()) > 1e3
+        assert float(tail_v.abs().max()) > 1e3 and float(tail_v.abs().max()) <= 1e4
+        assert float(wl.k[b, :, :f].float().abs().max()) < 10.0
+    full = W.static_cache_decode(variant="full")
+    assert torch.equal(full.allowed(), wl.allowed())
+    assert torch.equal(full.k, wl.k) and torch.equal(full.v, wl.v)
+
+
+def test_dit_segments_cut_rows_off_the_tile_grid():
+    seg = W.dit_segments(1005, 32, 4096)
+    counts = [int(seg[b].max()) + 1 for b in range(32)]
+    assert min(counts) >= 1 and max(counts) <= 6 and len(set(counts)) > 1
+    # ids are non-decreasing along a row (contiguous blocks)
+    assert bool((seg[:, 1:] >= seg[:, :-1]).all())
+    cuts = [c for b in range(32) for c in (torch.nonzero(seg[b, 1:] != seg[b, :-1]).flatten() + 1).tolist()]
+    assert cuts and any(c % 128 != 0 for c in cuts)  # partial tiles occur
