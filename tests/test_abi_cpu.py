@@ -144,3 +144,36 @@ def test_rope_rejects_bad_arguments(L, mutate):
     assert L.masked_gqa_rope(ctypes.byref(a), None) == M.MGQA_ERR_INVALID_ARG
     assert L.mgqa_last_error_detail() != b""
     assert L.masked_gqa_rope(None, None) == M.MGQA_ERR_INVALID_ARG
+
+
+def test_plain_c_program_links_and_calls_the_library(L, tmp_path):
+    # the boundary is a C ABI: a C program that includes only the header links
+    # libmgqa.so and gets the documented status codes (no GPU needed for these)
+    src = tmp_path / "use.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "masked_gqa_attn.h"
+int main(void) {
+  if (mgqa_abi_version() != MGQA_ABI_VERSION) return 1;
+  if (masked_gqa_attn_prefill(NULL, NULL) != MGQA_ERR_INVALID_ARG) return 2;
+  if (strlen(mgqa_last_error_detail()) == 0) return 3;
+  mgqa_args a;
+  memset(&a, 0, sizeof a);
+  a.dtype = MGQA_BF16; a.B = 1; a.Hq = 4; a.Hkv = 3; a.Lq = 8; a.Lk = 8; a.D = 64;
+  if (masked_gqa_attn_prefill(&a, NULL) != MGQA_ERR_INVALID_ARG) return 4;  /* Hq % Hkv */
+  if (masked_gqa_attn_decode_workspace_size(&a) != 0) return 5;
+  mgqa_rope_args r;
+  memset(&r, 0, sizeof r);
+  if (masked_gqa_rope(&r, NULL) != MGQA_ERR_INVALID_ARG) return 6;
+  printf("%s\n", mgqa_status_string(MGQA_ERR_UNSUPPORTED));
+  return 0;
+}
+''')
+    exe = tmp_path / "use"
+    libdir = os.path.dirname(M._LIB_PATH)
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), "-I", "/usr/local/cuda/include", str(src),
+                    "-L", libdir, "-lmgqa", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.strip() != ""
