@@ -68,7 +68,9 @@ typedef enum {
                                 on the device: kv_len < 0 or kv_len > Lk */
   MGQA_ERR_UNSUPPORTED = 2,  /* valid request this build has no kernel for */
   MGQA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
-  MGQA_ERR_TIMEOUT = 4       /* device: a bounded pipeline wait gave up */
+  MGQA_ERR_TIMEOUT = 4,      /* device: a bounded pipeline wait gave up */
+  MGQA_ERR_DEVICE_CHECK = 5  /* device, debug library only: a bounds or alignment
+                                check failed and the access was skipped */
 } mgqa_status;
 
 typedef enum {
@@ -96,8 +98,10 @@ typedef struct mgqa_args {
 
   /* optional mask forms, combined with AND (see above) */
   const uint32_t *mask_bits;    /* words; row (b, i) starts at b*stride_b + i*stride_q */
-  int64_t mask_stride_b;        /* in 32-bit words */
-  int64_t mask_stride_q;        /* in 32-bit words, >= ceil(Lk/32) */
+  int64_t mask_stride_b;        /* in 32-bit words: 0 (one mask for every batch row) or
+                                   >= ceil(Lk/32) */
+  int64_t mask_stride_q;        /* in 32-bit words: 0 (one row for every query: a key-
+                                   padding mask stored as [B][1][W]) or >= ceil(Lk/32) */
   const int32_t *kv_len;        /* [B]; values outside [0, Lk] are a device error
                                    (clamped; the static cache is full) */
   const int32_t *seg_q;         /* [B][Lq] contiguous; given together with seg_k */
@@ -201,7 +205,7 @@ MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaSt
  *   - F5-TTS page, module table and "Upstream-identical practice": the DiT
  *     rotates interleaved feature pairs (x-transformers), on its first
  *     pe_attn_head heads only -> `interleaved`, `heads`;
- *   - Qwen3-TTS page: the inverse-frequency table stays fp32; VoxCPM page,
+ *   - OmniVoice page, "Parity results": the inverse-frequency table stays fp32; VoxCPM page,
  *     "Upstream-identical practice", precision bullet: the LongRoPE table is
  *     built in fp32 -> `inv_freq` is a caller-built fp32 table (plain, scaled
  *     or LongRoPE-rescaled frequencies alike);

@@ -1,0 +1,54 @@
+/*
+ * masked_gqa_attn_debug.h -- extra entry points of the debug library,
+ * libmgqa_debug.so: the same sources as libmgqa.so built with MGQA_DEBUG.
+ * The engine pages have no counterpart; this is test equipment.
+ *
+ * The debug library exports everything masked_gqa_attn.h declares, with
+ * three differences on the device:
+ *   - bounds and alignment checks on the global, TMA and mask accesses: a
+ *     failed check writes MGQA_ERR_DEVICE_CHECK to *dev_error and skips the
+ *     access (no trap);
+ *   - event counters (read with mgqa_debug_counters);
+ *   - an injectable stall of the tensor-core prefill's load pipeline with a
+ *     shortened wait limit, so that a test can watch a bounded wait give up
+ *     (MGQA_ERR_TIMEOUT) without hanging the GPU.
+ * The debug state is one copy per device, in device memory; the functions
+ * below act on the current device and synchronise with it.
+ */
+#ifndef MASKED_GQA_ATTN_DEBUG_H
+#define MASKED_GQA_ATTN_DEBUG_H
+
+#include "masked_gqa_attn.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Number of event counters. */
+#define MGQA_DEBUG_NUM_COUNTERS 4
+/* counter 0: softmax warps of the tensor-core prefill that rescaled their
+ *            running output (the row max grew by more than 2^8 within a row);
+ * counter 1: key tiles the tensor-core prefill's softmax warps processed;
+ * counters 2, 3: unused (0). */
+
+/* Copies the first n (<= MGQA_DEBUG_NUM_COUNTERS) counters to host memory
+ * `out`. Synchronous. */
+MGQA_API mgqa_status mgqa_debug_counters(uint64_t *out, int32_t n);
+
+/* Zeroes the counters, removes any injected stall and restores the normal
+ * wait limit (2 s). Synchronous. */
+MGQA_API mgqa_status mgqa_debug_reset(void);
+
+/* From the next tensor-core prefill launch on, the TMA producer issues no
+ * load for non-empty key tile `tile` (its position in the row's list of
+ * non-empty tiles, >= 1) or any later one, and every pipeline wait gives up
+ * after `wait_limit_ns` (> 0). Every load issued before the stall lands
+ * before the CTA exits, and every MMA issued completes before the tensor
+ * memory is freed. tile < 0 removes the stall. Synchronous. */
+MGQA_API mgqa_status mgqa_debug_inject_prefill_stall(int32_t tile, uint64_t wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MASKED_GQA_ATTN_DEBUG_H */

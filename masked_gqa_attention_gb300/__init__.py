@@ -22,6 +22,7 @@ from typing import Optional
 import torch
 
 from .build import LIB as _LIB_PATH
+from .build import LIB_DEBUG as _LIB_DEBUG_PATH
 from .build import build as build_library
 
 __all__ = [
@@ -31,9 +32,11 @@ __all__ = [
     "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
     "masked_gqa_attn_decode_static", "DECODE_STATIC_SCRATCH_BYTES",
     "masked_gqa_attn_decode_append", "masked_gqa_pack_pair", "masked_gqa_unpack_pair",
+    "debug_lib", "MGQA_ERR_DEVICE_CHECK",
 ]
 
-MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT = range(5)
+(MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT,
+ MGQA_ERR_DEVICE_CHECK) = range(6)
 MGQA_BF16, MGQA_FP32, MGQA_FP16 = 0, 1, 2
 # size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
 DECODE_STATIC_SCRATCH_BYTES = 4 << 20
@@ -51,6 +54,13 @@ EXPORTED_SYMBOLS = (
     "masked_gqa_unpack_pair",
     "masked_gqa_rope",
 )
+# exported by the debug library only (include/masked_gqa_attn_debug.h)
+DEBUG_SYMBOLS = (
+    "mgqa_debug_counters",
+    "mgqa_debug_reset",
+    "mgqa_debug_inject_prefill_stall",
+)
+DEBUG_NUM_COUNTERS = 4
 
 
 class MgqaError(RuntimeError):
@@ -95,6 +105,40 @@ class MgqaRopeArgs(ctypes.Structure):
 
 
 _lib = None
+_lib_debug = None
+
+
+def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Argument and result types of the C ABI's entry points."""
+    P = ctypes.c_void_p
+    I64P = ctypes.POINTER(ctypes.c_int64)
+    I32 = ctypes.c_int32
+    L.masked_gqa_attn_prefill.argtypes = [ctypes.POINTER(MgqaArgs), P]
+    L.masked_gqa_attn_prefill.restype = ctypes.c_int
+    L.masked_gqa_attn_decode_workspace_size.argtypes = [ctypes.POINTER(MgqaArgs)]
+    L.masked_gqa_attn_decode_workspace_size.restype = ctypes.c_size_t
+    L.masked_gqa_attn_decode.argtypes = [ctypes.POINTER(MgqaArgs), P, ctypes.c_size_t, P]
+    L.masked_gqa_attn_decode.restype = ctypes.c_int
+    L.mgqa_status_string.argtypes = [ctypes.c_int]
+    L.mgqa_status_string.restype = ctypes.c_char_p
+    L.mgqa_last_error_detail.argtypes = []
+    L.mgqa_last_error_detail.restype = ctypes.c_char_p
+    L.masked_gqa_attn_decode_append.argtypes = [ctypes.POINTER(MgqaArgs), P, P, I64P, I64P, P, P,
+                                                ctypes.c_size_t, P]
+    L.masked_gqa_attn_decode_append.restype = ctypes.c_int
+    L.masked_gqa_pack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, I32, P, I64P, I32,
+                                       P, I64P, P, P]
+    L.masked_gqa_pack_pair.restype = ctypes.c_int
+    L.masked_gqa_unpack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, P, I64P, I32,
+                                         P, I64P, I32, P]
+    L.masked_gqa_unpack_pair.restype = ctypes.c_int
+    L.masked_gqa_attn_decode_static.argtypes = [ctypes.POINTER(MgqaArgs), P]
+    L.masked_gqa_attn_decode_static.restype = ctypes.c_int
+    L.masked_gqa_rope.argtypes = [ctypes.POINTER(MgqaRopeArgs), P]
+    L.masked_gqa_rope.restype = ctypes.c_int
+    L.mgqa_abi_version.argtypes = []
+    L.mgqa_abi_version.restype = ctypes.c_int32
+    return L
 
 
 def lib() -> ctypes.CDLL:
@@ -103,39 +147,28 @@ def lib() -> ctypes.CDLL:
     if _lib is None:
         if not os.path.exists(_LIB_PATH):
             raise RuntimeError(f"libmgqa.so is not built ({_LIB_PATH}); run build_library()")
-        L = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        L.masked_gqa_attn_prefill.argtypes = [ctypes.POINTER(MgqaArgs), P]
-        L.masked_gqa_attn_prefill.restype = ctypes.c_int
-        L.masked_gqa_attn_decode_workspace_size.argtypes = [ctypes.POINTER(MgqaArgs)]
-        L.masked_gqa_attn_decode_workspace_size.restype = ctypes.c_size_t
-        L.masked_gqa_attn_decode.argtypes = [ctypes.POINTER(MgqaArgs), P, ctypes.c_size_t, P]
-        L.masked_gqa_attn_decode.restype = ctypes.c_int
-        L.mgqa_status_string.argtypes = [ctypes.c_int]
-        L.mgqa_status_string.restype = ctypes.c_char_p
-        L.mgqa_last_error_detail.argtypes = []
-        L.mgqa_last_error_detail.restype = ctypes.c_char_p
-        L.masked_gqa_attn_decode_append.argtypes = [ctypes.POINTER(MgqaArgs), P, P,
-                                                    ctypes.POINTER(ctypes.c_int64),
-                                                    ctypes.POINTER(ctypes.c_int64), P, P,
-                                                    ctypes.c_size_t, P]
-        L.masked_gqa_attn_decode_append.restype = ctypes.c_int
-        I64P = ctypes.POINTER(ctypes.c_int64)
-        I32 = ctypes.c_int32
-        L.masked_gqa_pack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, I32, P, I64P, I32,
-                                           P, I64P, P, P]
-        L.masked_gqa_pack_pair.restype = ctypes.c_int
-        L.masked_gqa_unpack_pair.argtypes = [ctypes.c_int, I32, I32, I32, P, I64P, P, I64P, I32,
-                                             P, I64P, I32, P]
-        L.masked_gqa_unpack_pair.restype = ctypes.c_int
-        L.masked_gqa_attn_decode_static.argtypes = [ctypes.POINTER(MgqaArgs), P]
-        L.masked_gqa_attn_decode_static.restype = ctypes.c_int
-        L.masked_gqa_rope.argtypes = [ctypes.POINTER(MgqaRopeArgs), P]
-        L.masked_gqa_rope.restype = ctypes.c_int
-        L.mgqa_abi_version.argtypes = []
-        L.mgqa_abi_version.restype = ctypes.c_int32
-        _lib = L
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
+
+
+def debug_lib() -> ctypes.CDLL:
+    """Load libmgqa_debug.so: the same entry points built with device-side
+    bounds checks, event counters and an injectable pipeline stall, plus the
+    mgqa_debug_* functions (test equipment; raises if it has not been built)."""
+    global _lib_debug
+    if _lib_debug is None:
+        if not os.path.exists(_LIB_DEBUG_PATH):
+            raise RuntimeError(f"libmgqa_debug.so is not built ({_LIB_DEBUG_PATH}); "
+                               "run build_library()")
+        L = _bind(ctypes.CDLL(_LIB_DEBUG_PATH))
+        L.mgqa_debug_counters.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
+        L.mgqa_debug_counters.restype = ctypes.c_int
+        L.mgqa_debug_reset.argtypes = []
+        L.mgqa_debug_reset.restype = ctypes.c_int
+        L.mgqa_debug_inject_prefill_stall.argtypes = [ctypes.c_int32, ctypes.c_uint64]
+        L.mgqa_debug_inject_prefill_stall.restype = ctypes.c_int
+        _lib_debug = L
+    return _lib_debug
 
 
 def _check(status: int):
@@ -200,6 +233,9 @@ def make_args(q, k, v, out, *, scale=None, mask_bits=None, kv_len=None, seg_q=No
             raise ValueError("mask_bits must be 3-D int32/uint32 words")
         if mask_bits.stride(2) != 1:
             raise ValueError("mask_bits words must be contiguous along keys")
+        if (mask_bits.shape[0] not in (1, B) or mask_bits.shape[1] not in (1, Lq)
+                or mask_bits.shape[2] < (Lk + 31) // 32):
+            raise ValueError(f"mask_bits must be [B or 1, Lq or 1, >= {(Lk + 31) // 32}] words")
         a.mask_bits = mask_bits.data_ptr()
         a.mask_stride_b = mask_bits.stride(0) if mask_bits.shape[0] > 1 else 0
         a.mask_stride_q = mask_bits.stride(1) if mask_bits.shape[1] > 1 else 0

@@ -62,13 +62,15 @@ mgqa_status validate(const mgqa_args *a, bool decode) {
   if ((st = check_tensor("out", a->out, a->o_stride, es)) != MGQA_OK) return st;
   if (a->mask_bits) {
     if (!aligned(a->mask_bits, 4)) return fail(MGQA_ERR_INVALID_ARG, "mask_bits misaligned");
+    // a stride of 0 broadcasts one mask row over the queries (a key-padding
+    // mask given as [B][1][W]) or one mask over the batch rows
     const int64_t W = (a->Lk + 31) / 32;
-    if (a->mask_stride_q < W && a->Lq > 1)
-      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_q < ceil(Lk/32)");
     if (a->mask_stride_b < 0 || a->mask_stride_q < 0)
       return fail(MGQA_ERR_INVALID_ARG, "negative mask stride");
-    if (a->B > 1 && a->mask_stride_b < W && a->mask_stride_b != 0)
-      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_b too small");
+    if (a->Lq > 1 && a->mask_stride_q != 0 && a->mask_stride_q < W)
+      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_q is neither 0 nor >= ceil(Lk/32)");
+    if (a->B > 1 && a->mask_stride_b != 0 && a->mask_stride_b < W)
+      return fail(MGQA_ERR_INVALID_ARG, "mask_stride_b is neither 0 nor >= ceil(Lk/32)");
   }
   if ((a->seg_q == nullptr) != (a->seg_k == nullptr))
     return fail(MGQA_ERR_INVALID_ARG, "seg_q and seg_k must be given together");
@@ -144,6 +146,7 @@ const char *mgqa_status_string(mgqa_status s) {
     case MGQA_ERR_UNSUPPORTED: return "unsupported";
     case MGQA_ERR_CUDA: return "CUDA error";
     case MGQA_ERR_TIMEOUT: return "device wait timed out";
+    case MGQA_ERR_DEVICE_CHECK: return "device bounds check failed (debug library)";
   }
   return "unknown status";
 }

@@ -20,6 +20,22 @@ MGQA_DEV void report_error(int32_t *err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Bounds and alignment checks of the debug library (built with MGQA_DEBUG):
+// a failed check records MGQA_ERR_DEVICE_CHECK and the caller skips the
+// access. In the product library every check is the constant true.
+#ifdef MGQA_DEBUG
+MGQA_DEV bool dcheck(bool ok, int32_t *err) {
+  if (!ok) report_error(err, MGQA_ERR_DEVICE_CHECK);
+  return ok;
+}
+#define MGQA_DCHECK(cond, err) (::mgqa::dcheck((cond), (err)))
+#else
+#define MGQA_DCHECK(cond, err) true
+#endif
+
+// Longest a pipeline wait spins before it reports MGQA_ERR_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 MGQA_DEV float to_float(float x) { return x; }
 MGQA_DEV float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
 MGQA_DEV float to_float(__half x) { return __half2float(x); }
@@ -186,11 +202,8 @@ MGQA_DEV uint64_t globaltimer_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase: gives up after ~`limit_ns` of wall time
-// (measured with the global timer), records MGQA_ERR_TIMEOUT and returns
-// false. Never spins forever.
-// Non-blocking probe of the same phase (cheaper than try_wait when the phase
-// has already completed, the common case on a pipeline's fast path).
+// Non-blocking probe of an mbarrier phase (cheaper than try_wait when the
+// phase has already completed, the common case on a pipeline's fast path).
 MGQA_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -203,8 +216,11 @@ MGQA_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded wait on an mbarrier phase: gives up after ~`limit_ns` of wall time
+// (measured with the global timer), records MGQA_ERR_TIMEOUT and returns
+// false. Never spins forever.
 MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
-                        uint64_t limit_ns = 2000000000ull) {
+                        uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_test_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;

@@ -221,6 +221,7 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       const int kk = idx / PPR, part = idx % PPR;
       const int loc = sm.slot[bs + kk];
       const int64_t j = (int64_t)(x + S * (loc / C)) * C + loc % C;
+      if (!MGQA_DCHECK(j < p.Lk && g < p.Hkv, p.err)) continue;
       const T *ksrc = kg + j * p.ks_l, *vsrc = vg + j * p.vs_l;
       if (j == pos) {  // the appended row: read it from the step's input
         ksrc = static_cast<const T *>(p.k_new) + (int64_t)b * p.kn_b + (int64_t)g * p.kn_h;
@@ -534,13 +535,9 @@ template <typename T, int D, int NREP>
 mgqa_status launch_t(const DecodeParams &p, cudaStream_t s) {
   auto kern = decode_kernel<T, D, NREP>;
   const size_t smem = sizeof(DecodeSmem<T, D, NREP>);
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the decode kernel");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const mgqa_status st = ensure_smem_attr(kern, (int)smem, attr_done, "decode kernel");
+  if (st != MGQA_OK) return st;
   dim3 grid(S, p.Hq / NREP, p.B);
   const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));

@@ -1,6 +1,7 @@
 // Host-side interfaces between the C ABI (api.cu) and the kernel launchers.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -13,6 +14,23 @@ namespace mgqa {
 mgqa_status fail(mgqa_status code, const char *fmt, ...);
 // Empties the calling thread's error detail (entry points call it first).
 void clear_error_detail();
+
+// Raises `kern`'s dynamic shared-memory limit to `bytes` on the current
+// device the first time it launches there. The attribute belongs to a device,
+// so `done` (one per kernel instantiation, owned by its launcher) keeps a bit
+// per device; host threads that race here both set the same value, which is
+// harmless. Devices past 63 set the attribute on every launch.
+template <typename Kern>
+mgqa_status ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t> &done, const char *what) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MGQA_ERR_CUDA, "no current CUDA device");
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return MGQA_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the %s", what);
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return MGQA_OK;
+}
 
 // Launch with programmatic stream serialisation (the kernel itself calls
 // grid_dependency_wait() before touching global memory).

@@ -137,13 +137,9 @@ template <typename T, int D>
 mgqa_status launch_t(const SimtParams &p, cudaStream_t s) {
   auto kern = prefill_simt_kernel<T, D>;
   const size_t smem = 2 * kKeys * D * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the fp32 prefill kernel");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const mgqa_status st = ensure_smem_attr(kern, (int)smem, attr_done, "fp32 prefill kernel");
+  if (st != MGQA_OK) return st;
   dim3 grid((p.Lq + kRows - 1) / kRows, p.Hq, p.B);
   kern<<<grid, kThreads, smem, s>>>(p);
   const cudaError_t e = cudaGetLastError();

@@ -62,6 +62,24 @@ constexpr int BN = 128;       // keys per tile
 constexpr int MAXKT = 2048;   // key tiles per row (Lk <= 262144)
 constexpr int BOX = 16384;    // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
 
+// Debug library only (MGQA_DEBUG): event counters, an injected producer fault
+// and a settable wait limit, read and written by the mgqa_debug_* entry points.
+#ifdef MGQA_DEBUG
+struct DebugState {
+  unsigned long long counters[4];  // see mgqa_debug_counters
+  int fault_tile;                  // >= 0: the producer stops issuing at this non-empty tile
+  unsigned long long wait_limit_ns;
+};
+__device__ DebugState g_dbg = {{0ull, 0ull, 0ull, 0ull}, -1, kWaitLimitNs};
+MGQA_DEV uint64_t wait_limit() { return *(volatile unsigned long long *)&g_dbg.wait_limit_ns; }
+MGQA_DEV int fault_tile() { return *(volatile int *)&g_dbg.fault_tile; }
+MGQA_DEV void dbg_count(int i, unsigned long long n = 1ull) { atomicAdd(&g_dbg.counters[i], n); }
+#else
+MGQA_DEV uint64_t wait_limit() { return kWaitLimitNs; }
+MGQA_DEV int fault_tile() { return -1; }
+MGQA_DEV void dbg_count(int, unsigned long long = 1ull) {}
+#endif
+
 struct TcParams {
   MaskView mask;
   int B, Hq, Hkv, Lq, Lk, n_rep, nkt;
@@ -80,8 +98,9 @@ struct Layout {
   static constexpr int v_off = k_off + STAGES * KB * BOX;
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
   // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
-  // o_done[NT], spec (the speculative tile-0 loads have landed)
-  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 1;
+  // o_done[NT], spec (the speculative tile-0 loads have landed), drain (every MMA
+  // issued has completed; used when a wait gave up)
+  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
@@ -207,6 +226,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
   if (__any_sync(0xffffffffu, rescale)) {
     // O holds every P.V issued so far: this tile's S MMA was issued after the
     // previous tile's P.V, and its completion covers that MMA.
+    if ((threadIdx.x & 31) == 0) dbg_count(0);  // debug library: rescale events (per warp)
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -272,6 +292,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_pfull = bar_sfull + NT;
   uint64_t *bar_odone = bar_pfull + NT;
   uint64_t *bar_spec = bar_odone + NT;
+  uint64_t *bar_drain = bar_spec + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
@@ -303,6 +324,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bar_odone + t, 1);
     }
     mbar_init(bar_spec, 1);
+    mbar_init(bar_drain, 1);
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_q);
     tc::prefetch_tensormap(&tm_k);
@@ -318,24 +340,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   grid_dependency_wait();
   const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
+  const uint64_t lim = wait_limit();
 
   // ---- Q load, segment range of the query tile ----------------------------
   if (tid == 0) {
     // Q does not depend on the mask: start its load before classifying, and
     // key tile 0 with it (most masks keep it; checked after classifying)
-    if (row0 < p.Lq) {
+    if (row0 < p.Lq && MGQA_DCHECK(h0 + NT <= p.Hq && b < p.B, p.err)) {
       mbar_arrive_expect_tx(bar_q, NT * KB * BOX);
       for (int t = 0; t < NT; ++t)
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::q_off + (t * KB + c) * BOX, &tm_q, c * 64, row0, h0 + t, b,
                           bar_q);
     }
-    mbar_arrive_expect_tx(bar_kfull, KB * BOX);
-    for (int c = 0; c < KB; ++c)
-      tc::tma_load_4d(smem + Lay::k_off + c * BOX, &tm_k, c * 64, 0, g, b, bar_kfull);
-    mbar_arrive_expect_tx(bar_vfull, KB * BOX);
-    for (int c = 0; c < KB; ++c)
-      tc::tma_load_4d(smem + Lay::v_off + c * BOX, &tm_v, c * 64, 0, g, b, bar_vfull);
+    if (MGQA_DCHECK(g < p.Hkv, p.err)) {
+      mbar_arrive_expect_tx(bar_kfull, KB * BOX);
+      for (int c = 0; c < KB; ++c)
+        tc::tma_load_4d(smem + Lay::k_off + c * BOX, &tm_k, c * 64, 0, g, b, bar_kfull);
+      mbar_arrive_expect_tx(bar_vfull, KB * BOX);
+      for (int c = 0; c < KB; ++c)
+        tc::tma_load_4d(smem + Lay::v_off + c * BOX, &tm_v, c * 64, 0, g, b, bar_vfull);
+    }
   }
   if (warp == 0) {
     if (p.mask.seg_q) {
@@ -476,30 +501,57 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (warp == 0) {
     if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- TMA producer ----------------
-    if (lane == 0 && (nk == 0 || spec_miss)) {
-      // every speculative load lands before its stage is reused or the CTA exits
-      ok = mbar_wait(bar_q, 0, p.err) && mbar_wait(bar_kfull, 0, p.err) &&
-           mbar_wait(bar_vfull, 0, p.err);
-      mbar_arrive(bar_spec);  // tells the MMA warp that stage 0 is at its phase 1
-    }
-    if (lane == 0 && nk > 0) {
+    if (lane == 0) {
+      // list entries whose K (V) load has been issued; entry 0's went out
+      // speculatively unless the speculation missed, in which case stage 0
+      // was armed once more than the entries say
+      int k_issued = (nk > 0 && !spec_miss) ? 1 : 0, v_issued = k_issued;
+      const int extra0 = (nk == 0 || spec_miss) ? 1 : 0;
+      if (nk == 0 || spec_miss) {
+        // every speculative load lands before its stage is reused or the CTA exits
+        ok = mbar_wait(bar_q, 0, p.err, lim) && mbar_wait(bar_kfull, 0, p.err, lim) &&
+             mbar_wait(bar_vfull, 0, p.err, lim);
+        mbar_arrive(bar_spec);  // tells the MMA warp that stage 0 is at its phase 1
+      }
+      // debug library: an injected fault stops the loads at this tile (the
+      // consumers' bounded waits then give up and report MGQA_ERR_TIMEOUT)
+      const int stop_at = fault_tile();
       // (an L2 prefetch of the tiles ahead of their loads measured no faster)
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
         const int kt = list[n] & 0x7fff;
         if (n == 0 && !spec_miss) continue;  // tile 0 is already on its way
+        if (n == stop_at) break;
+        if (!MGQA_DCHECK(kt * BN < p.Lk && g < p.Hkv, p.err)) break;
         // K(n) reuses the stage K(n-STAGES) held; it is free once the S MMAs
         // that read it completed (V is released later, after P.V)
-        if (n >= STAGES && !(ok = mbar_wait(bar_kempty + st, (use - 1) & 1, p.err))) break;
+        if (n >= STAGES && !(ok = mbar_wait(bar_kempty + st, (use - 1) & 1, p.err, lim))) break;
         mbar_arrive_expect_tx(bar_kfull + st, KB * BOX);
+        k_issued = n + 1;
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::k_off + (st * KB + c) * BOX, &tm_k, c * 64, kt * BN, g, b,
                           bar_kfull + st);
-        if (n >= STAGES && !(ok = mbar_wait(bar_vempty + st, (use - 1) & 1, p.err))) break;
+        if (n >= STAGES && !(ok = mbar_wait(bar_vempty + st, (use - 1) & 1, p.err, lim))) break;
         mbar_arrive_expect_tx(bar_vfull + st, KB * BOX);
+        v_issued = n + 1;
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::v_off + (st * KB + c) * BOX, &tm_v, c * 64, kt * BN, g, b,
                           bar_vfull + st);
+      }
+      // No copy may still be in flight when the CTA exits. Only this thread
+      // arms the full barriers, so the last armed phase of each is the newest
+      // one it can reach and a parity wait on it is unambiguous. On the normal
+      // path the MMA warp has already seen every one of them land.
+      // times a stage's barrier was armed: entries n < issued with n % STAGES == st
+      auto arms = [&](int issued, int st) {
+        return (st == 0 ? extra0 : 0) + (issued > st ? (issued - 1 - st) / STAGES + 1 : 0);
+      };
+      mbar_wait(bar_q, 0, p.err, lim);
+#pragma unroll
+      for (int st = 0; st < STAGES; ++st) {
+        const int ka = arms(k_issued, st), va = arms(v_issued, st);
+        if (ka > 0) mbar_wait(bar_kfull + st, (ka - 1) & 1, p.err, lim);
+        if (va > 0) mbar_wait(bar_vfull + st, (va - 1) & 1, p.err, lim);
       }
     }
     __syncwarp();
@@ -528,7 +580,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       constexpr uint64_t kTileStep = (uint64_t)(KB * BOX) >> 4;
       // every lane waits; the outcome is made warp-uniform
       auto wait = [&](uint64_t *bar, uint32_t parity) {
-        const bool r = ok && mbar_wait(bar, parity, p.err);
+        const bool r = ok && mbar_wait(bar, parity, p.err, lim);
         ok = __all_sync(0xffffffffu, r);
         return ok;
       };
@@ -627,6 +679,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int last_use = (nk - 1 - s) / STAGES;
         wait(bar_kempty + s, last_use & 1) && wait(bar_vempty + s, last_use & 1);
       }
+      if (!ok) {
+        // a wait gave up: every MMA already issued completes before the tensor
+        // memory is freed (the commit arrives once they all have)
+        if (leader) tc::mma_commit(bar_drain);
+        __syncwarp();
+        mbar_wait(bar_drain, 0, p.err, lim);
+      }
     }
     __syncwarp();
     role_end();
@@ -657,17 +716,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool partial = (ent & 0x8000) != 0;
       uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
       if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
-      if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err);
-      __syncwarp();
-      tc::fence_after_sync();
-      if (neg) {
-        if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l);
-        else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l);
-      } else {
-        if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l);
-        else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l);
+      // warp-uniform outcome: the tile pass below is made of warp-wide
+      // tensor-memory loads and stores
+      if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err, lim);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {  // after a failed wait, tensor memory is left alone
+        tc::fence_after_sync();
+        if (neg) {
+          if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l);
+          else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l);
+        } else {
+          if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l);
+          else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l);
+        }
+        if (lane == 0) dbg_count(1);  // debug library: tiles processed (per warp)
+        tc::fence_before_sync();
       }
-      tc::fence_before_sync();
       mbar_arrive(bar_pfull + t);
     }
     // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
@@ -675,15 +739,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // by TMA tensor stores (rows past Lq are clipped by the store)
     float o_scale = 0.f;
     if (nk > 0) {
-      if (ok) ok = mbar_wait(bar_odone + t, 0, p.err);  // committed once, after the last P.V
-      __syncwarp();
+      if (ok) ok = mbar_wait(bar_odone + t, 0, p.err, lim);  // committed once, after the last P.V
+      ok = __all_sync(0xffffffffu, ok);
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;
     } else if (ok) {
-      ok = mbar_wait(bar_q, 0, p.err);  // the Q load must land before the buffer is reused
+      ok = mbar_wait(bar_q, 0, p.err, lim);  // the Q load must land before the buffer is reused
     }
+    ok = __all_sync(0xffffffffu, ok);
     uint32_t orow[D];
-    if (nk > 0) {
+    if (nk > 0 && ok) {  // after a failed wait the output rows are written as zeros
 #pragma unroll
       for (int c = 0; c < D / 32; ++c)
         tc::tmem_ld32(t_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&orow[c * 32]));
@@ -706,7 +771,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     fence_proxy_async_smem();
     named_sync(2 + t, 128);
-    if (warp == 4 + 4 * t && lane == 0) {
+    if (warp == 4 + 4 * t && lane == 0 && MGQA_DCHECK(row0 < p.Lq && h0 + t < p.Hq, p.err)) {
       for (int c = 0; c < KB; ++c) tc::tma_store_4d(&tm_o, ob + c * BOX, c * 64, row0, h0 + t, b);
       tc::tma_store_commit_and_wait_read();
     }
@@ -756,13 +821,9 @@ mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
                      const CUtensorMap &mo, const TcParams &p, cudaStream_t s) {
   using Lay = Layout<D, NT, STAGES>;
   auto kern = prefill_tc_kernel<T, D, NT, STAGES>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::smem_bytes) !=
-        cudaSuccess)
-      return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the tensor-core prefill");
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_done{0};
+  const mgqa_status st = ensure_smem_attr(kern, Lay::smem_bytes, attr_done, "tensor-core prefill");
+  if (st != MGQA_OK) return st;
   dim3 grid((p.Lq + BM - 1) / BM, p.Hq / NT, p.B);
   const cudaError_t e = launch_pdl(kern, grid, dim3(Lay::threads), Lay::smem_bytes, s, mq, mk, mv,
                                    mo, p);
@@ -811,3 +872,45 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
 }
 
 }  // namespace mgqa
+
+// ---- debug library entry points (include/masked_gqa_attn_debug.h) -----------
+#ifdef MGQA_DEBUG
+#include "../../include/masked_gqa_attn_debug.h"
+
+extern "C" MGQA_API mgqa_status mgqa_debug_counters(uint64_t *out, int32_t n) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (!out || n < 0 || n > MGQA_DEBUG_NUM_COUNTERS)
+    return fail(MGQA_ERR_INVALID_ARG, "mgqa_debug_counters: bad output or count");
+  DebugState st;
+  const cudaError_t e = cudaMemcpyFromSymbol(&st, g_dbg, sizeof(st));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the debug state: %s", cudaGetErrorString(e));
+  for (int i = 0; i < n; ++i) out[i] = st.counters[i];
+  return MGQA_OK;
+}
+
+extern "C" MGQA_API mgqa_status mgqa_debug_reset(void) {
+  using namespace mgqa;
+  clear_error_detail();
+  const DebugState st = {{0ull, 0ull, 0ull, 0ull}, -1, kWaitLimitNs};
+  const cudaError_t e = cudaMemcpyToSymbol(g_dbg, &st, sizeof(st));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "writing the debug state: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+
+extern "C" MGQA_API mgqa_status mgqa_debug_inject_prefill_stall(int32_t tile, uint64_t wait_limit_ns) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (tile == 0 || (tile > 0 && wait_limit_ns == 0))
+    return fail(MGQA_ERR_INVALID_ARG, "stall tile must be >= 1 (or < 0 to clear) with a wait limit > 0");
+  DebugState st;
+  cudaError_t e = cudaMemcpyFromSymbol(&st, g_dbg, sizeof(st));
+  if (e == cudaSuccess) {
+    st.fault_tile = tile < 0 ? -1 : tile;
+    st.wait_limit_ns = tile < 0 ? kWaitLimitNs : wait_limit_ns;
+    e = cudaMemcpyToSymbol(g_dbg, &st, sizeof(st));
+  }
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "writing the debug state: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+#endif  // MGQA_DEBUG

@@ -2,7 +2,7 @@
 //
 // Passages: F5-TTS page, module table and "Upstream-identical practice"
 // (interleaved feature pairs, x-transformers; only the first pe_attn_head
-// heads rotate); Qwen3-TTS page (the inverse-frequency table stays fp32) and
+// heads rotate); OmniVoice page, "Parity results" (the inverse-frequency table stays fp32) and
 // VoxCPM page, "Upstream-identical practice", precision bullet (LongRoPE table
 // built in fp32); OmniVoice page, "Memory & speed", packed_guidance paragraph
 // (positions restart at 0 for each packed sequence).

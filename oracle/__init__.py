@@ -18,7 +18,7 @@ arrays. What it computes, with the passages it follows:
 * VoxCPM page, "Upstream-identical practice", attention bullet: causal
   attention at prefill (query rows = the last Lq of the Lk positions);
 * rotary position embedding (``rope``): F5-TTS page (interleaved pairs, on
-  the first pe_attn_head heads), Qwen3-TTS and VoxCPM pages (fp32 inverse
+  the first pe_attn_head heads), OmniVoice page, "Parity results", and VoxCPM page, precision bullet (fp32 inverse
   frequencies, LongRoPE tables built in fp32), OmniVoice page, packed_guidance
   paragraph (positions restart per packed sequence).
 

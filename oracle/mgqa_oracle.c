@@ -142,7 +142,10 @@ int mgqa_oracle_attention(const double *q, const double *k, const double *v,
  * of the 16- or 32-bit input):
  *   - F5-TTS page, module table and "Upstream-identical practice": the DiT
  *     rotates interleaved feature pairs, on its first pe_attn_head heads only;
- *   - Qwen3-TTS / VoxCPM pages: the language models rotate with an fp32
+ *   - OmniVoice page, "Parity results" (the shared Qwen decoder keeps the
+ *     inverse frequencies in fp32) and VoxCPM page, "Upstream-identical
+ *     practice", precision bullet (the LongRoPE table is built in fp32): the
+ *     language models rotate with an fp32
  *     inverse-frequency table (LongRoPE: a table built in fp32);
  *   - OmniVoice page, "Memory & speed", packed_guidance paragraph: under
  *     packing every sequence's positions start at 0 (so positions are an

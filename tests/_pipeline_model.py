@@ -13,6 +13,14 @@ follow the kernel's loops step by step (the producer, the MMA warp with its
 waits placed inside MMA groups and its probes, the softmax and the epilogue),
 so a change of the kernel's protocol is mirrored here and checked on the CPU
 before it runs on a GPU.
+
+With ``stop_at`` set the model runs the kernel's failure path instead: the
+producer issues no load from that non-empty tile on (the debug library's
+injected stall), every wait is bounded (a waiter that can no longer make
+progress gives up, as the kernel's timed waits do), and the roles follow the
+kernel's code after a wait gave up. The run must then end, with no copy in
+flight when the roles are done (the CTA exits) and no MMA in flight when the
+tensor memory is freed.
 """
 from __future__ import annotations
 
@@ -55,8 +63,11 @@ class Barrier:
         return (self.completed & 1) != parity
 
 
-def _check(bar, parity, k, what):
-    """A parity test on `bar` that means phase k (parity k & 1)."""
+def _check(bar, parity, k, what, strict=True):
+    """A parity test on `bar` that means phase k (parity k & 1). With
+    strict=False (the failure path) only the hardware's answer is returned."""
+    if not strict:
+        return bar.parity_done(parity)
     if parity != (k & 1):
         raise ProtocolError(f"{what}: parity {parity} does not name phase {k}")
     done = bar.parity_done(parity)
@@ -74,9 +85,12 @@ class Model:
     when the first non-empty tile is not tile 0 (the speculative tile-0 loads
     are then wasted). `rng` drives every delay."""
 
-    def __init__(self, NT, STAGES, nk, spec_miss, rng, variant="kernel"):
+    def __init__(self, NT, STAGES, nk, spec_miss, rng, variant="kernel", stop_at=None):
         self.NT, self.STAGES, self.nk, self.spec_miss = NT, STAGES, nk, spec_miss
         self.rng, self.variant = rng, variant
+        self.stop_at = stop_at          # producer stall (failure path) or None
+        self.strict = stop_at is None   # protocol checks only on the normal path
+        self.timeouts = []              # waits that gave up (failure path)
         B = Barrier
         self.q = B("q", 1)
         self.kfull = [B(f"kfull{s}", 1) for s in range(STAGES)]
@@ -87,19 +101,20 @@ class Model:
         self.pfull = [B(f"pfull{t}", 1) for t in range(NT)]
         self.odone = [B(f"odone{t}", 1) for t in range(NT)]
         self.spec = B("spec", 1)
+        self.drain = B("drain", 1)
         self.t = 0.0
         self.events = []      # (time, seq, fn)
         self.seq = 0
         self.pipe_done = 0.0  # completion time of the last issued MMA
 
     # ---- asynchronous agents
-    def at(self, dt, fn):
+    def at(self, dt, fn, kind="step"):
         self.seq += 1
-        heapq.heappush(self.events, (self.t + dt, self.seq, fn))
+        heapq.heappush(self.events, (self.t + dt, self.seq, fn, kind))
 
     def tma(self, bar, nbytes):
         self.at(self.rng.expovariate(1.0) * self.rng.choice([0.1, 1.0, 5.0]),
-                lambda: bar.complete_tx(nbytes))
+                lambda: bar.complete_tx(nbytes), "tma")
 
     def mma(self, n_ops=1):
         start = max(self.t, self.pipe_done)
@@ -108,37 +123,69 @@ class Model:
     def commit(self, bar):
         # arrives once every MMA this thread issued before it has completed
         self.seq += 1
-        heapq.heappush(self.events, (max(self.t, self.pipe_done) + 1e-9, self.seq, bar.arrive))
+        heapq.heappush(self.events, (max(self.t, self.pipe_done) + 1e-9, self.seq, bar.arrive, "mma"))
+
+    @staticmethod
+    def W(bar, k, what):
+        """A bounded wait on `bar` for its phase k; evaluates to False when the
+        wait gave up (failure path only)."""
+        r = yield ("wait", bar, k & 1, k, what)
+        return r
 
     # ---- the roles, as generators of ("wait", bar, parity, k, what) / ("test", ...) /
     # ("delay", dt); everything else happens inline
     def producer(self):
-        m, S = self, self.STAGES
+        m, S, W = self, self.STAGES, self.W
         # kernel start: Q and the speculative key/value tile 0
         m.q.expect_tx_arrive(2); m.tma(m.q, 2)
         m.kfull[0].expect_tx_arrive(1); m.tma(m.kfull[0], 1)
         m.vfull[0].expect_tx_arrive(1); m.tma(m.vfull[0], 1)
         yield ("delay", m.rng.uniform(0, 3))  # classification
+        ok = True
+        k_issued = 1 if (m.nk > 0 and not m.spec_miss) else 0
+        v_issued = k_issued
+        extra0 = 1 if (m.nk == 0 or m.spec_miss) else 0
         if m.nk == 0 or m.spec_miss:
-            yield ("wait", m.q, 0, 0, "producer q")
-            yield ("wait", m.kfull[0], 0, 0, "producer spec k")
-            yield ("wait", m.vfull[0], 0, 0, "producer spec v")
+            ok = yield from W(m.q, 0, "producer q")
+            ok = ok and (yield from W(m.kfull[0], 0, "producer spec k"))
+            ok = ok and (yield from W(m.vfull[0], 0, "producer spec v"))
             if m.variant != "old-speculation":
                 m.spec.arrive()
         for n in range(m.nk):
+            if not ok:
+                break
             st, use = n % S, n // S
             if n == 0 and not m.spec_miss:
                 continue
+            if n == m.stop_at:
+                break
             if n >= S:
-                yield ("wait", m.kempty[st], (use - 1) & 1, use - 1, f"producer kempty n={n}")
+                ok = yield from W(m.kempty[st], use - 1, f"producer kempty n={n}")
+                if not ok:
+                    break
             m.kfull[st].expect_tx_arrive(1); m.tma(m.kfull[st], 1)
+            k_issued = n + 1
             if n >= S:
-                yield ("wait", m.vempty[st], (use - 1) & 1, use - 1, f"producer vempty n={n}")
+                ok = yield from W(m.vempty[st], use - 1, f"producer vempty n={n}")
+                if not ok:
+                    break
             m.vfull[st].expect_tx_arrive(1); m.tma(m.vfull[st], 1)
+            v_issued = n + 1
             yield ("delay", m.rng.uniform(0, 0.5))
+        # the kernel's exit drain: the last armed phase of every full barrier
+        def arms(issued, st):
+            return (extra0 if st == 0 else 0) + ((issued - 1 - st) // S + 1 if issued > st else 0)
+        m.armed_k = [arms(k_issued, st) for st in range(S)]
+        m.armed_v = [arms(v_issued, st) for st in range(S)]
+        yield from W(m.q, 0, "producer drain q")
+        for st in range(S):
+            if m.armed_k[st]:
+                yield from W(m.kfull[st], m.armed_k[st] - 1, f"producer drain kfull{st}")
+            if m.armed_v[st]:
+                yield from W(m.vfull[st], m.armed_v[st] - 1, f"producer drain vfull{st}")
 
     def mma_warp(self):
-        m, S, NT, nk = self, self.STAGES, self.NT, self.nk
+        m, S, NT, nk, W = self, self.STAGES, self.NT, self.nk, self.W
         if nk == 0:
             return
         shift = 1 if m.spec_miss else 0
@@ -155,33 +202,45 @@ class Model:
 
         D16, kLate = 8, 7
         yield ("delay", m.rng.uniform(0, 3))
+        ok = True
         if m.spec_miss:
             if m.variant == "old-speculation":
                 yield ("wait", m.kfull[0], 0, 0, "mma spec k (old)")
                 yield ("wait", m.vfull[0], 0, 0, "mma spec v (old)")
             else:
-                yield ("wait", m.spec, 0, 0, "mma spec")
-        yield ("wait", m.q, 0, 0, "mma q")
-        yield ("wait", m.kfull[0], fill(0, 0) & 1, fill(0, 0), "mma k0")
-        yield ("wait", m.vfull[0], fill(0, 0) & 1, fill(0, 0), "mma v0")
-        for t in range(NT):
-            issue_s(t, 0, 0, D16, D16)
+                ok = yield from W(m.spec, 0, "mma spec")
+        ok = ok and (yield from W(m.q, 0, "mma q"))
+        ok = ok and (yield from W(m.kfull[0], fill(0, 0), "mma k0"))
+        ok = ok and (yield from W(m.vfull[0], fill(0, 0), "mma v0"))
+        if ok:
+            for t in range(NT):
+                issue_s(t, 0, 0, D16, D16)
         p0_seen = False
         for n in range(nk):
+            if not ok:
+                break
             st = n % S
             has_next = n + 1 < nk
             st1, use1 = (n + 1) % S, (n + 1) // S
             p1_seen = False
             for t in range(NT):
+                if not ok:
+                    break
                 if not (p0_seen if t == 0 else p1_seen):
-                    yield ("wait", m.pfull[t], n & 1, n, f"mma pfull{t} n={n}")
+                    ok = yield from W(m.pfull[t], n, f"mma pfull{t} n={n}")
+                    if not ok:
+                        break
                 m.mma(4)
                 if has_next:
                     f1 = fill(st1, use1)
                     if t == 0:
-                        yield ("wait", m.kfull[st1], f1 & 1, f1, f"mma kfull n+1={n + 1}")
+                        ok = yield from W(m.kfull[st1], f1, f"mma kfull n+1={n + 1}")
+                        if not ok:
+                            break
                     if t == NT - 1:
-                        yield ("wait", m.vfull[st1], f1 & 1, f1, f"mma vfull n+1={n + 1}")
+                        ok = yield from W(m.vfull[st1], f1, f"mma vfull n+1={n + 1}")
+                        if not ok:
+                            break
                 m.mma(4)
                 if n == nk - 1:
                     m.commit(m.odone[t])
@@ -200,20 +259,30 @@ class Model:
                         issue_s(t, st1, 0, D16, D16)
                 yield ("delay", m.rng.uniform(0, 0.3))
         for s in range(min(S, nk)):
+            if not ok:
+                break
             last_use = (nk - 1 - s) // S
-            yield ("wait", m.kempty[s], last_use & 1, last_use, f"mma drain kempty{s}")
-            yield ("wait", m.vempty[s], last_use & 1, last_use, f"mma drain vempty{s}")
+            ok = yield from W(m.kempty[s], last_use, f"mma drain kempty{s}")
+            ok = ok and (yield from W(m.vempty[s], last_use, f"mma drain vempty{s}"))
+        if not ok and m.variant != "no-failure-drain":
+            # every MMA issued completes before the tensor memory is freed
+            m.commit(m.drain)
+            yield from W(m.drain, 0, "mma failure drain")
 
     def softmax(self, t):
-        m = self
+        m, W = self, self.W
+        ok = True
         for n in range(m.nk):
-            yield ("wait", m.sfull[t], n & 1, n, f"softmax{t} sfull n={n}")
-            yield ("delay", m.rng.uniform(0.2, 4.0))
+            if ok:
+                ok = yield from W(m.sfull[t], n, f"softmax{t} sfull n={n}")
+            if ok:  # after a failed wait the tile pass is skipped
+                yield ("delay", m.rng.uniform(0.2, 4.0))
             m.pfull[t].arrive()
         if m.nk > 0:
-            yield ("wait", m.odone[t], 0, 0, f"epilogue{t} odone")
-        else:
-            yield ("wait", m.q, 0, 0, f"epilogue{t} q")
+            if ok:
+                yield from W(m.odone[t], 0, f"epilogue{t} odone")
+        elif ok:
+            yield from W(m.q, 0, f"epilogue{t} q")
 
     def _check_end_state(self):
         # every barrier completed exactly the phases the protocol gives it
@@ -241,6 +310,7 @@ class Model:
     def run(self, max_steps=100000):
         actors = [self.producer(), self.mma_warp()] + [self.softmax(t) for t in range(self.NT)]
         state = {i: ("ready", None) for i in range(len(actors))}
+        since = {}  # actor -> time its current wait began
 
         def step(i, value=None):
             try:
@@ -249,6 +319,7 @@ class Model:
                 state[i] = ("done", None)
                 return
             state[i] = ("op", op)
+            since[i] = self.t
 
         for i in range(len(actors)):
             step(i)
@@ -261,21 +332,35 @@ class Model:
                         continue
                     if op[0] == "wait":
                         _, bar, parity, k, what = op
-                        if _check(bar, parity, k, what):
-                            step(i); progressed = True
+                        if _check(bar, parity, k, what, self.strict):
+                            step(i, True); progressed = True
                     elif op[0] == "test":
                         _, bar, parity, k, what = op
-                        step(i, _check(bar, parity, k, what)); progressed = True
+                        step(i, _check(bar, parity, k, what, self.strict)); progressed = True
                     elif op[0] == "delay":
                         state[i] = ("sleep", None)
                         self.at(op[1], lambda i=i: step(i))
                         progressed = True
-            if all(kind == "done" for kind, _ in state.values()) and not self.events:
-                self._check_end_state()
+            if all(kind == "done" for kind, _ in state.values()):
+                # the CTA exits: nothing of it may still be in flight
+                pending = sorted({kind for _, _, _, kind in self.events})
+                if "tma" in pending:
+                    raise ProtocolError("a copy is still in flight when the CTA exits")
+                if "mma" in pending or self.pipe_done > self.t + 1e-6:
+                    raise ProtocolError("an MMA is still in flight when the tensor memory is freed")
+                if self.strict:
+                    self._check_end_state()
                 return
             if not self.events:
-                blocked = [op[4] for kind, op in state.values() if kind == "op"]
-                raise ProtocolError(f"deadlock: blocked on {blocked}")
-            self.t, _, fn = heapq.heappop(self.events)
+                blocked = [(since[i], i, op[4]) for i, (kind, op) in state.items()
+                           if kind == "op" and op[0] == "wait"]
+                if self.strict or not blocked:
+                    raise ProtocolError(f"deadlock: blocked on {[b[2] for b in blocked]}")
+                # failure path: the longest-waiting wait runs out of time first
+                _, i, what = min(blocked)
+                self.timeouts.append(what)
+                step(i, False)
+                continue
+            self.t, _, fn, _ = heapq.heappop(self.events)
             fn()
         raise ProtocolError("schedule did not finish")

@@ -20,8 +20,11 @@ def L():
     return M.lib()
 
 
-def declared_symbols():
-    text = open(HEADER).read()
+DEBUG_HEADER = os.path.join(ROOT, "include", "masked_gqa_attn_debug.h")
+
+
+def declared_symbols(header=HEADER):
+    text = open(header).read()
     return re.findall(r"MGQA_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
 
 
@@ -35,6 +38,24 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
     assert L.mgqa_abi_version() == 3
     assert L.mgqa_status_string(M.MGQA_ERR_TIMEOUT) == b"device wait timed out"
+    assert b"debug" in L.mgqa_status_string(M.MGQA_ERR_DEVICE_CHECK)
+
+
+def test_debug_library_exports_the_debug_entry_points(L):
+    assert set(declared_symbols(DEBUG_HEADER)) == set(M.DEBUG_SYMBOLS)
+    Ld = M.debug_lib()
+    for name in declared_symbols() + declared_symbols(DEBUG_HEADER):
+        assert hasattr(Ld, name), name
+    # the product library carries none of the test equipment
+    for name in M.DEBUG_SYMBOLS:
+        assert not hasattr(L, name), name
+
+
+def test_debug_counter_count_is_checked_on_the_host(L):
+    Ld = M.debug_lib()
+    buf = (ctypes.c_uint64 * 8)()
+    assert Ld.mgqa_debug_counters(buf, 8) == M.MGQA_ERR_INVALID_ARG
+    assert Ld.mgqa_debug_inject_prefill_stall(0, 1000) == M.MGQA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("cname,py", [("mgqa_args", M.MgqaArgs), ("mgqa_rope_args", M.MgqaRopeArgs)])
@@ -90,6 +111,20 @@ def test_prefill_rejects_bad_arguments(L, mutate, code):
     st = L.masked_gqa_attn_prefill(ctypes.byref(a), None)
     assert st == code, L.mgqa_last_error_detail()
     assert L.mgqa_last_error_detail() != b""
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="on a GPU machine the call would launch on the fake pointers")
+@pytest.mark.parametrize("sq,sb", [(0, 32), (0, 0), (32, 0)])
+def test_broadcast_mask_strides_pass_validation(L, sq, sb):
+    # one key-padding row per batch row ([B][1][W], query stride 0) or one
+    # mask for the whole batch (batch stride 0): validation accepts both, so
+    # without a GPU the call fails only later, at the launch
+    a = _valid_args()
+    a.mask_bits = 1 << 22
+    a.mask_stride_q, a.mask_stride_b = sq, sb
+    st = L.masked_gqa_attn_prefill(ctypes.byref(a), None)
+    assert st == M.MGQA_ERR_CUDA, L.mgqa_last_error_detail()
 
 
 def test_null_args_rejected(L):

@@ -284,7 +284,8 @@ def test_causal_first_row_and_single_query(oracle_mod):
 
 
 # ---- rotary position embedding (F5-TTS page: interleaved pairs on the first
-# pe_attn_head heads; Qwen3-TTS / VoxCPM pages: fp32 inverse frequencies;
+# pe_attn_head heads; OmniVoice page, "Parity results", and VoxCPM page,
+# precision bullet: fp32 inverse frequencies;
 # OmniVoice page, packed_guidance: positions restart per packed sequence) ----
 
 def _rope_inputs(seed, B=2, H=3, L=5, D=8):

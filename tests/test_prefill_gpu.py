@@ -63,6 +63,34 @@ def test_padded_cfg_config(M, oracle_mod, variant):
     assert_lse_close(lse, ref_lse, 2e-3)
 
 
+def test_padded_cfg_broadcast_key_padding_mask(M, oracle_mod):
+    """The key-padding mask as one row of words per batch row ([B, 1, W],
+    query stride 0; OmniVoice page, "Upstream-identical practice", attention-
+    mask bullet) gives the oracle's result and the full 4D mask's bits."""
+    wl = W.padded_cfg(variant="bits")
+    full_out, full_lse = run_prefill(M, wl)
+    wl.mask_bits = wl.mask_bits[:, :1, :].contiguous()  # [2, 1, 32]: 128 B per batch row
+    d = to_device(wl)
+    out, lse = run_prefill(M, wl, d=d)
+    assert torch.equal(out, full_out) and torch.equal(lse, full_lse)
+    ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale,
+                                           mask_bits=wl.mask_bits.expand(2, 1024, 32))
+    assert_close_to_oracle(out, ref, torch.bfloat16, "broadcast key padding")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
+def test_broadcast_mask_over_batch_and_queries(M, oracle_mod):
+    """One mask row for every batch row and query (both strides 0), with holes."""
+    wl = W.random_case(12, 3, 4, 2, 300, 450, 128, dtype=torch.bfloat16, mask="bits")
+    row = wl.mask_bits[1:2, 5:6, :].contiguous()  # [1, 1, W]
+    wl.mask_bits = row
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale,
+                                           mask_bits=row.expand(3, 300, row.shape[2]))
+    assert_close_to_oracle(out, ref, torch.bfloat16, "broadcast over batch and queries")
+    assert_lse_close(lse, ref_lse, 2e-3)
+
+
 def test_padded_cfg_bits_equal_kvlen_bitwise(M):
     o1, l1 = run_prefill(M, W.padded_cfg(variant="bits"))
     o2, l2 = run_prefill(M, W.padded_cfg(variant="kvlen"))

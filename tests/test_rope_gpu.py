@@ -20,7 +20,7 @@ def M():
 
 
 def inv_freq_table(rot_dim, base=10000.0):
-    # the usual table, built in fp32 (Qwen3-TTS page: it stays fp32)
+    # the usual table, built in fp32 (OmniVoice page, "Parity results": it stays fp32)
     return (base ** (-torch.arange(0, rot_dim, 2, dtype=torch.float64) / rot_dim)).to(torch.float32)
 
 

@@ -283,6 +283,39 @@ def random_case(seed: int, B, Hq, Hkv, Lq, Lk, D, dtype=torch.bfloat16,
     return w
 
 
+def growing_scores(seed: int, B, Hq, Hkv, L, D, dtype=torch.bfloat16, mask: str = "none",
+                   growth: float = 2.5, tile: int = 128) -> Workload:
+    """Inputs whose row maxima climb from key tile to key tile: the keys of
+    tile t are N(0,1) values times (1 + growth * t), so with q ~ N(0,1) and
+    scale 1/sqrt(D) a row's largest score grows by about 2.6 * growth nats
+    (well over 8 powers of two for growth 2.5) at every tile boundary. Real
+    attention logits span that range; N(0,1) inputs never do. mask as in
+    :func:`random_case` ("none", "bits", "segment")."""
+    w = random_case(seed, B, Hq, Hkv, L, L, D, dtype=dtype, mask=mask)
+    f = 1.0 + growth * (torch.arange(L) // tile).to(torch.float32)
+    w.k = (w.k.to(torch.float32) * f[None, None, :, None]).to(dtype).contiguous()
+    w.name = f"growing_scores_{mask}"
+    w.info["growth"] = growth
+    return w
+
+
+def late_spike(seed: int, B, Hq, Hkv, L, D, dtype=torch.bfloat16, first: int = 127,
+               spike: float = 6.0) -> Workload:
+    """Two segments per row, [0, first) and [first, L): the second starts one
+    key before a tile edge (first = 127). That key is scaled near zero, so
+    the second segment's rows see one low score in their first non-empty
+    tile, then keys scaled by `spike` (scores far higher) in the next ones."""
+    g, q, k, v = random_qkv(seed, B, Hq, Hkv, L, L, D, dtype)
+    kf = k.to(torch.float32)
+    kf[:, :, first] *= 0.01
+    kf[:, :, (first // 128 + 1) * 128:] *= spike
+    seg = torch.zeros((B, L), dtype=torch.int32)
+    seg[:, first:] = 1
+    return Workload("late_spike", q, kf.to(dtype).contiguous(), v, 1.0 / math.sqrt(D),
+                    seg_q=seg, seg_k=seg.clone(), seed=seed,
+                    info=dict(dtype=str(dtype).replace("torch.", ""), first=first, spike=spike))
+
+
 CONFIGS = {
     1: tiny_fp32,
     2: padded_cfg,
