@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MGQA_ABI_VERSION 3
+#define MGQA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define MGQA_API __attribute__((visibility("default")))
@@ -125,15 +125,20 @@ MGQA_API mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t
 MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 
 /* One-query (Lq == 1) attention over a static KV cache of Lk slots. The
- * cache is cut into 128-slot chunks of absolute positions, dealt round-robin
- * to a fixed set of 16 CTAs per (request, KV-head group); masked slots are
- * never read, and the partial results are merged in a fixed order inside the
- * same launch, so the full-cache (mask_bits) and filled-span (kv_len) forms
- * of one mask give bit-identical outputs.
+ * cache is cut into 64-slot chunks of absolute positions, dealt round-robin
+ * to the CTAs of a thread-block cluster (16 CTAs, 8 where the device cannot
+ * co-schedule 16) per (request, KV-head group); masked slots are never read,
+ * and the cluster merges its partial results on chip in a fixed order, so the
+ * full-cache (mask_bits) and filled-span (kv_len) forms of one mask give
+ * bit-identical outputs. When the cache is long (over 16384 slots) and the
+ * grid would leave most of the GPU idle, several clusters serve each
+ * (request, head group) and merge through the workspace.
  * `workspace` is caller-owned device memory of at least
  * masked_gqa_attn_decode_workspace_size(args) bytes, 16-byte aligned, ZEROED
- * ONCE before its first use; each call leaves it ready for the next call.
- * Calls that share a workspace must be ordered on one stream. */
+ * ONCE before its first use; every call leaves its merge tickets (a fixed
+ * region at its start) at zero again, so the same workspace serves later
+ * calls of any shape that fits in it. Calls that share a workspace must be
+ * ordered on one stream. `stream` belongs to the current device. */
 MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
                                             size_t workspace_bytes, cudaStream_t stream);
 
@@ -179,8 +184,10 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
                                             cudaStream_t stream);
 
 /* Bytes of the fixed device scratch array behind masked_gqa_attn_decode_static
- * (one per GPU that loads the library, kept until the process exits). */
-#define MGQA_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
+ * (one per GPU that loads the library, kept until the process exits). Every
+ * valid decode call fits: the largest need is about 75 KB, for a call whose
+ * partial results merge through it. */
+#define MGQA_DECODE_STATIC_SCRATCH_BYTES (128u << 10)
 
 /* masked_gqa_attn_decode without a caller-supplied workspace. No passage of
  * the engine pages has a counterpart: this entry point exists for callers that
@@ -193,11 +200,12 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
  * returns MGQA_ERR_UNSUPPORTED. Nothing is allocated or freed: no cudaMalloc,
  * cudaFree or allocating library routine is called.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture. Every call
- * on a device shares the one array (the previous call's contents stay in it;
- * the merge tickets are cleared on `stream` before each launch), so calls whose
- * executions overlap on the GPU -- different streams, or different host
- * threads -- race and corrupt each other's results: order them on one stream. */
+ * device current; make that first call before any stream capture. `stream`
+ * must belong to the current device. Every call on a device shares the one
+ * array (the previous call's contents stay in it; a call that merges through
+ * it clears its merge tickets on `stream` first), so calls whose executions
+ * overlap on the GPU -- different streams, or different host threads -- race
+ * and corrupt each other's results: order them on one stream. */
 MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream);
 
 /* Rotary position embedding, in place, on q or k before attention (the

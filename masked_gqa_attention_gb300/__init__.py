@@ -39,7 +39,7 @@ __all__ = [
  MGQA_ERR_DEVICE_CHECK) = range(6)
 MGQA_BF16, MGQA_FP32, MGQA_FP16 = 0, 1, 2
 # size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
-DECODE_STATIC_SCRATCH_BYTES = 4 << 20
+DECODE_STATIC_SCRATCH_BYTES = 128 << 10
 
 EXPORTED_SYMBOLS = (
     "masked_gqa_attn_prefill",

@@ -235,6 +235,31 @@ MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
   return true;
 }
 
+// ---- thread-block clusters (distributed shared memory) ---------------------
+
+// Barrier over every thread of the cluster. The arrive releases this thread's
+// earlier shared-memory writes and the wait acquires the other CTAs' ones, so
+// after it each CTA may read what the others stored before they arrived. All
+// threads of every CTA of the cluster must execute it (the cluster's CTAs are
+// co-scheduled, so it cannot wait for a CTA that never started).
+MGQA_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address, in the cluster's shared window, of `p` (a variable of this CTA's
+// shared memory) in the CTA of cluster rank `rank`.
+MGQA_DEV uint32_t cluster_map(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+MGQA_DEV float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // 16-byte asynchronous copy global -> shared through the L1-bypassing path;
 // both addresses 16-byte aligned. Completion: cp_async_wait_all().
 MGQA_DEV void cp_async16(void *dst, const void *src) {
@@ -243,6 +268,12 @@ MGQA_DEV void cp_async16(void *dst, const void *src) {
 }
 MGQA_DEV void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+// Close the group of this thread's copies issued since the last commit.
+MGQA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N> MGQA_DEV void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // D (16x8 fp32) += A (16x16, row) * B (16x8, col), both bf16 or both fp16:

@@ -50,14 +50,26 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
-// kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.
-constexpr int kDecodeChunk = 128;
-constexpr int kDecodeSplits = 16;
+// Decode: the cache is cut into chunks of kDecodeChunk absolute slots; a
+// (request, head group) is served by G thread-block clusters of
+// kDecodeCluster CTAs (8 where the device cannot co-schedule 16), and split
+// x of those G * cluster CTAs owns chunks x, x + G * cluster, ...
+constexpr int kDecodeChunk = 64;
+constexpr int kDecodeCluster = 16;
+// Fixed ticket region at the start of a decode workspace (64 tickets).
+constexpr size_t kDecodeTicketBytes = 256;
 // Longest static cache the decode kernel accepts (bounds its merge tables).
 constexpr int kDecodeMaxLk = 32768;
 // Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).
 int decode_heads_per_cta(int n_rep);
+// Clusters per (request, head group) a decode call uses (G); G > 1 merges the
+// clusters through the workspace.
+int decode_clusters_per_group(const mgqa_args &a, int heads_per_cta);
+struct DecodeWsLayout {
+  int G;                       // clusters per (request, head group)
+  size_t ml, o, tick, total;   // byte offsets of the workspace regions; total size
+};
+DecodeWsLayout decode_ws_layout(const mgqa_args &a);
 size_t decode_workspace_bytes(const mgqa_args &a);
 mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
 mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,

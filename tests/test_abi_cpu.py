@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(L):
     for name in declared_symbols():
         assert hasattr(L, name), name
-    assert L.mgqa_abi_version() == 3
+    assert L.mgqa_abi_version() == 4
     assert L.mgqa_status_string(M.MGQA_ERR_TIMEOUT) == b"device wait timed out"
     assert b"debug" in L.mgqa_status_string(M.MGQA_ERR_DEVICE_CHECK)
 
@@ -140,10 +140,37 @@ def test_decode_validation(L):
     a.Lq = 1
     a.B, a.Hq, a.Hkv, a.Lk, a.D = 8, 16, 2, 8192, 64
     n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
-    # partial (m, l) and D floats per (b, head, split) plus tickets
-    assert n >= 8 * 16 * 16 * (64 + 2) * 4
+    # the static-cache decode merges inside one cluster per (request, head
+    # group): only the fixed ticket region is reserved
+    assert n == 256
     assert L.masked_gqa_attn_decode(ctypes.byref(a), None, n, None) == M.MGQA_ERR_INVALID_ARG
     assert L.masked_gqa_attn_decode(ctypes.byref(a), (1 << 20) + 4, n, None) == M.MGQA_ERR_INVALID_ARG
+    # one request over a 32768-slot cache: two clusters per head group merge
+    # through the workspace (tickets, then (m, l) and D floats per head and cluster)
+    a.B, a.Lk = 1, 32768
+    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
+    assert n == 256 + 256 + 16 * 2 * 64 * 4
+
+
+def test_every_decode_fits_the_static_scratch(L):
+    # the fixed scratch behind masked_gqa_attn_decode_static holds the
+    # workspace of every valid decode call
+    a = _valid_args()
+    a.Lq = 1
+    worst = 0
+    for B in (1, 2, 3, 4, 5, 8, 9, 16, 64):
+        for Hq, Hkv in ((1, 1), (8, 1), (8, 8), (16, 2), (16, 16), (32, 8), (64, 64)):
+            for D in (64, 128):
+                for Lk in (1, 4096, 16384, 16385, 24000, 32768):
+                    a.B, a.Hq, a.Hkv, a.D, a.Lk = B, Hq, Hkv, D, Lk
+                    for fld, H in (("q_stride", Hq), ("k_stride", Hkv), ("v_stride", Hkv),
+                                   ("o_stride", Hq)):
+                        Lx = 1 if fld in ("q_stride", "o_stride") else Lk
+                        getattr(a, fld)[:] = [H * Lx * D, Lx * D, D]
+                    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
+                    assert 0 < n <= M.DECODE_STATIC_SCRATCH_BYTES, (B, Hq, Hkv, D, Lk, n)
+                    worst = max(worst, n)
+    assert worst > 256  # some of these merge through the workspace
 
 
 def _valid_rope():

@@ -121,3 +121,39 @@ def test_cache_full_is_reported_and_clamped(M, oracle_mod):
     wl.kv_len[1] = 512
     ref, _, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
     assert_close_to_oracle(out, ref, torch.bfloat16, "decode clamped")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("B,Hq,Hkv,D", [(1, 16, 2, 64), (2, 8, 1, 128), (1, 4, 4, 64)])
+def test_long_cache_merges_clusters_through_the_workspace(M, oracle_mod, dtype, B, Hq, Hkv, D):
+    """A 32768-slot cache and a small grid: two clusters per (request, head
+    group), merged through the workspace after the in-cluster merge."""
+    wl = W.static_cache_decode(seed=B + Hq + D, variant="span", B=B, Hq=Hq, Hkv=Hkv, D=D,
+                               capacity=32768, lo=17000, hi=32768, dtype=dtype)
+    d = to_device(wl)
+    assert M.masked_gqa_attn_decode_workspace_size(d["q"], d["k"], d["v"], kv_len=d["kv_len"]) > 256
+    out, lse, ws = run_decode(M, wl)
+    ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
+    assert_close_to_oracle(out, ref, dtype, f"long cache {B}/{Hq}/{Hkv}/{D}")
+    assert_lse_close(lse, ref_lse, 1e-5 if dtype == torch.float32 else 1e-3)
+    assert int(ws[:256].abs().sum()) == 0  # the tickets are back at zero
+    full = W.static_cache_decode(seed=B + Hq + D, variant="full", B=B, Hq=Hq, Hkv=Hkv, D=D,
+                                 capacity=32768, lo=17000, hi=32768, dtype=dtype)
+    o2, l2, _ = run_decode(M, full, ws=ws)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+def test_one_workspace_serves_shapes_back_to_back(M, oracle_mod):
+    """A workspace zeroed once serves later calls of other shapes (the merge
+    tickets live in a fixed region that every call returns to zero)."""
+    shapes = [dict(B=1, Hq=16, Hkv=2, D=64, capacity=32768, lo=20000, hi=32768),
+              dict(B=2, Hq=8, Hkv=1, D=128, capacity=32768, lo=17000, hi=30000),
+              dict(B=8, Hq=16, Hkv=2, D=64, capacity=8192, lo=256, hi=3100),
+              dict(B=1, Hq=4, Hkv=4, D=64, capacity=32768, lo=16500, hi=32768)]
+    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+    for i, kw in enumerate(shapes * 2):
+        wl = W.static_cache_decode(seed=300 + i, variant="span", **kw)
+        out, lse, _ = run_decode(M, wl, ws=ws)
+        ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
+        assert_close_to_oracle(out, ref, torch.bfloat16, f"shape {i}")
+        assert_lse_close(lse, ref_lse, 1e-3)
