@@ -126,19 +126,18 @@ MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 
 /* One-query (Lq == 1) attention over a static KV cache of Lk slots. The
  * cache is cut into 64-slot chunks of absolute positions, dealt round-robin
- * to the CTAs of a thread-block cluster (16 CTAs, 8 where the device cannot
- * co-schedule 16) per (request, KV-head group); masked slots are never read,
- * and the cluster merges its partial results on chip in a fixed order, so the
- * full-cache (mask_bits) and filled-span (kv_len) forms of one mask give
- * bit-identical outputs. When the cache is long (over 16384 slots) and the
- * grid would leave most of the GPU idle, several clusters serve each
- * (request, head group) and merge through the workspace.
+ * to a fixed set of 16 CTAs per (request, KV-head group); masked slots are
+ * never read, and the partial results are merged in a fixed order inside the
+ * same launch, so the full-cache (mask_bits) and filled-span (kv_len) forms
+ * of one mask give bit-identical outputs.
  * `workspace` is caller-owned device memory of at least
  * masked_gqa_attn_decode_workspace_size(args) bytes, 16-byte aligned, ZEROED
- * ONCE before its first use; every call leaves its merge tickets (a fixed
- * region at its start) at zero again, so the same workspace serves later
- * calls of any shape that fits in it. Calls that share a workspace must be
- * ordered on one stream. `stream` belongs to the current device. */
+ * ONCE before its first use. It starts with the merge tickets, in a region
+ * that nothing else writes and that every call leaves at zero again, so one
+ * workspace serves later calls of any shape that fits in it (with up to 4096
+ * (request, head group) pairs; larger shapes need it zeroed again after a
+ * call of another shape). Calls that share a workspace must be ordered on one
+ * stream. `stream` belongs to the current device. */
 MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
                                             size_t workspace_bytes, cudaStream_t stream);
 
@@ -184,10 +183,10 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
                                             cudaStream_t stream);
 
 /* Bytes of the fixed device scratch array behind masked_gqa_attn_decode_static
- * (one per GPU that loads the library, kept until the process exits). Every
- * valid decode call fits: the largest need is about 75 KB, for a call whose
- * partial results merge through it. */
-#define MGQA_DECODE_STATIC_SCRATCH_BYTES (128u << 10)
+ * (one per GPU that loads the library, kept until the process exits). It holds
+ * the workspace of every decode call with B * Hq <= 989 at head dim 64, or
+ * B * Hq <= 502 at head dim 128. */
+#define MGQA_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
 
 /* masked_gqa_attn_decode without a caller-supplied workspace. No passage of
  * the engine pages has a counterpart: this entry point exists for callers that
@@ -202,8 +201,8 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
  * The first call on each device looks up the array's device address with that
  * device current; make that first call before any stream capture. `stream`
  * must belong to the current device. Every call on a device shares the one
- * array (the previous call's contents stay in it; a call that merges through
- * it clears its merge tickets on `stream` first), so calls whose executions
+ * array (the previous call's contents stay in it; each call clears its merge
+ * tickets on `stream` first), so calls whose executions
  * overlap on the GPU -- different streams, or different host threads -- race
  * and corrupt each other's results: order them on one stream. */
 MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream);

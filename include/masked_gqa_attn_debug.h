@@ -47,6 +47,16 @@ MGQA_API mgqa_status mgqa_debug_reset(void);
  * memory is freed. tile < 0 removes the stall. Synchronous. */
 MGQA_API mgqa_status mgqa_debug_inject_prefill_stall(int32_t tile, uint64_t wait_limit_ns);
 
+/* Per-CTA timeline of the most recent decode launch, for the first n_ctas
+ * (<= 512) CTAs in launch order (x fastest): 16 values per CTA -- the SM
+ * clock at the kernel's phase boundaries 0..8 (entry; after the grid-
+ * dependency wait; the allowed-slot words formed; the first batch's copies
+ * issued; the first batch landed; every batch computed; the in-CTA merge; the
+ * ticket taken; the merged output written, by the last CTA only), 0 in slots
+ * 9..12, the global timer (ns) at entry and at the ticket, and the SM id.
+ * Synchronous. */
+MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,7 +39,7 @@ __all__ = [
  MGQA_ERR_DEVICE_CHECK) = range(6)
 MGQA_BF16, MGQA_FP32, MGQA_FP16 = 0, 1, 2
 # size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
-DECODE_STATIC_SCRATCH_BYTES = 128 << 10
+DECODE_STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTED_SYMBOLS = (
     "masked_gqa_attn_prefill",
@@ -59,6 +59,7 @@ DEBUG_SYMBOLS = (
     "mgqa_debug_counters",
     "mgqa_debug_reset",
     "mgqa_debug_inject_prefill_stall",
+    "mgqa_debug_decode_timeline",
 )
 DEBUG_NUM_COUNTERS = 4
 
@@ -167,6 +168,8 @@ def debug_lib() -> ctypes.CDLL:
         L.mgqa_debug_reset.restype = ctypes.c_int
         L.mgqa_debug_inject_prefill_stall.argtypes = [ctypes.c_int32, ctypes.c_uint64]
         L.mgqa_debug_inject_prefill_stall.restype = ctypes.c_int
+        L.mgqa_debug_decode_timeline.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
+        L.mgqa_debug_decode_timeline.restype = ctypes.c_int
         _lib_debug = L
     return _lib_debug
 

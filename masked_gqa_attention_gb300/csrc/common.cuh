@@ -216,6 +216,13 @@ MGQA_DEV bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// 2^x on the MUFU unit (approximate, flushes denormals; 2^-inf = 0).
+MGQA_DEV float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Bounded wait on an mbarrier phase: gives up after ~`limit_ns` of wall time
 // (measured with the global timer), records MGQA_ERR_TIMEOUT and returns
 // false. Never spins forever.
@@ -258,6 +265,17 @@ MGQA_DEV float ld_cluster_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global to this CTA's shared
+// memory, both addresses 16-byte aligned; completion is counted in bytes on
+// the mbarrier `bar` (armed by an arrive.expect_tx of the phase's total).
+MGQA_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
 }
 
 // 16-byte asynchronous copy global -> shared through the L1-bypassing path;

@@ -1,6 +1,5 @@
-// One-query attention over a static KV cache: the splits of a (request,
-// KV-head group) form a thread-block cluster and merge their partial results
-// through distributed shared memory, inside one launch.
+// One-query attention over a static KV cache, split over a fixed set of CTAs
+// per (request, KV-head group) and merged by log-sum-exp in the same launch.
 //
 // Passages: VoxCPM page, "Upstream-identical practice", attention bullet
 // (decode against the static cache under an explicit boolean mask; slots past
@@ -8,38 +7,37 @@
 // attention_span paragraph (attend only to the filled blocks of the 8192-slot
 // cache instead of all of it).
 //
-// Design: NS = G * SC CTAs serve one (request b, head group hg) -- the NREP
-// query heads of one KV head -- as G clusters of SC CTAs (SC = 16, or 8 where
-// the device cannot co-schedule 16; G = 1 unless the cache is long and the
-// grid small). The cache is cut into 64-slot chunks of absolute positions;
-// split x owns chunks x, x + NS, x + 2 NS, ...
-//   1. Every input of the mask test (kv_len, the split's mask words, segment
-//      ids) and q are loaded at once. One thread per slot then tests every mask
-//      form; warp ballots give the allowed-slot words, compacted into a dense
-//      ascending list. Masked slots are never read; empty chunks cost nothing.
-//   2. The allowed K and V rows are gathered with 16-byte asynchronous copies
-//      (consecutive threads on one row) into padded shared-memory rows, two
-//      batches of CAPB rows in flight: batch n + 2 is issued as soon as batch
-//      n has been consumed.
+// Design: S = 16 CTAs serve one (request b, head group hg) -- the NREP query
+// heads of one KV head. The cache is cut into 64-slot chunks of absolute
+// positions; CTA x owns chunks x, x + S, x + 2S, ...  A call is a short chain
+// of dependent steps, each kept to one memory round trip or one barrier:
+//   1. Every input of the mask test (kv_len, the CTA's mask words, segment
+//      ids) and q are loaded together. Each warp tests the slots of its
+//      chunks (one lane per slot, ballots) and stores the allowed-slot words.
+//   2. The non-empty chunks, in ascending order, fill batches of CAPR rows at
+//      fixed positions (row = chunk position in the batch * 64 + slot). Each
+//      chunk arrives as TMA tensor boxes of 64 rows (128-byte swizzled for the
+//      16-bit types, so the fragment loads are conflict-free), one mbarrier per
+//      batch. Masked rows then get a zero V row in shared memory, so they add
+//      exact zeros (a chunk past the filled length is never fetched; only the
+//      masked tail of a partly filled chunk is read and discarded); the row a
+//      fused append adds is written in from the step's input.
 //   3. bf16 / fp16: both products on the tensor cores (mma.sync m16n8k16, the
-//      <= 8 query heads padded to 16 rows); each compute warp keeps a running
-//      (m, l, O) over its 16 rows of every batch, and the warps merge in
-//      ascending order. fp32: CUDA cores, per-head batch softmax.
-//   4. The CTA's partial (m, l, O) stays in its shared memory. After a cluster
-//      barrier, cluster rank r merges a 1/SC slice of the NREP x D outputs by
-//      reading the SC partials through distributed shared memory in ascending
-//      rank, and writes them (G = 1). With G > 1 each cluster's merged partial
-//      goes to the caller's workspace instead, and the last CTA to take a
-//      ticket merges the G partials in ascending cluster order.
-// The chunk-to-split assignment and every summation order depend only on the
-// set of allowed slots, so a full-cache bitmask and the equivalent filled
-// length give bit-identical outputs.
+//      <= 8 query heads padded to 16 rows). All warps share one running
+//      maximum per head (exchanged once per batch), so the in-CTA merge of the
+//      warps' outputs is a plain sum. fp32: CUDA cores, per-head batch softmax.
+//   4. Every CTA writes its partial (m, l, O) to the workspace and takes a
+//      ticket; the last of the S CTAs merges them in ascending order.
+// The chunk-to-CTA assignment, the batch layout and every summation order
+// depend only on the set of allowed slots, so a full-cache bitmask and the
+// equivalent filled length give bit-identical outputs.
 #include <cfloat>
 #include <cmath>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace mgqa {
 namespace {
@@ -60,15 +58,41 @@ struct DecodeParams {
   float *lse;
   int32_t *err;
   int B, Hq, Hkv, Lk, n_rep, nch;
-  int G;              // clusters per (request, head group)
-  float2 *ws_ml;      // G > 1: [B][Hq][G] (m in log2 units, l) of each cluster
-  float *ws_o;        // G > 1: [B][Hq][G][D] unnormalised cluster outputs
-  unsigned *ws_tick;  // G > 1: [B][Hq / NREP] arrival tickets
+  unsigned *ws_tick;  // [B][Hq / NREP] arrival tickets
+  float2 *ws_ml;      // [B][Hq][S]    (m in log2 units, l)
+  float *ws_o;        // [B][Hq][S][D] unnormalised partial outputs
 };
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int C = kDecodeChunk;
+constexpr int S = kDecodeSplits;
+constexpr int kMaxCI = kDecodeMaxLk / C / S;  // chunks per CTA (32)
+constexpr int kCPW = kMaxCI / kWarps;         // chunks per warp in the mask test
+static_assert(kMaxCI <= 32, "one ballot covers the CTA's chunks");
+
+// Debug library only (MGQA_DEBUG): a per-CTA timeline of the kernel's phases
+// (SM clock at each phase boundary, the global timer at entry and exit, the
+// SM id), read with mgqa_debug_decode_timeline.
+#ifdef MGQA_DEBUG
+constexpr int kTlCtas = 512, kTlStamps = 16;
+__device__ unsigned long long g_dec_tl[kTlCtas][kTlStamps];
+MGQA_DEV void dec_stamp(int k) {
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (threadIdx.x == 0 && cta < (unsigned)kTlCtas) {
+    g_dec_tl[cta][k] = clock64();
+    if (k == 0) {
+      g_dec_tl[cta][13] = globaltimer_ns();
+      unsigned sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      g_dec_tl[cta][15] = sm;
+    }
+    if (k == 7) g_dec_tl[cta][14] = globaltimer_ns();
+  }
+}
+#else
+MGQA_DEV void dec_stamp(int) {}
+#endif
 
 // bf16 and fp16 run the two products on the tensor cores; fp32 on the CUDA cores.
 // (A causal mask needs nothing here: the single query is the last position.)
@@ -77,124 +101,133 @@ constexpr bool use_mma() {
   return sizeof(T) == 2;
 }
 
-template <typename T, int D, int NREP, int SC>
+// Shared memory of one decode CTA. K and V of a batch are CPB chunk slots of
+// KB TMA boxes (64 rows each): 16-bit rows are 128-byte swizzled boxes of 64
+// columns, fp32 rows plain boxes of D columns.
+template <typename T, int D, int NREP>
 struct DecodeSmem {
   static constexpr bool kMma = use_mma<T>();
-  // dense K/V rows per batch buffer (two buffers): 16 KB of K per buffer for
-  // the 16-bit types at D = 64, 8 KB otherwise
-  static constexpr int CAPB = kMma ? (D == 64 ? 128 : 64) : (D == 64 ? 64 : 32);
-  static constexpr int RS = kMma ? D + 8 : D;  // padded rows: conflict-free fragments
-  static constexpr int CW = kMma ? CAPB / 16 : kWarps;  // compute warps (16 rows each)
-  static constexpr int kMaxCI = kDecodeMaxLk / C / SC;  // chunks of one split (G = 1)
-  struct Rows {
-    alignas(128) T k[2][CAPB][RS];
-    alignas(128) T v[2][CAPB][RS];
+  static constexpr int KB = kMma ? D / 64 : 1;                 // boxes per row
+  static constexpr int BOXB = kMma ? 64 * 128 : 64 * D * 4;    // bytes of one box
+  static constexpr int CHB = KB * BOXB;                        // bytes of one chunk slot
+  static constexpr int CPB = 32768 / CHB;                      // chunks per batch: 32 KB of K
+  static constexpr int CAPR = CPB * C;                         // positional rows per batch
+  static constexpr int RPW = CAPR / kWarps;                    // rows per warp
+  static_assert(CAPR <= kThreads && RPW >= 8, "batch layout");
+  static constexpr int WOB = kWarps * NREP * D * 4;            // per-warp O (after the last batch)
+  static_assert(WOB <= CPB * CHB, "per-warp O fits in the K buffer");
+  // byte offsets (the base is 1024-byte aligned)
+  static constexpr int k_off = 0;
+  static constexpr int v_off = CPB * CHB;
+  static constexpr int misc_off = 2 * CPB * CHB;
+  struct Misc {
+    float q[NREP][D];                 // fp32 path
+    float s[NREP][kMma ? 1 : CAPR];   // fp32 path: one batch's scores / weights
+    float fo[NREP], fb[NREP];         // fp32 path
+    float wmax[kWarps][NREP], wsum[kWarps][NREP];
+    float mrun[NREP];
+    uint32_t words[kMaxCI][2];        // allowed-slot words of the CTA's chunks
+    alignas(16) T newk[D], newv[D];   // the row a fused append adds
+    alignas(8) uint64_t bar;          // one phase per batch
+    int is_last;
   };
-  struct WarpParts {  // per-warp (m, l, O) for the in-CTA merge (after the last batch)
-    float o[CW][NREP][D];
-    float m[CW][NREP], l[CW][NREP];
-  };
-  union {
-    Rows r;
-    WarpParts w;
-  } u;
-  float q[NREP][D];
-  float s[NREP][kMma ? 1 : CAPB];  // fp32 path: one batch's scores / weights
-  float fo[NREP], fb[NREP];
-  // this CTA's partial, read by the cluster merge
-  float pm[NREP], pl[NREP];
-  float po[NREP][D];
-  uint32_t words[kMaxCI][C / 32];  // mask words (bits form), then allowed-slot words
-  int base[kMaxCI];                // dense index of each chunk's first allowed slot
-  uint16_t slot[kMaxCI * C];       // dense list: chunk-local slot index (i * C + t)
-  int n_all;
-  int is_last;
+  static constexpr int total = misc_off + (int)sizeof(Misc) + 1024;  // + alignment slack
+  // byte address of 16-byte segment `seg` of positional row r (16-bit types)
+  static MGQA_DEV uint32_t seg_off(int r, int seg) {
+    const int r64 = r % C;
+    return (r / C) * CHB + (seg / 8) * BOXB + r64 * 128 + (((seg % 8) ^ (r64 & 7)) << 4);
+  }
+  // byte address of row r (fp32: plain rows)
+  static MGQA_DEV uint32_t row_off(int r) { return (r / C) * CHB + (r % C) * (D * 4); }
 };
 
-// 16-byte pieces of the allowed rows [r0, r0 + nb) of the dense list into
-// buffer `buf`; the appended row is read from the step's input.
-template <typename T, int D, int NREP, int SC>
-MGQA_DEV void gather_batch(DecodeSmem<T, D, NREP, SC> &sm, const DecodeParams &p, int buf, int r0,
-                           int nb, const T *kg, const T *vg, int split, int NS, int b, int g,
-                           int pos) {
-  using Sm = DecodeSmem<T, D, NREP, SC>;
-  constexpr int PPR = D * sizeof(T) / 16;  // pieces per row
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < nb * PPR; idx += kThreads) {
-    const int kk = idx / PPR, part = idx % PPR;
-    const int loc = sm.slot[r0 + kk];
-    const int64_t j = (int64_t)(split + NS * (loc / C)) * C + loc % C;
-    if (!MGQA_DCHECK(j < p.Lk && g < p.Hkv, p.err)) continue;
-    const T *ksrc = kg + j * p.ks_l, *vsrc = vg + j * p.vs_l;
-    if (j == pos) {  // the appended row: read it from the step's input
-      ksrc = static_cast<const T *>(p.k_new) + (int64_t)b * p.kn_b + (int64_t)g * p.kn_h;
-      vsrc = static_cast<const T *>(p.v_new) + (int64_t)b * p.vn_b + (int64_t)g * p.vn_h;
-    }
-    cp_async16(reinterpret_cast<char *>(&sm.u.r.k[buf][kk][0]) + part * 16,
-               reinterpret_cast<const char *>(ksrc) + part * 16);
-    cp_async16(reinterpret_cast<char *>(&sm.u.r.v[buf][kk][0]) + part * 16,
-               reinterpret_cast<const char *>(vsrc) + part * 16);
-  }
-  if constexpr (Sm::kMma) {
-    // rows past nb in the last 16-row group feed the P.V MMA with P = 0: keep
-    // them finite (the buffer may hold anything)
-    const int tail = min(Sm::CAPB, (nb + 15) & ~15) - nb;
-    for (int idx = tid; idx < tail * (D / 8); idx += kThreads)
-      *reinterpret_cast<uint4 *>(&sm.u.r.v[buf][nb + idx / (D / 8)][(idx % (D / 8)) * 8]) =
-          make_uint4(0u, 0u, 0u, 0u);
-  }
-}
+// Two CTAs per SM: the 16 x (head groups) x B grid of the static-cache
+// workloads (256 CTAs) then runs in one wave on 152 SMs.
+template <typename T, int D, int NREP>
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const __grid_constant__ DecodeParams p) {
+  using Sm = DecodeSmem<T, D, NREP>;
+  constexpr int CAPR = Sm::CAPR, CPB = Sm::CPB, RPW = Sm::RPW;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char *kbuf = smem + Sm::k_off, *vbuf = smem + Sm::v_off;
+  auto &sm = *reinterpret_cast<typename Sm::Misc *>(smem + Sm::misc_off);
+  float(*wo)[NREP][D] = reinterpret_cast<float(*)[NREP][D]>(kbuf);  // after the last batch
 
-template <typename T, int D, int NREP, int SC>
-__global__ void __launch_bounds__(kThreads)
-decode_kernel(const __grid_constant__ DecodeParams p) {
-  using Sm = DecodeSmem<T, D, NREP, SC>;
-  constexpr int CAPB = Sm::CAPB;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  auto &sm = *reinterpret_cast<Sm *>(smem_raw);
-
-  const int split = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
-  const int rank = split % SC;  // the CTA's rank in its (SC, 1, 1) cluster
-  const int cl = split / SC;    // the cluster's index among the G of this (b, hg)
-  const int NS = SC * p.G;
+  const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) allow_dependents();
+  dec_stamp(0);
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);  // thread 0 arms each batch once
+    fence_mbarrier_init();
+    tc::prefetch_tensormap(&tm_k);
+    tc::prefetch_tensormap(&tm_v);
+    allow_dependents();
+  }
   grid_dependency_wait();  // everything below may read what the previous kernel wrote
+  dec_stamp(1);
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
-  const int nci = split < p.nch ? (p.nch - split + NS - 1) / NS : 0;  // my chunks
+  const int nci = x < p.nch ? (p.nch - x + S - 1) / S : 0;  // my chunks
+  const int gq = lane >> 2, tq = lane & 3;                   // mma fragment coordinates
 
   // ---- 1. every load the mask test and the products need, issued together
   const int kvl_raw = p.kv_len ? __ldg(p.kv_len + b) : p.Lk;
   const T *qb = static_cast<const T *>(p.q) + (int64_t)b * p.qs_b;
-  constexpr int QPT = (NREP * D + kThreads - 1) / kThreads;
-  float qv[QPT];
+  uint32_t qa[use_mma<T>() ? D / 16 : 1][2];  // Q as the A fragment (rows gq + 8: padding)
+  if constexpr (use_mma<T>()) {
 #pragma unroll
-  for (int u = 0; u < QPT; ++u) {
-    const int i = tid + u * kThreads;
-    qv[u] = i < NREP * D ? to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]) : 0.f;
-  }
-  if (p.bits) {
-    const int W = (p.Lk + 31) >> 5;
-    for (int w = tid; w < 2 * nci; w += kThreads) {
-      const int word = ((split + NS * (w >> 1)) * C >> 5) + (w & 1);
-      sm.words[w >> 1][w & 1] = word < W ? __ldg(p.bits + (int64_t)b * p.ms_b + word) : 0u;
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = qa[kk][1] = 0u;
+      if (gq < NREP) {
+        const T *qr = qb + (int64_t)(h0 + gq) * p.qs_h + kk * 16 + 2 * tq;
+        qa[kk][0] = *reinterpret_cast<const uint32_t *>(qr);
+        qa[kk][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
+      }
     }
+  } else {
+    for (int i = tid; i < NREP * D; i += kThreads)
+      sm.q[i / D][i % D] = to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]);
   }
+  uint32_t wbits[kCPW][2];
+  int segk[kCPW][2];
   const int segq = p.seg_q ? __ldg(p.seg_q + b) : 0;
-  constexpr int kPasses = (Sm::kMaxCI * C + kThreads - 1) / kThreads;
-  int segk[kPasses];
-  if (p.seg_k) {
 #pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) {
-      const int i = ps * (kThreads / C) + tid / C, t = tid % C;
-      const int j = (split + NS * i) * C + t;
-      segk[ps] = (i < nci && j < p.Lk) ? __ldg(p.seg_k + (int64_t)b * p.Lk + j) : -1;
+  for (int u = 0; u < kCPW; ++u) {
+    const int i = warp + u * kWarps;
+    const int j0 = (x + S * i) * C;
+    wbits[u][0] = wbits[u][1] = 0xffffffffu;
+    segk[u][0] = segk[u][1] = segq;
+    if (i < nci) {
+      if (p.bits) {
+        const int W = (p.Lk + 31) >> 5;
+        const uint32_t *mrow = p.bits + (int64_t)b * p.ms_b + (j0 >> 5);
+        wbits[u][0] = __ldg(mrow);
+        wbits[u][1] = ((j0 >> 5) + 1 < W) ? __ldg(mrow + 1) : 0u;
+      }
+      if (p.seg_k) {
+        const int32_t *sk = p.seg_k + (int64_t)b * p.Lk + j0;
+        segk[u][0] = (j0 + lane < p.Lk) ? __ldg(sk + lane) : -1;
+        segk[u][1] = (j0 + 32 + lane < p.Lk) ? __ldg(sk + 32 + lane) : -1;
+      }
     }
+  }
+  const T *kg = static_cast<const T *>(p.k) + (int64_t)b * p.ks_b + (int64_t)g * p.ks_h;
+  const T *vg = static_cast<const T *>(p.v) + (int64_t)b * p.vs_b + (int64_t)g * p.vs_h;
+  const T *kn = p.append ? static_cast<const T *>(p.k_new) + (int64_t)b * p.kn_b + (int64_t)g * p.kn_h
+                         : nullptr;
+  const T *vn = p.append ? static_cast<const T *>(p.v_new) + (int64_t)b * p.vn_b + (int64_t)g * p.vn_h
+                         : nullptr;
+  constexpr int SEGS = D * (int)sizeof(T) / 16;  // 16-byte segments of a row
+  if (p.append && tid < 2 * SEGS) {  // the appended row, wherever it lands
+    const uint4 *src = reinterpret_cast<const uint4 *>(tid < SEGS ? kn : vn);
+    reinterpret_cast<uint4 *>(tid < SEGS ? sm.newk : sm.newv)[tid % SEGS] = src[tid % SEGS];
   }
   int kvl = kvl_raw;
   if (kvl < 0 || kvl > p.Lk) {
-    if (split == 0 && hg == 0 && tid == 0) report_error(p.err, MGQA_ERR_INVALID_ARG);
+    if (x == 0 && hg == 0 && tid == 0) report_error(p.err, MGQA_ERR_INVALID_ARG);
     kvl = kvl < 0 ? 0 : p.Lk;
   }
   // append: the new row sits at slot `pos`, and the step attends to it too;
@@ -204,199 +237,215 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     if (kvl < p.Lk) {
       pos = kvl;
       kvl += 1;
-    } else if (split == 0 && hg == 0 && tid == 0) {
+    } else if (x == 0 && hg == 0 && tid == 0) {
       report_error(p.err, MGQA_ERR_INVALID_ARG);
     }
-    if (p.kv_len_out && split == 0 && hg == 0 && tid == 0) p.kv_len_out[b] = kvl;
+    if (p.kv_len_out && x == 0 && hg == 0 && tid == 0) p.kv_len_out[b] = kvl;
   }
+  // allowed-slot words: lane = slot within each 32-slot half of a chunk
 #pragma unroll
-  for (int u = 0; u < QPT; ++u) {
-    const int i = tid + u * kThreads;
-    if (i < NREP * D) sm.q[i / D][i % D] = qv[u];
-  }
-  __syncthreads();  // mask words
-
-  // allowed-slot words (one thread per slot, ballots); the chunk counts
+  for (int u = 0; u < kCPW; ++u) {
+    const int i = warp + u * kWarps;
+    if (i < nci) {  // warp-uniform
 #pragma unroll
-  for (int ps = 0; ps < kPasses; ++ps) {
-    const int i = ps * (kThreads / C) + tid / C, t = tid % C;
-    if (ps * (kThreads / C) >= nci) break;  // CTA-uniform
-    const int j = (split + NS * i) * C + t;
-    bool a = i < nci && j < p.Lk && j < kvl;
-    if (p.bits && i < nci) a = a && ((sm.words[i][t >> 5] >> (t & 31)) & 1u);
-    if (p.seg_k) a = a && segq >= 0 && segk[ps] == segq;
-    const uint32_t word = __ballot_sync(0xffffffffu, a);
-    __syncwarp();  // every lane has read its mask word before lane 0 overwrites it
-    if (lane == 0 && i < nci) sm.words[i][t >> 5] = word;
-  }
-  __syncthreads();
-  // prefix of the chunk counts (one warp; nci <= kMaxCI <= 64)
-  if (warp == 0) {
-    int run = 0;
-    for (int c0 = 0; c0 < nci; c0 += 32) {
-      const int i = c0 + lane;
-      const int cnt = i < nci ? __popc(sm.words[i][0]) + __popc(sm.words[i][1]) : 0;
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (i < nci) sm.base[i] = run + incl - cnt;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) sm.n_all = run;
-  }
-  __syncthreads();
-  // dense list of allowed slots, ascending
-  for (int ps = 0; ps * (kThreads / C) < nci; ++ps) {
-    const int i = ps * (kThreads / C) + tid / C, t = tid % C;
-    if (i < nci) {
-      const uint32_t wd = sm.words[i][t >> 5];
-      if ((wd >> (t & 31)) & 1u) {
-        const int rk = sm.base[i] + (t >= 32 ? __popc(sm.words[i][0]) : 0) +
-                       __popc(wd & ((1u << (t & 31)) - 1u));
-        sm.slot[rk] = (uint16_t)(i * C + t);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int j = (x + S * i) * C + hh * 32 + lane;
+        bool a = j < p.Lk && j < kvl && ((wbits[u][hh] >> lane) & 1u);
+        if (p.seg_k) a = a && segq >= 0 && segk[u][hh] == segq;
+        const uint32_t w = __ballot_sync(0xffffffffu, a);
+        if (lane == 0) sm.words[i][hh] = w;
       }
     }
   }
   __syncthreads();
-  const int n_all = sm.n_all;
-  const int nbatch = (n_all + CAPB - 1) / CAPB;
+  dec_stamp(2);
+  // the non-empty chunks in ascending order: bit i set for chunk i (every warp
+  // forms the same mask)
+  const uint32_t nem = __ballot_sync(0xffffffffu, lane < nci && (sm.words[lane][0] | sm.words[lane][1]));
+  const int n_ne = __popc(nem);
+  const int nbatch = (n_ne + CPB - 1) / CPB;
 
-  // ---- 2-3. batches of dense rows, two in flight
-  const T *kg = static_cast<const T *>(p.k) + (int64_t)b * p.ks_b + (int64_t)g * p.ks_h;
-  const T *vg = static_cast<const T *>(p.v) + (int64_t)b * p.vs_b + (int64_t)g * p.vs_h;
-  for (int bt = 0; bt < 2 && bt < nbatch; ++bt) {
-    gather_batch<T, D, NREP, SC>(sm, p, bt, bt * CAPB, min(CAPB, n_all - bt * CAPB), kg, vg, split,
-                                 NS, b, g, pos);
-    cp_async_commit();
+  // rank of chunk `lane` among the non-empty chunks (-1: empty, or not mine)
+  const int my_rank = ((nem >> lane) & 1u) ? __popc(nem & ((1u << lane) - 1u)) : -1;
+  // allowed-slot words of the chunk in batch position cs of batch bt (0: none);
+  // cs is the same for the whole warp (a warp's rows lie in one chunk slot)
+  auto chunk_words = [&](int bt, int cs, int &chunk) -> uint2 {
+    const uint32_t m = __ballot_sync(0xffffffffu, my_rank == bt * CPB + cs);
+    if (!m) {
+      chunk = -1;
+      return make_uint2(0u, 0u);
+    }
+    chunk = __ffs(m) - 1;
+    return make_uint2(sm.words[chunk][0], sm.words[chunk][1]);
+  };
+
+  // running state: mma path -- every lane holds head gq's shared maximum, its
+  // rows' part of l and its fragment of O; fp32 path -- as in the batch softmax
+  float m_run = -INFINITY, l_part = 0.f;
+  float ow[use_mma<T>() ? D / 8 : 1][4];
+  if constexpr (use_mma<T>()) {
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) ow[dt][0] = ow[dt][1] = ow[dt][2] = ow[dt][3] = 0.f;
   }
-
-  constexpr int EPL = 16 / sizeof(T);  // elements per 16-byte lane load (fp32 path)
-  constexpr int GL = D / EPL;          // lanes per row
-  constexpr int SPW = 32 / GL;         // rows per warp pass
-  constexpr int ROWS_W = CAPB / kWarps;
-  static_assert(GL <= 32 && (Sm::kMma || ROWS_W % SPW == 0), "lane layout");
   constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, dim pair) per thread
   float o[ITEMS][2];
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) o[u][0] = o[u][1] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;  // meaningful in warp r < NREP
-  const int e = lane % GL, sub = lane / GL;
-  // tensor-core path: Q as the A fragment (heads gq < NREP; rows gq + 8 are padding)
-  constexpr int RW = 16;  // dense rows per compute warp per batch
-  const int gq = lane >> 2, tq = lane & 3;
-  uint32_t qa[Sm::kMma ? D / 16 : 1][2];
-  float ow[Sm::kMma ? D / 8 : 1][4];
-  float wm_run = -INFINITY, wl_run = 0.f;
-  if constexpr (Sm::kMma) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = qa[kk][1] = 0u;
-      if (gq < NREP) {
-        qa[kk][0] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
-        qa[kk][1] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
-      }
-    }
-#pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt) ow[dt][0] = ow[dt][1] = ow[dt][2] = ow[dt][3] = 0.f;
-  }
+  float m_h = -INFINITY, l_h = 0.f;  // fp32 path: head `warp`'s running (m, l)
+  bool ok = true;
+  int failed_bt = -1;
 
   for (int bt = 0; bt < nbatch; ++bt) {
-    const int buf = bt & 1;
-    const int nb = min(CAPB, n_all - bt * CAPB);
-    if (bt + 1 < nbatch) cp_async_wait<1>(); else cp_async_wait<0>();
-    __syncthreads();  // batch bt landed for every thread
+    // ---- 2. gather: thread 0 fetches the batch's chunks as TMA boxes
+    const int nbc = min(CPB, n_ne - bt * CPB);  // chunks in this batch
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&sm.bar, (uint32_t)(nbc * 2 * Sm::CHB));
+      uint32_t rem = nem;  // drop the chunks of the earlier batches
+      for (int e = 0; e < bt * CPB; ++e) rem &= rem - 1u;
+      for (int cs = 0; cs < nbc; ++cs) {
+        const int chunk = __ffs(rem) - 1;
+        rem &= rem - 1u;
+        const int row = (x + S * chunk) * C;
+        if (!MGQA_DCHECK(row < p.Lk && g < p.Hkv, p.err)) continue;
+        for (int bx = 0; bx < Sm::KB; ++bx) {
+          tc::tma_load_4d(kbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_k, bx * 64, row, g, b, &sm.bar);
+          tc::tma_load_4d(vbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_v, bx * 64, row, g, b, &sm.bar);
+        }
+      }
+    }
+    if (bt == 0) dec_stamp(3);
+    ok = ok && mbar_wait(&sm.bar, bt & 1, p.err);
+    ok = __syncthreads_and(ok);  // the batch landed, for every thread
+    if (bt == 0) dec_stamp(4);
+    if (!ok) {
+      failed_bt = bt;
+      break;
+    }
+    // masked rows: a zero V row (exact zeros through the product); the row a
+    // fused append adds: the step's input (thread r owns positional row r)
+    if (warp * 32 < CAPR) {  // warp-uniform: whole warps own rows
+      const int r = tid;
+      int chunk = -1;
+      const uint2 w2 = chunk_words(bt, r / C, chunk);
+      const bool allowed = ((((r % C) < 32) ? w2.x : w2.y) >> (r % 32)) & 1u;
+      const bool is_new = allowed && pos >= 0 && (x + S * chunk) * C + (r % C) == pos;
+      if (!allowed || is_new) {
+#pragma unroll
+        for (int sg = 0; sg < SEGS; ++sg) {
+          const uint4 kz = is_new ? reinterpret_cast<const uint4 *>(sm.newk)[sg] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 vz = is_new ? reinterpret_cast<const uint4 *>(sm.newv)[sg] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t off = use_mma<T>() ? Sm::seg_off(r, sg) : Sm::row_off(r) + sg * 16;
+          if (is_new) *reinterpret_cast<uint4 *>(kbuf + off) = kz;
+          *reinterpret_cast<uint4 *>(vbuf + off) = vz;
+        }
+        fence_proxy_async_smem();  // ordered before a later batch's TMA into this row
+      }
+    }
+    __syncthreads();
+    if (bt == 0) dec_stamp(9);
 
-    if constexpr (Sm::kMma) {
-      // warp w owns dense rows [w*16, w*16 + 16) of the batch and keeps its
-      // own running (m, l, O) for head gq; warps merge after the last batch
-      const int r0 = warp * RW;
-      if (warp < Sm::CW && r0 < nb) {
-        const int n8 = min(2, (nb - r0 + 7) / 8);  // 8-row tiles holding a valid row
-        float c[2][4];
+    // ---- 3. the batch's products
+    int chunk_w = -1;
+    const uint2 ww = chunk_words(bt, (warp * RPW) / C, chunk_w);  // a warp's rows share a chunk
+    auto row_allowed = [&](int row) {
+      return (((row % C) < 32 ? ww.x : ww.y) >> (row % 32)) & 1u;
+    };
+    if constexpr (use_mma<T>()) {
+      constexpr int NG = RPW / 16;  // 16-row groups per warp
+      const int r0 = warp * RPW;
+      float c[NG][2][4];
+#pragma unroll
+      for (int g16 = 0; g16 < NG; ++g16)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-          if (nt >= n8) continue;  // warp-uniform
+          float *cc = c[g16][nt];
+          cc[0] = cc[1] = cc[2] = cc[3] = 0.f;
+          const int kr = r0 + g16 * 16 + nt * 8 + gq;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const T *kr = &sm.u.r.k[buf][r0 + nt * 8 + gq][kk * 16 + 2 * tq];
-            mma_16816<T>(c[nt], qa[kk][0], 0u, qa[kk][1], 0u,
-                         *reinterpret_cast<const uint32_t *>(kr),
-                         *reinterpret_cast<const uint32_t *>(kr + 8));
+            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(kbuf + Sm::seg_off(kr, 2 * kk) + 4 * tq);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(kbuf + Sm::seg_off(kr, 2 * kk + 1) + 4 * tq);
+            mma_16816<T>(c[g16][nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
           }
         }
-        float mx = -INFINITY;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int g16 = 0; g16 < NG; ++g16)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int row = r0 + nt * 8 + 2 * tq + h;
-            c[nt][h] = row < nb ? c[nt][h] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, c[nt][h]);
+            const int row = r0 + g16 * 16 + nt * 8 + 2 * tq + h;
+            c[g16][nt][h] = row_allowed(row) ? c[g16][nt][h] * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, c[g16][nt][h]);
           }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(wm_run, mx);
-        const float f = (wm_run == -INFINITY) ? 0.f : exp2f(wm_run - m_new);
-        float ps = 0.f;
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (tq == 0 && gq < NREP) sm.wmax[warp][gq] = mx;
+      __syncthreads();
+      if (bt == 0) dec_stamp(10);
+      float mb = -INFINITY;
+      if (gq < NREP) {
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) mb = fmaxf(mb, sm.wmax[w][gq]);
+      }
+      // finite: the batch holds an allowed row (padding rows gq >= NREP use 0)
+      const float m_new = gq < NREP ? fmaxf(m_run, mb) : 0.f;
+      const float f = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
+      m_run = m_new;
+      l_part *= f;
+#pragma unroll
+      for (int dt = 0; dt < D / 8; ++dt) {
+        ow[dt][0] *= f;
+        ow[dt][1] *= f;
+      }
+#pragma unroll
+      for (int g16 = 0; g16 < NG; ++g16) {
         uint32_t pa[2];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          const float p0 = exp2f(c[nt][0] - m_new), p1 = exp2f(c[nt][1] - m_new);
-          ps += p0 + p1;
+          const float p0 = fast_exp2(c[g16][nt][0] - m_new), p1 = fast_exp2(c[g16][nt][1] - m_new);
+          l_part += p0 + p1;
           pa[nt] = pack2<T>(p0, p1);
-        }
-        ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-        ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-        wl_run = wl_run * f + ps;
-        wm_run = m_new;
-#pragma unroll
-        for (int dt = 0; dt < D / 8; ++dt) {
-          ow[dt][0] *= f;
-          ow[dt][1] *= f;
         }
 #pragma unroll
         for (int dt = 0; dt < D / 8; ++dt) {
           uint32_t b0, b1;
-          ldmatrix_x2_trans(b0, b1, &sm.u.r.v[buf][r0 + (lane & 15)][dt * 8]);
+          ldmatrix_x2_trans(b0, b1, vbuf + Sm::seg_off(r0 + g16 * 16 + (lane & 15), dt));
           mma_16816<T>(ow[dt], pa[0], 0u, pa[1], 0u, b0, b1);
         }
       }
     } else {
-      // scores (log2 units)
+      // scores (log2 units): GL lanes share a row, 16 bytes each
+      constexpr int EPL = 16 / sizeof(T), GL = D / EPL, SPW = 32 / GL;
+      static_assert(GL <= 32 && RPW % SPW == 0, "lane layout");
+      const int e = lane % GL, sub = lane / GL;
       {
         float qr[NREP][EPL];
 #pragma unroll
         for (int r = 0; r < NREP; ++r)
 #pragma unroll
           for (int i = 0; i < EPL; ++i) qr[r][i] = sm.q[r][e * EPL + i];
-        for (int it = 0; it < ROWS_W / SPW; ++it) {
-          const int row_first = warp * ROWS_W + it * SPW;
-          if (row_first >= nb) break;  // warp-uniform
-          const int row = row_first + sub;
-          const bool valid = row < nb;
+        for (int it = 0; it < RPW / SPW; ++it) {
+          const int row = warp * RPW + it * SPW + sub;
           float acc[NREP];
 #pragma unroll
           for (int r = 0; r < NREP; ++r) acc[r] = 0.f;
-          if (valid) {
-            const uint4 uu = *reinterpret_cast<const uint4 *>(&sm.u.r.k[buf][row][e * EPL]);
-            float kf[EPL];
-            unpack16_t<T>(uu, kf);
+          const uint4 uu = *reinterpret_cast<const uint4 *>(kbuf + Sm::row_off(row) + e * 16);
+          float kf[EPL];
+          unpack16_t<T>(uu, kf);
 #pragma unroll
-            for (int r = 0; r < NREP; ++r)
+          for (int r = 0; r < NREP; ++r)
 #pragma unroll
-              for (int i = 0; i < EPL; ++i) acc[r] = fmaf(qr[r][i], kf[i], acc[r]);
-          }
+            for (int i = 0; i < EPL; ++i) acc[r] = fmaf(qr[r][i], kf[i], acc[r]);
 #pragma unroll
           for (int off = GL / 2; off > 0; off >>= 1)
 #pragma unroll
             for (int r = 0; r < NREP; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
-          if (e == 0 && valid) {
+          if (e == 0) {
+            const bool al = row_allowed(row);
 #pragma unroll
-            for (int r = 0; r < NREP; ++r) sm.s[r][row] = acc[r] * p.scale_log2;
+            for (int r = 0; r < NREP; ++r) sm.s[r][row] = al ? acc[r] * p.scale_log2 : -INFINITY;
           }
         }
       }
@@ -405,29 +454,29 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       if (warp < NREP) {
         const int r = warp;
         float mb = -INFINITY;
-        for (int i = lane; i < nb; i += 32) mb = fmaxf(mb, sm.s[r][i]);
+        for (int i = lane; i < CAPR; i += 32) mb = fmaxf(mb, sm.s[r][i]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
         float lb = 0.f;
-        for (int i = lane; i < nb; i += 32) {
+        for (int i = lane; i < CAPR; i += 32) {
           const float pr = exp2f(sm.s[r][i] - mb);
           sm.s[r][i] = pr;
           lb += pr;
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) lb += __shfl_xor_sync(0xffffffffu, lb, off);
-        const float m_new = fmaxf(m_run, mb);
-        const float f_old = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+        const float m_new = fmaxf(m_h, mb);
+        const float f_old = (m_h == -INFINITY) ? 0.f : exp2f(m_h - m_new);
         const float f_b = exp2f(mb - m_new);
-        l_run = l_run * f_old + lb * f_b;
-        m_run = m_new;
+        l_h = l_h * f_old + lb * f_b;
+        m_h = m_new;
         if (lane == 0) {
           sm.fo[r] = f_old;
           sm.fb[r] = f_b;
         }
       }
       __syncthreads();
-      // P.V over the dense rows, ascending
+      // P.V over the batch's rows, ascending
 #pragma unroll
       for (int u = 0; u < ITEMS; ++u) {
         const int idx = tid + u * kThreads;
@@ -435,9 +484,9 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
           const int r = idx / (D / 2), dp = idx % (D / 2);
           float a0 = 0.f, a1 = 0.f;
 #pragma unroll 4
-          for (int kk = 0; kk < nb; ++kk) {
+          for (int kk = 0; kk < CAPR; ++kk) {
             const float pr = sm.s[r][kk];
-            const float2 vv = *reinterpret_cast<const float2 *>(&sm.u.r.v[buf][kk][2 * dp]);
+            const float2 vv = *reinterpret_cast<const float2 *>(vbuf + Sm::row_off(kk) + dp * 8);
             a0 = fmaf(pr, vv.x, a0);
             a1 = fmaf(pr, vv.y, a1);
           }
@@ -446,26 +495,31 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
         }
       }
     }
-    __syncthreads();  // buffer `buf` (and the scores) are free again
-    if (bt + 2 < nbatch) {
-      gather_batch<T, D, NREP, SC>(sm, p, buf, (bt + 2) * CAPB, min(CAPB, n_all - (bt + 2) * CAPB),
-                                   kg, vg, split, NS, b, g, pos);
-      cp_async_commit();
-    }
+    __syncthreads();  // the batch buffers (and the exchange slots) are free again
   }
+  if (failed_bt >= 0) {
+    // a batch's copies did not arrive in time: let them land (bounded) before
+    // the buffers are reused or the CTA exits
+    mbar_wait(&sm.bar, failed_bt & 1, p.err);
+    __syncthreads();
+  }
+  dec_stamp(5);
 
-  if constexpr (Sm::kMma) {
-    // in-CTA merge of the compute warps' (m, l, O), ascending warp order (the
-    // row buffers are free: every batch has been consumed)
-    if (warp < Sm::CW && gq < NREP) {
+  // in-CTA merge: every warp used the same maximum, so O and l are sums
+  float M = -INFINITY;
+  if constexpr (use_mma<T>()) {
+    float l = l_part;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (gq < NREP) {
       if (tq == 0) {
-        sm.u.w.m[warp][gq] = wm_run;
-        sm.u.w.l[warp][gq] = wl_run;
+        sm.wsum[warp][gq] = l;
+        if (warp == 0) sm.mrun[gq] = m_run;
       }
 #pragma unroll
       for (int dt = 0; dt < D / 8; ++dt) {
-        sm.u.w.o[warp][gq][dt * 8 + 2 * tq] = ow[dt][0];
-        sm.u.w.o[warp][gq][dt * 8 + 2 * tq + 1] = ow[dt][1];
+        wo[warp][gq][dt * 8 + 2 * tq] = ow[dt][0];
+        wo[warp][gq][dt * 8 + 2 * tq + 1] = ow[dt][1];
       }
     }
     __syncthreads();
@@ -474,48 +528,32 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
       const int idx = tid + u * kThreads;
       if (idx < NREP * D / 2) {
         const int r = idx / (D / 2), dp = idx % (D / 2);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < Sm::CW; ++w) M = fmaxf(M, sm.u.w.m[w][r]);
         float a0 = 0.f, a1 = 0.f;
-        if (M != -INFINITY) {
 #pragma unroll
-          for (int w = 0; w < Sm::CW; ++w) {
-            if (sm.u.w.m[w][r] == -INFINITY) continue;
-            const float wt = exp2f(sm.u.w.m[w][r] - M);
-            a0 = fmaf(sm.u.w.o[w][r][2 * dp], wt, a0);
-            a1 = fmaf(sm.u.w.o[w][r][2 * dp + 1], wt, a1);
-          }
+        for (int w = 0; w < kWarps; ++w) {
+          a0 += wo[w][r][2 * dp];
+          a1 += wo[w][r][2 * dp + 1];
         }
         o[u][0] = a0;
         o[u][1] = a1;
       }
     }
     if (warp < NREP) {
-      const int r = warp;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < Sm::CW; ++w) M = fmaxf(M, sm.u.w.m[w][r]);
       float L = 0.f;
-      if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < Sm::CW; ++w)
-          if (sm.u.w.m[w][r] != -INFINITY) L = fmaf(sm.u.w.l[w][r], exp2f(sm.u.w.m[w][r] - M), L);
-      }
-      m_run = M;
-      l_run = L;
+      for (int w = 0; w < kWarps; ++w) L += sm.wsum[w][warp];
+      l_h = L;
+      m_h = sm.mrun[warp];
     }
   }
+  M = m_h;  // meaningful in warp r < NREP (head r)
+  dec_stamp(6);
 
   // append: the CTA owning slot pos stores the new row into the cache (once
   // per KV head: only its first head group); no CTA of this step reads that
   // slot from the cache
-  if (pos >= 0 && (pos / C) % NS == split && h0 % p.n_rep == 0) {
+  if (pos >= 0 && (pos / C) % S == x && h0 % p.n_rep == 0) {
     constexpr int PPR = D * sizeof(T) / 16;
-    const char *kn = static_cast<const char *>(p.k_new) +
-                     ((int64_t)b * p.kn_b + (int64_t)g * p.kn_h) * sizeof(T);
-    const char *vn = static_cast<const char *>(p.v_new) +
-                     ((int64_t)b * p.vn_b + (int64_t)g * p.vn_h) * sizeof(T);
     char *kd = const_cast<char *>(reinterpret_cast<const char *>(kg + (int64_t)pos * p.ks_l));
     char *vd = const_cast<char *>(reinterpret_cast<const char *>(vg + (int64_t)pos * p.vs_l));
     for (int part = tid; part < 2 * PPR; part += kThreads) {
@@ -526,215 +564,122 @@ decode_kernel(const __grid_constant__ DecodeParams p) {
     }
   }
 
-  // ---- 4. this CTA's partial into its shared memory; cluster merge
+  // ---- 4. partial of this CTA; the last of the S CTAs merges all of them
+  const int64_t hrow0 = ((int64_t)b * p.Hq + h0) * S;  // ws row of (head h0, split 0)
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) {
     const int idx = tid + u * kThreads;
     if (idx < NREP * D / 2) {
       const int r = idx / (D / 2), dp = idx % (D / 2);
-      sm.po[r][2 * dp] = o[u][0];
-      sm.po[r][2 * dp + 1] = o[u][1];
+      reinterpret_cast<float2 *>(p.ws_o + (hrow0 + (int64_t)r * S + x) * D)[dp] =
+          make_float2(o[u][0], o[u][1]);
     }
   }
-  if (warp < NREP && lane == 0) {
-    sm.pm[warp] = m_run;
-    sm.pl[warp] = (m_run == -INFINITY) ? 0.f : l_run;
-  }
-  cluster_sync();  // every CTA's partial is visible cluster-wide
-  constexpr int PER = NREP * D / SC;  // outputs merged by each CTA of the cluster
-  static_assert(PER >= 1 && PER <= kThreads, "merge slice");
-  const int64_t hrow = (int64_t)b * p.Hq + h0;  // output row of head h0
-  if (tid < PER) {
-    const int oi = rank * PER + tid;
-    const int h = oi / D, d = oi % D;
-    float mv[SC], lv[SC], ov[SC];
-#pragma unroll
-    for (int xx = 0; xx < SC; ++xx) {  // all loads in flight at once
-      mv[xx] = ld_cluster_f32(cluster_map(&sm.pm[h], xx));
-      lv[xx] = ld_cluster_f32(cluster_map(&sm.pl[h], xx));
-      ov[xx] = ld_cluster_f32(cluster_map(&sm.po[h][d], xx));
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int xx = 0; xx < SC; ++xx) M = fmaxf(M, mv[xx]);
-    float L = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int xx = 0; xx < SC; ++xx) {
-        if (mv[xx] == -INFINITY) continue;
-        const float w = exp2f(mv[xx] - M);
-        L = fmaf(lv[xx], w, L);
-        acc = fmaf(ov[xx], w, acc);
-      }
-    }
-    if (p.G == 1) {
-      T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + h) * p.os_h;
-      orow[d] = from_float<T>(L > 0.f ? acc / L : 0.f);
-      if (d == 0 && p.lse) p.lse[hrow + h] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
-    } else {
-      const int64_t wr = (hrow + h) * p.G + cl;
-      p.ws_o[wr * D + d] = acc;
-      if (d == 0) p.ws_ml[wr] = make_float2(M, L);
-      __threadfence();  // visible GPU-wide before this CTA takes its ticket
-    }
-  }
-  cluster_sync();  // no CTA leaves while another may still read its shared memory
-  if (p.G == 1) return;
-
-  // G > 1: the last of the NS CTAs merges the G cluster partials
+  if (warp < NREP && lane == 0)
+    p.ws_ml[hrow0 + (int64_t)warp * S + x] =
+        (ok && M != -INFINITY) ? make_float2(M, l_h) : make_float2(-INFINITY, 0.f);
+  // the barrier orders every thread's partial before thread 0's release
+  // (the acq_rel ticket, at GPU scope); the last CTA acquires through it
   __syncthreads();
   unsigned *tick = p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg;
   if (tid == 0) {
     unsigned t;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(tick) : "memory");
-    sm.is_last = (t == (unsigned)(NS - 1));
+    sm.is_last = (t == (unsigned)(S - 1));
   }
   __syncthreads();
+  dec_stamp(7);
   if (!sm.is_last) return;
-  for (int oi = tid; oi < NREP * D; oi += kThreads) {
-    const int h = oi / D, d = oi % D;
-    const int64_t wr0 = (hrow + h) * p.G;
-    float M = -INFINITY;
-    for (int c2 = 0; c2 < p.G; ++c2) M = fmaxf(M, __ldcg(&p.ws_ml[wr0 + c2].x));
-    float L = 0.f, acc = 0.f;
-    if (M != -INFINITY) {
-      for (int c2 = 0; c2 < p.G; ++c2) {
-        const float2 ml = __ldcg(&p.ws_ml[wr0 + c2]);
-        if (ml.x == -INFINITY) continue;
-        const float w = exp2f(ml.x - M);
-        L = fmaf(ml.y, w, L);
-        acc = fmaf(__ldcg(&p.ws_o[(wr0 + c2) * D + d]), w, acc);
+
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) {
+    const int idx = tid + u * kThreads;
+    if (idx < NREP * D / 2) {
+      const int r = idx / (D / 2), dp = idx % (D / 2);
+      const int64_t hr = hrow0 + (int64_t)r * S;
+      // every split wrote its partial this call (empty ones: m = -inf, zeros),
+      // so all loads go out in one round
+      float2 ml[S], ov[S];
+#pragma unroll
+      for (int xx = 0; xx < S; ++xx) {
+        ml[xx] = __ldcg(&p.ws_ml[hr + xx]);
+        ov[xx] = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hr + xx) * D) + dp);
       }
+      float Mx = -INFINITY;
+#pragma unroll
+      for (int xx = 0; xx < S; ++xx) Mx = fmaxf(Mx, ml[xx].x);
+      float L = 0.f, o0 = 0.f, o1 = 0.f;
+      if (Mx != -INFINITY) {
+#pragma unroll
+        for (int xx = 0; xx < S; ++xx) {
+          if (ml[xx].x == -INFINITY) continue;
+          const float w = exp2f(ml[xx].x - Mx);
+          L = fmaf(ml[xx].y, w, L);
+          o0 = fmaf(ov[xx].x, w, o0);
+          o1 = fmaf(ov[xx].y, w, o1);
+        }
+      }
+      const float inv = (L > 0.f) ? 1.f / L : 0.f;
+      T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
+      orow[2 * dp] = from_float<T>(o0 * inv);
+      orow[2 * dp + 1] = from_float<T>(o1 * inv);
+      if (dp == 0 && p.lse)
+        p.lse[(int64_t)b * p.Hq + h0 + r] = (L > 0.f) ? (Mx + log2f(L)) * kLn2 : -INFINITY;
     }
-    T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + h) * p.os_h;
-    orow[d] = from_float<T>(L > 0.f ? acc / L : 0.f);
-    if (d == 0 && p.lse) p.lse[hrow + h] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   if (tid == 0) *tick = 0u;
+  dec_stamp(8);
 }
 
-// Cluster size the device can co-schedule for this kernel: 16 (non-portable)
-// when at least one such cluster fits, else 8. Decided once per device.
 template <typename T, int D, int NREP>
-int cluster_size_for_device() {
-  static std::atomic<uint64_t> known{0}, is16{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
-  const uint64_t bit = 1ull << dev;
-  if (known.load(std::memory_order_acquire) & bit)
-    return (is16.load(std::memory_order_relaxed) & bit) ? 16 : 8;
-  auto kern = decode_kernel<T, D, NREP, 16>;
-  const size_t smem = sizeof(DecodeSmem<T, D, NREP, 16>);
-  int n = 0;
-  bool ok16 = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                  cudaSuccess &&
-              cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
-                  cudaSuccess;
-  if (ok16) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16, 1, 1);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    ok16 = cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0;
-  }
-  if (!ok16) (void)cudaGetLastError();  // a refused query leaves no error behind
-  if (ok16) is16.fetch_or(bit, std::memory_order_relaxed);
-  known.fetch_or(bit, std::memory_order_release);
-  return ok16 ? 16 : 8;
-}
-
-template <typename T, int D, int NREP, int SC>
-mgqa_status launch_t(const DecodeParams &p, cudaStream_t s) {
-  auto kern = decode_kernel<T, D, NREP, SC>;
-  const size_t smem = sizeof(DecodeSmem<T, D, NREP, SC>);
+mgqa_status launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                     cudaStream_t s) {
+  auto kern = decode_kernel<T, D, NREP>;
+  constexpr int smem = DecodeSmem<T, D, NREP>::total;
   static std::atomic<uint64_t> attr_done{0};
-  const mgqa_status st = ensure_smem_attr(kern, (int)smem, attr_done, "decode kernel");
+  const mgqa_status st = ensure_smem_attr(kern, smem, attr_done, "decode kernel");
   if (st != MGQA_OK) return st;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(SC * p.G, p.Hq / NREP, p.B);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = SC;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  dim3 grid(S, p.Hq / NREP, p.B);
+  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, mk, mv, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
 
-template <typename T, int D, int NREP>
-mgqa_status launch_sc(const DecodeParams &p, cudaStream_t s) {
-  if (cluster_size_for_device<T, D, NREP>() == 16) return launch_t<T, D, NREP, 16>(p, s);
-  return launch_t<T, D, NREP, 8>(p, s);
-}
-
 template <typename T, int D>
-mgqa_status launch_nrep(const DecodeParams &p, int hpc, cudaStream_t s) {
+mgqa_status launch_nrep(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                        int hpc, cudaStream_t s) {
   switch (hpc) {
-    case 1: return launch_sc<T, D, 1>(p, s);
-    case 2: return launch_sc<T, D, 2>(p, s);
-    case 4: return launch_sc<T, D, 4>(p, s);
-    case 8: return launch_sc<T, D, 8>(p, s);
+    case 1: return launch_t<T, D, 1>(mk, mv, p, s);
+    case 2: return launch_t<T, D, 2>(mk, mv, p, s);
+    case 4: return launch_t<T, D, 4>(mk, mv, p, s);
+    case 8: return launch_t<T, D, 8>(mk, mv, p, s);
     default: return fail(MGQA_ERR_UNSUPPORTED, "decode: heads per CTA %d", hpc);
   }
 }
 
 }  // namespace
 
-// Clusters per (request, head group). One cluster of 16 reads at most 2048
-// rows per CTA of a 32768-slot cache; more clusters pay only when the grid
-// would otherwise leave most SMs idle and each CTA would gather over 1024 rows.
-int decode_clusters_per_group(const mgqa_args &a, int hpc) {
-  const int nch = (a.Lk + kDecodeChunk - 1) / kDecodeChunk;
-  const int64_t groups = (int64_t)a.B * (a.Hq / hpc);
-  int G = 1;
-  while (G < 8 && groups <= (int64_t)(kDecodeTicketBytes / sizeof(unsigned)) &&
-         groups * kDecodeCluster * (2 * G) <= 2 * 152 &&
-         (int64_t)((nch + kDecodeCluster * G - 1) / (kDecodeCluster * G)) * kDecodeChunk > 1024)
-    G *= 2;
-  return G;
-}
-
-// The workspace holds the merge tickets and cluster partials of G > 1 calls;
-// a G = 1 call (the usual one) leaves it untouched. The tickets sit in a fixed
-// region at offset 0 that nothing else ever writes and every call returns to
-// zero, so a workspace zeroed once serves later calls of any shape.
-DecodeWsLayout decode_ws_layout(const mgqa_args &a) {
-  const int hpc = decode_heads_per_cta(a.Hq / a.Hkv);
-  const int G = decode_clusters_per_group(a, hpc);
-  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  DecodeWsLayout w;
-  w.G = G;
-  w.tick = 0;
-  w.ml = kDecodeTicketBytes;
-  if (G == 1) {
-    w.o = w.total = w.ml;
-    return w;
-  }
-  const size_t rows = (size_t)a.B * a.Hq * G;
-  w.o = w.ml + up(rows * sizeof(float2));
-  w.total = w.o + up(rows * a.D * sizeof(float));
-  return w;
-}
-
 int decode_heads_per_cta(int n_rep) {
   for (int h : {8, 4, 2, 1})
     if (n_rep % h == 0) return h;
   return 1;
+}
+
+// Tickets first, in a region of at least kDecodeTicketSlots entries that
+// nothing else ever writes and every call returns to zero: a workspace zeroed
+// once serves later calls of any shape with at most that many (request, head
+// group) pairs. Then the partial (m, l) and O of every (request, head, split).
+DecodeWsLayout decode_ws_layout(const mgqa_args &a) {
+  const int hpc = decode_heads_per_cta(a.Hq / a.Hkv);
+  const size_t pairs = (size_t)a.B * (a.Hq / hpc);
+  const size_t rows = (size_t)a.B * a.Hq * S;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  DecodeWsLayout w;
+  w.tick = 0;
+  w.ml = up((pairs > kDecodeTicketSlots ? pairs : kDecodeTicketSlots) * sizeof(unsigned));
+  w.o = w.ml + up(rows * sizeof(float2));
+  w.total = w.o + up(rows * a.D * sizeof(float));
+  return w;
 }
 
 size_t decode_workspace_bytes(const mgqa_args &a) { return decode_ws_layout(a).total; }
@@ -760,12 +705,10 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
   p.lse = a.lse; p.err = a.dev_error;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lk = a.Lk; p.n_rep = a.Hq / a.Hkv;
   p.nch = (a.Lk + kDecodeChunk - 1) / kDecodeChunk;
-  const int hpc = decode_heads_per_cta(p.n_rep);
-  p.G = L.G;
   char *base = static_cast<char *>(ws);
+  p.ws_tick = reinterpret_cast<unsigned *>(base + L.tick);
   p.ws_ml = reinterpret_cast<float2 *>(base + L.ml);
   p.ws_o = reinterpret_cast<float *>(base + L.o);
-  p.ws_tick = reinterpret_cast<unsigned *>(base + L.tick);
   p.append = k_new != nullptr;
   if (p.append) {
     p.k_new = k_new;
@@ -774,15 +717,25 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
     p.vn_b = v_new_stride[0]; p.vn_h = v_new_stride[1];
     p.kv_len_out = kv_len_out;
   }
+  const int hpc = decode_heads_per_cta(p.n_rep);
+  // the cache as TMA boxes of 64 slots: 64-column 128-byte-swizzled boxes for
+  // the 16-bit types, whole fp32 rows otherwise
+  const bool half16 = a.dtype != MGQA_FP32;
+  CUtensorMap mk, mv;
+  if (!make_tma_map_4d(&mk, a.dtype, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride, half16 ? 64 : a.D,
+                       kDecodeChunk, half16) ||
+      !make_tma_map_4d(&mv, a.dtype, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride, half16 ? 64 : a.D,
+                       kDecodeChunk, half16))
+    return fail(MGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the decode cache");
   if (a.dtype == MGQA_BF16) {
-    if (a.D == 64) return launch_nrep<__nv_bfloat16, 64>(p, hpc, s);
-    if (a.D == 128) return launch_nrep<__nv_bfloat16, 128>(p, hpc, s);
+    if (a.D == 64) return launch_nrep<__nv_bfloat16, 64>(mk, mv, p, hpc, s);
+    if (a.D == 128) return launch_nrep<__nv_bfloat16, 128>(mk, mv, p, hpc, s);
   } else if (a.dtype == MGQA_FP16) {
-    if (a.D == 64) return launch_nrep<__half, 64>(p, hpc, s);
-    if (a.D == 128) return launch_nrep<__half, 128>(p, hpc, s);
+    if (a.D == 64) return launch_nrep<__half, 64>(mk, mv, p, hpc, s);
+    if (a.D == 128) return launch_nrep<__half, 128>(mk, mv, p, hpc, s);
   } else {
-    if (a.D == 64) return launch_nrep<float, 64>(p, hpc, s);
-    if (a.D == 128) return launch_nrep<float, 128>(p, hpc, s);
+    if (a.D == 64) return launch_nrep<float, 64>(mk, mv, p, hpc, s);
+    if (a.D == 128) return launch_nrep<float, 128>(mk, mv, p, hpc, s);
   }
   return fail(MGQA_ERR_UNSUPPORTED, "decode: head dim %d", a.D);
 }
@@ -791,7 +744,7 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
 
 // ---- decode with library-owned scratch -------------------------------------
 // For callers that cannot hand the library any device memory of its own: the
-// cluster partials and merge tickets of a call live in one fixed array that
+// partial results and merge tickets of a call live in one fixed array that
 // every GPU loading this library keeps until the process exits.
 
 namespace mgqa {
@@ -835,17 +788,32 @@ extern "C" mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cuda
                       "(pass a workspace to masked_gqa_attn_decode instead)",
                       need, mgqa::kStaticScratchBytes);
   void *ws = nullptr;
-  const mgqa_status st = mgqa::static_scratch(&ws);
+  const mgqa::DecodeWsLayout lay = mgqa::decode_ws_layout(*args);
+  mgqa_status st = mgqa::static_scratch(&ws);
   if (st != MGQA_OK) return st;
   // The merge tickets must start at zero. The array is zero when the library
   // loads and every call returns its tickets to zero, but a call cut short
-  // (its process or context lost mid-kernel) would not: calls that merge
-  // through the array clear the ticket region on the caller's stream first
-  // (calls that merge inside one cluster never touch the array).
-  const mgqa::DecodeWsLayout lay = mgqa::decode_ws_layout(*args);
-  if (lay.G > 1 &&
-      cudaMemsetAsync(static_cast<char *>(ws) + lay.tick, 0, mgqa::kDecodeTicketBytes, stream) !=
-          cudaSuccess)
+  // (its context lost mid-kernel) would not: clear this call's tickets on the
+  // caller's stream first.
+  const size_t pairs = (size_t)args->B * (args->Hq / mgqa::decode_heads_per_cta(args->Hq / args->Hkv));
+  if (cudaMemsetAsync(static_cast<char *>(ws) + lay.tick, 0, pairs * sizeof(unsigned), stream) !=
+      cudaSuccess)
     return mgqa::fail(MGQA_ERR_CUDA, "clearing the decode scratch tickets failed");
   return masked_gqa_attn_decode(args, ws, mgqa::kStaticScratchBytes, stream);
 }
+
+// ---- debug library entry point (include/masked_gqa_attn_debug.h) ------------
+#ifdef MGQA_DEBUG
+#include "../../include/masked_gqa_attn_debug.h"
+
+extern "C" MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (!out || n_ctas < 0 || n_ctas > kTlCtas)
+    return fail(MGQA_ERR_INVALID_ARG, "mgqa_debug_decode_timeline: bad output or count");
+  const cudaError_t e =
+      cudaMemcpyFromSymbol(out, g_dec_tl, (size_t)n_ctas * kTlStamps * sizeof(uint64_t));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the timeline: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+#endif  // MGQA_DEBUG

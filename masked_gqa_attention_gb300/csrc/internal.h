@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/masked_gqa_attn.h"
@@ -50,24 +51,19 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
-// Decode: the cache is cut into chunks of kDecodeChunk absolute slots; a
-// (request, head group) is served by G thread-block clusters of
-// kDecodeCluster CTAs (8 where the device cannot co-schedule 16), and split
-// x of those G * cluster CTAs owns chunks x, x + G * cluster, ...
+// Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
+// kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.
 constexpr int kDecodeChunk = 64;
-constexpr int kDecodeCluster = 16;
-// Fixed ticket region at the start of a decode workspace (64 tickets).
-constexpr size_t kDecodeTicketBytes = 256;
+constexpr int kDecodeSplits = 16;
+// Ticket region at the start of a decode workspace: room for this many
+// (request, head group) pairs before the region grows with the shape.
+constexpr size_t kDecodeTicketSlots = 4096;
 // Longest static cache the decode kernel accepts (bounds its merge tables).
 constexpr int kDecodeMaxLk = 32768;
 // Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).
 int decode_heads_per_cta(int n_rep);
-// Clusters per (request, head group) a decode call uses (G); G > 1 merges the
-// clusters through the workspace.
-int decode_clusters_per_group(const mgqa_args &a, int heads_per_cta);
 struct DecodeWsLayout {
-  int G;                       // clusters per (request, head group)
-  size_t ml, o, tick, total;   // byte offsets of the workspace regions; total size
+  size_t tick, ml, o, total;  // byte offsets of the workspace regions; total size
 };
 DecodeWsLayout decode_ws_layout(const mgqa_args &a);
 size_t decode_workspace_bytes(const mgqa_args &a);
@@ -80,6 +76,13 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
 mgqa_status pack_pair(bool unpack, mgqa_dtype dt, int B, int H, int D, const void *a,
                       const int64_t *as, int La, const void *b, const int64_t *bs, int Lb,
                       const void *packed, const int64_t *ps, int32_t *seg, cudaStream_t s);
+
+// 4-D tensor map over a [B][H][L][D] view with element strides st = (batch,
+// head, position), for TMA boxes of box_x columns x box_y rows (128-byte
+// swizzle or none). false when the driver entry point is missing or the
+// encoding is refused.
+bool make_tma_map_4d(CUtensorMap *m, mgqa_dtype dt, const void *base, int B, int H, int L, int D,
+                     const int64_t *st, int box_x, int box_y, bool swizzle128);
 
 // Prefill on the CUDA cores (fp32 I/O).
 mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s);

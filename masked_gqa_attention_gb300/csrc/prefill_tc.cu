@@ -784,37 +784,49 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
 // ---- host side ----------------------------------------------------------------
 
+}  // namespace
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+static EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load(std::memory_order_acquire);
+  if (!f) {
     void *ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(ptr);
+      fn.store(f, std::memory_order_release);
+    }
   }
-  return fn;
+  return f;
 }
 
-// 16-bit [B][H][L][D] view with element strides (b, h, l) -> 4-D map, box 64 x 128.
-bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, int B, int H, int L, int D,
-              const int64_t *st) {
+bool make_tma_map_4d(CUtensorMap *m, mgqa_dtype dt, const void *base, int B, int H, int L, int D,
+                     const int64_t *st, int box_x, int box_y, bool swizzle128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const size_t es = dt == MGQA_FP32 ? 4 : 2;
+  const CUtensorMapDataType t = dt == MGQA_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                : dt == MGQA_FP16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)L, (cuuint64_t)H, (cuuint64_t)B};
-  const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint64_t strides[3] = {(cuuint64_t)st[2] * es, (cuuint64_t)st[1] * es,
+                                 (cuuint64_t)st[0] * es};
+  const cuuint32_t box[4] = {(cuuint32_t)box_x, (cuuint32_t)box_y, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, dt, 4, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(m, t, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <typename T, int D, int NT, int STAGES>
 mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
@@ -849,13 +861,12 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
     return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill takes bf16 or fp16");
   const int nkt = (a.Lk + BN - 1) / BN;
   if (nkt > MAXKT) return fail(MGQA_ERR_UNSUPPORTED, "Lk > %d", MAXKT * BN);
-  const CUtensorMapDataType dt =
-      a.dtype == MGQA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // 16-bit [B][H][L][D] views, boxes of 64 columns x 128 rows, 128-byte swizzle
   CUtensorMap mq, mk, mv, mo;
-  if (!make_map(&mq, dt, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride) ||
-      !make_map(&mk, dt, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride) ||
-      !make_map(&mv, dt, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride) ||
-      !make_map(&mo, dt, a.out, a.B, a.Hq, a.Lq, a.D, a.o_stride))
+  if (!make_tma_map_4d(&mq, a.dtype, a.q, a.B, a.Hq, a.Lq, a.D, a.q_stride, 64, BM, true) ||
+      !make_tma_map_4d(&mk, a.dtype, a.k, a.B, a.Hkv, a.Lk, a.D, a.k_stride, 64, BN, true) ||
+      !make_tma_map_4d(&mv, a.dtype, a.v, a.B, a.Hkv, a.Lk, a.D, a.v_stride, 64, BN, true) ||
+      !make_tma_map_4d(&mo, a.dtype, a.out, a.B, a.Hq, a.Lq, a.D, a.o_stride, 64, BM, true))
     return fail(MGQA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   TcParams p{};
   p.mask = MaskView{a.mask_bits, a.mask_stride_b, a.mask_stride_q, a.kv_len, a.seg_q, a.seg_k,

@@ -140,37 +140,32 @@ def test_decode_validation(L):
     a.Lq = 1
     a.B, a.Hq, a.Hkv, a.Lk, a.D = 8, 16, 2, 8192, 64
     n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
-    # the static-cache decode merges inside one cluster per (request, head
-    # group): only the fixed ticket region is reserved
-    assert n == 256
+    # a fixed 4096-entry ticket region, then (m, l) and D floats per
+    # (request, head, split), 16 splits
+    assert n == 4096 * 4 + 8 * 16 * 16 * 8 + 8 * 16 * 16 * 64 * 4
     assert L.masked_gqa_attn_decode(ctypes.byref(a), None, n, None) == M.MGQA_ERR_INVALID_ARG
     assert L.masked_gqa_attn_decode(ctypes.byref(a), (1 << 20) + 4, n, None) == M.MGQA_ERR_INVALID_ARG
-    # one request over a 32768-slot cache: two clusters per head group merge
-    # through the workspace (tickets, then (m, l) and D floats per head and cluster)
-    a.B, a.Lk = 1, 32768
-    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
-    assert n == 256 + 256 + 16 * 2 * 64 * 4
+    assert L.masked_gqa_attn_decode(ctypes.byref(a), 1 << 20, n - 16, None) == M.MGQA_ERR_INVALID_ARG
 
 
-def test_every_decode_fits_the_static_scratch(L):
-    # the fixed scratch behind masked_gqa_attn_decode_static holds the
-    # workspace of every valid decode call
+def _decode_args(BHq, D):
     a = _valid_args()
-    a.Lq = 1
-    worst = 0
-    for B in (1, 2, 3, 4, 5, 8, 9, 16, 64):
-        for Hq, Hkv in ((1, 1), (8, 1), (8, 8), (16, 2), (16, 16), (32, 8), (64, 64)):
-            for D in (64, 128):
-                for Lk in (1, 4096, 16384, 16385, 24000, 32768):
-                    a.B, a.Hq, a.Hkv, a.D, a.Lk = B, Hq, Hkv, D, Lk
-                    for fld, H in (("q_stride", Hq), ("k_stride", Hkv), ("v_stride", Hkv),
-                                   ("o_stride", Hq)):
-                        Lx = 1 if fld in ("q_stride", "o_stride") else Lk
-                        getattr(a, fld)[:] = [H * Lx * D, Lx * D, D]
-                    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
-                    assert 0 < n <= M.DECODE_STATIC_SCRATCH_BYTES, (B, Hq, Hkv, D, Lk, n)
-                    worst = max(worst, n)
-    assert worst > 256  # some of these merge through the workspace
+    a.Lq, a.B, a.Hq, a.Hkv, a.Lk, a.D = 1, BHq, 1, 1, 8192, D
+    for fld, Lx in (("q_stride", 1), ("k_stride", 8192), ("v_stride", 8192), ("o_stride", 1)):
+        getattr(a, fld)[:] = [Lx * D, Lx * D, D]
+    return a
+
+
+@pytest.mark.parametrize("D,limit", [(64, 989), (128, 502)])
+def test_static_scratch_limit_is_as_documented(L, D, limit):
+    # masked_gqa_attn_decode_static holds the workspace of every call with
+    # B * Hq up to the documented limit, and of none beyond it
+    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(_decode_args(limit, D)))
+    assert 0 < n <= M.DECODE_STATIC_SCRATCH_BYTES
+    n = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(_decode_args(limit + 1, D)))
+    assert n > M.DECODE_STATIC_SCRATCH_BYTES
+    text = open(HEADER).read()
+    assert f"B * Hq <= {limit} at head dim {D}" in text.replace("\n * ", " ")
 
 
 def _valid_rope():

@@ -68,8 +68,9 @@ def test_repeated_calls_reuse_workspace(M):
     for _ in range(3):
         o2, l2, _ = run_decode(M, wl, ws=ws)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    # the tickets are back at zero after every call
-    assert int(ws[-4 * 8 * 16:].view(torch.int32).abs().sum()) == 0
+    # the tickets (the workspace's first 4 bytes per (request, head group))
+    # are back at zero after every call
+    assert int(ws[:4 * 8 * 2].view(torch.int32).abs().sum()) == 0
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
@@ -125,13 +126,12 @@ def test_cache_full_is_reported_and_clamped(M, oracle_mod):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("B,Hq,Hkv,D", [(1, 16, 2, 64), (2, 8, 1, 128), (1, 4, 4, 64)])
-def test_long_cache_merges_clusters_through_the_workspace(M, oracle_mod, dtype, B, Hq, Hkv, D):
-    """A 32768-slot cache and a small grid: two clusters per (request, head
-    group), merged through the workspace after the in-cluster merge."""
+def test_long_cache_many_batches(M, oracle_mod, dtype, B, Hq, Hkv, D):
+    """A 32768-slot cache filled past 17000 slots: every CTA runs several
+    batches of rows (the running maximum carried from batch to batch); the
+    bitmask and filled-length forms stay bit-identical."""
     wl = W.static_cache_decode(seed=B + Hq + D, variant="span", B=B, Hq=Hq, Hkv=Hkv, D=D,
                                capacity=32768, lo=17000, hi=32768, dtype=dtype)
-    d = to_device(wl)
-    assert M.masked_gqa_attn_decode_workspace_size(d["q"], d["k"], d["v"], kv_len=d["kv_len"]) > 256
     out, lse, ws = run_decode(M, wl)
     ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
     assert_close_to_oracle(out, ref, dtype, f"long cache {B}/{Hq}/{Hkv}/{D}")
@@ -149,8 +149,8 @@ def test_one_workspace_serves_shapes_back_to_back(M, oracle_mod):
     shapes = [dict(B=1, Hq=16, Hkv=2, D=64, capacity=32768, lo=20000, hi=32768),
               dict(B=2, Hq=8, Hkv=1, D=128, capacity=32768, lo=17000, hi=30000),
               dict(B=8, Hq=16, Hkv=2, D=64, capacity=8192, lo=256, hi=3100),
-              dict(B=1, Hq=4, Hkv=4, D=64, capacity=32768, lo=16500, hi=32768)]
-    ws = torch.zeros(1 << 16, dtype=torch.uint8, device="cuda")
+              dict(B=3, Hq=4, Hkv=4, D=128, capacity=5000, lo=1, hi=5000)]
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     for i, kw in enumerate(shapes * 2):
         wl = W.static_cache_decode(seed=300 + i, variant="span", **kw)
         out, lse, _ = run_decode(M, wl, ws=ws)

@@ -44,8 +44,7 @@ def _static_call(M, d, masks, wl):
 def test_static_scratch_decode_matches_workspace_decode(M, oracle_mod):
     cases = [
         W.static_cache_decode(variant="full"),  # the 8-request, 8192-slot cache
-        # one request over a 32768-slot cache: two clusters per head group
-        # merge through the scratch array
+        # one request over a long cache: several batches per CTA
         W.static_cache_decode(seed=98, variant="span", B=1, Hq=16, Hkv=2, D=64,
                               capacity=32768, lo=20000, hi=32768),
         W.static_cache_decode(seed=99, variant="span", B=5, Hq=8, Hkv=2, D=128,
@@ -86,10 +85,16 @@ def test_static_scratch_decode_allocates_nothing(M):
     assert torch.cuda.mem_get_info()[0] == free0
 
 
-def test_static_scratch_holds_the_largest_merge(M):
-    """The largest workspace a decode call can need fits the fixed scratch
-    (calls that merge inside one cluster leave it untouched)."""
-    q = torch.zeros((9, 8, 1, 128), dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros((9, 1, 1, 128), dtype=torch.bfloat16, device="cuda").expand(9, 1, 16385, 128)
-    need = M.masked_gqa_attn_decode_workspace_size(q, k, k)
-    assert 256 < need <= M.DECODE_STATIC_SCRATCH_BYTES
+def test_static_scratch_rejects_oversized_calls(M):
+    L = M.lib()
+    # 64 requests x 32 heads need more than the fixed scratch (B * Hq over the
+    # documented limit); the cache is a broadcast view and the call is
+    # rejected before any launch
+    q = torch.zeros((64, 32, 1, 128), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((64, 8, 1, 128), dtype=torch.bfloat16, device="cuda").expand(64, 8, 32768, 128)
+    a = M.make_args(q, k, k, q.clone())
+    need = L.masked_gqa_attn_decode_workspace_size(ctypes.byref(a))
+    assert need > M.DECODE_STATIC_SCRATCH_BYTES
+    st = L.masked_gqa_attn_decode_static(ctypes.byref(a), torch.cuda.current_stream().cuda_stream)
+    assert st == M.MGQA_ERR_UNSUPPORTED
+    assert b"scratch" in L.mgqa_last_error_detail()
