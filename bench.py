@@ -2,23 +2,23 @@
 """Benchmark of the masked GQA attention library on synthetic engine-shaped
 workloads; prints ONE JSON line (rank 0).
 
-Headline workload (one "step"): the OmniVoice-shaped padded
-classifier-free-guidance prefill -- batch 2 (conditional row: 1024 valid keys;
-unconditional row: 384 valid keys, rest padded), 16 query heads, 8 KV heads,
-head_dim 128, 1024 positions, bf16, 4D key-padding mask as packed bits --
-called 32 times (the 32 unmasking steps), each call on the next of 8
-rotating input sets (201 MB > L2) so every call reads HBM. The step is
-captured once in a CUDA graph and replayed.
+Headline workload (one "step"): the largest single-GPU configuration, the
+DiT-style bidirectional batch -- 32 rows x 4096 positions, 16 query heads, 4
+KV heads, head_dim 128, bf16, each row cut into 1..6 block-diagonal segments
+at seeded, tile-unaligned cut points -- called 20 times (10 Euler steps x the
+classifier-free-guidance pair). The inputs (805 MB) are larger than L2, the
+step is captured once in a CUDA graph and replayed.
 
-Also measured in the same run and reported under "decode" and
-"other_workloads": static-cache decode (8 requests, 16/2 heads, dim 64,
-8192-slot cache, filled 256..3100, 16 rotating cache sets of 33.5 MB),
-packed-guidance prefill (one 1408-position row, segments 1024 + 384), the
-DiT batch (32 rows x 4096 positions, 1..6 segments per row), and the rotary
-position embedding of the headline's q and k (12 rotating sets, 144 MB).
+Every other configuration is measured in the same run and reported under
+"configs", each with its own roofline block, CPU-oracle baseline and clock
+sample: the tiny fp32 case, the OmniVoice-shaped padded CFG prefill (32 calls
+per step over 8 rotating input sets, 201 MB), the packed-guidance prefill,
+the static-cache decode (8 requests, 8192-slot caches filled 256..3100, 16
+rotating cache sets of 33.5 MB), and the rotary embedding of the padded-CFG q
+and k.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
-sample of the same workload (the baseline arm).
+sample of the headline workload (the baseline arm).
 """
 from __future__ import annotations
 
@@ -40,7 +40,8 @@ import torch  # noqa: E402
 import workloads as W  # noqa: E402
 
 METRIC = "masked GQA prefill TFLOP/s & cache-decode GB/s, as % of GB300 roofline"
-CALLS_PER_STEP = 32
+DIT_CALLS = 20          # 10 Euler steps x the CFG pair
+CFG_CALLS = 32          # the 32 unmasking steps of the padded-CFG prefill
 PREFILL_SETS = 8
 DECODE_SETS = 16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -213,45 +214,6 @@ def bench_prefill_graph(M, wl, dev, calls, nsets, steps, warmup, world):
     return secs, sets
 
 
-def bench_prefill_e2e(M, wl, dev, calls, steps, warmup, world):
-    """Through the C ABI from pinned host buffers: per step H2D of q/k/v/mask,
-    `calls` prefill calls, D2H of the output."""
-    import ctypes
-    host = {n: (getattr(wl, n).pin_memory() if getattr(wl, n) is not None else None)
-            for n in ("q", "k", "v", "mask_bits", "kv_len", "seg_q", "seg_k")}
-    d = {n: (torch.empty_like(t, device=dev) if t is not None else None) for n, t in host.items()}
-    out = torch.empty_like(d["q"])
-    out_host = torch.empty_like(host["q"]).pin_memory()
-    a = make_args(M, d, out, wl)
-    L = M.lib()
-    stream = torch.cuda.Stream(device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
-    d2h = out_host.numel() * out_host.element_size()
-
-    def step():
-        with torch.cuda.stream(stream):
-            for n, t in host.items():
-                if t is not None:
-                    d[n].copy_(t, non_blocking=True)
-            for _ in range(calls):
-                st = L.masked_gqa_attn_prefill(ctypes.byref(a), stream.cuda_stream)
-                if st != 0:
-                    raise RuntimeError(L.mgqa_last_error_detail())
-            out_host.copy_(out, non_blocking=True)
-
-    for _ in range(warmup):
-        step()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    return e0.elapsed_time(e1) / 1e3, h2d, d2h
-
-
 def bench_rope(M, dev, reps=20, warmup=3, nsets=12):
     """Rotary embedding of the headline shapes' q [2,16,1024,128] and
     k [2,8,1024,128] (bf16, full rotary dim, positions = row index); one call =
@@ -386,52 +348,141 @@ def traffic_from_profiles(kernel_file: str):
     return None
 
 
-# ---------------------------------------------------------------- arms
+# ---------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(wl, heads: int):
-    """Time the oracle on the first `heads` query heads of the workload (both rows)."""
+def cpu_oracle(wl, rows=None, heads=None):
+    """Time one oracle call on the rows / leading query heads given (all by
+    default); returns (allowed FLOPs of the sample, seconds, threads used)."""
     import oracle
     oracle.build()
+    q, k, v = wl.q, wl.k, wl.v
+    masks = wl.masks()
+    if rows is not None:
+        q, k, v = q[rows], k[rows], v[rows]
+        masks = {n: (t[rows] if (t is not None and n != "causal") else t) for n, t in masks.items()}
     n_rep = wl.q.shape[1] // wl.k.shape[1]
-    hk = max(1, math.ceil(heads / n_rep))
-    q = wl.q[:, :heads].contiguous()
-    k = wl.k[:, :hk].contiguous()
-    v = wl.v[:, :hk].contiguous()
+    if heads is not None:
+        hk = max(1, math.ceil(heads / n_rep))
+        q, k, v = q[:, :heads], k[:, :hk], v[:, :hk]
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
     t0 = time.perf_counter()
-    _, _, used = oracle.attention(q, k, v, scale=wl.scale, **wl.masks())
+    _, _, used = oracle.attention(q, k, v, scale=wl.scale, **masks)
     secs = time.perf_counter() - t0
-    flops = wl.flops() * heads / wl.q.shape[1]
+    B = wl.q.shape[0]
+    frac = (len(rows) / B if rows is not None else 1.0) * ((heads or wl.q.shape[1]) / wl.q.shape[1])
+    if rows is not None:  # allowed pairs of the sampled rows only
+        sub = W.Workload("sample", wl.q[rows], wl.k[rows], wl.v[rows], wl.scale,
+                         **{n: (t[rows] if t is not None else None) for n, t in
+                            dict(mask_bits=wl.mask_bits, kv_len=wl.kv_len, seg_q=wl.seg_q,
+                                 seg_k=wl.seg_k).items()})
+        flops = sub.flops() * ((heads or wl.q.shape[1]) / wl.q.shape[1])
+    else:
+        flops = wl.flops() * frac
     return flops, secs, used
+
+
+def cpu_block(wl, unit, work_of_call, min_secs, rows=None, heads=None, sample=""):
+    """The oracle on the host cores, repeated for at least min_secs; value in
+    `unit` per second (TFLOP/s from FLOPs, GB/s from bytes)."""
+    tot_w, tot_s, reps, used = 0.0, 0.0, 0, 0
+    while tot_s < min_secs and reps < 200:
+        f, secs, used = cpu_oracle(wl, rows=rows, heads=heads)
+        w = f if work_of_call is None else work_of_call * (
+            (len(rows) / wl.q.shape[0]) if rows is not None else 1.0)
+        tot_w += w
+        tot_s += secs
+        reps += 1
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    return {"value": tot_w / tot_s / scale, "unit": unit, "cores": used, "kind": "oracle",
+            "sample": f"{reps} x {sample}, {tot_s:.1f} s",
+            "s_per_call": tot_s / reps / ((len(rows) / wl.q.shape[0]) if rows is not None else 1.0)}
+
+
+# ---------------------------------------------------------------- blocks
+
+def prefill_roofline(wl, per_call, bf16, pk_kind):
+    f = wl.flops()
+    return {"bound": "tensor", "achieved": f / per_call / 1e12, "peak": bf16, "unit": "TFLOP/s",
+            "frac": f / per_call / 1e12 / bf16, "traffic": traffic_from_profiles("prefill_tc.cu"),
+            "peak_kind": f"bf16 burst, {pk_kind}", "flops_per_launch": f,
+            "nonempty_tile_TFLOP_s": wl.nonempty_tile_flops() / per_call / 1e12,
+            "frac_nonempty_tiles": wl.nonempty_tile_flops() / per_call / 1e12 / bf16,
+            "kernel": "prefill_tc"}
+
+
+def fp32_alu_peak_tflops():
+    """FP32 FMA peak of the CUDA cores: 152 SMs x 128 FP32 lanes x 2 FLOPs x
+    2.07 GHz (the maximum SM clock)."""
+    return 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    wl = W.padded_cfg(variant="bits")
-    heads = 2
+    wl = W.dit_batch()
+    rows, heads = [0], 4
     for _ in range(args.warmup):
-        cpu_oracle_sample(wl, heads)
+        cpu_oracle(wl, rows=rows, heads=heads)
     tot_f, tot_s, used = 0.0, 0.0, 0
     for _ in range(args.steps):
-        f, s, used = cpu_oracle_sample(wl, heads)
+        f, s, used = cpu_oracle(wl, rows=rows, heads=heads)
         tot_f += f
         tot_s += s
     value = tot_f / tot_s / 1e12
-    sample = (f"{heads} of 16 query heads (both CFG rows) of one padded-CFG prefill call "
-              f"(2x1024 positions, head_dim 128) per step")
+    sample = (f"batch row 0, query heads 0..{heads - 1} of one DiT-batch prefill call "
+              f"(4096 positions, head_dim 128, that row's segments) per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": tot_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "padded_cfg_bits (B=2, Hq=16, Hkv=8, D=128, L=1024; keys 1024/384)"},
+        "config": {"workload": "dit_batch (B=32, Hq=16, Hkv=4, D=128, L=4096; 1..6 segments per row)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": used, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
+
+
+def bench_dit_e2e(M, wl, dev, calls, steps, warmup, world):
+    """Through the C ABI from pinned host buffers: every call of a step copies
+    its q/k/v and segment ids in and its output back out."""
+    import ctypes
+    host = {n: (getattr(wl, n).pin_memory() if getattr(wl, n) is not None else None)
+            for n in ("q", "k", "v", "mask_bits", "kv_len", "seg_q", "seg_k")}
+    d = {n: (torch.empty_like(t, device=dev) if t is not None else None) for n, t in host.items()}
+    out = torch.empty_like(d["q"])
+    out_host = torch.empty_like(host["q"]).pin_memory()
+    a = make_args(M, d, out, wl)
+    L = M.lib()
+    stream = torch.cuda.Stream(device=dev)
+    h2d = calls * sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = calls * out_host.numel() * out_host.element_size()
+
+    def step():
+        with torch.cuda.stream(stream):
+            for _ in range(calls):
+                for n, t in host.items():
+                    if t is not None:
+                        d[n].copy_(t, non_blocking=True)
+                st = L.masked_gqa_attn_prefill(ctypes.byref(a), stream.cuda_stream)
+                if st != 0:
+                    raise RuntimeError(L.mgqa_last_error_detail())
+                out_host.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1) / 1e3, h2d, d2h
 
 
 def run_gpu(args):
@@ -448,108 +499,159 @@ def run_gpu(args):
     hbm = peak_value(pk, "hbm_gbs") or FALLBACK_PEAKS["hbm_gbs"]
     bf16 = peak_value(pk, "bf16_tflops") or FALLBACK_PEAKS["bf16_tflops"]
 
-    if args.only == "prefill":
-        wl = W.padded_cfg(variant="bits")
-        secs, _ = bench_prefill_graph(M, wl, dev, CALLS_PER_STEP, PREFILL_SETS, args.steps,
-                                      args.warmup, world)
-        print(json.dumps({"leg": "prefill", "us_per_call": secs / (args.steps * CALLS_PER_STEP) * 1e6}))
-        return 0
-    if args.only == "decode":
-        wd = W.static_cache_decode(variant="span")
-        t = bench_decode(M, wd, dev, args.steps, args.warmup, world)
-        print(json.dumps({"leg": "decode", "us_per_call": t * 1e6}))
+    if args.only is not None:  # profiling aid: one leg, raw timings
+        if args.only == "decode":
+            t = bench_decode(M, W.static_cache_decode(variant="span"), dev, args.steps,
+                             args.warmup, world)
+            print(json.dumps({"leg": "decode", "us_per_call": t * 1e6}))
+            return 0
+        maker, calls, nsets = {"prefill": (lambda: W.padded_cfg(variant="bits"), CFG_CALLS, PREFILL_SETS),
+                               "packed": (W.packed_guidance, 32, PREFILL_SETS),
+                               "dit": (lambda: W.dit_batch(B=args.rows or 32), DIT_CALLS, 1)}[args.only]
+        secs, _ = bench_prefill_graph(M, maker(), dev, calls, nsets, args.steps, args.warmup, world)
+        print(json.dumps({"leg": args.only, "us_per_call": secs / (args.steps * calls) * 1e6}))
         return 0
 
     clocks = ClockSampler(local)
-    # ---- headline: padded CFG prefill, 32 calls per step
-    wl = W.padded_cfg(variant="bits")
-    flops_call = wl.flops()
+    cpu = rank == 0 and not args.no_cpu_baseline
+    configs = {}
+
+    # ---- headline: the DiT batch, 20 calls per step
+    wl = W.dit_batch()
     clocks.start()
-    secs, _ = bench_prefill_graph(M, wl, dev, CALLS_PER_STEP, PREFILL_SETS, args.steps,
-                                  args.warmup, world)
+    secs, _ = bench_prefill_graph(M, wl, dev, DIT_CALLS, 1, args.steps, args.warmup, world)
     clk = clocks.stop()
     secs = max_over_ranks(secs, world)
-    calls = args.steps * CALLS_PER_STEP
+    calls = args.steps * DIT_CALLS
     per_call = secs / calls
-    value = whole_job_rate(calls * flops_call, world, secs) / 1e12
-    achieved = flops_call / per_call / 1e12
-
-    e2e_secs, h2d, d2h = bench_prefill_e2e(M, wl, dev, CALLS_PER_STEP, max(3, args.steps // 10),
-                                           3, world)
-    e2e_steps = max(3, args.steps // 10)
+    value = whole_job_rate(calls * wl.flops(), world, secs) / 1e12
+    roof = prefill_roofline(wl, per_call, bf16, pk_kind)
+    e2e_steps = 2
+    e2e_secs, h2d, d2h = bench_dit_e2e(M, wl, dev, DIT_CALLS, e2e_steps, 1, world)
     e2e_secs = max_over_ranks(e2e_secs, world)
-    e2e_value = whole_job_rate(e2e_steps * CALLS_PER_STEP * flops_call, world, e2e_secs) / 1e12
+    e2e_value = whole_job_rate(e2e_steps * DIT_CALLS * wl.flops(), world, e2e_secs) / 1e12
+    dit_cpu = None
+    if cpu:
+        dit_cpu = cpu_block(wl, "TFLOP/s", None, 2.0, rows=[0, 13], sample=(
+            "batch rows 0 and 13 (all 16 heads, 4096 queries, their own segments) of one DiT "
+            "call; s_per_call extrapolates to the 32 rows"))
+    configs["dit_batch"] = {
+        "workload": "B=32, Hq=16, Hkv=4, D=128, L=4096, bf16, 1..6 segments per row; 20 calls per step",
+        "us_per_call": per_call * 1e6, "value": roof["achieved"], "unit": "TFLOP/s",
+        "roofline": roof, "clocks": clk, "cpu_baseline": dit_cpu}
+    del wl
+    torch.cuda.empty_cache()
 
-    # ---- decode: static cache, full-cache bits and filled-span variants
-    dec = {}
-    for variant in ("full", "span"):
+    # ---- padded CFG prefill (bits and kv_len forms), 32 calls per step
+    for variant in ("bits", "kvlen"):
+        wc = W.padded_cfg(variant=variant)
+        clocks.start()
+        so, _ = bench_prefill_graph(M, wc, dev, CFG_CALLS, PREFILL_SETS, 20, 3, world)
+        ck = clocks.stop()
+        pc = so / (20 * CFG_CALLS)
+        blk = {"workload": f"B=2 CFG rows (keys 1024 / 384 valid), Hq=16, Hkv=8, D=128, L=1024, bf16, "
+                           f"{'4D key-padding mask as packed bits' if variant == 'bits' else 'per-row key lengths'}; "
+                           f"32 calls per step over {PREFILL_SETS} rotating sets (201 MB > L2)",
+               "us_per_call": pc * 1e6, "unit": "TFLOP/s",
+               "roofline": prefill_roofline(wc, pc, bf16, pk_kind), "clocks": ck}
+        blk["value"] = blk["roofline"]["achieved"]
+        if cpu and variant == "bits":
+            blk["cpu_baseline"] = cpu_block(wc, "TFLOP/s", None, 3.0,
+                                            sample="whole padded-CFG prefill call (2 rows x 16 heads x 1024 queries)")
+        configs[f"padded_cfg_{variant}"] = blk
+        del wc
+
+    # ---- packed guidance prefill
+    wp = W.packed_guidance()
+    clocks.start()
+    so, _ = bench_prefill_graph(M, wp, dev, 32, PREFILL_SETS, 20, 3, world)
+    ck = clocks.stop()
+    pc = so / (20 * 32)
+    configs["packed_guidance"] = {
+        "workload": "1 row of 1024 + 384 positions, segments 0 / 1, Hq=16, Hkv=8, D=128, bf16; 32 calls "
+                    f"per step over {PREFILL_SETS} rotating sets",
+        "us_per_call": pc * 1e6, "unit": "TFLOP/s", "roofline": prefill_roofline(wp, pc, bf16, pk_kind),
+        "clocks": ck}
+    configs["packed_guidance"]["value"] = configs["packed_guidance"]["roofline"]["achieved"]
+    if cpu:
+        configs["packed_guidance"]["cpu_baseline"] = cpu_block(
+            wp, "TFLOP/s", None, 2.0, sample="whole packed-guidance prefill call (16 heads x 1408 queries)")
+
+    # ---- tiny fp32 (CUDA cores)
+    wt = W.tiny_fp32()
+    clocks.start()
+    so, _ = bench_prefill_graph(M, wt, dev, 32, 8, 20, 3, world)
+    ck = clocks.stop()
+    pc = so / (20 * 32)
+    alu = fp32_alu_peak_tflops()
+    configs["tiny_fp32"] = {
+        "workload": "B=2, Hq=4, Hkv=2, D=64, L=128, fp32, key padding (row 1: last 48 keys); 32 calls per step",
+        "us_per_call": pc * 1e6, "value": wt.flops() / pc / 1e12, "unit": "TFLOP/s",
+        "roofline": {"bound": "alu", "achieved": wt.flops() / pc / 1e12, "peak": alu, "unit": "TFLOP/s",
+                     "frac": wt.flops() / pc / 1e12 / alu, "traffic": None,
+                     "peak_kind": "FP32 FMA: 152 SMs x 128 lanes x 2 x 2.07 GHz", "kernel": "prefill_simt"},
+        "clocks": ck}
+    if cpu:
+        configs["tiny_fp32"]["cpu_baseline"] = cpu_block(wt, "TFLOP/s", None, 1.0,
+                                                         sample="whole tiny fp32 call")
+
+    # ---- static-cache decode: full-cache bitmask and filled-span forms
+    for variant in ("span", "full"):
         wd = W.static_cache_decode(variant=variant)
-        t = bench_decode(M, wd, dev, max(10, args.steps // 2), args.warmup, world)
+        clocks.start()
+        t = bench_decode(M, wd, dev, 30, 5, world)
+        ck = clocks.stop()
         nb = decode_needed_bytes(wd)
-        dec[variant] = {"us_per_call": t * 1e6, "needed_bytes": nb, "GB_s": nb / t / 1e9,
-                        "frac": nb / t / 1e9 / hbm}
-    wd = W.static_cache_decode(variant="span")
-    de2e, dh2d, dd2h = bench_decode_e2e(M, wd, dev, 200, 20, world)
-    nb = decode_needed_bytes(wd)
+        blk = {"workload": f"B=8, Hq=16, Hkv=2, D=64, bf16, 8192-slot caches filled 256..3100 "
+                           f"({'per-row filled lengths' if variant == 'span' else 'full-cache bitmask'}); "
+                           f"{DECODE_SETS} rotating cache sets (537 MB > L2)",
+               "us_per_call": t * 1e6, "value": nb / t / 1e9, "unit": "GB/s",
+               "roofline": {"bound": "hbm", "achieved": nb / t / 1e9, "peak": hbm, "unit": "GB/s",
+                            "frac": nb / t / 1e9 / hbm, "traffic": traffic_from_profiles("decode.cu"),
+                            "peak_kind": pk_kind, "bytes_per_launch": nb, "kernel": "decode"},
+               "clocks": ck}
+        if variant == "span":
+            de2e, dh2d, dd2h = bench_decode_e2e(M, wd, dev, 200, 20, world)
+            blk["e2e"] = {"value": nb / de2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": dh2d,
+                          "d2h_bytes_per_step": dd2h}
+            if cpu:
+                blk["cpu_baseline"] = cpu_block(wd, "GB/s", nb, 1.0,
+                                                sample="whole decode call (8 requests x 16 heads)")
+        configs[f"static_cache_decode_{variant}"] = blk
 
-    # ---- the other prefill workloads
-    others = {}
-    for name, maker, calls_o in (("packed_guidance", W.packed_guidance, 32),
-                                 ("dit_batch", W.dit_batch, 20)):
-        wo = maker()
-        nsets = 8 if name == "packed_guidance" else 1
-        so, _ = bench_prefill_graph(M, wo, dev, calls_o, nsets, 3, 2, world)
-        pc = so / (3 * calls_o)
-        others[name] = {"us_per_call": pc * 1e6, "allowed_TFLOP_s": wo.flops() / pc / 1e12,
-                        "nonempty_tile_TFLOP_s": wo.nonempty_tile_flops() / pc / 1e12,
-                        "frac_nonempty_of_peak": wo.nonempty_tile_flops() / pc / 1e12 / bf16}
-        del wo
+    # ---- rotary embedding of the padded-CFG q and k
+    clocks.start()
     t_rope, b_rope = bench_rope(M, dev)
-    others["rope"] = {"workload": "rotary embedding of q [2,16,1024,128] and k [2,8,1024,128], "
-                                  "bf16, 12 rotating sets (144 MB > L2)",
-                      "us_per_call": t_rope * 1e6, "bytes_per_call": b_rope,
-                      "GB_s": b_rope / t_rope / 1e9, "frac_of_hbm": b_rope / t_rope / 1e9 / hbm}
+    ck = clocks.stop()
+    configs["rope_qk"] = {"workload": "rotary embedding of q [2,16,1024,128] and k [2,8,1024,128], "
+                                      "bf16, 12 rotating sets (144 MB > L2)",
+                          "us_per_call": t_rope * 1e6, "value": b_rope / t_rope / 1e9, "unit": "GB/s",
+                          "roofline": {"bound": "hbm", "achieved": b_rope / t_rope / 1e9, "peak": hbm,
+                                       "unit": "GB/s", "frac": b_rope / t_rope / 1e9 / hbm,
+                                       "traffic": traffic_from_profiles("rope.cu"),
+                                       "peak_kind": pk_kind, "bytes_per_launch": b_rope,
+                                       "kernel": "rope"},
+                          "clocks": ck}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "padded_cfg_bits: B=2 CFG rows (keys 1024 / 384 valid), Hq=16, "
-                               "Hkv=8, D=128, L=1024, bf16, 4D key-padding mask as packed bits; "
-                               "32 calls per step",
-                   "l2": f"{PREFILL_SETS} rotating input sets (201 MB > L2)",
+        "config": {"workload": "dit_batch: B=32 rows, Hq=16, Hkv=4, D=128, L=4096, bf16, 1..6 "
+                               "block-diagonal segments per row at seeded cut points; 20 calls per step "
+                               "(10 Euler steps x CFG pair)",
+                   "l2": "inputs 805 MB > L2 (no rotation needed)",
                    "graph": "each step captured once in a CUDA graph", "parallelism": f"replicas x{world}"},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": calls,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": achieved / bf16, "traffic": traffic_from_profiles("prefill_tc.cu"),
-                     "peak_kind": f"bf16 burst, {pk_kind}",
-                     "flops_per_launch": flops_call, "kernel": "prefill_tc"},
-        "decode": {"workload": "static_cache_decode: B=8, Hq=16, Hkv=2, D=64, bf16, 8192 slots, "
-                               "filled 256..3100; 16 rotating cache sets (537 MB > L2)",
-                   "value": dec["span"]["GB_s"], "unit": "GB/s", "variants": dec,
-                   "roofline": {"bound": "hbm", "achieved": dec["span"]["GB_s"], "peak": hbm,
-                                "unit": "GB/s", "frac": dec["span"]["GB_s"] / hbm,
-                                "traffic": traffic_from_profiles("decode.cu"),
-                                "peak_kind": pk_kind, "bytes_per_launch": nb},
-                   "e2e": {"value": nb / de2e / 1e9, "unit": "GB/s", "h2d_bytes_per_step": dh2d,
-                           "d2h_bytes_per_step": dd2h}},
-        "other_workloads": others,
+        "roofline": roof,
+        "configs": configs,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        tot_f, tot_s, reps = 0.0, 0.0, 0
-        while tot_s < 10.0 and reps < 100:
-            f, s, used = cpu_oracle_sample(wl, 16)
-            tot_f += f
-            tot_s += s
-            reps += 1
-        line["cpu_baseline"] = {"value": tot_f / tot_s / 1e12, "unit": "TFLOP/s", "cores": used,
-                                "kind": "oracle",
-                                "sample": f"{reps} whole padded-CFG prefill calls (2 rows x 16 heads "
-                                          f"x 1024 queries), {tot_s:.1f} s"}
+    if dit_cpu is not None:
+        line["cpu_baseline"] = {k: v for k, v in dit_cpu.items() if k != "s_per_call"}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
@@ -561,13 +663,16 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mgqa", choices=["mgqa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
-                    help="profiling aid: run only the headline prefill or only the decode leg "
-                         "and print its raw timings")
+    ap.add_argument("--only", choices=["prefill", "packed", "dit", "decode"], default=None,
+                    help="profiling aid: time only one workload (padded-CFG prefill, packed "
+                         "guidance, DiT batch or the decode) and print its raw timing")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="with --only dit: the first ROWS batch rows of the DiT workload (a "
+                         "smaller capture of the same kernel)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -133,3 +133,34 @@ def test_dit_segments_cut_rows_off_the_tile_grid():
     assert bool((seg[:, 1:] >= seg[:, :-1]).all())
     cuts = [c for b in range(32) for c in (torch.nonzero(seg[b, 1:] != seg[b, :-1]).flatten() + 1).tolist()]
     assert cuts and any(c % 128 != 0 for c in cuts)  # partial tiles occur
+
+
+def test_cpu_oracle_block_whole_call(bench):
+    wl = W.tiny_fp32()
+    blk = bench.cpu_block(wl, "TFLOP/s", None, 0.01, sample="whole tiny call")
+    assert blk["kind"] == "oracle" and blk["cores"] >= 1 and blk["value"] > 0
+    assert blk["s_per_call"] > 0
+    # TFLOP/s = allowed FLOPs / seconds per call
+    assert abs(blk["value"] * 1e12 * blk["s_per_call"] - wl.flops()) < 1e-6 * wl.flops()
+
+
+def test_cpu_oracle_block_row_sample_counts_the_sampled_rows(bench):
+    wl = W.random_case(3, 4, 4, 2, 200, 200, 64, dtype=torch.bfloat16, mask="segment")
+    f, secs, used = bench.cpu_oracle(wl, rows=[0, 2])
+    sub = W.Workload("s", wl.q[[0, 2]], wl.k[[0, 2]], wl.v[[0, 2]], wl.scale,
+                     seg_q=wl.seg_q[[0, 2]], seg_k=wl.seg_k[[0, 2]])
+    assert f == sub.flops() and secs > 0 and used >= 1
+    blk = bench.cpu_block(wl, "TFLOP/s", None, 0.01, rows=[0, 2], sample="rows 0, 2")
+    # seconds per call extrapolate the sample to all 4 rows
+    assert blk["s_per_call"] > 0
+
+
+def test_cpu_oracle_block_bytes_for_decode(bench):
+    wl = W.static_cache_decode(variant="span", B=2, capacity=512, lo=100, hi=400)
+    nb = bench.decode_needed_bytes(wl)
+    blk = bench.cpu_block(wl, "GB/s", nb, 0.01, sample="whole decode call")
+    assert blk["unit"] == "GB/s" and abs(blk["value"] * 1e9 * blk["s_per_call"] - nb) < 1e-6 * nb
+
+
+def test_fp32_alu_peak_from_unit_counts(bench):
+    assert abs(bench.fp32_alu_peak_tflops() - 152 * 128 * 2 * 2.07e9 / 1e12) < 1e-9
