@@ -329,20 +329,24 @@ def bench_decode_e2e(M, wl, dev, steps, warmup, world):
     return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
 
 
-def traffic_from_profiles(kernel_file: str):
+def traffic_from_profiles(kernel_file: str, workload: str = None):
     """DRAM bytes per launch recorded by an ncu capture of the current kernel
-    source (profiles/*.md line 'traffic: <bytes> source-sha256: <hex>'), or None."""
+    source (profiles/*.md line 'traffic: <bytes> source-sha256: <hex> <file>
+    [<workload>]'), or None."""
     import glob
     import hashlib
     src = os.path.join(ROOT, "masked_gqa_attention_gb300", "csrc", kernel_file)
     if not os.path.exists(src):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    for p in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+    for p in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(p):
-            if line.startswith("traffic:") and f"source-sha256: {sha}" in line and kernel_file in line:
+            parts = line.split()
+            if (len(parts) >= 5 and parts[0] == "traffic:" and parts[2] == "source-sha256:"
+                    and parts[3] == sha and parts[4] == kernel_file
+                    and (workload is None or (len(parts) > 5 and parts[5] == workload))):
                 try:
-                    return float(line.split()[1])
+                    return float(parts[1])
                 except ValueError:
                     pass
     return None
@@ -400,10 +404,11 @@ def cpu_block(wl, unit, work_of_call, min_secs, rows=None, heads=None, sample=""
 
 # ---------------------------------------------------------------- blocks
 
-def prefill_roofline(wl, per_call, bf16, pk_kind):
+def prefill_roofline(wl, per_call, bf16, pk_kind, workload):
     f = wl.flops()
     return {"bound": "tensor", "achieved": f / per_call / 1e12, "peak": bf16, "unit": "TFLOP/s",
-            "frac": f / per_call / 1e12 / bf16, "traffic": traffic_from_profiles("prefill_tc.cu"),
+            "frac": f / per_call / 1e12 / bf16,
+            "traffic": traffic_from_profiles("prefill_tc.cu", workload),
             "peak_kind": f"bf16 burst, {pk_kind}", "flops_per_launch": f,
             "nonempty_tile_TFLOP_s": wl.nonempty_tile_flops() / per_call / 1e12,
             "frac_nonempty_tiles": wl.nonempty_tile_flops() / per_call / 1e12 / bf16,
@@ -525,7 +530,7 @@ def run_gpu(args):
     calls = args.steps * DIT_CALLS
     per_call = secs / calls
     value = whole_job_rate(calls * wl.flops(), world, secs) / 1e12
-    roof = prefill_roofline(wl, per_call, bf16, pk_kind)
+    roof = prefill_roofline(wl, per_call, bf16, pk_kind, "dit_batch")
     e2e_steps = 2
     e2e_secs, h2d, d2h = bench_dit_e2e(M, wl, dev, DIT_CALLS, e2e_steps, 1, world)
     e2e_secs = max_over_ranks(e2e_secs, world)
@@ -553,7 +558,7 @@ def run_gpu(args):
                            f"{'4D key-padding mask as packed bits' if variant == 'bits' else 'per-row key lengths'}; "
                            f"32 calls per step over {PREFILL_SETS} rotating sets (201 MB > L2)",
                "us_per_call": pc * 1e6, "unit": "TFLOP/s",
-               "roofline": prefill_roofline(wc, pc, bf16, pk_kind), "clocks": ck}
+               "roofline": prefill_roofline(wc, pc, bf16, pk_kind, f"padded_cfg_{variant}"), "clocks": ck}
         blk["value"] = blk["roofline"]["achieved"]
         if cpu and variant == "bits":
             blk["cpu_baseline"] = cpu_block(wc, "TFLOP/s", None, 3.0,
@@ -570,7 +575,8 @@ def run_gpu(args):
     configs["packed_guidance"] = {
         "workload": "1 row of 1024 + 384 positions, segments 0 / 1, Hq=16, Hkv=8, D=128, bf16; 32 calls "
                     f"per step over {PREFILL_SETS} rotating sets",
-        "us_per_call": pc * 1e6, "unit": "TFLOP/s", "roofline": prefill_roofline(wp, pc, bf16, pk_kind),
+        "us_per_call": pc * 1e6, "unit": "TFLOP/s",
+        "roofline": prefill_roofline(wp, pc, bf16, pk_kind, "packed_guidance"),
         "clocks": ck}
     configs["packed_guidance"]["value"] = configs["packed_guidance"]["roofline"]["achieved"]
     if cpu:
@@ -607,7 +613,8 @@ def run_gpu(args):
                            f"{DECODE_SETS} rotating cache sets (537 MB > L2)",
                "us_per_call": t * 1e6, "value": nb / t / 1e9, "unit": "GB/s",
                "roofline": {"bound": "hbm", "achieved": nb / t / 1e9, "peak": hbm, "unit": "GB/s",
-                            "frac": nb / t / 1e9 / hbm, "traffic": traffic_from_profiles("decode.cu"),
+                            "frac": nb / t / 1e9 / hbm,
+                            "traffic": traffic_from_profiles("decode.cu", "static_cache_decode"),
                             "peak_kind": pk_kind, "bytes_per_launch": nb, "kernel": "decode"},
                "clocks": ck}
         if variant == "span":

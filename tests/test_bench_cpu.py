@@ -74,9 +74,13 @@ def test_traffic_only_for_the_profiled_source(bench, tmp_path, monkeypatch):
     src = src_dir / "k.cu"
     src.write_text("// kernel v1\n")
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
-    (tmp_path / "profiles" / "k.md").write_text(f"notes\n\ntraffic: 123456 source-sha256: {sha} k.cu\n")
+    (tmp_path / "profiles" / "k.md").write_text(
+        f"notes\n\ntraffic: 123456 source-sha256: {sha} k.cu\n"
+        f"traffic: 777 source-sha256: {sha} k.cu other_workload\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.traffic_from_profiles("k.cu") == 123456.0
+    assert bench.traffic_from_profiles("k.cu", "other_workload") == 777.0
+    assert bench.traffic_from_profiles("k.cu", "missing_workload") is None
     src.write_text("// kernel v2\n")  # the kernel changed since the capture
     assert bench.traffic_from_profiles("k.cu") is None
     assert bench.traffic_from_profiles("missing.cu") is None
