@@ -17,6 +17,8 @@ arrays. What it computes, with the passages it follows:
   block-diagonal mask, each block equal to its run alone;
 * VoxCPM page, "Upstream-identical practice", attention bullet: causal
   attention at prefill (query rows = the last Lq of the Lk positions);
+* RMS normalisation of head vectors (``rms_norm``): OmniVoice page, "Parity
+  results" (q and k normalised separately before the rotation);
 * rotary position embedding (``rope``): F5-TTS page (interleaved pairs, on
   the first pe_attn_head heads), OmniVoice page, "Parity results", and VoxCPM page, precision bullet (fp32 inverse
   frequencies, LongRoPE tables built in fp32), OmniVoice page, packed_guidance
@@ -71,6 +73,9 @@ def _load():
             g = lib.mgqa_oracle_rope
             g.argtypes = [P, I, I, I, I, P, P, I, I, I]
             g.restype = I
+            n = lib.mgqa_oracle_rms_norm
+            n.argtypes = [P, I, I, I, I, P, ctypes.c_double, I]
+            n.restype = I
             _lib = lib
     return _lib
 
@@ -167,4 +172,25 @@ def rope(x, *, inv_freq, positions=None, rot_dim=None, heads=None, interleaved=F
         f.ctypes.data_as(ctypes.c_void_p), rot_dim, heads, int(bool(interleaved)))
     if rc != 0:
         raise ValueError("oracle rejected the rope arguments")
+    return x64
+
+
+def rms_norm(x, *, weight, eps=1e-6, heads=None):
+    """RMS normalisation over the head dim, in fp64 (see mgqa_oracle_rms_norm):
+    y = x / sqrt(mean(x^2) + eps) * weight, for heads h < `heads` (default all).
+
+    x: [B, H, L, D] (any float type, widened exactly); weight: [D] fp32.
+    Returns the normalised copy as fp64.
+    """
+    x64 = _f64(x).copy()
+    B, H, L, D = x64.shape
+    heads = H if heads is None else int(heads)
+    w = weight.detach().cpu().numpy() if hasattr(weight, "detach") else weight
+    w = np.ascontiguousarray(np.asarray(w), dtype=np.float32)
+    if w.shape != (D,):
+        raise ValueError(f"weight must be [{D}] fp32")
+    rc = _load().mgqa_oracle_rms_norm(x64.ctypes.data_as(ctypes.c_void_p), B, H, L, D,
+                                      w.ctypes.data_as(ctypes.c_void_p), float(eps), heads)
+    if rc != 0:
+        raise ValueError("oracle rejected the rms_norm arguments")
     return x64

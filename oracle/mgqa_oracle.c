@@ -183,3 +183,26 @@ int mgqa_oracle_rope(double *x, int B, int H, int L, int D, const int32_t *posit
             }
     return 0;
 }
+
+/*
+ * RMS normalisation of every head vector before the rotation (OmniVoice page,
+ * "Parity results": the shared Qwen decoder normalises q and k separately,
+ * as transformers does, before applying the rotary embedding):
+ *   y[d] = x[d] / sqrt(mean_d(x^2) + eps) * w[d]
+ * over the head dim D of every row of x [B][H][L][D] (fp64 values), in place,
+ * for heads h < `heads` only. Returns 0, or -1 on bad sizes.
+ */
+int mgqa_oracle_rms_norm(double *x, int B, int H, int L, int D, const float *w, double eps,
+                         int heads) {
+    if (B < 0 || H <= 0 || L < 0 || D <= 0 || heads < 0 || heads > H || eps < 0.0) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < heads; ++h)
+            for (int l = 0; l < L; ++l) {
+                double *row = x + (((long)b * H + h) * L + l) * D;
+                double ss = 0.0;
+                for (int d = 0; d < D; ++d) ss += row[d] * row[d];
+                const double r = 1.0 / sqrt(ss / D + eps);
+                for (int d = 0; d < D; ++d) row[d] = row[d] * r * (double)w[d];
+            }
+    return 0;
+}

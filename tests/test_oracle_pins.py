@@ -386,3 +386,47 @@ def test_rope_angle_is_the_fp32_product(oracle_mod):
     x = np.array([[[[1.0, 0.0]]]])
     y = oracle_mod.rope(x, inv_freq=np.array([f]), positions=np.array([[3]], np.int32))
     assert y[0, 0, 0, 0] == math.cos(theta32) and y[0, 0, 0, 1] == math.sin(theta32)
+
+
+
+# ---- RMS normalisation of q and k (OmniVoice page, "Parity results": the shared
+# Qwen decoder normalises q and k separately before the rotation) ----
+
+def test_rms_norm_hand_worked(oracle_mod):
+    # x = (3, 4): mean of squares 12.5, so y = x / sqrt(12.5) * w
+    x = np.array([[[[3.0, 4.0]]]])
+    y = oracle_mod.rms_norm(x, weight=np.array([1.0, 2.0], np.float32), eps=0.0)
+    s = math.sqrt(12.5)
+    assert np.allclose(y[0, 0, 0], [3.0 / s, 8.0 / s], rtol=0, atol=1e-15)
+    # eps enters under the root: x = (1, 1), eps = 3 -> 1 / sqrt(1 + 3) = 1/2
+    y = oracle_mod.rms_norm(np.ones((1, 1, 1, 2)), weight=np.ones(2, np.float32), eps=3.0)
+    assert np.array_equal(y, np.full((1, 1, 1, 2), 0.5))
+
+
+def test_rms_norm_unit_mean_square_and_scale_invariance(oracle_mod):
+    x = _rope_inputs(8, H=3, D=16)
+    y = oracle_mod.rms_norm(x, weight=np.ones(16, np.float32), eps=0.0)
+    assert np.allclose((y ** 2).mean(-1), 1.0, rtol=1e-14, atol=0)
+    y2 = oracle_mod.rms_norm(7.5 * x, weight=np.ones(16, np.float32), eps=0.0)
+    assert np.allclose(y2, y, rtol=1e-13, atol=1e-15)
+
+
+def test_rms_norm_matches_library_and_spares_heads(oracle_mod):
+    x = _rope_inputs(9, B=2, H=4, L=5, D=8)
+    w = np.linspace(0.5, 2.0, 8).astype(np.float32)
+    y = oracle_mod.rms_norm(x, weight=w, eps=1e-6, heads=2)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x[:, :2]), (8,),
+                                       weight=torch.from_numpy(w).double(), eps=1e-6)
+    assert np.allclose(y[:, :2], ref.numpy(), rtol=1e-14, atol=1e-15)
+    assert np.array_equal(y[:, 2:], x[:, 2:])  # heads past `heads` untouched
+
+
+def test_rms_norm_then_rope_keeps_the_normalised_length(oracle_mod):
+    # the rotation after the norm preserves each vector's length, so with a
+    # unit weight every rotated head vector has mean square 1
+    x = _rope_inputs(10, H=2, D=8)
+    f = (10000.0 ** (-np.arange(0, 8, 2) / 8)).astype(np.float32)
+    pos = np.array([[0, 9, 99, 999, 4095], [1, 2, 3, 4, 5]], np.int32)
+    y = oracle_mod.rope(oracle_mod.rms_norm(x, weight=np.ones(8, np.float32), eps=0.0),
+                        inv_freq=f, positions=pos, interleaved=False)
+    assert np.allclose((y ** 2).mean(-1), 1.0, rtol=1e-13, atol=0)
