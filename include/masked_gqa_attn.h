@@ -223,7 +223,13 @@ MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaSt
  *   (e0, e1) = (2i, 2i+1) if interleaved, else (i, i + rot_dim/2)
  *   x[e0], x[e1] <- x[e0] cos(theta) - x[e1] sin(theta),
  *                   x[e0] sin(theta) + x[e1] cos(theta)     (fp32, rounded to dtype)
- * Features >= rot_dim and heads >= `heads` are left as they are. */
+ * Features >= rot_dim and heads >= `heads` are left as they are.
+ * With norm_weight (OmniVoice page, "Parity results": the Qwen decoder
+ * normalises q and k separately, as transformers does, before the rotation),
+ * each rotated head vector is first RMS-normalised over all D features:
+ *   x[d] <- x[d] / sqrt(mean_d(x^2) + norm_eps) * norm_weight[d]   (fp32)
+ * and the rotation then acts on the normalised values (features >= rot_dim
+ * keep their normalised value); one rounding to dtype at the end. */
 typedef struct {
   mgqa_dtype dtype;             /* MGQA_BF16, MGQA_FP16 or MGQA_FP32 */
   int32_t B, H, L, D;           /* x is [B][H][L][D] */
@@ -234,6 +240,9 @@ typedef struct {
   int32_t rot_dim;              /* even, 2 <= rot_dim <= D */
   int32_t heads;                /* 1 <= heads <= H */
   int32_t interleaved;          /* nonzero: pairs (2i, 2i+1); zero: pairs (i, i + rot_dim/2) */
+  const float *norm_weight;     /* optional device [D] fp32: RMS-normalise each rotated head
+                                   vector over its D features first (see below); D <= 256 */
+  float norm_eps;               /* with norm_weight: finite, >= 0 */
 } mgqa_rope_args;
 
 /* Host-detectable argument errors return MGQA_ERR_INVALID_ARG (detail in
@@ -241,6 +250,44 @@ typedef struct {
  * nothing, never synchronises; MGQA_OK once the kernel is enqueued. All
  * pointers are caller-owned device memory. */
 MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *args, cudaStream_t stream);
+
+/* The rotary embedding (and optional RMS normalisation) applied INSIDE an
+ * attention call, to the query rows as they are loaded and, for the fused
+ * decode step, to the appended key row -- the same arithmetic as
+ * masked_gqa_rope (same bits), without its extra pass over q and k. */
+typedef struct {
+  const float *inv_freq;        /* device [rot_dim / 2] fp32 angular frequencies */
+  const int32_t *positions;     /* optional device int32 -- prefill: [B][Lq], the query rows'
+                                   positions (NULL: the query index i); decode step: [B], the
+                                   new token's position (NULL: kv_len[b], its cache slot) */
+  int32_t rot_dim;              /* even, 2 <= rot_dim <= D */
+  int32_t interleaved;          /* nonzero: pairs (2i, 2i+1); zero: pairs (i, i + rot_dim/2) */
+  int32_t q_heads;              /* query heads h < q_heads are normalised / rotated (1..Hq) */
+  int32_t k_heads;              /* decode step: the appended key row of KV heads g < k_heads
+                                   is normalised / rotated (0..Hkv); ignored by the prefill */
+  const float *q_norm_weight;   /* optional device [D] fp32: RMS-normalise those q rows first */
+  const float *k_norm_weight;   /* optional device [D] fp32: the same for the appended k row */
+  float norm_eps;               /* with a norm weight: finite, >= 0 */
+} mgqa_qk_rope;
+
+/* masked_gqa_attn_prefill with `rope` applied to the query rows inside the
+ * kernel (each CTA transforms its query tile in shared memory once, before
+ * its first product). The keys must already be rotated (and normalised), e.g.
+ * by masked_gqa_rope with the same table: the result equals masked_gqa_rope
+ * on q and then masked_gqa_attn_prefill, bit for bit. bf16 and fp16 only
+ * (MGQA_ERR_UNSUPPORTED for fp32: rotate with masked_gqa_rope instead). */
+MGQA_API mgqa_status masked_gqa_attn_prefill_rope(const mgqa_args *args, const mgqa_qk_rope *rope,
+                                                  cudaStream_t stream);
+
+/* masked_gqa_attn_decode_append with `rope` applied inside the kernel to the
+ * step's query and to its new key row before that row is attended to and
+ * written into the cache (the cache keeps rotated keys), at the new token's
+ * position (rope->positions[b], or kv_len[b]). Equals masked_gqa_rope on q
+ * and on k_new and then masked_gqa_attn_decode_append, bit for bit. */
+MGQA_API mgqa_status masked_gqa_attn_decode_append_rope(
+    const mgqa_args *args, const void *k_new, const void *v_new, const int64_t *k_new_stride,
+    const int64_t *v_new_stride, int32_t *kv_len_out, const mgqa_qk_rope *rope, void *workspace,
+    size_t workspace_bytes, cudaStream_t stream);
 
 /* Static description of a status code. */
 MGQA_API const char *mgqa_status_string(mgqa_status status);

@@ -32,7 +32,8 @@ __all__ = [
     "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
     "masked_gqa_attn_decode_static", "DECODE_STATIC_SCRATCH_BYTES",
     "masked_gqa_attn_decode_append", "masked_gqa_pack_pair", "masked_gqa_unpack_pair",
-    "debug_lib", "MGQA_ERR_DEVICE_CHECK",
+    "debug_lib", "MGQA_ERR_DEVICE_CHECK", "MgqaQkRope", "make_qk_rope",
+    "masked_gqa_attn_prefill_rope", "masked_gqa_attn_decode_append_rope", "masked_gqa_rope",
 ]
 
 (MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT,
@@ -53,6 +54,8 @@ EXPORTED_SYMBOLS = (
     "masked_gqa_pack_pair",
     "masked_gqa_unpack_pair",
     "masked_gqa_rope",
+    "masked_gqa_attn_prefill_rope",
+    "masked_gqa_attn_decode_append_rope",
 )
 # exported by the debug library only (include/masked_gqa_attn_debug.h)
 DEBUG_SYMBOLS = (
@@ -102,6 +105,18 @@ class MgqaRopeArgs(ctypes.Structure):
         ("positions", ctypes.c_void_p),
         ("inv_freq", ctypes.c_void_p),
         ("rot_dim", ctypes.c_int32), ("heads", ctypes.c_int32), ("interleaved", ctypes.c_int32),
+        ("norm_weight", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+    ]
+
+
+class MgqaQkRope(ctypes.Structure):
+    """Mirror of ``mgqa_qk_rope`` in include/masked_gqa_attn.h."""
+    _fields_ = [
+        ("inv_freq", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+        ("rot_dim", ctypes.c_int32), ("interleaved", ctypes.c_int32),
+        ("q_heads", ctypes.c_int32), ("k_heads", ctypes.c_int32),
+        ("q_norm_weight", ctypes.c_void_p), ("k_norm_weight", ctypes.c_void_p),
+        ("norm_eps", ctypes.c_float),
     ]
 
 
@@ -139,6 +154,11 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.masked_gqa_rope.restype = ctypes.c_int
     L.mgqa_abi_version.argtypes = []
     L.mgqa_abi_version.restype = ctypes.c_int32
+    L.masked_gqa_attn_prefill_rope.argtypes = [ctypes.POINTER(MgqaArgs), ctypes.POINTER(MgqaQkRope), P]
+    L.masked_gqa_attn_prefill_rope.restype = ctypes.c_int
+    L.masked_gqa_attn_decode_append_rope.argtypes = [ctypes.POINTER(MgqaArgs), P, P, I64P, I64P, P,
+                                                     ctypes.POINTER(MgqaQkRope), P, ctypes.c_size_t, P]
+    L.masked_gqa_attn_decode_append_rope.restype = ctypes.c_int
     return L
 
 
@@ -385,13 +405,14 @@ def masked_gqa_unpack_pair(packed, La, *, stream=None):
 
 
 def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, interleaved=False,
-                    stream=None):
+                    norm_weight=None, norm_eps=1e-6, stream=None):
     """Rotate x [B, H, L, D] (bf16, fp16 or fp32, head dim contiguous) in place by
     rotary position embedding and return it: theta = fl32(position * inv_freq[i])
     for pair i of the first rot_dim features (default D) of the first `heads`
     heads (default H); positions int32 [B, L] (default: the row index);
     inv_freq fp32 [rot_dim / 2]; interleaved pairs (2i, 2i+1) or half-split
-    pairs (i, i + rot_dim/2)."""
+    pairs (i, i + rot_dim/2). norm_weight (fp32 [D], optional): RMS-normalise
+    each rotated head vector over its D features before the rotation."""
     _dev(x, "x")
     B, H, L, D = x.shape
     if x.stride(3) != 1:
@@ -413,5 +434,94 @@ def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, in
     a.positions = _ptr(positions)
     a.inv_freq = inv_freq.data_ptr()
     a.rot_dim, a.heads, a.interleaved = rot_dim, heads, int(bool(interleaved))
+    if norm_weight is not None:
+        _dev(norm_weight, "norm_weight", torch.float32)
+        if not norm_weight.is_contiguous() or norm_weight.numel() != D:
+            raise ValueError(f"norm_weight must be a contiguous fp32 tensor of {D} values")
+        a.norm_weight = norm_weight.data_ptr()
+        a.norm_eps = float(norm_eps)
     _check(lib().masked_gqa_rope(ctypes.byref(a), _stream_handle(stream)))
     return x
+
+
+def make_qk_rope(inv_freq, D, *, positions=None, rot_dim=None, interleaved=False, q_heads,
+                 k_heads=0, q_norm_weight=None, k_norm_weight=None, norm_eps=1e-6) -> MgqaQkRope:
+    """Fill an MgqaQkRope: inv_freq fp32 [rot_dim / 2] (rot_dim defaults to D),
+    positions int32 (prefill [B, Lq]; decode step [B]) or None, optional fp32
+    [D] norm weights."""
+    rot_dim = D if rot_dim is None else int(rot_dim)
+    _dev(inv_freq, "inv_freq", torch.float32)
+    if not inv_freq.is_contiguous() or inv_freq.numel() != rot_dim // 2:
+        raise ValueError(f"inv_freq must be a contiguous fp32 tensor of {rot_dim // 2} values")
+    r = MgqaQkRope()
+    r.inv_freq = inv_freq.data_ptr()
+    if positions is not None:
+        _dev(positions, "positions", torch.int32)
+        if not positions.is_contiguous():
+            raise ValueError("positions must be contiguous")
+        r.positions = positions.data_ptr()
+    r.rot_dim, r.interleaved = rot_dim, int(bool(interleaved))
+    r.q_heads, r.k_heads = int(q_heads), int(k_heads)
+    for name, t in (("q_norm_weight", q_norm_weight), ("k_norm_weight", k_norm_weight)):
+        if t is not None:
+            _dev(t, name, torch.float32)
+            if not t.is_contiguous() or t.numel() != D:
+                raise ValueError(f"{name} must be a contiguous fp32 tensor of {D} values")
+            setattr(r, name, t.data_ptr())
+    r.norm_eps = float(norm_eps)
+    return r
+
+
+def masked_gqa_attn_prefill_rope(q, k, v, out=None, *, inv_freq, positions=None, rot_dim=None,
+                                 interleaved=False, q_heads=None, q_norm_weight=None,
+                                 norm_eps=1e-6, scale=None, mask_bits=None, kv_len=None,
+                                 seg_q=None, seg_k=None, lse=None, dev_error=None, causal=False,
+                                 stream=None):
+    """masked_gqa_attn_prefill with the rotary embedding (and optional RMS
+    norm) applied to q inside the kernel; k must already be rotated. Returns out."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
+                  seg_k=seg_k, lse=lse, dev_error=dev_error, causal=causal)
+    if positions is not None and tuple(positions.shape) != (q.shape[0], q.shape[2]):
+        raise ValueError("positions must be int32 [B, Lq]")
+    r = make_qk_rope(inv_freq, q.shape[3], positions=positions, rot_dim=rot_dim,
+                     interleaved=interleaved, q_heads=q.shape[1] if q_heads is None else q_heads,
+                     q_norm_weight=q_norm_weight, norm_eps=norm_eps)
+    _check(lib().masked_gqa_attn_prefill_rope(ctypes.byref(a), ctypes.byref(r),
+                                              _stream_handle(stream)))
+    return out
+
+
+def masked_gqa_attn_decode_append_rope(q, k_cache, v_cache, k_new, v_new, kv_len, out=None, *,
+                                       workspace: torch.Tensor, inv_freq, positions=None,
+                                       rot_dim=None, interleaved=False, q_heads=None,
+                                       k_heads=None, q_norm_weight=None, k_norm_weight=None,
+                                       norm_eps=1e-6, kv_len_out=None, scale=None, lse=None,
+                                       dev_error=None, stream=None):
+    """masked_gqa_attn_decode_append with the rotary embedding (and optional
+    RMS norms) applied inside the kernel to q and to the new key row, at the
+    new token's position (positions int32 [B], default kv_len); the cache
+    receives the rotated key row. Returns out."""
+    if out is None:
+        out = torch.empty_like(q)
+    a = make_args(q, k_cache, v_cache, out, scale=scale, kv_len=kv_len, lse=lse,
+                  dev_error=dev_error)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _dev(t, name, q.dtype)
+        if t.dim() != 4 or t.shape[2] != 1 or t.stride(3) != 1:
+            raise ValueError(f"{name} must be [B, Hkv, 1, D] with a unit-stride head dim")
+    if positions is not None and tuple(positions.shape) != (q.shape[0],):
+        raise ValueError("positions must be int32 [B]")
+    r = make_qk_rope(inv_freq, q.shape[3], positions=positions, rot_dim=rot_dim,
+                     interleaved=interleaved, q_heads=q.shape[1] if q_heads is None else q_heads,
+                     k_heads=k_cache.shape[1] if k_heads is None else k_heads,
+                     q_norm_weight=q_norm_weight, k_norm_weight=k_norm_weight, norm_eps=norm_eps)
+    ks = (ctypes.c_int64 * 2)(k_new.stride(0), k_new.stride(1))
+    vs = (ctypes.c_int64 * 2)(v_new.stride(0), v_new.stride(1))
+    _dev(workspace, "workspace")
+    _check(lib().masked_gqa_attn_decode_append_rope(
+        ctypes.byref(a), k_new.data_ptr(), v_new.data_ptr(), ks, vs,
+        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), ctypes.byref(r), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+    return out

@@ -83,6 +83,62 @@ mgqa_status validate(const mgqa_args *a, bool decode) {
   return MGQA_OK;
 }
 
+// The fused rotary embedding of a call with head dim D, Hq / Hkv heads.
+mgqa_status validate_rope(const mgqa_qk_rope *r, const mgqa_args &a, bool decode, FusedRope *out) {
+  if (!r) return fail(MGQA_ERR_INVALID_ARG, "rope is null");
+  if (!r->inv_freq || !aligned(r->inv_freq, 4))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: inv_freq missing or misaligned");
+  if (r->rot_dim < 2 || r->rot_dim > a.D || (r->rot_dim & 1))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: rot_dim must be even and in [2, D]");
+  if (r->q_heads < 1 || r->q_heads > a.Hq)
+    return fail(MGQA_ERR_INVALID_ARG, "rope: q_heads must be in [1, Hq]");
+  if (decode && (r->k_heads < 0 || r->k_heads > a.Hkv))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: k_heads must be in [0, Hkv]");
+  if (r->positions && !aligned(r->positions, 4))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: positions misaligned");
+  if ((r->q_norm_weight && !aligned(r->q_norm_weight, 4)) ||
+      (r->k_norm_weight && !aligned(r->k_norm_weight, 4)))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: norm weight misaligned");
+  if ((r->q_norm_weight || r->k_norm_weight) && !(std::isfinite(r->norm_eps) && r->norm_eps >= 0.f))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: norm_eps must be finite and >= 0");
+  out->inv_freq = r->inv_freq;
+  out->positions = r->positions;
+  out->half = r->rot_dim / 2;
+  out->interleaved = r->interleaved != 0;
+  out->q_heads = r->q_heads;
+  out->k_heads = decode ? r->k_heads : 0;
+  out->q_norm = r->q_norm_weight;
+  out->k_norm = decode ? r->k_norm_weight : nullptr;
+  out->eps = r->norm_eps;
+  return MGQA_OK;
+}
+
+mgqa_status validate_append(const mgqa_args *args, const void *k_new, const void *v_new,
+                            const int64_t *k_new_stride, const int64_t *v_new_stride,
+                            int32_t *kv_len_out, void *workspace) {
+  mgqa_status st = validate(args, true);
+  if (st != MGQA_OK) return st;
+  if (!args->kv_len) return fail(MGQA_ERR_INVALID_ARG, "append needs kv_len");
+  if (args->mask_bits || args->seg_q)
+    return fail(MGQA_ERR_INVALID_ARG, "append takes the kv_len form only");
+  if (!k_new || !v_new || !k_new_stride || !v_new_stride)
+    return fail(MGQA_ERR_INVALID_ARG, "append needs k_new, v_new and their strides");
+  const size_t es = args->dtype == MGQA_FP32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))
+    return fail(MGQA_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
+  for (int t = 0; t < 2; ++t)
+    if (k_new_stride[t] < 0 || v_new_stride[t] < 0 || (k_new_stride[t] * (int64_t)es) % 16 ||
+        (v_new_stride[t] * (int64_t)es) % 16)
+      return fail(MGQA_ERR_INVALID_ARG, "k_new / v_new strides must be multiples of 16 bytes");
+  if (kv_len_out && kv_len_out == args->kv_len)
+    return fail(MGQA_ERR_INVALID_ARG, "kv_len_out must not alias kv_len");
+  if (kv_len_out && (reinterpret_cast<uintptr_t>(kv_len_out) % 4))
+    return fail(MGQA_ERR_INVALID_ARG, "kv_len_out misaligned");
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
+    return fail(MGQA_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
+  return MGQA_OK;
+}
+
 }  // namespace
 }  // namespace mgqa
 
@@ -115,28 +171,38 @@ mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_n
                                           const int64_t *v_new_stride, int32_t *kv_len_out,
                                           void *workspace, size_t workspace_bytes,
                                           cudaStream_t stream) {
-  mgqa_status st = mgqa::validate(args, true);
+  const mgqa_status st = mgqa::validate_append(args, k_new, v_new, k_new_stride, v_new_stride,
+                                               kv_len_out, workspace);
   if (st != MGQA_OK) return st;
-  if (!args->kv_len) return mgqa::fail(MGQA_ERR_INVALID_ARG, "append needs kv_len");
-  if (args->mask_bits || args->seg_q)
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "append takes the kv_len form only");
-  if (!k_new || !v_new || !k_new_stride || !v_new_stride)
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "append needs k_new, v_new and their strides");
-  const size_t es = args->dtype == MGQA_FP32 ? 4 : 2;
-  if ((reinterpret_cast<uintptr_t>(k_new) % 16) || (reinterpret_cast<uintptr_t>(v_new) % 16))
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
-  for (int t = 0; t < 2; ++t)
-    if (k_new_stride[t] < 0 || v_new_stride[t] < 0 || (k_new_stride[t] * (int64_t)es) % 16 ||
-        (v_new_stride[t] * (int64_t)es) % 16)
-      return mgqa::fail(MGQA_ERR_INVALID_ARG, "k_new / v_new strides must be multiples of 16 bytes");
-  if (kv_len_out && kv_len_out == args->kv_len)
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "kv_len_out must not alias kv_len");
-  if (kv_len_out && (reinterpret_cast<uintptr_t>(kv_len_out) % 4))
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "kv_len_out misaligned");
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
   return mgqa::launch_decode_append(*args, k_new, v_new, k_new_stride, v_new_stride, kv_len_out,
                                     workspace, workspace_bytes, stream);
+}
+
+mgqa_status masked_gqa_attn_decode_append_rope(const mgqa_args *args, const void *k_new,
+                                               const void *v_new, const int64_t *k_new_stride,
+                                               const int64_t *v_new_stride, int32_t *kv_len_out,
+                                               const mgqa_qk_rope *rope, void *workspace,
+                                               size_t workspace_bytes, cudaStream_t stream) {
+  mgqa_status st = mgqa::validate_append(args, k_new, v_new, k_new_stride, v_new_stride,
+                                         kv_len_out, workspace);
+  if (st != MGQA_OK) return st;
+  mgqa::FusedRope fr;
+  if ((st = mgqa::validate_rope(rope, *args, true, &fr)) != MGQA_OK) return st;
+  return mgqa::launch_decode_append(*args, k_new, v_new, k_new_stride, v_new_stride, kv_len_out,
+                                    workspace, workspace_bytes, stream, fr);
+}
+
+mgqa_status masked_gqa_attn_prefill_rope(const mgqa_args *args, const mgqa_qk_rope *rope,
+                                         cudaStream_t stream) {
+  mgqa_status st = mgqa::validate(args, false);
+  if (st != MGQA_OK) return st;
+  if (args->dtype == MGQA_FP32)
+    return mgqa::fail(MGQA_ERR_UNSUPPORTED,
+                      "the fused rotary embedding runs on the bf16 / fp16 path; rotate fp32 inputs "
+                      "with masked_gqa_rope");
+  mgqa::FusedRope fr;
+  if ((st = mgqa::validate_rope(rope, *args, false, &fr)) != MGQA_OK) return st;
+  return mgqa::launch_prefill_tc(*args, stream, fr);
 }
 
 const char *mgqa_status_string(mgqa_status s) {

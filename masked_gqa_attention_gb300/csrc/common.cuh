@@ -103,6 +103,46 @@ MGQA_DEV int load_kv_len(const int32_t *kv_len, int b, int Lk, int32_t *err, boo
   return n;
 }
 
+// ---- rotary embedding and RMS normalisation ---------------------------------
+// Every kernel that normalises or rotates a head vector uses these, with
+// every step rounded once, so a fused path gives the same bits as the
+// standalone kernel followed by attention.
+
+// theta = fl32(position * inv_freq)
+MGQA_DEV float rope_theta(int pos, float f) { return __fmul_rn((float)pos, f); }
+
+// (a, c) -> (a cos - c sin, a sin + c cos)
+MGQA_DEV void rope_rotate(float a, float c, float cs, float sn, float &x0, float &x1) {
+  x0 = __fsub_rn(__fmul_rn(a, cs), __fmul_rn(c, sn));
+  x1 = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(c, cs));
+}
+
+// The sum of squares of a head vector in one fixed order: lane partial l
+// accumulates x_d^2 for d = l, l + 32, l + 64, ... (a product, then fused
+// multiply-adds), and the 32 partials combine as an xor butterfly with
+// offsets 16, 8, 4, 2, 1.
+MGQA_DEV float rms_partial_add(float p, float x, bool first) {
+  return first ? __fmul_rn(x, x) : __fmaf_rn(x, x, p);
+}
+MGQA_DEV float rms_butterfly_warp(float p) {  // every lane of the warp takes part
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
+  return p;
+}
+// The same butterfly on 32 partials held by one thread (p is overwritten).
+MGQA_DEV float rms_butterfly_local(float (&p)[32]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int l = 0; l < o; ++l) p[l] = __fadd_rn(p[l], p[l + o]);
+  return p[0];
+}
+// 1 / sqrt(ss / D + eps)
+MGQA_DEV float rms_scale(float ss, int D, float eps) {
+  return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), eps)));
+}
+MGQA_DEV float rms_apply(float x, float r, float w) { return __fmul_rn(__fmul_rn(x, r), w); }
+
 // ---- mask forms -----------------------------------------------------------
 
 // The mask forms of one call; any pointer may be null (form absent).

@@ -61,6 +61,7 @@ struct DecodeParams {
   unsigned *ws_tick;  // [B][Hq / NREP] arrival tickets
   float2 *ws_ml;      // [B][Hq][S]    (m in log2 units, l)
   float *ws_o;        // [B][Hq][S][D] unnormalised partial outputs
+  FusedRope rope;     // applied to q and the appended row (inv_freq null: none)
 };
 
 constexpr int kThreads = 256;
@@ -121,7 +122,9 @@ struct DecodeSmem {
   static constexpr int v_off = CPB * CHB;
   static constexpr int misc_off = 2 * CPB * CHB;
   struct Misc {
-    float q[NREP][D];                 // fp32 path
+    float q[NREP][D];                 // fp32 path, and any path with a fused rotation
+    float knew[D];                    // fused rotation: the appended key row
+    float2 cs[D / 2];                 // fused rotation: (cos, sin) of the new position
     float s[NREP][kMma ? 1 : CAPR];   // fp32 path: one batch's scores / weights
     float fo[NREP], fb[NREP];         // fp32 path
     float wmax[kWarps][NREP], wsum[kWarps][NREP];
@@ -176,18 +179,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   // ---- 1. every load the mask test and the products need, issued together
   const int kvl_raw = p.kv_len ? __ldg(p.kv_len + b) : p.Lk;
   const T *qb = static_cast<const T *>(p.q) + (int64_t)b * p.qs_b;
+  const bool rope = p.rope.inv_freq != nullptr;
   uint32_t qa[use_mma<T>() ? D / 16 : 1][2];  // Q as the A fragment (rows gq + 8: padding)
   if constexpr (use_mma<T>()) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       qa[kk][0] = qa[kk][1] = 0u;
-      if (gq < NREP) {
+      if (gq < NREP && !rope) {
         const T *qr = qb + (int64_t)(h0 + gq) * p.qs_h + kk * 16 + 2 * tq;
         qa[kk][0] = *reinterpret_cast<const uint32_t *>(qr);
         qa[kk][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
       }
     }
-  } else {
+  }
+  if (!use_mma<T>() || rope) {
     for (int i = tid; i < NREP * D; i += kThreads)
       sm.q[i / D][i % D] = to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]);
   }
@@ -259,6 +264,67 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   __syncthreads();
   dec_stamp(2);
+  if (rope) {
+    // the step's query rows and new key row, normalised and rotated at the new
+    // token's position with the arithmetic of the standalone kernel
+    const int npos = p.rope.positions ? __ldg(p.rope.positions + b) : (pos >= 0 ? pos : kvl);
+    const bool krow = p.append && g < p.rope.k_heads;
+    if (krow)
+      for (int d = tid; d < D; d += kThreads) sm.knew[d] = to_float(sm.newk[d]);
+    for (int i = tid; i < p.rope.half; i += kThreads) {
+      float sn, cs;
+      sincosf(rope_theta(npos, __ldg(p.rope.inv_freq + i)), &sn, &cs);
+      sm.cs[i] = make_float2(cs, sn);
+    }
+    __syncthreads();
+    // RMS norm: one warp per row, lane partials over d = lane (mod 32)
+    for (int task = warp; task <= NREP; task += kWarps) {
+      const bool is_k = task == NREP;
+      const float *wn = is_k ? p.rope.k_norm : p.rope.q_norm;
+      if (!wn || (is_k ? !krow : h0 + task >= p.rope.q_heads)) continue;  // warp-uniform
+      float *row = is_k ? sm.knew : sm.q[task];
+      float part = 0.f;
+      for (int d = lane, k = 0; d < D; d += 32, ++k) part = rms_partial_add(part, row[d], k == 0);
+      const float rs = rms_scale(rms_butterfly_warp(part), D, p.rope.eps);
+      for (int d = lane; d < D; d += 32) row[d] = rms_apply(row[d], rs, __ldg(wn + d));
+    }
+    __syncthreads();
+    // rotation, then one rounding to the I/O type (q stays a float holding it)
+    for (int it = tid; it < (NREP + 1) * (D / 2); it += kThreads) {
+      const int task = it / (D / 2), i = it % (D / 2);
+      const bool is_k = task == NREP;
+      if (is_k ? !krow : h0 + task >= p.rope.q_heads) continue;
+      float *row = is_k ? sm.knew : sm.q[task];
+      const bool normed = is_k ? p.rope.k_norm != nullptr : p.rope.q_norm != nullptr;
+      if (i < p.rope.half) {
+        const int e0 = p.rope.interleaved ? 2 * i : i;
+        const int e1 = p.rope.interleaved ? 2 * i + 1 : i + p.rope.half;
+        float y0, y1;
+        rope_rotate(row[e0], row[e1], sm.cs[i].x, sm.cs[i].y, y0, y1);
+        if (is_k) {
+          sm.newk[e0] = from_float<T>(y0);
+          sm.newk[e1] = from_float<T>(y1);
+        } else {
+          row[e0] = to_float(from_float<T>(y0));
+          row[e1] = to_float(from_float<T>(y1));
+        }
+      } else if (normed) {  // features past rot_dim keep their normalised value
+        for (int d = 2 * p.rope.half + (i - p.rope.half); d < D; d += D / 2 - p.rope.half) {
+          if (is_k) sm.newk[d] = from_float<T>(row[d]);
+          else row[d] = to_float(from_float<T>(row[d]));
+        }
+      }
+    }
+    __syncthreads();
+    if constexpr (use_mma<T>()) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (gq < NREP) {
+          qa[kk][0] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
+          qa[kk][1] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
+        }
+    }
+  }
   // the non-empty chunks in ascending order: bit i set for chunk i (every warp
   // forms the same mask)
   const uint32_t nem = __ballot_sync(0xffffffffu, lane < nci && (sm.words[lane][0] | sm.words[lane][1]));
@@ -556,11 +622,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     constexpr int PPR = D * sizeof(T) / 16;
     char *kd = const_cast<char *>(reinterpret_cast<const char *>(kg + (int64_t)pos * p.ks_l));
     char *vd = const_cast<char *>(reinterpret_cast<const char *>(vg + (int64_t)pos * p.vs_l));
+    // the staged rows: the step's input, normalised and rotated when fused
     for (int part = tid; part < 2 * PPR; part += kThreads) {
       if (part < PPR)
-        reinterpret_cast<uint4 *>(kd)[part] = reinterpret_cast<const uint4 *>(kn)[part];
+        reinterpret_cast<uint4 *>(kd)[part] = reinterpret_cast<const uint4 *>(sm.newk)[part];
       else
-        reinterpret_cast<uint4 *>(vd)[part - PPR] = reinterpret_cast<const uint4 *>(vn)[part - PPR];
+        reinterpret_cast<uint4 *>(vd)[part - PPR] = reinterpret_cast<const uint4 *>(sm.newv)[part - PPR];
     }
   }
 
@@ -690,7 +757,8 @@ mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStr
 
 mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
                                  const int64_t *k_new_stride, const int64_t *v_new_stride,
-                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s) {
+                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s,
+                                 const FusedRope &rope) {
   const DecodeWsLayout L = decode_ws_layout(a);
   if (ws_bytes < L.total) return fail(MGQA_ERR_INVALID_ARG, "decode workspace too small");
   DecodeParams p{};
@@ -709,6 +777,7 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
   p.ws_tick = reinterpret_cast<unsigned *>(base + L.tick);
   p.ws_ml = reinterpret_cast<float2 *>(base + L.ml);
   p.ws_o = reinterpret_cast<float *>(base + L.o);
+  p.rope = rope;
   p.append = k_new != nullptr;
   if (p.append) {
     p.k_new = k_new;

@@ -51,6 +51,18 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Rotary embedding (and RMS normalisation) applied inside an attention
+// kernel; inactive when inv_freq is null.
+struct FusedRope {
+  const float *inv_freq = nullptr;
+  const int32_t *positions = nullptr;
+  int half = 0;         // rot_dim / 2
+  int interleaved = 0;
+  int q_heads = 0, k_heads = 0;
+  const float *q_norm = nullptr, *k_norm = nullptr;
+  float eps = 0.f;
+};
+
 // Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
 // kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.
 constexpr int kDecodeChunk = 64;
@@ -70,7 +82,8 @@ size_t decode_workspace_bytes(const mgqa_args &a);
 mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
 mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
                                  const int64_t *k_new_stride, const int64_t *v_new_stride,
-                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s);
+                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s,
+                                 const FusedRope &rope = FusedRope());
 
 // Packed-guidance row copies (pack or unpack one pair of sequences).
 mgqa_status pack_pair(bool unpack, mgqa_dtype dt, int B, int H, int D, const void *a,
@@ -87,7 +100,8 @@ bool make_tma_map_4d(CUtensorMap *m, mgqa_dtype dt, const void *base, int B, int
 // Prefill on the CUDA cores (fp32 I/O).
 mgqa_status launch_prefill_simt(const mgqa_args &a, cudaStream_t s);
 
-// Prefill on the tensor cores (bf16 I/O): TMA + tcgen05 + TMEM.
-mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s);
+// Prefill on the tensor cores (bf16 / fp16 I/O): TMA + tcgen05 + TMEM.
+mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s,
+                              const FusedRope &rope = FusedRope());
 
 }  // namespace mgqa

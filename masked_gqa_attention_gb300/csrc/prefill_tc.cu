@@ -88,6 +88,7 @@ struct TcParams {
   int64_t os[3];
   float *lse;
   int32_t *err;
+  FusedRope rope;  // applied to the query tile in shared memory (inv_freq null: none)
 };
 
 template <int D, int NT, int STAGES>
@@ -99,8 +100,9 @@ struct Layout {
   static constexpr int bar_off = v_off + STAGES * KB * BOX;
   // barriers: q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[NT], p_full[NT],
   // o_done[NT], spec (the speculative tile-0 loads have landed), drain (every MMA
-  // issued has completed; used when a wait gave up)
-  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2;
+  // issued has completed; used when a wait gave up), q_rot[NT] (head t's query
+  // tile is rotated; fused rotary embedding only)
+  static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2 + NT;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
   static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
@@ -166,6 +168,72 @@ MGQA_DEV void tile_mask_words(const TcParams &p, int b, int i, bool row_ok, int 
 #pragma unroll
     for (int w = 0; w < BN / 32; ++w) mw[w] = 0u;
   }
+}
+
+// 16-bit value `hi` (0: low half) of a packed pair, as a float.
+template <typename T> MGQA_DEV float half_of(uint32_t v, int hi);
+template <> MGQA_DEV float half_of<__nv_bfloat16>(uint32_t v, int hi) {
+  return __uint_as_float(hi ? (v & 0xffff0000u) : (v << 16));
+}
+template <> MGQA_DEV float half_of<__half>(uint32_t v, int hi) {
+  return __half2float(__ushort_as_half((unsigned short)(hi ? (v >> 16) : (v & 0xffffu))));
+}
+
+// The rotary embedding's pairs of one row held as floats, in place. Interleaved
+// pairs and half-split pairs over the whole head dim (HALF = D / 2) index the
+// row with constants, so it stays in registers; a partial half-split rotation
+// (HALF = 0: rp.half at run time) indexes it at run time.
+template <int D, bool INTERLEAVED, int HALF>
+MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
+  const int half = HALF > 0 ? HALF : rp.half;
+#pragma unroll
+  for (int i = 0; i < D / 2; ++i) {
+    if (i >= half) break;
+    const int e0 = INTERLEAVED ? 2 * i : i;
+    const int e1 = INTERLEAVED ? 2 * i + 1 : i + half;
+    float sn, cs, y0, y1;
+    sincosf(rope_theta(pos, __ldg(rp.inv_freq + i)), &sn, &cs);
+    rope_rotate(x[e0], x[e1], cs, sn, y0, y1);
+    x[e0] = y0;
+    x[e1] = y1;
+  }
+}
+
+// RMS normalisation and rotary embedding of query row r of one head's tile
+// in shared memory (128-byte-swizzled 64-column boxes), in place: the same
+// arithmetic as the standalone rotary-embedding kernel.
+template <typename T, int D>
+MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &rp) {
+  uint32_t w[D / 2];
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(tile + (c >> 3) * BOX + r * 128 +
+                                                      (((c & 7) ^ (r & 7)) << 4));
+    w[4 * c] = u.x;
+    w[4 * c + 1] = u.y;
+    w[4 * c + 2] = u.z;
+    w[4 * c + 3] = u.w;
+  }
+  float x[D];
+#pragma unroll
+  for (int d = 0; d < D; ++d) x[d] = half_of<T>(w[d >> 1], d & 1);
+  if (rp.q_norm) {
+    float part[32];
+#pragma unroll
+    for (int d = 0; d < D; ++d) part[d % 32] = rms_partial_add(part[d % 32], x[d], d < 32);
+    const float rs = rms_scale(rms_butterfly_local(part), D, rp.eps);
+#pragma unroll
+    for (int d = 0; d < D; ++d) x[d] = rms_apply(x[d], rs, __ldg(rp.q_norm + d));
+  }
+  if (rp.interleaved) rope_row_pairs<D, true, 0>(x, rp, pos);
+  else if (rp.half == D / 2) rope_row_pairs<D, false, D / 2>(x, rp, pos);
+  else rope_row_pairs<D, false, 0>(x, rp, pos);
+#pragma unroll
+  for (int d = 0; d < D; d += 2) w[d >> 1] = pack2<T>(x[d], x[d + 1]);  // one rounding
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c)
+    *reinterpret_cast<uint4 *>(tile + (c >> 3) * BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 // One 128-key tile of one softmax row (thread = row): the whole score row is
@@ -293,6 +361,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_odone = bar_pfull + NT;
   uint64_t *bar_spec = bar_odone + NT;
   uint64_t *bar_drain = bar_spec + 1;
+  uint64_t *bar_qrot = bar_drain + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
   int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
@@ -325,6 +394,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     mbar_init(bar_spec, 1);
     mbar_init(bar_drain, 1);
+    for (int t = 0; t < NT; ++t) mbar_init(bar_qrot + t, 128);
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_q);
     tc::prefetch_tensormap(&tm_k);
@@ -626,8 +696,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (spec_miss) wait(bar_spec, 0);
       wait(bar_q, 0) && wait(bar_kfull, par(0, 0)) && wait(bar_vfull, par(0, 0));
       tc::fence_after_sync();
-      if (ok)
-        for (int t = 0; t < NT; ++t) issue_s(t, 0, 0, D / 16);
+      for (int t = 0; t < NT && ok; ++t) {
+        // a fused rotary embedding rewrites the query tile first
+        if (p.rope.inv_freq && !wait(bar_qrot + t, 0)) break;
+        tc::fence_after_sync();
+        issue_s(t, 0, 0, D / 16);
+      }
       // The MMA queue is shallow: an issuing thread stalls in it until the
       // pipe has nearly drained, so any wait between two groups of MMAs
       // leaves the pipe idle. The waits for the next tile's K and V therefore
@@ -707,6 +781,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t t_s = tmem + lane_base + t * BN;
     const uint32_t t_o = tmem + lane_base + NT * BN + t * D;
     const int segq = p.mask.seg_q ? __ldg(p.mask.seg_q + (int64_t)b * p.Lq + ic) : 0;
+    if (p.rope.inv_freq) {
+      // rotary embedding (and RMS norm) of this head's query row, in shared
+      // memory, before the head's first product
+      if (ok) ok = mbar_wait(bar_q, 0, p.err, lim);
+      if (ok && row_ok && h0 + t < p.rope.q_heads) {
+        const int pos = p.rope.positions ? __ldg(p.rope.positions + (int64_t)b * p.Lq + i) : i;
+        rope_q_row<T, D>(smem + Lay::q_off + t * KB * BOX, r, pos, p.rope);
+      }
+      fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
+      mbar_arrive(bar_qrot + t);
+    }
     const bool neg = p.scale_log2 < 0.f;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
@@ -856,7 +941,7 @@ mgqa_status dispatch_d(int D, bool pair, const CUtensorMap &mq, const CUtensorMa
 
 }  // namespace
 
-mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
+mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s, const FusedRope &rope) {
   if (a.dtype != MGQA_BF16 && a.dtype != MGQA_FP16)
     return fail(MGQA_ERR_UNSUPPORTED, "tensor-core prefill takes bf16 or fp16");
   const int nkt = (a.Lk + BN - 1) / BN;
@@ -877,6 +962,7 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s) {
   p.out = a.out;
   p.os[0] = a.o_stride[0]; p.os[1] = a.o_stride[1]; p.os[2] = a.o_stride[2];
   p.lse = a.lse; p.err = a.dev_error;
+  p.rope = rope;
   const bool pair = (p.n_rep % 2) == 0;
   if (a.dtype == MGQA_BF16) return dispatch_d<__nv_bfloat16>(a.D, pair, mq, mk, mv, mo, p, s);
   return dispatch_d<__half>(a.D, pair, mq, mk, mv, mo, p, s);

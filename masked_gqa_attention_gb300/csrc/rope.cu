@@ -16,6 +16,13 @@
 // loads are in flight together (a store could alias a later head's load, so
 // the compiler would not hoist the loads by itself); interleaved 16-bit pairs
 // move as one 32-bit word when the rows allow it.
+// With a norm weight (OmniVoice page, "Parity results": the Qwen decoder
+// normalises q and k separately before the rotation) one warp takes each
+// rotated head vector: RMS normalisation over all D features, then the
+// rotation of the first rot_dim. Both paths use the shared helpers of
+// common.cuh, so the fused attention paths give the same bits.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,7 +34,9 @@ struct RopeParams {
   int64_t s_b, s_h, s_l;
   const int32_t *positions;
   const float *inv_freq;
-  int B, L, half, heads, interleaved;
+  int B, L, D, half, heads, interleaved;
+  const float *norm_w;  // [D] or null
+  float eps;
 };
 
 constexpr int kRopeThreads = 256;
@@ -65,9 +74,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   const int64_t bl = idx / p.half;
   const int l = (int)(bl % p.L), b = (int)(bl / p.L);
   const int pos = p.positions ? __ldg(p.positions + bl) : l;
-  const float theta = __fmul_rn((float)pos, __ldg(p.inv_freq + i));
   float sn, cs;
-  sincosf(theta, &sn, &cs);
+  sincosf(rope_theta(pos, __ldg(p.inv_freq + i)), &sn, &cs);
   const int e0 = p.interleaved ? 2 * i : i;
   const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
   T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
@@ -79,14 +87,62 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
         load_pair<T, PAIRED>(row + (int64_t)(h0 + u) * p.s_h, e0, e1, a[u], c[u]);
 #pragma unroll
     for (int u = 0; u < kHeadBatch; ++u)
-      if (h0 + u < p.heads)
-        store_pair<T, PAIRED>(row + (int64_t)(h0 + u) * p.s_h, e0, e1, a[u] * cs - c[u] * sn,
-                              a[u] * sn + c[u] * cs);
+      if (h0 + u < p.heads) {
+        float y0, y1;
+        rope_rotate(a[u], c[u], cs, sn, y0, y1);
+        store_pair<T, PAIRED>(row + (int64_t)(h0 + u) * p.s_h, e0, e1, y0, y1);
+      }
   }
+}
+
+// One warp per rotated head vector (b, l, h < heads): RMS normalisation over
+// the D features, then the rotation of the first rot_dim; D <= 256.
+constexpr int kNormWarps = 8;
+template <typename T>
+__global__ void __launch_bounds__(32 * kNormWarps)
+rope_norm_kernel(const __grid_constant__ RopeParams p) {
+  __shared__ float rowbuf[kNormWarps][256];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int64_t task = (int64_t)blockIdx.x * kNormWarps + wl;  // (b, l, h) with h fastest
+  if (task >= (int64_t)p.B * p.L * p.heads) return;             // warp-uniform
+  const int h = (int)(task % p.heads);
+  const int64_t bl = task / p.heads;
+  const int l = (int)(bl % p.L), b = (int)(bl / p.L);
+  T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)h * p.s_h + (int64_t)l * p.s_l;
+  float *buf = rowbuf[wl];
+  float part = 0.f;
+  for (int d = lane, k = 0; d < p.D; d += 32, ++k) {
+    const float x = to_float(row[d]);
+    buf[d] = x;
+    part = rms_partial_add(part, x, k == 0);
+  }
+  const float r = rms_scale(rms_butterfly_warp(part), p.D, p.eps);
+  for (int d = lane; d < p.D; d += 32) buf[d] = rms_apply(buf[d], r, __ldg(p.norm_w + d));
+  __syncwarp();
+  const int pos = p.positions ? __ldg(p.positions + bl) : l;
+  for (int i = lane; i < p.half; i += 32) {
+    const int e0 = p.interleaved ? 2 * i : i;
+    const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
+    float sn, cs, y0, y1;
+    sincosf(rope_theta(pos, __ldg(p.inv_freq + i)), &sn, &cs);
+    rope_rotate(buf[e0], buf[e1], cs, sn, y0, y1);
+    row[e0] = from_float<T>(y0);
+    row[e1] = from_float<T>(y1);
+  }
+  for (int d = 2 * p.half + lane; d < p.D; d += 32) row[d] = from_float<T>(buf[d]);
 }
 
 template <typename T>
 mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
+  if (p.norm_w) {
+    const int64_t tasks = (int64_t)p.B * p.L * p.heads;
+    const int64_t blocks = (tasks + kNormWarps - 1) / kNormWarps;
+    if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
+    rope_norm_kernel<T><<<(unsigned)blocks, 32 * kNormWarps, 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
+    return MGQA_OK;
+  }
   const int64_t total = (int64_t)p.B * p.L * p.half;
   const int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
   if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
@@ -119,6 +175,10 @@ extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStr
   if (a->heads < 1 || a->heads > a->H)
     return fail(MGQA_ERR_INVALID_ARG, "rope: heads must be in [1, H]");
   if (!a->x || !a->inv_freq) return fail(MGQA_ERR_INVALID_ARG, "rope: x or inv_freq is null");
+  if (a->norm_weight && (a->D > 256 || !(a->norm_eps >= 0.f) || !std::isfinite(a->norm_eps) ||
+                         reinterpret_cast<uintptr_t>(a->norm_weight) % 4 != 0))
+    return fail(MGQA_ERR_INVALID_ARG, "rope: the norm needs D <= 256, a finite eps >= 0 and an "
+                                      "aligned fp32 weight");
   const size_t es = a->dtype == MGQA_FP32 ? 4 : 2;
   if (reinterpret_cast<uintptr_t>(a->x) % es != 0 ||
       reinterpret_cast<uintptr_t>(a->inv_freq) % 4 != 0 ||
@@ -135,8 +195,10 @@ extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStr
   p.s_b = a->x_stride[0]; p.s_h = a->x_stride[1]; p.s_l = a->x_stride[2];
   p.positions = a->positions;
   p.inv_freq = a->inv_freq;
-  p.B = a->B; p.L = a->L; p.half = a->rot_dim / 2; p.heads = a->heads;
+  p.B = a->B; p.L = a->L; p.D = a->D; p.half = a->rot_dim / 2; p.heads = a->heads;
   p.interleaved = a->interleaved != 0;
+  p.norm_w = a->norm_weight;
+  p.eps = a->norm_eps;
   if (a->dtype == MGQA_BF16) return launch_t<__nv_bfloat16>(p, stream);
   if (a->dtype == MGQA_FP16) return launch_t<__half>(p, stream);
   return launch_t<float>(p, stream);

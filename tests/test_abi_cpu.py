@@ -58,7 +58,8 @@ def test_debug_counter_count_is_checked_on_the_host(L):
     assert Ld.mgqa_debug_inject_prefill_stall(0, 1000) == M.MGQA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("cname,py", [("mgqa_args", M.MgqaArgs), ("mgqa_rope_args", M.MgqaRopeArgs)])
+@pytest.mark.parametrize("cname,py", [("mgqa_args", M.MgqaArgs), ("mgqa_rope_args", M.MgqaRopeArgs),
+                                     ("mgqa_qk_rope", M.MgqaQkRope)])
 def test_struct_layout_matches_header(tmp_path, cname, py):
     fields = [f for f, _ in py._fields_]
     src = tmp_path / "off.c"
@@ -234,3 +235,53 @@ int main(void) {
     r = subprocess.run([str(exe)], capture_output=True, text=True)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.strip() != ""
+
+
+def _valid_qk_rope():
+    r = M.MgqaQkRope()
+    r.inv_freq = 1 << 22  # fake, never dereferenced: validation fails before any launch
+    r.rot_dim, r.interleaved, r.q_heads, r.k_heads = 128, 0, 16, 8
+    r.norm_eps = 1e-6
+    return r
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda r: setattr(r, "inv_freq", 0),
+    lambda r: setattr(r, "inv_freq", (1 << 22) + 2),
+    lambda r: setattr(r, "rot_dim", 127),
+    lambda r: setattr(r, "rot_dim", 130),
+    lambda r: setattr(r, "q_heads", 0),
+    lambda r: setattr(r, "q_heads", 17),
+    lambda r: setattr(r, "positions", (1 << 23) + 1),
+    lambda r: (setattr(r, "q_norm_weight", 1 << 23), setattr(r, "norm_eps", -1.0)),
+    lambda r: (setattr(r, "q_norm_weight", 1 << 23), setattr(r, "norm_eps", float("nan"))),
+    lambda r: setattr(r, "k_norm_weight", (1 << 23) + 2),
+])
+def test_fused_rope_arguments_are_checked(L, mutate):
+    r = _valid_qk_rope()
+    mutate(r)
+    a = _valid_args()
+    assert L.masked_gqa_attn_prefill_rope(ctypes.byref(a), ctypes.byref(r), None) == M.MGQA_ERR_INVALID_ARG
+    assert L.mgqa_last_error_detail() != b""
+
+
+def test_fused_rope_decode_arguments_are_checked(L):
+    a = _valid_args()
+    a.Lq, a.Hkv = 1, 8
+    a.kv_len = 1 << 22
+    r = _valid_qk_rope()
+    r.k_heads = 9  # more than Hkv
+    st = L.masked_gqa_attn_decode_append_rope(ctypes.byref(a), 1 << 20, 1 << 20,
+                                              (ctypes.c_int64 * 2)(1024, 128), (ctypes.c_int64 * 2)(1024, 128),
+                                              None, ctypes.byref(r), 1 << 20, 1 << 20, None)
+    assert st == M.MGQA_ERR_INVALID_ARG and b"k_heads" in L.mgqa_last_error_detail()
+    assert L.masked_gqa_attn_prefill_rope(ctypes.byref(a), None, None) == M.MGQA_ERR_INVALID_ARG
+
+
+def test_fused_rope_prefill_refuses_fp32(L):
+    a = _valid_args()
+    a.dtype = M.MGQA_FP32
+    for fld, H in (("q_stride", 16), ("k_stride", 8), ("v_stride", 8), ("o_stride", 16)):
+        getattr(a, fld)[:] = [H * 1024 * 128, 1024 * 128, 128]
+    r = _valid_qk_rope()
+    assert L.masked_gqa_attn_prefill_rope(ctypes.byref(a), ctypes.byref(r), None) == M.MGQA_ERR_UNSUPPORTED
