@@ -253,6 +253,89 @@ def bench_rope(M, dev, reps=20, warmup=3, nsets=12):
     return e0.elapsed_time(e1) / 1e3 / (reps * nsets), nbytes
 
 
+def time_calls(fn, reps=20, warmup=3):
+    """Capture fn (a sequence of launches on the current stream) in a CUDA
+    graph; seconds per replay over `reps` replays."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / reps
+
+
+def bench_fused_rope(M, dev, nsets=8):
+    """The rotary embedding with the Qwen3-style q/k norm, fused into the
+    attention against the standalone kernel followed by the plain call:
+    (a) the padded-CFG prefill (q rotated in the kernel; k pre-rotated), (b)
+    the static-cache decode step with its append. Seconds per call."""
+    f128 = (10000.0 ** (-torch.arange(0, 128, 2, dtype=torch.float64) / 128)).to(torch.float32).to(dev)
+    f64 = (10000.0 ** (-torch.arange(0, 64, 2, dtype=torch.float64) / 64)).to(torch.float32).to(dev)
+    g = torch.Generator().manual_seed(1007)
+    w128 = (0.5 + torch.rand(128, generator=g)).to(dev)
+    w64 = (0.5 + torch.rand(64, generator=g)).to(dev)
+    wl = W.padded_cfg(variant="kvlen")
+    sets = []
+    for _ in range(nsets):
+        d = device_inputs(wl, dev)
+        sets.append((d, torch.empty_like(d["q"])))
+
+    def prefill_fused():
+        for d, out in sets:
+            M.masked_gqa_attn_prefill_rope(d["q"], d["k"], d["v"], out, inv_freq=f128,
+                                           q_norm_weight=w128, scale=wl.scale, kv_len=d["kv_len"])
+
+    def prefill_unfused():
+        for d, out in sets:
+            M.masked_gqa_rope(d["q"], f128, norm_weight=w128)
+            M.masked_gqa_attn_prefill(d["q"], d["k"], d["v"], out, scale=wl.scale, kv_len=d["kv_len"])
+
+    tp_f = time_calls(prefill_fused) / nsets
+    tp_u = time_calls(prefill_unfused) / nsets
+    del sets
+    wd = W.static_cache_decode(variant="span")
+    B, Hq, Hkv, _, Lk, D = wd.shape
+    dsets = []
+    for _ in range(DECODE_SETS):
+        d = device_inputs(wd, dev)
+        kn = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).to(dev)
+        vn = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).to(dev)
+        ws = M.new_decode_workspace(d["q"], d["k"], d["v"], kv_len=d["kv_len"])
+        dsets.append((d, kn, vn, ws, torch.empty_like(d["kv_len"]), torch.empty_like(d["q"])))
+    pos = [ds[0]["kv_len"][:, None].contiguous() for ds in dsets]
+
+    def step_fused():
+        for d, kn, vn, ws, lo, out in dsets:
+            M.masked_gqa_attn_decode_append_rope(d["q"], d["k"], d["v"], kn, vn, d["kv_len"], out,
+                                                 workspace=ws, inv_freq=f64, q_norm_weight=w64,
+                                                 k_norm_weight=w64, kv_len_out=lo, scale=wd.scale)
+
+    def step_unfused():
+        for (d, kn, vn, ws, lo, out), p in zip(dsets, pos):
+            M.masked_gqa_rope(d["q"], f64, positions=p, norm_weight=w64)
+            M.masked_gqa_rope(kn, f64, positions=p, norm_weight=w64)
+            M.masked_gqa_attn_decode_append(d["q"], d["k"], d["v"], kn, vn, d["kv_len"], out,
+                                            workspace=ws, kv_len_out=lo, scale=wd.scale)
+
+    td_f = time_calls(step_fused) / DECODE_SETS
+    td_u = time_calls(step_unfused) / DECODE_SETS
+    return tp_f, tp_u, td_f, td_u
+
+
 def decode_needed_bytes(wl):
     B, Hq, Hkv, Lq, Lk, D = wl.shape
     es = wl.k.element_size()
@@ -639,6 +722,25 @@ def run_gpu(args):
                                        "peak_kind": pk_kind, "bytes_per_launch": b_rope,
                                        "kernel": "rope"},
                           "clocks": ck}
+
+    # ---- the rotary embedding (+ q/k RMS norm) fused into the attention calls
+    clocks.start()
+    tp_f, tp_u, td_f, td_u = bench_fused_rope(M, dev)
+    ck = clocks.stop()
+    wr = W.padded_cfg(variant="kvlen")
+    configs["fused_rope"] = {
+        "workload": "rotary embedding with the q/k RMS norm (fp32 table, half-split pairs, all heads) "
+                    "inside the call: padded-CFG prefill (kv_len form; q rotated in the kernel, k "
+                    "already rotated) and the static-cache decode step with its append (q and the new "
+                    "key row rotated in the kernel), each against masked_gqa_rope + the plain call",
+        "prefill_fused_us": tp_f * 1e6, "prefill_unfused_us": tp_u * 1e6,
+        "prefill_fused_TFLOP_s": wr.flops() / tp_f / 1e12,
+        "decode_step_fused_us": td_f * 1e6, "decode_step_unfused_us": td_u * 1e6,
+        "value": tp_u / tp_f, "unit": "x (prefill: unfused time / fused time)",
+        "roofline": {"bound": "tensor", "achieved": wr.flops() / tp_f / 1e12, "peak": bf16,
+                     "unit": "TFLOP/s", "frac": wr.flops() / tp_f / 1e12 / bf16, "traffic": None,
+                     "peak_kind": f"bf16 burst, {pk_kind}", "kernel": "prefill_tc (fused rotary)"},
+        "clocks": ck}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
