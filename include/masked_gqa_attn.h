@@ -274,8 +274,9 @@ typedef struct {
  * kernel (each CTA transforms its query tile in shared memory once, before
  * its first product). The keys must already be rotated (and normalised), e.g.
  * by masked_gqa_rope with the same table: the result equals masked_gqa_rope
- * on q and then masked_gqa_attn_prefill, bit for bit. bf16 and fp16 only
- * (MGQA_ERR_UNSUPPORTED for fp32: rotate with masked_gqa_rope instead). */
+ * on q and then masked_gqa_attn_prefill, bit for bit. bf16 and fp16 only, and
+ * half-split rotations over D, D/2 or D/4 features (interleaved ones of any
+ * width); MGQA_ERR_UNSUPPORTED otherwise (rotate with masked_gqa_rope). */
 MGQA_API mgqa_status masked_gqa_attn_prefill_rope(const mgqa_args *args, const mgqa_qk_rope *rope,
                                                   cudaStream_t stream);
 

@@ -202,6 +202,12 @@ mgqa_status masked_gqa_attn_prefill_rope(const mgqa_args *args, const mgqa_qk_ro
                       "with masked_gqa_rope");
   mgqa::FusedRope fr;
   if ((st = mgqa::validate_rope(rope, *args, false, &fr)) != MGQA_OK) return st;
+  // the kernel keeps a query row in registers, which needs the pairing fixed
+  // at compile time: half-split rotations over D, D/2 or D/4 features
+  if (!fr.interleaved && fr.half != args->D / 2 && fr.half != args->D / 4 && fr.half != args->D / 8)
+    return mgqa::fail(MGQA_ERR_UNSUPPORTED,
+                      "fused prefill: half-split rotary dims must be D, D/2 or D/4 (rotate with "
+                      "masked_gqa_rope for other widths)");
   return mgqa::launch_prefill_tc(*args, stream, fr);
 }
 

@@ -111,6 +111,24 @@ MGQA_DEV int load_kv_len(const int32_t *kv_len, int b, int Lk, int32_t *err, boo
 // theta = fl32(position * inv_freq)
 MGQA_DEV float rope_theta(int pos, float f) { return __fmul_rn((float)pos, f); }
 
+// sin and cos of theta (|theta| < 2^22): Cody-Waite argument reduction
+// (W. J. Cody and W. Waite, Software Manual for the Elementary Functions,
+// 1980) by 2 pi, written as a float head and a float tail of its value, with
+// one rounding per fused multiply-add, to r in about [-pi, pi]; then the
+// MUFU sine and cosine of r. Error: at most about 5e-7 (the unit's 2^-21.4 on
+// [-pi, pi] plus half an ulp of pi from the reduction); short and branch-free,
+// so kernels can unroll it over a row.
+MGQA_DEV void rope_sincos(float theta, float &sn, float &cs) {
+  constexpr double kTwoPi = 6.283185307179586476925286766559;
+  constexpr float kHi = (float)kTwoPi;
+  constexpr float kLo = (float)(kTwoPi - (double)kHi);
+  constexpr float kInv = (float)(1.0 / kTwoPi);
+  const float k = rintf(__fmul_rn(theta, kInv));
+  const float r = __fmaf_rn(-k, kLo, __fmaf_rn(-k, kHi, theta));
+  sn = __sinf(r);
+  cs = __cosf(r);
+}
+
 // (a, c) -> (a cos - c sin, a sin + c cos)
 MGQA_DEV void rope_rotate(float a, float c, float cs, float sn, float &x0, float &x1) {
   x0 = __fsub_rn(__fmul_rn(a, cs), __fmul_rn(c, sn));
@@ -129,10 +147,25 @@ MGQA_DEV float rms_butterfly_warp(float p) {  // every lane of the warp takes pa
   for (int o = 16; o > 0; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
   return p;
 }
-// The same butterfly on 32 partials held by one thread (p is overwritten).
-MGQA_DEV float rms_butterfly_local(float (&p)[32]) {
+// The same sum for a row held by one thread: the partials of lanes l and
+// l + 16 are formed and combined at once (the butterfly's first step), then
+// the remaining steps run on 16 values.
+template <int D>
+MGQA_DEV float rms_sum_row(const float (&x)[D]) {
+  static_assert(D % 32 == 0, "row of whole lanes");
+  float p[16];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int l = 0; l < 16; ++l) {
+    float a = 0.f, c = 0.f;
+#pragma unroll
+    for (int d = l, k = 0; d < D; d += 32, ++k) {
+      a = rms_partial_add(a, x[d], k == 0);
+      c = rms_partial_add(c, x[d + 16], k == 0);
+    }
+    p[l] = __fadd_rn(a, c);
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1)
 #pragma unroll
     for (int l = 0; l < o; ++l) p[l] = __fadd_rn(p[l], p[l + o]);
   return p[0];

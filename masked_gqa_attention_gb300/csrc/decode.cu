@@ -273,7 +273,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       for (int d = tid; d < D; d += kThreads) sm.knew[d] = to_float(sm.newk[d]);
     for (int i = tid; i < p.rope.half; i += kThreads) {
       float sn, cs;
-      sincosf(rope_theta(npos, __ldg(p.rope.inv_freq + i)), &sn, &cs);
+      rope_sincos(rope_theta(npos, __ldg(p.rope.inv_freq + i)), sn, cs);
       sm.cs[i] = make_float2(cs, sn);
     }
     __syncthreads();

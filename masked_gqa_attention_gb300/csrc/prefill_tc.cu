@@ -179,20 +179,19 @@ template <> MGQA_DEV float half_of<__half>(uint32_t v, int hi) {
   return __half2float(__ushort_as_half((unsigned short)(hi ? (v >> 16) : (v & 0xffffu))));
 }
 
-// The rotary embedding's pairs of one row held as floats, in place. Interleaved
-// pairs and half-split pairs over the whole head dim (HALF = D / 2) index the
-// row with constants, so it stays in registers; a partial half-split rotation
-// (HALF = 0: rp.half at run time) indexes it at run time.
+// The rotary embedding's pairs of one row held as floats, in place. Every
+// index is a constant (interleaved pairs stop at rp.half; half-split pairs
+// have HALF as a template argument), so the row stays in registers.
 template <int D, bool INTERLEAVED, int HALF>
 MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
-  const int half = HALF > 0 ? HALF : rp.half;
+  const int half = INTERLEAVED ? rp.half : HALF;
 #pragma unroll
   for (int i = 0; i < D / 2; ++i) {
     if (i >= half) break;
     const int e0 = INTERLEAVED ? 2 * i : i;
     const int e1 = INTERLEAVED ? 2 * i + 1 : i + half;
     float sn, cs, y0, y1;
-    sincosf(rope_theta(pos, __ldg(rp.inv_freq + i)), &sn, &cs);
+    rope_sincos(rope_theta(pos, __ldg(rp.inv_freq + i)), sn, cs);
     rope_rotate(x[e0], x[e1], cs, sn, y0, y1);
     x[e0] = y0;
     x[e1] = y1;
@@ -204,36 +203,30 @@ MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
 // arithmetic as the standalone rotary-embedding kernel.
 template <typename T, int D>
 MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &rp) {
-  uint32_t w[D / 2];
+  float x[D];  // the row as floats (16-bit values are exact in fp32)
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const uint4 u = *reinterpret_cast<const uint4 *>(tile + (c >> 3) * BOX + r * 128 +
                                                       (((c & 7) ^ (r & 7)) << 4));
-    w[4 * c] = u.x;
-    w[4 * c + 1] = u.y;
-    w[4 * c + 2] = u.z;
-    w[4 * c + 3] = u.w;
+    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[8 * c + j] = half_of<T>(w4[j >> 1], j & 1);
   }
-  float x[D];
-#pragma unroll
-  for (int d = 0; d < D; ++d) x[d] = half_of<T>(w[d >> 1], d & 1);
   if (rp.q_norm) {
-    float part[32];
-#pragma unroll
-    for (int d = 0; d < D; ++d) part[d % 32] = rms_partial_add(part[d % 32], x[d], d < 32);
-    const float rs = rms_scale(rms_butterfly_local(part), D, rp.eps);
+    const float rs = rms_scale(rms_sum_row<D>(x), D, rp.eps);
 #pragma unroll
     for (int d = 0; d < D; ++d) x[d] = rms_apply(x[d], rs, __ldg(rp.q_norm + d));
   }
+  // half-split widths D/2, D/4, D/8 (the host refuses others)
   if (rp.interleaved) rope_row_pairs<D, true, 0>(x, rp, pos);
   else if (rp.half == D / 2) rope_row_pairs<D, false, D / 2>(x, rp, pos);
-  else rope_row_pairs<D, false, 0>(x, rp, pos);
+  else if (rp.half == D / 4) rope_row_pairs<D, false, D / 4>(x, rp, pos);
+  else rope_row_pairs<D, false, D / 8>(x, rp, pos);
 #pragma unroll
-  for (int d = 0; d < D; d += 2) w[d >> 1] = pack2<T>(x[d], x[d + 1]);  // one rounding
-#pragma unroll
-  for (int c = 0; c < D / 8; ++c)
+  for (int c = 0; c < D / 8; ++c)  // one rounding to the I/O type
     *reinterpret_cast<uint4 *>(tile + (c >> 3) * BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
-        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        make_uint4(pack2<T>(x[8 * c], x[8 * c + 1]), pack2<T>(x[8 * c + 2], x[8 * c + 3]),
+                   pack2<T>(x[8 * c + 4], x[8 * c + 5]), pack2<T>(x[8 * c + 6], x[8 * c + 7]));
 }
 
 // One 128-key tile of one softmax row (thread = row): the whole score row is

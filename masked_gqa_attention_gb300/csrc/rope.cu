@@ -8,8 +8,9 @@
 // (positions restart at 0 for each packed sequence).
 //
 // One thread per (row b, position l, pair i): it forms theta = fl32(pos * f_i)
-// once, takes its sine and cosine (accurate sincosf: positions reach several
-// thousand radians) and rotates pair i of every rotated head at (b, l).
+// once, takes its sine and cosine (positions reach thousands of radians: the
+// shared reduced-argument sine and cosine of common.cuh) and rotates pair i
+// of every rotated head at (b, l).
 // Consecutive threads take consecutive pairs, so each warp reads and writes
 // whole runs of a row (interleaved: one contiguous run; half-split: two).
 // The pairs of kHeadBatch heads are loaded before any is stored, so their
@@ -75,7 +76,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   const int l = (int)(bl % p.L), b = (int)(bl / p.L);
   const int pos = p.positions ? __ldg(p.positions + bl) : l;
   float sn, cs;
-  sincosf(rope_theta(pos, __ldg(p.inv_freq + i)), &sn, &cs);
+  rope_sincos(rope_theta(pos, __ldg(p.inv_freq + i)), sn, cs);
   const int e0 = p.interleaved ? 2 * i : i;
   const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
   T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
@@ -124,7 +125,7 @@ rope_norm_kernel(const __grid_constant__ RopeParams p) {
     const int e0 = p.interleaved ? 2 * i : i;
     const int e1 = p.interleaved ? 2 * i + 1 : i + p.half;
     float sn, cs, y0, y1;
-    sincosf(rope_theta(pos, __ldg(p.inv_freq + i)), &sn, &cs);
+    rope_sincos(rope_theta(pos, __ldg(p.inv_freq + i)), sn, cs);
     rope_rotate(buf[e0], buf[e1], cs, sn, y0, y1);
     row[e0] = from_float<T>(y0);
     row[e1] = from_float<T>(y1);

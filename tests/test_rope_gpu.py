@@ -55,11 +55,12 @@ def test_rope_matches_oracle(M, oracle_mod, dtype, interleaved, case):
     got = xd.cpu()
     if dtype != torch.float32:
         # per element: rounding the fp32 result to the output type (unit
-        # roundoff 2^-8 for bf16, 2^-11 for fp16) plus the fp32 arithmetic
-        # (a few ulp of |a| + |c| <= 1e-5 here) and fp16's subnormal spacing
+        # roundoff 2^-8 for bf16, 2^-11 for fp16) plus the fp32 arithmetic: a
+        # few ulp of |a| + |c|, and the sine and cosine's own error (at most
+        # about 5e-7 after the reduction by 2 pi) times |a| + |c| <= 10 here
         u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -11
         err = np.abs(got.double().numpy() - ref)
-        assert np.all(err <= u * np.abs(ref) + 4e-6), float((err - u * np.abs(ref)).max())
+        assert np.all(err <= u * np.abs(ref) + 1e-5), float((err - u * np.abs(ref)).max())
     # what must not rotate is bit-for-bit the input
     assert torch.equal(got[:, heads:], x[:, heads:])
     assert torch.equal(got[..., rot:], x[..., rot:])
@@ -107,3 +108,22 @@ def test_rope_rejects_host_tensors_and_bad_tables(M):
         M.masked_gqa_rope(x, inv_freq_table(64))
     with pytest.raises(ValueError):
         M.masked_gqa_rope(x.cuda(), inv_freq_table(32).cuda())
+
+
+def test_reduced_sincos_error_bound(M):
+    """The rotation's sine and cosine (reduction by 2 pi, then the MUFU unit)
+    against fp64 over the angles of positions up to 32768: rotating (1, 0) by
+    theta gives (cos theta, sin theta) of the fp32 angle exactly as computed."""
+    g = torch.Generator().manual_seed(77)
+    L = 4096
+    x = torch.zeros(1, 1, L, 2, dtype=torch.float32)
+    x[..., 0] = 1.0
+    pos = torch.randint(0, 32768, (1, L), generator=g, dtype=torch.int32)
+    f = torch.tensor([0.99], dtype=torch.float32)
+    xd = x.cuda()
+    M.masked_gqa_rope(xd, f.cuda(), positions=pos.cuda(), interleaved=True)
+    torch.cuda.synchronize()
+    theta = (pos.to(torch.float32) * f[0]).double()[0]   # the fp32 product, widened
+    got = xd.cpu().double()[0, 0]
+    err = torch.maximum((got[:, 0] - torch.cos(theta)).abs(), (got[:, 1] - torch.sin(theta)).abs())
+    assert float(err.max()) <= 1e-6, float(err.max())
