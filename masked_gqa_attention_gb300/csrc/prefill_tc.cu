@@ -333,7 +333,9 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
   tc::tmem_wait_st();
 }
 
-template <typename T, int D, int NT, int STAGES>
+// ROPE: the query tile is normalised / rotated in shared memory first (a
+// separate instantiation, so the plain kernel carries none of that code).
+template <typename T, int D, int NT, int STAGES, bool ROPE>
 __global__ void __launch_bounds__(128 * (1 + NT), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -691,7 +693,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tc::fence_after_sync();
       for (int t = 0; t < NT && ok; ++t) {
         // a fused rotary embedding rewrites the query tile first
-        if (p.rope.inv_freq && !wait(bar_qrot + t, 0)) break;
+        if (ROPE && !wait(bar_qrot + t, 0)) break;
         tc::fence_after_sync();
         issue_s(t, 0, 0, D / 16);
       }
@@ -774,7 +776,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t t_s = tmem + lane_base + t * BN;
     const uint32_t t_o = tmem + lane_base + NT * BN + t * D;
     const int segq = p.mask.seg_q ? __ldg(p.mask.seg_q + (int64_t)b * p.Lq + ic) : 0;
-    if (p.rope.inv_freq) {
+    if constexpr (ROPE) {
       // rotary embedding (and RMS norm) of this head's query row, in shared
       // memory, before the head's first product
       if (ok) ok = mbar_wait(bar_q, 0, p.err, lim);
@@ -906,11 +908,11 @@ bool make_tma_map_4d(CUtensorMap *m, mgqa_dtype dt, const void *base, int B, int
 
 namespace {
 
-template <typename T, int D, int NT, int STAGES>
+template <typename T, int D, int NT, int STAGES, bool ROPE>
 mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                      const CUtensorMap &mo, const TcParams &p, cudaStream_t s) {
   using Lay = Layout<D, NT, STAGES>;
-  auto kern = prefill_tc_kernel<T, D, NT, STAGES>;
+  auto kern = prefill_tc_kernel<T, D, NT, STAGES, ROPE>;
   static std::atomic<uint64_t> attr_done{0};
   const mgqa_status st = ensure_smem_attr(kern, Lay::smem_bytes, attr_done, "tensor-core prefill");
   if (st != MGQA_OK) return st;
@@ -921,14 +923,16 @@ mgqa_status launch_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtenso
   return MGQA_OK;
 }
 
-template <typename T>
+template <typename T, bool ROPE>
 mgqa_status dispatch_d(int D, bool pair, const CUtensorMap &mq, const CUtensorMap &mk,
                        const CUtensorMap &mv, const CUtensorMap &mo, const TcParams &p,
                        cudaStream_t s) {
   if (D == 128)
-    return pair ? launch_t<T, 128, 2, 2>(mq, mk, mv, mo, p, s) : launch_t<T, 128, 1, 2>(mq, mk, mv, mo, p, s);
+    return pair ? launch_t<T, 128, 2, 2, ROPE>(mq, mk, mv, mo, p, s)
+                : launch_t<T, 128, 1, 2, ROPE>(mq, mk, mv, mo, p, s);
   if (D == 64)
-    return pair ? launch_t<T, 64, 2, 3>(mq, mk, mv, mo, p, s) : launch_t<T, 64, 1, 3>(mq, mk, mv, mo, p, s);
+    return pair ? launch_t<T, 64, 2, 3, ROPE>(mq, mk, mv, mo, p, s)
+                : launch_t<T, 64, 1, 3, ROPE>(mq, mk, mv, mo, p, s);
   return fail(MGQA_ERR_UNSUPPORTED, "head dim %d", D);
 }
 
@@ -957,8 +961,12 @@ mgqa_status launch_prefill_tc(const mgqa_args &a, cudaStream_t s, const FusedRop
   p.lse = a.lse; p.err = a.dev_error;
   p.rope = rope;
   const bool pair = (p.n_rep % 2) == 0;
-  if (a.dtype == MGQA_BF16) return dispatch_d<__nv_bfloat16>(a.D, pair, mq, mk, mv, mo, p, s);
-  return dispatch_d<__half>(a.D, pair, mq, mk, mv, mo, p, s);
+  const bool rope_on = rope.inv_freq != nullptr;
+  if (a.dtype == MGQA_BF16)
+    return rope_on ? dispatch_d<__nv_bfloat16, true>(a.D, pair, mq, mk, mv, mo, p, s)
+                   : dispatch_d<__nv_bfloat16, false>(a.D, pair, mq, mk, mv, mo, p, s);
+  return rope_on ? dispatch_d<__half, true>(a.D, pair, mq, mk, mv, mo, p, s)
+                 : dispatch_d<__half, false>(a.D, pair, mq, mk, mv, mo, p, s);
 }
 
 }  // namespace mgqa

@@ -85,8 +85,9 @@ class Model:
     when the first non-empty tile is not tile 0 (the speculative tile-0 loads
     are then wasted). `rng` drives every delay."""
 
-    def __init__(self, NT, STAGES, nk, spec_miss, rng, variant="kernel", stop_at=None):
+    def __init__(self, NT, STAGES, nk, spec_miss, rng, variant="kernel", stop_at=None, rope=False):
         self.NT, self.STAGES, self.nk, self.spec_miss = NT, STAGES, nk, spec_miss
+        self.rope = rope  # the fused rotary embedding: q_rot[t] before head t's first product
         self.rng, self.variant = rng, variant
         self.stop_at = stop_at          # producer stall (failure path) or None
         self.strict = stop_at is None   # protocol checks only on the normal path
@@ -102,6 +103,7 @@ class Model:
         self.odone = [B(f"odone{t}", 1) for t in range(NT)]
         self.spec = B("spec", 1)
         self.drain = B("drain", 1)
+        self.qrot = [B(f"qrot{t}", 1) for t in range(NT)]
         self.t = 0.0
         self.events = []      # (time, seq, fn)
         self.seq = 0
@@ -212,9 +214,14 @@ class Model:
         ok = ok and (yield from W(m.q, 0, "mma q"))
         ok = ok and (yield from W(m.kfull[0], fill(0, 0), "mma k0"))
         ok = ok and (yield from W(m.vfull[0], fill(0, 0), "mma v0"))
-        if ok:
-            for t in range(NT):
-                issue_s(t, 0, 0, D16, D16)
+        for t in range(NT):
+            if not ok:
+                break
+            if m.rope:
+                ok = yield from W(m.qrot[t], 0, f"mma qrot{t}")
+                if not ok:
+                    break
+            issue_s(t, 0, 0, D16, D16)
         p0_seen = False
         for n in range(nk):
             if not ok:
@@ -272,6 +279,11 @@ class Model:
     def softmax(self, t):
         m, W = self, self.W
         ok = True
+        if m.rope:  # rotate the head's query tile once Q has landed
+            ok = yield from W(m.q, 0, f"softmax{t} q for rotation")
+            if ok:
+                yield ("delay", m.rng.uniform(0.5, 3.0))
+            m.qrot[t].arrive()
         for n in range(m.nk):
             if ok:
                 ok = yield from W(m.sfull[t], n, f"softmax{t} sfull n={n}")
@@ -302,6 +314,9 @@ class Model:
             for bar, want in ((self.sfull[t], nk), (self.pfull[t], nk), (self.odone[t], 1 if nk else 0)):
                 if bar.completed != want:
                     raise ProtocolError(f"{bar.name}: {bar.completed} phases, expected {want}")
+        for t in range(NT):
+            if self.qrot[t].completed != (1 if self.rope else 0):
+                raise ProtocolError(f"qrot{t}: {self.qrot[t].completed} phases")
         want_spec = 1 if (nk == 0 or self.spec_miss) and self.variant != "old-speculation" else 0
         if self.spec.completed != want_spec:
             raise ProtocolError(f"spec: {self.spec.completed} phases, expected {want_spec}")

@@ -15,14 +15,15 @@ import pytest
 from _pipeline_model import Model, ProtocolError
 
 
+@pytest.mark.parametrize("rope", [False, True])
 @pytest.mark.parametrize("NT", [1, 2])
 @pytest.mark.parametrize("STAGES", [2, 3])
 @pytest.mark.parametrize("spec_miss", [False, True])
-def test_every_schedule_is_sound(NT, STAGES, spec_miss):
+def test_every_schedule_is_sound(NT, STAGES, spec_miss, rope):
     for nk in range(0, 7):
         for seed in range(60):
             rng = random.Random(1000003 * seed + 7919 * nk + 31 * NT + STAGES + (5 if spec_miss else 0))
-            Model(NT, STAGES, nk, spec_miss, rng).run()
+            Model(NT, STAGES, nk, spec_miss, rng, rope=rope).run()
 
 
 def test_model_finds_the_old_speculation_race():
@@ -37,15 +38,16 @@ def test_model_finds_the_old_speculation_race():
     assert any("two phases past" in f or "older phase" in f for f in found), found[:3]
 
 
+@pytest.mark.parametrize("rope", [False, True])
 @pytest.mark.parametrize("NT", [1, 2])
 @pytest.mark.parametrize("STAGES", [2, 3])
 @pytest.mark.parametrize("spec_miss", [False, True])
-def test_stalled_producer_ends_cleanly(NT, STAGES, spec_miss):
+def test_stalled_producer_ends_cleanly(NT, STAGES, spec_miss, rope):
     for nk in range(2, 7):
         for stop in range(1, nk):
             for seed in range(25):
                 rng = random.Random(7919 * seed + 131 * nk + 17 * stop + NT + STAGES)
-                m = Model(NT, STAGES, nk, spec_miss, rng, stop_at=stop)
+                m = Model(NT, STAGES, nk, spec_miss, rng, stop_at=stop, rope=rope)
                 m.run()
                 assert m.timeouts, "the stall was not noticed"
 
