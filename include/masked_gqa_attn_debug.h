@@ -47,14 +47,18 @@ MGQA_API mgqa_status mgqa_debug_reset(void);
  * memory is freed. tile < 0 removes the stall. Synchronous. */
 MGQA_API mgqa_status mgqa_debug_inject_prefill_stall(int32_t tile, uint64_t wait_limit_ns);
 
-/* Per-CTA timeline of the most recent decode launch, for the first n_ctas
- * (<= 512) CTAs in launch order (x fastest): 16 values per CTA -- the SM
+/* Per-CTA timeline of the decode launches since the previous read, for the
+ * first n_ctas (<= 512) CTAs in launch order (x fastest), as written by the
+ * most recent launch that reached each stamp: 16 values per CTA -- the SM
  * clock at the kernel's phase boundaries 0..8 (entry; after the grid-
  * dependency wait; the allowed-slot words formed; the first batch's copies
  * issued; the first batch landed; every batch computed; the in-CTA merge; the
- * ticket taken; the merged output written, by the last CTA only), 0 in slots
- * 9..12, the global timer (ns) at entry and at the ticket, and the SM id.
- * Synchronous. */
+ * ticket taken; the merged output written, by the last CTA only), then at
+ * four points inside the first batch of the 16-bit path: 9 (masked rows
+ * fixed up), 10 (the shared maximum exchanged), 11 (this warp's scores and
+ * maximum formed), 12 (the batch's bytes armed); the global timer (ns) at
+ * entry and at the ticket, and the SM id. A stamp a CTA did not reach reads
+ * 0. Reading clears the record for all CTAs. Synchronous. */
 MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas);
 
 #ifdef __cplusplus

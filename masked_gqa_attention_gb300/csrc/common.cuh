@@ -224,6 +224,10 @@ MGQA_DEV void named_sync(int id, int nthreads) {
 // kernel in the stream start its own set-up early.
 MGQA_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 MGQA_DEV void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// A hint that brings the line of p into the L2 (and its page translation
+// into the SM's TLBs). Nothing is read into the SM and the L2 is the point
+// of coherence, so it may precede grid_dependency_wait().
+MGQA_DEV void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // ---- mbarrier / bulk-copy primitives (PTX) --------------------------------
 
@@ -393,6 +397,29 @@ MGQA_DEV void ldmatrix_x2_trans(uint32_t &b0, uint32_t &b1, const void *row) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
                : "=r"(b0), "=r"(b1)
                : "r"(smem_u32(row)));
+}
+
+// Four 8x8 16-bit tiles from shared memory; lane i gives the address of row
+// i % 8 of tile i / 8. Lane t receives row t / 4, elements 2 (t % 4) and
+// 2 (t % 4) + 1 of each tile (the .trans form: of each tile's transpose).
+MGQA_DEV void ldmatrix_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(row)));
+}
+MGQA_DEV void ldmatrix_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3,
+                                const void *row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(smem_u32(row)));
+}
+
+// Transpose of an 8x8 16-bit matrix held as a warp fragment (lane t: row
+// t / 4, elements 2 (t % 4) and 2 (t % 4) + 1, low half first).
+MGQA_DEV uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
 }  // namespace mgqa

@@ -113,10 +113,11 @@ struct DecodeSmem {
   static constexpr int CHB = KB * BOXB;                        // bytes of one chunk slot
   static constexpr int CPB = 32768 / CHB;                      // chunks per batch: 32 KB of K
   static constexpr int CAPR = CPB * C;                         // positional rows per batch
-  static constexpr int RPW = CAPR / kWarps;                    // rows per warp
+  static constexpr int RPW = CAPR / kWarps;                    // rows per warp (fp32 path)
   static_assert(CAPR <= kThreads && RPW >= 8, "batch layout");
-  static constexpr int WOB = kWarps * NREP * D * 4;            // per-warp O (after the last batch)
-  static_assert(WOB <= CPB * CHB, "per-warp O fits in the K buffer");
+  static constexpr int DP = D + 4;                             // per-warp O row pitch (floats)
+  static constexpr int WOB = kWarps * NREP * DP * 4;           // per-warp O (after the last batch)
+  static_assert(WOB <= 2 * CPB * CHB, "per-warp O fits in the K and V buffers");
   // byte offsets (the base is 1024-byte aligned)
   static constexpr int k_off = 0;
   static constexpr int v_off = CPB * CHB;
@@ -157,7 +158,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char *kbuf = smem + Sm::k_off, *vbuf = smem + Sm::v_off;
   auto &sm = *reinterpret_cast<typename Sm::Misc *>(smem + Sm::misc_off);
-  float(*wo)[NREP][D] = reinterpret_cast<float(*)[NREP][D]>(kbuf);  // after the last batch
+  float(*wo)[NREP][Sm::DP] = reinterpret_cast<float(*)[NREP][Sm::DP]>(kbuf);  // K, V: after the last batch
 
   const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -169,10 +170,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     tc::prefetch_tensormap(&tm_v);
     allow_dependents();
   }
-  grid_dependency_wait();  // everything below may read what the previous kernel wrote
-  dec_stamp(1);
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
+  if (warp == 1 && lane < 8) {
+    // warm the L2 lines and page translations this CTA touches first
+    const char *pf = nullptr;
+    const int64_t r0 = (int64_t)x * C;
+    if (lane == 0) pf = static_cast<const char *>(p.q) + ((int64_t)b * p.qs_b + (int64_t)h0 * p.qs_h) * sizeof(T);
+    if (lane == 1 && p.kv_len) pf = reinterpret_cast<const char *>(p.kv_len + b);
+    if (lane == 2 && p.bits && r0 < p.Lk) pf = reinterpret_cast<const char *>(p.bits + (int64_t)b * p.ms_b + (r0 >> 5));
+    if (lane == 3 && r0 < p.Lk)
+      pf = static_cast<const char *>(p.k) + ((int64_t)b * p.ks_b + (int64_t)g * p.ks_h + r0 * p.ks_l) * sizeof(T);
+    if (lane == 4 && r0 < p.Lk)
+      pf = static_cast<const char *>(p.v) + ((int64_t)b * p.vs_b + (int64_t)g * p.vs_h + r0 * p.vs_l) * sizeof(T);
+    if (lane == 5) pf = reinterpret_cast<const char *>(p.ws_o + (((int64_t)b * p.Hq + h0) * S + x) * D);
+    if (lane == 6) pf = reinterpret_cast<const char *>(p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg);
+    if (lane == 7 && p.seg_k && r0 < p.Lk) pf = reinterpret_cast<const char *>(p.seg_k + (int64_t)b * p.Lk + r0);
+    if (pf) prefetch_l2(pf);
+  }
+  grid_dependency_wait();  // everything below may read what the previous kernel wrote
+  dec_stamp(1);
   const int nci = x < p.nch ? (p.nch - x + S - 1) / S : 0;  // my chunks
   const int gq = lane >> 2, tq = lane & 3;                   // mma fragment coordinates
 
@@ -345,13 +362,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     return make_uint2(sm.words[chunk][0], sm.words[chunk][1]);
   };
 
-  // running state: mma path -- every lane holds head gq's shared maximum, its
-  // rows' part of l and its fragment of O; fp32 path -- as in the batch softmax
-  float m_run = -INFINITY, l_part = 0.f;
-  float ow[use_mma<T>() ? D / 8 : 1][4];
+  // running state: mma path -- every lane holds the shared maximum of heads
+  // 2 tq and 2 tq + 1, its rows' part of their l and its fragment of O^T
+  // (rows: features, columns: heads); fp32 path -- as in the batch softmax
+  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+  float ot[use_mma<T>() ? D / 16 : 1][4];
   if constexpr (use_mma<T>()) {
 #pragma unroll
-    for (int dt = 0; dt < D / 8; ++dt) ow[dt][0] = ow[dt][1] = ow[dt][2] = ow[dt][3] = 0.f;
+    for (int mt = 0; mt < D / 16; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
   }
   constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, dim pair) per thread
   float o[ITEMS][2];
@@ -364,18 +382,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   for (int bt = 0; bt < nbatch; ++bt) {
     // ---- 2. gather: thread 0 fetches the batch's chunks as TMA boxes
     const int nbc = min(CPB, n_ne - bt * CPB);  // chunks in this batch
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&sm.bar, (uint32_t)(nbc * 2 * Sm::CHB));
-      uint32_t rem = nem;  // drop the chunks of the earlier batches
-      for (int e = 0; e < bt * CPB; ++e) rem &= rem - 1u;
-      for (int cs = 0; cs < nbc; ++cs) {
-        const int chunk = __ffs(rem) - 1;
-        rem &= rem - 1u;
-        const int row = (x + S * chunk) * C;
-        if (!MGQA_DCHECK(row < p.Lk && g < p.Hkv, p.err)) continue;
-        for (int bx = 0; bx < Sm::KB; ++bx) {
-          tc::tma_load_4d(kbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_k, bx * 64, row, g, b, &sm.bar);
-          tc::tma_load_4d(vbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_v, bx * 64, row, g, b, &sm.bar);
+    // (lane i of warp 0 holds chunk i: the chunks of rank bt * CPB + cs go to
+    // chunk slot cs, one lane each, after lane 0 armed the batch's bytes)
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(&sm.bar, (uint32_t)(nbc * 2 * Sm::CHB));
+      if (bt == 0) dec_stamp(12);
+      __syncwarp();
+      const int cs = my_rank - bt * CPB;
+      if (my_rank >= 0 && cs >= 0 && cs < nbc) {
+        const int row = (x + S * lane) * C;
+        if (MGQA_DCHECK(row < p.Lk && g < p.Hkv, p.err)) {
+#pragma unroll
+          for (int bx = 0; bx < Sm::KB; ++bx) {
+            tc::tma_load_4d(kbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_k, bx * 64, row, g, b, &sm.bar);
+            tc::tma_load_4d(vbuf + cs * Sm::CHB + bx * Sm::BOXB, &tm_v, bx * 64, row, g, b, &sm.bar);
+          }
         }
       }
     }
@@ -389,7 +410,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     // masked rows: a zero V row (exact zeros through the product); the row a
     // fused append adds: the step's input (thread r owns positional row r)
-    if (warp * 32 < CAPR) {  // warp-uniform: whole warps own rows
+    // (the mma path reads only the rows of fetched chunk slots)
+    if (warp * 32 < (use_mma<T>() ? nbc * C : CAPR)) {  // warp-uniform: whole warps own rows
       const int r = tid;
       int chunk = -1;
       const uint2 w2 = chunk_words(bt, r / C, chunk);
@@ -411,77 +433,106 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     if (bt == 0) dec_stamp(9);
 
     // ---- 3. the batch's products
-    int chunk_w = -1;
-    const uint2 ww = chunk_words(bt, (warp * RPW) / C, chunk_w);  // a warp's rows share a chunk
-    auto row_allowed = [&](int row) {
-      return (((row % C) < 32 ? ww.x : ww.y) >> (row % 32)) & 1u;
-    };
     if constexpr (use_mma<T>()) {
-      constexpr int NG = RPW / 16;  // 16-row groups per warp
-      const int r0 = warp * RPW;
-      float c[NG][2][4];
+      // S^T = K q^T and O^T += V^T P^T: the cache rows are the M side of the
+      // score product (16 per mma, no padding rows) and the heads its N side
+      // (8, padded with zero q rows); P^T becomes the B operand of the second
+      // product by an in-register transpose of its two 8 x 8 halves. Warp w
+      // takes the 16-row groups w, w + 8, ... of the fetched chunk slots.
+      constexpr int GPW = CAPR / 16 / kWarps;  // groups per warp
+      const int ngrp = nbc * (C / 16);         // groups of fetched rows
+      const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: tile, row within it
+      float sc[GPW][4];  // (row gq | gq + 8) x (head 2 tq | 2 tq + 1), log2 units
 #pragma unroll
-      for (int g16 = 0; g16 < NG; ++g16)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          float *cc = c[g16][nt];
-          cc[0] = cc[1] = cc[2] = cc[3] = 0.f;
-          const int kr = r0 + g16 * 16 + nt * 8 + gq;
+      for (int j = 0; j < GPW; ++j) {
+        const int gi = warp + j * kWarps;
+        sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = -INFINITY;
+        if (gi < ngrp) {  // warp-uniform
+          int chunk;
+          const uint2 w2 = chunk_words(bt, gi * 16 / C, chunk);
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          const int krow = gi * 16 + (mi & 1) * 8 + rr;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(kbuf + Sm::seg_off(kr, 2 * kk) + 4 * tq);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(kbuf + Sm::seg_off(kr, 2 * kk + 1) + 4 * tq);
-            mma_16816<T>(c[g16][nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(a0, a1, a2, a3, kbuf + Sm::seg_off(krow, 2 * kk + (mi >> 1)));
+            mma_16816<T>(acc, a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
           }
+          const int s0 = (gi * 16) % C + gq, s1 = s0 + 8;  // slots within the chunk
+          const bool al0 = ((s0 < 32 ? w2.x : w2.y) >> (s0 % 32)) & 1u;
+          const bool al1 = ((s1 < 32 ? w2.x : w2.y) >> (s1 % 32)) & 1u;
+          sc[j][0] = al0 ? acc[0] * p.scale_log2 : -INFINITY;
+          sc[j][1] = al0 ? acc[1] * p.scale_log2 : -INFINITY;
+          sc[j][2] = al1 ? acc[2] * p.scale_log2 : -INFINITY;
+          sc[j][3] = al1 ? acc[3] * p.scale_log2 : -INFINITY;
         }
-      float mx = -INFINITY;
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int g16 = 0; g16 < NG; ++g16)
+      for (int j = 0; j < GPW; ++j) {
+        mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][2]));
+        mx1 = fmaxf(mx1, fmaxf(sc[j][1], sc[j][3]));
+      }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = r0 + g16 * 16 + nt * 8 + 2 * tq + h;
-            c[g16][nt][h] = row_allowed(row) ? c[g16][nt][h] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, c[g16][nt][h]);
-          }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      if (tq == 0 && gq < NREP) sm.wmax[warp][gq] = mx;
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      if (bt == 0) dec_stamp(11);
+      if (gq == 0) {
+        if (2 * tq < NREP) sm.wmax[warp][2 * tq] = mx0;
+        if (2 * tq + 1 < NREP) sm.wmax[warp][2 * tq + 1] = mx1;
+      }
       __syncthreads();
       if (bt == 0) dec_stamp(10);
-      float mb = -INFINITY;
-      if (gq < NREP) {
+      // finite: the batch holds an allowed row (padding heads use 0)
+      float m_new[2], f[2];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) mb = fmaxf(mb, sm.wmax[w][gq]);
-      }
-      // finite: the batch holds an allowed row (padding rows gq >= NREP use 0)
-      const float m_new = gq < NREP ? fmaxf(m_run, mb) : 0.f;
-      const float f = (m_run == -INFINITY) ? 0.f : fast_exp2(m_run - m_new);
-      m_run = m_new;
-      l_part *= f;
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * tq + e;
+        float mb = -INFINITY;
+        if (h < NREP) {
 #pragma unroll
-      for (int dt = 0; dt < D / 8; ++dt) {
-        ow[dt][0] *= f;
-        ow[dt][1] *= f;
-      }
-#pragma unroll
-      for (int g16 = 0; g16 < NG; ++g16) {
-        uint32_t pa[2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const float p0 = fast_exp2(c[g16][nt][0] - m_new), p1 = fast_exp2(c[g16][nt][1] - m_new);
-          l_part += p0 + p1;
-          pa[nt] = pack2<T>(p0, p1);
+          for (int w = 0; w < kWarps; ++w) mb = fmaxf(mb, sm.wmax[w][h]);
         }
+        m_new[e] = h < NREP ? fmaxf(m_run[e], mb) : 0.f;
+        f[e] = (m_run[e] == -INFINITY) ? 0.f : fast_exp2(m_run[e] - m_new[e]);
+        m_run[e] = m_new[e];
+        l_part[e] *= f[e];
+      }
 #pragma unroll
-        for (int dt = 0; dt < D / 8; ++dt) {
-          uint32_t b0, b1;
-          ldmatrix_x2_trans(b0, b1, vbuf + Sm::seg_off(r0 + g16 * 16 + (lane & 15), dt));
-          mma_16816<T>(ow[dt], pa[0], 0u, pa[1], 0u, b0, b1);
+      for (int mt = 0; mt < D / 16; ++mt) {
+        ot[mt][0] *= f[0];
+        ot[mt][1] *= f[1];
+        ot[mt][2] *= f[0];
+        ot[mt][3] *= f[1];
+      }
+#pragma unroll
+      for (int j = 0; j < GPW; ++j) {
+        const int gi = warp + j * kWarps;
+        if (gi < ngrp) {  // warp-uniform
+          const float p0 = fast_exp2(sc[j][0] - m_new[0]), p1 = fast_exp2(sc[j][1] - m_new[1]);
+          const float p2 = fast_exp2(sc[j][2] - m_new[0]), p3 = fast_exp2(sc[j][3] - m_new[1]);
+          l_part[0] += p0 + p2;
+          l_part[1] += p1 + p3;
+          // P^T (heads x rows) as the B operand: rows 0..7 of the group, then 8..15
+          const uint32_t b0 = movmatrix_trans(pack2<T>(p0, p1));
+          const uint32_t b1 = movmatrix_trans(pack2<T>(p2, p3));
+          const int vrow = gi * 16 + (mi >> 1) * 8 + rr;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(a0, a1, a2, a3, vbuf + Sm::seg_off(vrow, 2 * mt + (mi & 1)));
+            mma_16816<T>(ot[mt], a0, a1, a2, a3, b0, b1);
+          }
         }
       }
     } else {
+      int chunk_w = -1;
+      const uint2 ww = chunk_words(bt, (warp * RPW) / C, chunk_w);  // a warp's rows share a chunk
+      auto row_allowed = [&](int row) {
+        return (((row % C) < 32 ? ww.x : ww.y) >> (row % 32)) & 1u;
+      };
       // scores (log2 units): GL lanes share a row, 16 bytes each
       constexpr int EPL = 16 / sizeof(T), GL = D / EPL, SPW = 32 / GL;
       static_assert(GL <= 32 && RPW % SPW == 0, "lane layout");
@@ -574,18 +625,34 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   // in-CTA merge: every warp used the same maximum, so O and l are sums
   float M = -INFINITY;
   if constexpr (use_mma<T>()) {
-    float l = l_part;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (gq < NREP) {
-      if (tq == 0) {
-        sm.wsum[warp][gq] = l;
-        if (warp == 0) sm.mrun[gq] = m_run;
+    // warps past the first batch's groups never held a row: nothing to add
+    const int nact = min(kWarps, min(CPB, n_ne) * (C / 16));
+    float l0 = l_part[0], l1 = l_part[1];
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    const int h0l = 2 * tq, h1l = 2 * tq + 1;
+    if (gq == 0 && warp == 0) {
+      if (h0l < NREP) sm.mrun[h0l] = m_run[0];
+      if (h1l < NREP) sm.mrun[h1l] = m_run[1];
+    }
+    if (warp < nact) {  // warp-uniform
+      if (gq == 0) {
+        if (h0l < NREP) sm.wsum[warp][h0l] = l0;
+        if (h1l < NREP) sm.wsum[warp][h1l] = l1;
       }
 #pragma unroll
-      for (int dt = 0; dt < D / 8; ++dt) {
-        wo[warp][gq][dt * 8 + 2 * tq] = ow[dt][0];
-        wo[warp][gq][dt * 8 + 2 * tq + 1] = ow[dt][1];
+      for (int mt = 0; mt < D / 16; ++mt) {
+        if (h0l < NREP) {
+          wo[warp][h0l][mt * 16 + gq] = ot[mt][0];
+          wo[warp][h0l][mt * 16 + gq + 8] = ot[mt][2];
+        }
+        if (h1l < NREP) {
+          wo[warp][h1l][mt * 16 + gq] = ot[mt][1];
+          wo[warp][h1l][mt * 16 + gq + 8] = ot[mt][3];
+        }
       }
     }
     __syncthreads();
@@ -595,10 +662,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       if (idx < NREP * D / 2) {
         const int r = idx / (D / 2), dp = idx % (D / 2);
         float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          a0 += wo[w][r][2 * dp];
-          a1 += wo[w][r][2 * dp + 1];
+        for (int w = 0; w < nact; ++w) {
+          const float2 v2 = *reinterpret_cast<const float2 *>(&wo[w][r][2 * dp]);
+          a0 += v2.x;
+          a1 += v2.y;
         }
         o[u][0] = a0;
         o[u][1] = a1;
@@ -606,8 +673,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     if (warp < NREP) {
       float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) L += sm.wsum[w][warp];
+      for (int w = 0; w < nact; ++w) L += sm.wsum[w][warp];
       l_h = L;
       m_h = sm.mrun[warp];
     }
@@ -880,9 +946,11 @@ extern "C" MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_
   clear_error_detail();
   if (!out || n_ctas < 0 || n_ctas > kTlCtas)
     return fail(MGQA_ERR_INVALID_ARG, "mgqa_debug_decode_timeline: bad output or count");
-  const cudaError_t e =
-      cudaMemcpyFromSymbol(out, g_dec_tl, (size_t)n_ctas * kTlStamps * sizeof(uint64_t));
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_dec_tl, (size_t)n_ctas * kTlStamps * sizeof(uint64_t));
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the timeline: %s", cudaGetErrorString(e));
+  static const unsigned long long zeros[kTlCtas][kTlStamps] = {};
+  e = cudaMemcpyToSymbol(g_dec_tl, zeros, sizeof(zeros));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "clearing the timeline: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
 #endif  // MGQA_DEBUG
