@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MGQA_ABI_VERSION 4
+#define MGQA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define MGQA_API __attribute__((visibility("default")))
@@ -120,24 +120,25 @@ typedef struct mgqa_args {
  * Returns MGQA_OK once the kernel is enqueued. */
 MGQA_API mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream);
 
-/* Bytes of device workspace masked_gqa_attn_decode needs for these arguments
- * (0 when the arguments are invalid). */
+/* Nominal workspace size for these decode arguments: 16 for supported
+ * arguments, 0 when they are invalid (a validity check). The decode kernel
+ * merges its splits on chip and never reads or writes a workspace; the
+ * workspace parameters below are kept so that callers written against earlier
+ * versions keep working. */
 MGQA_API size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args);
 
 /* One-query (Lq == 1) attention over a static KV cache of Lk slots. The
  * cache is cut into 64-slot chunks of absolute positions, dealt round-robin
- * to a fixed set of 16 CTAs per (request, KV-head group); masked slots are
- * never read, and the partial results are merged in a fixed order inside the
- * same launch, so the full-cache (mask_bits) and filled-span (kv_len) forms
- * of one mask give bit-identical outputs.
- * `workspace` is caller-owned device memory of at least
- * masked_gqa_attn_decode_workspace_size(args) bytes, 16-byte aligned, ZEROED
- * ONCE before its first use. It starts with the merge tickets, in a region
- * that nothing else writes and that every call leaves at zero again, so one
- * workspace serves later calls of any shape that fits in it (with up to 4096
- * (request, head group) pairs; larger shapes need it zeroed again after a
- * call of another shape). Calls that share a workspace must be ordered on one
- * stream. `stream` belongs to the current device. */
+ * to the 16 CTAs of one thread-block cluster per (request, KV-head group);
+ * masked slots are never read. The CTAs' partial results are exchanged
+ * through the cluster's shared memory and merged in a fixed order inside the
+ * same launch, so the full-cache (mask_bits) and filled-span (kv_len) forms of
+ * one mask give bit-identical outputs. The launch needs 16-CTA clusters (a
+ * non-portable size, available on this library's sm_103a target); a GPU
+ * partition too small to hold one returns MGQA_ERR_CUDA.
+ * `workspace` / `workspace_bytes` are ignored (may be NULL / 0). Calls on
+ * different streams are independent: no state is shared between calls.
+ * `stream` belongs to the current device. */
 MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace,
                                             size_t workspace_bytes, cudaStream_t stream);
 
@@ -153,8 +154,8 @@ MGQA_API mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspa
  * kv_len, so a captured graph can ping-pong two length buffers). args->kv_len
  * is required; packed bits and segment ids are not accepted here. A request
  * whose cache is already full (kv_len[b] == Lk) appends nothing, attends over
- * the whole cache, and sets *dev_error to MGQA_ERR_INVALID_ARG. Workspace as
- * for masked_gqa_attn_decode. */
+ * the whole cache, and sets *dev_error to MGQA_ERR_INVALID_ARG. The workspace
+ * parameters are ignored, as for masked_gqa_attn_decode. */
 MGQA_API mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_new,
                                                    const void *v_new, const int64_t *k_new_stride,
                                                    const int64_t *v_new_stride,
@@ -182,29 +183,16 @@ MGQA_API mgqa_status masked_gqa_unpack_pair(mgqa_dtype dtype, int32_t B, int32_t
                                             void *b, const int64_t *b_stride, int32_t Lb,
                                             cudaStream_t stream);
 
-/* Bytes of the fixed device scratch array behind masked_gqa_attn_decode_static
- * (one per GPU that loads the library, kept until the process exits). It holds
- * the workspace of every decode call with B * Hq <= 989 at head dim 64, or
- * B * Hq <= 502 at head dim 128. */
-#define MGQA_DECODE_STATIC_SCRATCH_BYTES (4u << 20)
-
-/* masked_gqa_attn_decode without a caller-supplied workspace. No passage of
- * the engine pages has a counterpart: this entry point exists for callers that
+/* masked_gqa_attn_decode without a workspace argument. No passage of the
+ * engine pages has a counterpart: this entry point exists for callers that
  * cannot allocate device memory for the library, such as code running inside
  * a host framework that owns every device buffer and hands an extension only
  * its inputs and outputs, or a latency-critical per-token loop that must not
- * call the allocator. The caller still passes q/k/v, out and the mask forms.
- * Scratch comes from a fixed array of MGQA_DECODE_STATIC_SCRATCH_BYTES in the
- * library; a call whose masked_gqa_attn_decode_workspace_size exceeds it
- * returns MGQA_ERR_UNSUPPORTED. Nothing is allocated or freed: no cudaMalloc,
- * cudaFree or allocating library routine is called.
- * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture. `stream`
- * must belong to the current device. Every call on a device shares the one
- * array (the previous call's contents stay in it; each call clears its merge
- * tickets on `stream` first), so calls whose executions
- * overlap on the GPU -- different streams, or different host threads -- race
- * and corrupt each other's results: order them on one stream. */
+ * call the allocator. The caller passes q/k/v, out and the mask forms; the
+ * kernel's scratch is on-chip shared memory of its own launch, so nothing is
+ * allocated or freed (no cudaMalloc, cudaFree or allocating library routine
+ * is called), nothing persists between calls and calls on different streams
+ * do not interfere. `stream` must belong to the current device. */
 MGQA_API mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream);
 
 /* Rotary position embedding, in place, on q or k before attention (the

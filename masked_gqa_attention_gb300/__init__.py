@@ -9,8 +9,8 @@ Entry points (same names as the C ABI):
   * :func:`masked_gqa_attn_prefill` -- bidirectional full-sequence attention
     under a packed-bit mask, per-row key lengths and/or segment ids;
   * :func:`masked_gqa_attn_decode` -- one query per row over a static KV
-    cache, with a caller-owned workspace
-    (:func:`masked_gqa_attn_decode_workspace_size` bytes, zeroed once).
+    cache, merged on chip (the ``workspace`` arguments are accepted and
+    ignored).
 """
 from __future__ import annotations
 
@@ -30,7 +30,7 @@ __all__ = [
     "MGQA_ERR_TIMEOUT", "MgqaError", "MgqaArgs", "lib", "make_args",
     "masked_gqa_attn_prefill", "masked_gqa_attn_decode",
     "masked_gqa_attn_decode_workspace_size", "new_decode_workspace", "build_library",
-    "masked_gqa_attn_decode_static", "DECODE_STATIC_SCRATCH_BYTES",
+    "masked_gqa_attn_decode_static",
     "masked_gqa_attn_decode_append", "masked_gqa_pack_pair", "masked_gqa_unpack_pair",
     "debug_lib", "MGQA_ERR_DEVICE_CHECK", "MgqaQkRope", "make_qk_rope",
     "masked_gqa_attn_prefill_rope", "masked_gqa_attn_decode_append_rope", "masked_gqa_rope",
@@ -39,8 +39,6 @@ __all__ = [
 (MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT,
  MGQA_ERR_DEVICE_CHECK) = range(6)
 MGQA_BF16, MGQA_FP32, MGQA_FP16 = 0, 1, 2
-# size of the library's fixed decode scratch (MGQA_DECODE_STATIC_SCRATCH_BYTES)
-DECODE_STATIC_SCRATCH_BYTES = 4 << 20
 
 EXPORTED_SYMBOLS = (
     "masked_gqa_attn_prefill",
@@ -300,6 +298,14 @@ def masked_gqa_attn_prefill(q, k, v, out=None, *, scale=None, mask_bits=None, kv
     return out
 
 
+def _workspace(ws):
+    """(pointer, bytes) of an optional decode workspace (ignored by the kernel)."""
+    if ws is None:
+        return None, 0
+    _dev(ws, "workspace")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
 def masked_gqa_attn_decode_workspace_size(q, k, v, **masks) -> int:
     out = q  # shape/dtype stand-in; the library only reads the sizes
     a = make_args(q, k, v, out, **masks)
@@ -310,12 +316,13 @@ def masked_gqa_attn_decode_workspace_size(q, k, v, **masks) -> int:
 
 
 def new_decode_workspace(q, k, v, **masks) -> torch.Tensor:
-    """A zeroed workspace tensor (uint8) sized for these decode arguments."""
+    """A workspace tensor (uint8) of the nominal size for these decode
+    arguments; the kernel never touches it (kept for earlier callers)."""
     n = masked_gqa_attn_decode_workspace_size(q, k, v, **masks)
     return torch.zeros(n, dtype=torch.uint8, device=q.device)
 
 
-def masked_gqa_attn_decode(q, k, v, out=None, *, workspace: torch.Tensor, scale=None,
+def masked_gqa_attn_decode(q, k, v, out=None, *, workspace: Optional[torch.Tensor] = None, scale=None,
                            mask_bits=None, kv_len=None, seg_q=None, seg_k=None, lse=None,
                            dev_error=None, stream=None):
     """One query per row (q [B, Hq, 1, D]) over a static cache k/v [B, Hkv, Lk, D]."""
@@ -323,18 +330,16 @@ def masked_gqa_attn_decode(q, k, v, out=None, *, workspace: torch.Tensor, scale=
         out = torch.empty_like(q)
     a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
                   seg_k=seg_k, lse=lse, dev_error=dev_error)
-    _dev(workspace, "workspace")
-    _check(lib().masked_gqa_attn_decode(ctypes.byref(a), workspace.data_ptr(),
-                                        workspace.numel() * workspace.element_size(),
-                                        _stream_handle(stream)))
+    wp, wn = _workspace(workspace)
+    _check(lib().masked_gqa_attn_decode(ctypes.byref(a), wp, wn, _stream_handle(stream)))
     return out
 
 
 def masked_gqa_attn_decode_static(q, k, v, out=None, *, scale=None, mask_bits=None, kv_len=None,
                                   seg_q=None, seg_k=None, lse=None, dev_error=None, stream=None):
-    """masked_gqa_attn_decode with the library's fixed scratch instead of a
-    workspace, for callers that may not allocate device memory. Calls on one
-    device share that scratch: keep them ordered on one stream."""
+    """masked_gqa_attn_decode without a workspace argument, for callers that
+    may not allocate device memory: the kernel's scratch is its own on-chip
+    shared memory, so nothing is allocated and calls do not share state."""
     if out is None:
         out = torch.empty_like(q)
     a = make_args(q, k, v, out, scale=scale, mask_bits=mask_bits, kv_len=kv_len, seg_q=seg_q,
@@ -344,7 +349,8 @@ def masked_gqa_attn_decode_static(q, k, v, out=None, *, scale=None, mask_bits=No
 
 
 def masked_gqa_attn_decode_append(q, k_cache, v_cache, k_new, v_new, kv_len, out=None, *,
-                                  workspace: torch.Tensor, kv_len_out=None, scale=None, lse=None,
+                                  workspace: Optional[torch.Tensor] = None, kv_len_out=None,
+                                  scale=None, lse=None,
                                   dev_error=None, stream=None):
     """One decode step fused with its cache append: k_new/v_new [B, Hkv, 1, D]
     go to slot kv_len[b] of k_cache/v_cache [B, Hkv, Lk, D] (written in place),
@@ -360,11 +366,10 @@ def masked_gqa_attn_decode_append(q, k_cache, v_cache, k_new, v_new, kv_len, out
             raise ValueError(f"{name} must be [B, Hkv, 1, D] with a unit-stride head dim")
     ks = (ctypes.c_int64 * 2)(k_new.stride(0), k_new.stride(1))
     vs = (ctypes.c_int64 * 2)(v_new.stride(0), v_new.stride(1))
-    _dev(workspace, "workspace")
+    wp, wn = _workspace(workspace)
     _check(lib().masked_gqa_attn_decode_append(
         ctypes.byref(a), k_new.data_ptr(), v_new.data_ptr(), ks, vs,
-        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), wp, wn, _stream_handle(stream)))
     return out
 
 
@@ -450,6 +455,8 @@ def make_qk_rope(inv_freq, D, *, positions=None, rot_dim=None, interleaved=False
     positions int32 (prefill [B, Lq]; decode step [B]) or None, optional fp32
     [D] norm weights."""
     rot_dim = D if rot_dim is None else int(rot_dim)
+    if inv_freq is None:
+        raise ValueError("inv_freq is required")
     _dev(inv_freq, "inv_freq", torch.float32)
     if not inv_freq.is_contiguous() or inv_freq.numel() != rot_dim // 2:
         raise ValueError(f"inv_freq must be a contiguous fp32 tensor of {rot_dim // 2} values")
@@ -494,7 +501,8 @@ def masked_gqa_attn_prefill_rope(q, k, v, out=None, *, inv_freq, positions=None,
 
 
 def masked_gqa_attn_decode_append_rope(q, k_cache, v_cache, k_new, v_new, kv_len, out=None, *,
-                                       workspace: torch.Tensor, inv_freq, positions=None,
+                                       workspace: Optional[torch.Tensor] = None, inv_freq=None,
+                                       positions=None,
                                        rot_dim=None, interleaved=False, q_heads=None,
                                        k_heads=None, q_norm_weight=None, k_norm_weight=None,
                                        norm_eps=1e-6, kv_len_out=None, scale=None, lse=None,
@@ -519,9 +527,9 @@ def masked_gqa_attn_decode_append_rope(q, k_cache, v_cache, k_new, v_new, kv_len
                      q_norm_weight=q_norm_weight, k_norm_weight=k_norm_weight, norm_eps=norm_eps)
     ks = (ctypes.c_int64 * 2)(k_new.stride(0), k_new.stride(1))
     vs = (ctypes.c_int64 * 2)(v_new.stride(0), v_new.stride(1))
-    _dev(workspace, "workspace")
+    wp, wn = _workspace(workspace)
     _check(lib().masked_gqa_attn_decode_append_rope(
         ctypes.byref(a), k_new.data_ptr(), v_new.data_ptr(), ks, vs,
-        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), ctypes.byref(r), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+        _ptr(_dev(kv_len_out, "kv_len_out", torch.int32)), ctypes.byref(r), wp, wn,
+        _stream_handle(stream)))
     return out

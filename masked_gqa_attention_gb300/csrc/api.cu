@@ -115,7 +115,7 @@ mgqa_status validate_rope(const mgqa_qk_rope *r, const mgqa_args &a, bool decode
 
 mgqa_status validate_append(const mgqa_args *args, const void *k_new, const void *v_new,
                             const int64_t *k_new_stride, const int64_t *v_new_stride,
-                            int32_t *kv_len_out, void *workspace) {
+                            int32_t *kv_len_out) {
   mgqa_status st = validate(args, true);
   if (st != MGQA_OK) return st;
   if (!args->kv_len) return fail(MGQA_ERR_INVALID_ARG, "append needs kv_len");
@@ -134,8 +134,6 @@ mgqa_status validate_append(const mgqa_args *args, const void *k_new, const void
     return fail(MGQA_ERR_INVALID_ARG, "kv_len_out must not alias kv_len");
   if (kv_len_out && (reinterpret_cast<uintptr_t>(kv_len_out) % 4))
     return fail(MGQA_ERR_INVALID_ARG, "kv_len_out misaligned");
-  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
-    return fail(MGQA_ERR_INVALID_ARG, "workspace missing or not 16-byte aligned");
   return MGQA_OK;
 }
 
@@ -153,17 +151,16 @@ mgqa_status masked_gqa_attn_prefill(const mgqa_args *args, cudaStream_t stream) 
 
 size_t masked_gqa_attn_decode_workspace_size(const mgqa_args *args) {
   if (mgqa::validate(args, true) != MGQA_OK) return 0;
-  return mgqa::decode_workspace_bytes(*args);
+  return mgqa::kDecodeWorkspaceBytes;
 }
 
 mgqa_status masked_gqa_attn_decode(const mgqa_args *args, void *workspace, size_t workspace_bytes,
                                    cudaStream_t stream) {
+  (void)workspace;  // merged on chip: nothing is read or written there
+  (void)workspace_bytes;
   mgqa_status st = mgqa::validate(args, true);
   if (st != MGQA_OK) return st;
-  if (!workspace) return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace is null");
-  if ((reinterpret_cast<uintptr_t>(workspace) % 16) != 0)
-    return mgqa::fail(MGQA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
-  return mgqa::launch_decode(*args, workspace, workspace_bytes, stream);
+  return mgqa::launch_decode(*args, stream);
 }
 
 mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_new,
@@ -171,11 +168,13 @@ mgqa_status masked_gqa_attn_decode_append(const mgqa_args *args, const void *k_n
                                           const int64_t *v_new_stride, int32_t *kv_len_out,
                                           void *workspace, size_t workspace_bytes,
                                           cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
   const mgqa_status st = mgqa::validate_append(args, k_new, v_new, k_new_stride, v_new_stride,
-                                               kv_len_out, workspace);
+                                               kv_len_out);
   if (st != MGQA_OK) return st;
   return mgqa::launch_decode_append(*args, k_new, v_new, k_new_stride, v_new_stride, kv_len_out,
-                                    workspace, workspace_bytes, stream);
+                                    stream);
 }
 
 mgqa_status masked_gqa_attn_decode_append_rope(const mgqa_args *args, const void *k_new,
@@ -183,13 +182,15 @@ mgqa_status masked_gqa_attn_decode_append_rope(const mgqa_args *args, const void
                                                const int64_t *v_new_stride, int32_t *kv_len_out,
                                                const mgqa_qk_rope *rope, void *workspace,
                                                size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
   mgqa_status st = mgqa::validate_append(args, k_new, v_new, k_new_stride, v_new_stride,
-                                         kv_len_out, workspace);
+                                         kv_len_out);
   if (st != MGQA_OK) return st;
   mgqa::FusedRope fr;
   if ((st = mgqa::validate_rope(rope, *args, true, &fr)) != MGQA_OK) return st;
   return mgqa::launch_decode_append(*args, k_new, v_new, k_new_stride, v_new_stride, kv_len_out,
-                                    workspace, workspace_bytes, stream, fr);
+                                    stream, fr);
 }
 
 mgqa_status masked_gqa_attn_prefill_rope(const mgqa_args *args, const mgqa_qk_rope *rope,

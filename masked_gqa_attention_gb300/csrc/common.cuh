@@ -319,6 +319,31 @@ MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
   return true;
 }
 
+// mbar_wait for a phase completed by other CTAs of the cluster (their
+// st.async bytes): acquires at cluster scope.
+MGQA_DEV bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int32_t *err, uint64_t limit_ns) {
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+  };
+  uint64_t t0 = 0;
+  for (uint32_t n = 0; !try_wait(); ++n) {
+    if (n == 0u) t0 = globaltimer_ns();
+    if ((n & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) {
+      report_error(err, MGQA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ---- thread-block clusters (distributed shared memory) ---------------------
 
 // Barrier over every thread of the cluster. The arrive releases this thread's
@@ -329,6 +354,23 @@ MGQA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int32_t *err,
 MGQA_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The two halves of that barrier, for a wait placed long after the arrive:
+// the arrive releases this thread's earlier writes (an mbarrier's
+// initialisation included), the wait returns once every thread of the
+// cluster arrived. Both by all threads of every CTA.
+MGQA_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+MGQA_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Store two floats into shared memory of a CTA of the cluster (`addr` and
+// the mbarrier `bar` both in that CTA, as cluster_map addresses); 8 bytes of
+// completion are counted on `bar`, which releases them at cluster scope.
+MGQA_DEV void st_async_f32x2(uint32_t addr, float a, float b, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+                   addr),
+               "f"(a), "f"(b), "r"(bar)
+               : "memory");
 }
 
 // Address, in the cluster's shared window, of `p` (a variable of this CTA's

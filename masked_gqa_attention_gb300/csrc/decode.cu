@@ -1,5 +1,6 @@
-// One-query attention over a static KV cache, split over a fixed set of CTAs
-// per (request, KV-head group) and merged by log-sum-exp in the same launch.
+// One-query attention over a static KV cache: a cluster of 16 CTAs per
+// (request, KV-head group), whose partial results are merged on chip in the
+// same launch.
 //
 // Passages: VoxCPM page, "Upstream-identical practice", attention bullet
 // (decode against the static cache under an explicit boolean mask; slots past
@@ -7,33 +8,40 @@
 // attention_span paragraph (attend only to the filled blocks of the 8192-slot
 // cache instead of all of it).
 //
-// Design: S = 16 CTAs serve one (request b, head group hg) -- the NREP query
-// heads of one KV head. The cache is cut into 64-slot chunks of absolute
-// positions; CTA x owns chunks x, x + S, x + 2S, ...  A call is a short chain
-// of dependent steps, each kept to one memory round trip or one barrier:
+// Design: the S = 16 CTAs of one cluster serve one (request b, head group hg)
+// -- the NREP query heads of one KV head. The cache is cut into 64-slot chunks
+// of absolute positions; CTA x (its rank in the cluster) owns chunks x, x + S,
+// x + 2S, ...  A call is a short chain of dependent steps, each kept to one
+// memory round trip or one barrier:
 //   1. Every input of the mask test (kv_len, the CTA's mask words, segment
 //      ids) and q are loaded together. Each warp tests the slots of its
 //      chunks (one lane per slot, ballots) and stores the allowed-slot words.
 //   2. The non-empty chunks, in ascending order, fill batches of CAPR rows at
 //      fixed positions (row = chunk position in the batch * 64 + slot). Each
 //      chunk arrives as TMA tensor boxes of 64 rows (128-byte swizzled for the
-//      16-bit types, so the fragment loads are conflict-free), one mbarrier per
-//      batch. Masked rows then get a zero V row in shared memory, so they add
-//      exact zeros (a chunk past the filled length is never fetched; only the
-//      masked tail of a partly filled chunk is read and discarded); the row a
-//      fused append adds is written in from the step's input.
-//   3. bf16 / fp16: both products on the tensor cores (mma.sync m16n8k16, the
-//      <= 8 query heads padded to 16 rows). All warps share one running
-//      maximum per head (exchanged once per batch), so the in-CTA merge of the
-//      warps' outputs is a plain sum. fp32: CUDA cores, per-head batch softmax.
-//   4. Every CTA writes its partial (m, l, O) to the workspace and takes a
-//      ticket; the last of the S CTAs merges them in ascending order.
+//      16-bit types, so the fragment loads are conflict-free), issued by one
+//      lane per chunk, one mbarrier per batch. Masked rows then get a zero V
+//      row in shared memory, so they add exact zeros (a chunk past the filled
+//      length is never fetched; only the masked tail of a partly filled chunk
+//      is read and discarded); the row a fused append adds is written in from
+//      the step's input.
+//   3. bf16 / fp16: S^T = K q^T and O^T += V^T P^T on the tensor cores
+//      (mma.sync m16n8k16), the cache rows on the M side and the <= 8 heads on
+//      the N side, so no product carries padding rows; only fetched chunk
+//      slots are computed. All warps share one running maximum per head
+//      (exchanged once per batch), so the in-CTA merge of the warps' outputs
+//      is a plain sum. fp32: CUDA cores, per-head batch softmax.
+//   4. CTA x owns 1/S of the (head, feature) outputs. Every CTA stores its
+//      partial (m, l) and the matching slice of its unnormalised O into each
+//      owner's shared memory (st.async, counted in bytes on the owner's
+//      mbarrier); each owner merges the S partials of its slice in ascending
+//      split order and writes them. No global workspace, no ticket.
 // The chunk-to-CTA assignment, the batch layout and every summation order
 // depend only on the set of allowed slots, so a full-cache bitmask and the
 // equivalent filled length give bit-identical outputs.
 #include <cfloat>
 #include <cmath>
-#include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,16 +66,15 @@ struct DecodeParams {
   float *lse;
   int32_t *err;
   int B, Hq, Hkv, Lk, n_rep, nch;
-  unsigned *ws_tick;  // [B][Hq / NREP] arrival tickets
-  float2 *ws_ml;      // [B][Hq][S]    (m in log2 units, l)
-  float *ws_o;        // [B][Hq][S][D] unnormalised partial outputs
-  FusedRope rope;     // applied to q and the appended row (inv_freq null: none)
+  FusedRope rope;  // applied to q and the appended row (inv_freq null: none)
 };
 
-constexpr int kThreads = 256;
+// 4 warps a CTA, 3 CTAs an SM (<= 75 KB of shared memory each): the 16-CTA
+// clusters of the static-cache workloads then all fit on the GPU at once.
+constexpr int kThreads = 128;
 constexpr int kWarps = kThreads / 32;
 constexpr int C = kDecodeChunk;
-constexpr int S = kDecodeSplits;
+constexpr int S = kDecodeSplits;              // CTAs of a cluster
 constexpr int kMaxCI = kDecodeMaxLk / C / S;  // chunks per CTA (32)
 constexpr int kCPW = kMaxCI / kWarps;         // chunks per warp in the mask test
 static_assert(kMaxCI <= 32, "one ballot covers the CTA's chunks");
@@ -114,26 +121,37 @@ struct DecodeSmem {
   static constexpr int CPB = 32768 / CHB;                      // chunks per batch: 32 KB of K
   static constexpr int CAPR = CPB * C;                         // positional rows per batch
   static constexpr int RPW = CAPR / kWarps;                    // rows per warp (fp32 path)
-  static_assert(CAPR <= kThreads && RPW >= 8, "batch layout");
+  static_assert(RPW >= 16 && CAPR % (16 * kWarps) == 0, "batch layout");
   static constexpr int DP = D + 4;                             // per-warp O row pitch (floats)
   static constexpr int WOB = kWarps * NREP * DP * 4;           // per-warp O (after the last batch)
   static_assert(WOB <= 2 * CPB * CHB, "per-warp O fits in the K and V buffers");
+  static constexpr int E = NREP * D / S;                       // outputs each CTA merges
+  static_assert(E >= 2 && E % 2 == 0, "whole feature pairs per CTA");
+  // The fused rotation's rows (and the fp32 path's q): for the 16-bit types in
+  // the K buffer, which nothing else uses before the first batch's copies.
+  struct Rot {
+    float q[NREP][D];
+    float knew[D];
+    float2 cs[D / 2];
+  };
+  static_assert((int)sizeof(Rot) <= CPB * CHB, "rotation rows fit in the K buffer");
   // byte offsets (the base is 1024-byte aligned)
   static constexpr int k_off = 0;
   static constexpr int v_off = CPB * CHB;
   static constexpr int misc_off = 2 * CPB * CHB;
   struct Misc {
-    float q[NREP][D];                 // fp32 path, and any path with a fused rotation
-    float knew[D];                    // fused rotation: the appended key row
-    float2 cs[D / 2];                 // fused rotation: (cos, sin) of the new position
+    alignas(16) unsigned char rot[kMma ? 16 : sizeof(Rot)];
     float s[NREP][kMma ? 1 : CAPR];   // fp32 path: one batch's scores / weights
     float fo[NREP], fb[NREP];         // fp32 path
     float wmax[kWarps][NREP], wsum[kWarps][NREP];
-    float mrun[NREP];
+    float mrun[NREP], lrun[NREP];     // running (m, l) per head (l: fp32 path)
     uint32_t words[kMaxCI][2];        // allowed-slot words of the CTA's chunks
     alignas(16) T newk[D], newv[D];   // the row a fused append adds
+    alignas(16) T qh[kMma ? NREP : 1][D + 8];  // q as loaded (rows padded: conflict-free fragments)
+    float2 rx_ml[S][NREP];            // every split's (m, l) of each head
+    alignas(8) float rx_o[S][E];      // every split's partial O of this CTA's outputs
     alignas(8) uint64_t bar;          // one phase per batch
-    int is_last;
+    alignas(8) uint64_t rx_bar;       // the partials of this CTA's outputs
   };
   static constexpr int total = misc_off + (int)sizeof(Misc) + 1024;  // + alignment slack
   // byte address of 16-byte segment `seg` of positional row r (16-bit types)
@@ -145,31 +163,43 @@ struct DecodeSmem {
   static MGQA_DEV uint32_t row_off(int r) { return (r / C) * CHB + (r % C) * (D * 4); }
 };
 
-// Two CTAs per SM: the 16 x (head groups) x B grid of the static-cache
-// workloads (256 CTAs) then runs in one wave on 152 SMs.
 template <typename T, int D, int NREP>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const __grid_constant__ DecodeParams p) {
   using Sm = DecodeSmem<T, D, NREP>;
-  constexpr int CAPR = Sm::CAPR, CPB = Sm::CPB, RPW = Sm::RPW;
+  constexpr int CAPR = Sm::CAPR, CPB = Sm::CPB, RPW = Sm::RPW, E = Sm::E;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char *kbuf = smem + Sm::k_off, *vbuf = smem + Sm::v_off;
   auto &sm = *reinterpret_cast<typename Sm::Misc *>(smem + Sm::misc_off);
+  auto &rot = *reinterpret_cast<typename Sm::Rot *>(Sm::kMma ? kbuf : sm.rot);
   float(*wo)[NREP][Sm::DP] = reinterpret_cast<float(*)[NREP][Sm::DP]>(kbuf);  // K, V: after the last batch
 
-  const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
+  const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;  // x: rank in the cluster
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   dec_stamp(0);
   if (tid == 0) {
     mbar_init(&sm.bar, 1);  // thread 0 arms each batch once
+    mbar_init(&sm.rx_bar, 1);
+    // every split delivers this CTA's slice of its partial: (m, l) of each
+    // head and E floats of O
+    mbar_arrive_expect_tx(&sm.rx_bar, (uint32_t)(S * (E * 4 + NREP * 8)));
     fence_mbarrier_init();
     tc::prefetch_tensormap(&tm_k);
     tc::prefetch_tensormap(&tm_v);
     allow_dependents();
   }
+  // the receive barriers: armed in every CTA before any split delivers
+  cluster_arrive();
+#ifdef MGQA_DEBUG
+  {
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    if (tid == 0) MGQA_DCHECK(rank == (uint32_t)x, p.err);
+  }
+#endif
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
   if (warp == 1 && lane < 8) {
@@ -183,8 +213,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       pf = static_cast<const char *>(p.k) + ((int64_t)b * p.ks_b + (int64_t)g * p.ks_h + r0 * p.ks_l) * sizeof(T);
     if (lane == 4 && r0 < p.Lk)
       pf = static_cast<const char *>(p.v) + ((int64_t)b * p.vs_b + (int64_t)g * p.vs_h + r0 * p.vs_l) * sizeof(T);
-    if (lane == 5) pf = reinterpret_cast<const char *>(p.ws_o + (((int64_t)b * p.Hq + h0) * S + x) * D);
-    if (lane == 6) pf = reinterpret_cast<const char *>(p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg);
+    if (lane == 5) pf = static_cast<const char *>(p.out) + ((int64_t)b * p.os_b + (int64_t)h0 * p.os_h) * sizeof(T);
     if (lane == 7 && p.seg_k && r0 < p.Lk) pf = reinterpret_cast<const char *>(p.seg_k + (int64_t)b * p.Lk + r0);
     if (pf) prefetch_l2(pf);
   }
@@ -197,21 +226,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   const int kvl_raw = p.kv_len ? __ldg(p.kv_len + b) : p.Lk;
   const T *qb = static_cast<const T *>(p.q) + (int64_t)b * p.qs_b;
   const bool rope = p.rope.inv_freq != nullptr;
-  uint32_t qa[use_mma<T>() ? D / 16 : 1][2];  // Q as the A fragment (rows gq + 8: padding)
-  if constexpr (use_mma<T>()) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qa[kk][0] = qa[kk][1] = 0u;
-      if (gq < NREP && !rope) {
-        const T *qr = qb + (int64_t)(h0 + gq) * p.qs_h + kk * 16 + 2 * tq;
-        qa[kk][0] = *reinterpret_cast<const uint32_t *>(qr);
-        qa[kk][1] = *reinterpret_cast<const uint32_t *>(qr + 8);
-      }
-    }
+  constexpr int SEGS = D * (int)sizeof(T) / 16;  // 16-byte segments of a row
+  static_assert(2 * SEGS <= kThreads && (!use_mma<T>() || NREP * SEGS <= kThreads),
+                "one thread per row segment");
+  // q lands in shared memory within this round trip (a load first used by
+  // the products could otherwise be scheduled next to them)
+  if (use_mma<T>() && !rope && tid < NREP * SEGS) {
+    const int h = tid / SEGS, sg = tid % SEGS;
+    reinterpret_cast<uint4 *>(sm.qh[h])[sg] =
+        reinterpret_cast<const uint4 *>(qb + (int64_t)(h0 + h) * p.qs_h)[sg];
   }
   if (!use_mma<T>() || rope) {
     for (int i = tid; i < NREP * D; i += kThreads)
-      sm.q[i / D][i % D] = to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]);
+      rot.q[i / D][i % D] = to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]);
   }
   uint32_t wbits[kCPW][2];
   int segk[kCPW][2];
@@ -242,10 +269,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                          : nullptr;
   const T *vn = p.append ? static_cast<const T *>(p.v_new) + (int64_t)b * p.vn_b + (int64_t)g * p.vn_h
                          : nullptr;
-  constexpr int SEGS = D * (int)sizeof(T) / 16;  // 16-byte segments of a row
   if (p.append && tid < 2 * SEGS) {  // the appended row, wherever it lands
     const uint4 *src = reinterpret_cast<const uint4 *>(tid < SEGS ? kn : vn);
     reinterpret_cast<uint4 *>(tid < SEGS ? sm.newk : sm.newv)[tid % SEGS] = src[tid % SEGS];
+  }
+  if (tid < NREP) {
+    sm.mrun[tid] = -INFINITY;
+    sm.lrun[tid] = 0.f;
   }
   int kvl = kvl_raw;
   if (kvl < 0 || kvl > p.Lk) {
@@ -281,17 +311,28 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   __syncthreads();
   dec_stamp(2);
+  uint32_t qa[use_mma<T>() ? D / 16 : 1][2];  // q as the B operand (column gq: head gq)
+  if constexpr (use_mma<T>()) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = qa[kk][1] = 0u;
+      if (gq < NREP && !rope) {
+        qa[kk][0] = *reinterpret_cast<const uint32_t *>(&sm.qh[gq][kk * 16 + 2 * tq]);
+        qa[kk][1] = *reinterpret_cast<const uint32_t *>(&sm.qh[gq][kk * 16 + 2 * tq + 8]);
+      }
+    }
+  }
   if (rope) {
     // the step's query rows and new key row, normalised and rotated at the new
     // token's position with the arithmetic of the standalone kernel
     const int npos = p.rope.positions ? __ldg(p.rope.positions + b) : (pos >= 0 ? pos : kvl);
     const bool krow = p.append && g < p.rope.k_heads;
     if (krow)
-      for (int d = tid; d < D; d += kThreads) sm.knew[d] = to_float(sm.newk[d]);
+      for (int d = tid; d < D; d += kThreads) rot.knew[d] = to_float(sm.newk[d]);
     for (int i = tid; i < p.rope.half; i += kThreads) {
       float sn, cs;
       rope_sincos(rope_theta(npos, __ldg(p.rope.inv_freq + i)), sn, cs);
-      sm.cs[i] = make_float2(cs, sn);
+      rot.cs[i] = make_float2(cs, sn);
     }
     __syncthreads();
     // RMS norm: one warp per row, lane partials over d = lane (mod 32)
@@ -299,7 +340,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       const bool is_k = task == NREP;
       const float *wn = is_k ? p.rope.k_norm : p.rope.q_norm;
       if (!wn || (is_k ? !krow : h0 + task >= p.rope.q_heads)) continue;  // warp-uniform
-      float *row = is_k ? sm.knew : sm.q[task];
+      float *row = is_k ? rot.knew : rot.q[task];
       float part = 0.f;
       for (int d = lane, k = 0; d < D; d += 32, ++k) part = rms_partial_add(part, row[d], k == 0);
       const float rs = rms_scale(rms_butterfly_warp(part), D, p.rope.eps);
@@ -311,13 +352,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       const int task = it / (D / 2), i = it % (D / 2);
       const bool is_k = task == NREP;
       if (is_k ? !krow : h0 + task >= p.rope.q_heads) continue;
-      float *row = is_k ? sm.knew : sm.q[task];
+      float *row = is_k ? rot.knew : rot.q[task];
       const bool normed = is_k ? p.rope.k_norm != nullptr : p.rope.q_norm != nullptr;
       if (i < p.rope.half) {
         const int e0 = p.rope.interleaved ? 2 * i : i;
         const int e1 = p.rope.interleaved ? 2 * i + 1 : i + p.rope.half;
         float y0, y1;
-        rope_rotate(row[e0], row[e1], sm.cs[i].x, sm.cs[i].y, y0, y1);
+        rope_rotate(row[e0], row[e1], rot.cs[i].x, rot.cs[i].y, y0, y1);
         if (is_k) {
           sm.newk[e0] = from_float<T>(y0);
           sm.newk[e1] = from_float<T>(y1);
@@ -337,9 +378,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         if (gq < NREP) {
-          qa[kk][0] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq], sm.q[gq][kk * 16 + 2 * tq + 1]);
-          qa[kk][1] = pack2<T>(sm.q[gq][kk * 16 + 2 * tq + 8], sm.q[gq][kk * 16 + 2 * tq + 9]);
+          qa[kk][0] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq], rot.q[gq][kk * 16 + 2 * tq + 1]);
+          qa[kk][1] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq + 8], rot.q[gq][kk * 16 + 2 * tq + 9]);
         }
+      // the rotation rows live in the K buffer: ordered before the copies
+      // that will overwrite it
+      fence_proxy_async_smem();
+      __syncthreads();
     }
   }
   // the non-empty chunks in ascending order: bit i set for chunk i (every warp
@@ -351,7 +396,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   // rank of chunk `lane` among the non-empty chunks (-1: empty, or not mine)
   const int my_rank = ((nem >> lane) & 1u) ? __popc(nem & ((1u << lane) - 1u)) : -1;
   // allowed-slot words of the chunk in batch position cs of batch bt (0: none);
-  // cs is the same for the whole warp (a warp's rows lie in one chunk slot)
+  // cs is the same for the whole warp
   auto chunk_words = [&](int bt, int cs, int &chunk) -> uint2 {
     const uint32_t m = __ballot_sync(0xffffffffu, my_rank == bt * CPB + cs);
     if (!m) {
@@ -364,26 +409,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
   // running state: mma path -- every lane holds the shared maximum of heads
   // 2 tq and 2 tq + 1, its rows' part of their l and its fragment of O^T
-  // (rows: features, columns: heads); fp32 path -- as in the batch softmax
+  // (rows: features, columns: heads); fp32 path -- per head in shared memory
   float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
   float ot[use_mma<T>() ? D / 16 : 1][4];
   if constexpr (use_mma<T>()) {
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
   }
-  constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, dim pair) per thread
+  constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, feature pair) per thread
   float o[ITEMS][2];
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) o[u][0] = o[u][1] = 0.f;
-  float m_h = -INFINITY, l_h = 0.f;  // fp32 path: head `warp`'s running (m, l)
   bool ok = true;
   int failed_bt = -1;
 
   for (int bt = 0; bt < nbatch; ++bt) {
-    // ---- 2. gather: thread 0 fetches the batch's chunks as TMA boxes
+    // ---- 2. gather: lane i of warp 0 holds chunk i; the chunk of rank
+    // bt * CPB + cs goes to chunk slot cs, after lane 0 armed the batch's bytes
     const int nbc = min(CPB, n_ne - bt * CPB);  // chunks in this batch
-    // (lane i of warp 0 holds chunk i: the chunks of rank bt * CPB + cs go to
-    // chunk slot cs, one lane each, after lane 0 armed the batch's bytes)
     if (warp == 0) {
       if (lane == 0) mbar_arrive_expect_tx(&sm.bar, (uint32_t)(nbc * 2 * Sm::CHB));
       if (bt == 0) dec_stamp(12);
@@ -409,108 +452,116 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       break;
     }
     // masked rows: a zero V row (exact zeros through the product); the row a
-    // fused append adds: the step's input (thread r owns positional row r)
-    // (the mma path reads only the rows of fetched chunk slots)
-    if (warp * 32 < (use_mma<T>() ? nbc * C : CAPR)) {  // warp-uniform: whole warps own rows
-      const int r = tid;
-      int chunk = -1;
-      const uint2 w2 = chunk_words(bt, r / C, chunk);
-      const bool allowed = ((((r % C) < 32) ? w2.x : w2.y) >> (r % 32)) & 1u;
-      const bool is_new = allowed && pos >= 0 && (x + S * chunk) * C + (r % C) == pos;
-      if (!allowed || is_new) {
+    // fused append adds: the step's input. The mma path reads only the rows
+    // of fetched chunk slots, so a batch of whole chunks without the new row
+    // needs no pass (the same decision in every warp: one ballot over the
+    // chunk lanes).
+    const uint32_t fixm = __ballot_sync(
+        0xffffffffu, my_rank >= bt * CPB && my_rank < bt * CPB + nbc &&
+                         ((sm.words[lane][0] & sm.words[lane][1]) != 0xffffffffu ||
+                          (pos >= 0 && (pos / C) % S == x && (pos / C) / S == lane)));
+    if (fixm != 0u || (!use_mma<T>() && nbc < CPB)) {
+      const int lim = use_mma<T>() ? nbc * C : CAPR;
+      for (int r0 = warp * 32; r0 < lim; r0 += kThreads) {  // warp-uniform: 32 rows of one chunk slot
+        const int r = r0 + lane;
+        int chunk = -1;
+        const uint2 w2 = chunk_words(bt, r / C, chunk);
+        const bool allowed = ((((r % C) < 32) ? w2.x : w2.y) >> (r % 32)) & 1u;
+        const bool is_new = allowed && pos >= 0 && (x + S * chunk) * C + (r % C) == pos;
+        if (!allowed || is_new) {
 #pragma unroll
-        for (int sg = 0; sg < SEGS; ++sg) {
-          const uint4 kz = is_new ? reinterpret_cast<const uint4 *>(sm.newk)[sg] : make_uint4(0u, 0u, 0u, 0u);
-          const uint4 vz = is_new ? reinterpret_cast<const uint4 *>(sm.newv)[sg] : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t off = use_mma<T>() ? Sm::seg_off(r, sg) : Sm::row_off(r) + sg * 16;
-          if (is_new) *reinterpret_cast<uint4 *>(kbuf + off) = kz;
-          *reinterpret_cast<uint4 *>(vbuf + off) = vz;
+          for (int sg = 0; sg < SEGS; ++sg) {
+            const uint4 kz = is_new ? reinterpret_cast<const uint4 *>(sm.newk)[sg] : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 vz = is_new ? reinterpret_cast<const uint4 *>(sm.newv)[sg] : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t off = use_mma<T>() ? Sm::seg_off(r, sg) : Sm::row_off(r) + sg * 16;
+            if (is_new) *reinterpret_cast<uint4 *>(kbuf + off) = kz;
+            *reinterpret_cast<uint4 *>(vbuf + off) = vz;
+          }
+          fence_proxy_async_smem();  // ordered before a later batch's TMA into this row
         }
-        fence_proxy_async_smem();  // ordered before a later batch's TMA into this row
       }
+      __syncthreads();
     }
-    __syncthreads();
     if (bt == 0) dec_stamp(9);
 
     // ---- 3. the batch's products
     if constexpr (use_mma<T>()) {
       // S^T = K q^T and O^T += V^T P^T: the cache rows are the M side of the
       // score product (16 per mma, no padding rows) and the heads its N side
-      // (8, padded with zero q rows); P^T becomes the B operand of the second
-      // product by an in-register transpose of its two 8 x 8 halves. Warp w
-      // takes the 16-row groups w, w + 8, ... of the fetched chunk slots.
-      constexpr int GPW = CAPR / 16 / kWarps;  // groups per warp
-      const int ngrp = nbc * (C / 16);         // groups of fetched rows
+      // (8, padded with zero q columns); P^T becomes the B operand of the
+      // second product by an in-register transpose of its two 8 x 8 halves.
+      // Warp w takes the 16-row groups w, w + kWarps, ... of the fetched
+      // slots: nbc groups for every warp, so the loops below are unrolled for
+      // each batch size and their groups overlap.
       const int mi = lane >> 3, rr = lane & 7;  // ldmatrix: tile, row within it
-      float sc[GPW][4];  // (row gq | gq + 8) x (head 2 tq | 2 tq + 1), log2 units
+      auto products = [&](auto njc) {
+        constexpr int NJ = decltype(njc)::value;
+        float sc[NJ][4];  // (row gq | gq + 8) x (head 2 tq | 2 tq + 1), log2 units
 #pragma unroll
-      for (int j = 0; j < GPW; ++j) {
-        const int gi = warp + j * kWarps;
-        sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = -INFINITY;
-        if (gi < ngrp) {  // warp-uniform
+        for (int j = 0; j < NJ; ++j) {
+          const int gi = warp + j * kWarps;
           int chunk;
           const uint2 w2 = chunk_words(bt, gi * 16 / C, chunk);
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          // two accumulators (even / odd k steps) halve the dependent chain
+          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
           const int krow = gi * 16 + (mi & 1) * 8 + rr;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4(a0, a1, a2, a3, kbuf + Sm::seg_off(krow, 2 * kk + (mi >> 1)));
-            mma_16816<T>(acc, a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
+            mma_16816<T>(acc[kk & 1], a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
           }
           const int s0 = (gi * 16) % C + gq, s1 = s0 + 8;  // slots within the chunk
           const bool al0 = ((s0 < 32 ? w2.x : w2.y) >> (s0 % 32)) & 1u;
           const bool al1 = ((s1 < 32 ? w2.x : w2.y) >> (s1 % 32)) & 1u;
-          sc[j][0] = al0 ? acc[0] * p.scale_log2 : -INFINITY;
-          sc[j][1] = al0 ? acc[1] * p.scale_log2 : -INFINITY;
-          sc[j][2] = al1 ? acc[2] * p.scale_log2 : -INFINITY;
-          sc[j][3] = al1 ? acc[3] * p.scale_log2 : -INFINITY;
+          sc[j][0] = al0 ? (acc[0][0] + acc[1][0]) * p.scale_log2 : -INFINITY;
+          sc[j][1] = al0 ? (acc[0][1] + acc[1][1]) * p.scale_log2 : -INFINITY;
+          sc[j][2] = al1 ? (acc[0][2] + acc[1][2]) * p.scale_log2 : -INFINITY;
+          sc[j][3] = al1 ? (acc[0][3] + acc[1][3]) * p.scale_log2 : -INFINITY;
         }
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < GPW; ++j) {
-        mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][2]));
-        mx1 = fmaxf(mx1, fmaxf(sc[j][1], sc[j][3]));
-      }
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      if (bt == 0) dec_stamp(11);
-      if (gq == 0) {
-        if (2 * tq < NREP) sm.wmax[warp][2 * tq] = mx0;
-        if (2 * tq + 1 < NREP) sm.wmax[warp][2 * tq + 1] = mx1;
-      }
-      __syncthreads();
-      if (bt == 0) dec_stamp(10);
-      // finite: the batch holds an allowed row (padding heads use 0)
-      float m_new[2], f[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int h = 2 * tq + e;
-        float mb = -INFINITY;
-        if (h < NREP) {
-#pragma unroll
-          for (int w = 0; w < kWarps; ++w) mb = fmaxf(mb, sm.wmax[w][h]);
+        for (int j = 0; j < NJ; ++j) {
+          mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][2]));
+          mx1 = fmaxf(mx1, fmaxf(sc[j][1], sc[j][3]));
         }
-        m_new[e] = h < NREP ? fmaxf(m_run[e], mb) : 0.f;
-        f[e] = (m_run[e] == -INFINITY) ? 0.f : fast_exp2(m_run[e] - m_new[e]);
-        m_run[e] = m_new[e];
-        l_part[e] *= f[e];
-      }
 #pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        ot[mt][0] *= f[0];
-        ot[mt][1] *= f[1];
-        ot[mt][2] *= f[0];
-        ot[mt][3] *= f[1];
-      }
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        if (bt == 0) dec_stamp(11);
+        if (gq == 0) {
+          if (2 * tq < NREP) sm.wmax[warp][2 * tq] = mx0;
+          if (2 * tq + 1 < NREP) sm.wmax[warp][2 * tq + 1] = mx1;
+        }
+        __syncthreads();
+        if (bt == 0) dec_stamp(10);
+        // finite: the batch holds an allowed row (padding heads use 0)
+        float m_new[2], f[2];
 #pragma unroll
-      for (int j = 0; j < GPW; ++j) {
-        const int gi = warp + j * kWarps;
-        if (gi < ngrp) {  // warp-uniform
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * tq + e;
+          float mb = -INFINITY;
+          if (h < NREP) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) mb = fmaxf(mb, sm.wmax[w][h]);
+          }
+          m_new[e] = h < NREP ? fmaxf(m_run[e], mb) : 0.f;
+          f[e] = (m_run[e] == -INFINITY) ? 0.f : fast_exp2(m_run[e] - m_new[e]);
+          m_run[e] = m_new[e];
+          l_part[e] *= f[e];
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+          ot[mt][0] *= f[0];
+          ot[mt][1] *= f[1];
+          ot[mt][2] *= f[0];
+          ot[mt][3] *= f[1];
+        }
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+          const int gi = warp + j * kWarps;
           const float p0 = fast_exp2(sc[j][0] - m_new[0]), p1 = fast_exp2(sc[j][1] - m_new[1]);
           const float p2 = fast_exp2(sc[j][2] - m_new[0]), p3 = fast_exp2(sc[j][3] - m_new[1]);
           l_part[0] += p0 + p2;
@@ -526,6 +577,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             mma_16816<T>(ot[mt], a0, a1, a2, a3, b0, b1);
           }
         }
+      };
+      // groups per warp: nbc (warp w's groups w + j kWarps lie in chunk slot j)
+      static_assert(C / 16 == kWarps && CPB <= 4, "one group per warp per chunk slot");
+      switch (nbc) {
+        case 1: products(std::integral_constant<int, 1>()); break;
+        case 2: if constexpr (CPB >= 2) products(std::integral_constant<int, 2>()); break;
+        case 3: if constexpr (CPB >= 3) products(std::integral_constant<int, 3>()); break;
+        default: if constexpr (CPB >= 4) products(std::integral_constant<int, 4>()); break;
       }
     } else {
       int chunk_w = -1;
@@ -542,7 +601,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
         for (int r = 0; r < NREP; ++r)
 #pragma unroll
-          for (int i = 0; i < EPL; ++i) qr[r][i] = sm.q[r][e * EPL + i];
+          for (int i = 0; i < EPL; ++i) qr[r][i] = rot.q[r][e * EPL + i];
         for (int it = 0; it < RPW / SPW; ++it) {
           const int row = warp * RPW + it * SPW + sub;
           float acc[NREP];
@@ -568,8 +627,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
       __syncthreads();
       // per-head batch softmax, folded into the running (m, l)
-      if (warp < NREP) {
-        const int r = warp;
+      for (int r = warp; r < NREP; r += kWarps) {  // warp-uniform
+        const float m_h = sm.mrun[r], l_h = sm.lrun[r];
         float mb = -INFINITY;
         for (int i = lane; i < CAPR; i += 32) mb = fmaxf(mb, sm.s[r][i]);
 #pragma unroll
@@ -585,11 +644,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         const float m_new = fmaxf(m_h, mb);
         const float f_old = (m_h == -INFINITY) ? 0.f : exp2f(m_h - m_new);
         const float f_b = exp2f(mb - m_new);
-        l_h = l_h * f_old + lb * f_b;
-        m_h = m_new;
+        __syncwarp();
         if (lane == 0) {
           sm.fo[r] = f_old;
           sm.fb[r] = f_b;
+          sm.mrun[r] = m_new;
+          sm.lrun[r] = l_h * f_old + lb * f_b;
         }
       }
       __syncthreads();
@@ -622,11 +682,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   }
   dec_stamp(5);
 
-  // in-CTA merge: every warp used the same maximum, so O and l are sums
-  float M = -INFINITY;
+  // in-CTA merge: every warp used the same maximum, so O and l are sums;
+  // warps past the first batch's groups never held a row
+  const int nact = use_mma<T>() ? min(kWarps, min(CPB, n_ne) * (C / 16)) : 0;
   if constexpr (use_mma<T>()) {
-    // warps past the first batch's groups never held a row: nothing to add
-    const int nact = min(kWarps, min(CPB, n_ne) * (C / 16));
     float l0 = l_part[0], l1 = l_part[1];
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -671,14 +730,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         o[u][1] = a1;
       }
     }
-    if (warp < NREP) {
-      float L = 0.f;
-      for (int w = 0; w < nact; ++w) L += sm.wsum[w][warp];
-      l_h = L;
-      m_h = sm.mrun[warp];
-    }
   }
-  M = m_h;  // meaningful in warp r < NREP (head r)
   dec_stamp(6);
 
   // append: the CTA owning slot pos stores the new row into the cache (once
@@ -697,70 +749,64 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
   }
 
-  // ---- 4. partial of this CTA; the last of the S CTAs merges all of them
-  const int64_t hrow0 = ((int64_t)b * p.Hq + h0) * S;  // ws row of (head h0, split 0)
+  // ---- 4. every split delivers each owner its slice: output pair e (head
+  // e / D, feature e % D) belongs to CTA e / E
+  cluster_wait();  // every CTA of the cluster armed its receive barrier
 #pragma unroll
   for (int u = 0; u < ITEMS; ++u) {
     const int idx = tid + u * kThreads;
     if (idx < NREP * D / 2) {
-      const int r = idx / (D / 2), dp = idx % (D / 2);
-      reinterpret_cast<float2 *>(p.ws_o + (hrow0 + (int64_t)r * S + x) * D)[dp] =
-          make_float2(o[u][0], o[u][1]);
+      const int e = 2 * idx, y = e / E;
+      st_async_f32x2(cluster_map(&sm.rx_o[x][e % E], y), o[u][0], o[u][1], cluster_map(&sm.rx_bar, y));
     }
   }
-  if (warp < NREP && lane == 0)
-    p.ws_ml[hrow0 + (int64_t)warp * S + x] =
-        (ok && M != -INFINITY) ? make_float2(M, l_h) : make_float2(-INFINITY, 0.f);
-  // the barrier orders every thread's partial before thread 0's release
-  // (the acq_rel ticket, at GPU scope); the last CTA acquires through it
-  __syncthreads();
-  unsigned *tick = p.ws_tick + (int64_t)b * (p.Hq / NREP) + hg;
-  if (tid == 0) {
-    unsigned t;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(t) : "l"(tick) : "memory");
-    sm.is_last = (t == (unsigned)(S - 1));
+  for (int t = tid; t < S * NREP; t += kThreads) {
+    const int r = t / S, y = t % S;
+    // this CTA's partial (m, l) of head r; m = -inf: nothing allowed (or a
+    // batch that never arrived), and the owner skips the split
+    const float m = sm.mrun[r];
+    float l = sm.lrun[r];
+    if constexpr (use_mma<T>()) {
+      l = 0.f;
+      for (int w = 0; w < nact; ++w) l += sm.wsum[w][r];
+    }
+    const bool has = ok && m != -INFINITY;
+    st_async_f32x2(cluster_map(&sm.rx_ml[x][r], y), has ? m : -INFINITY, has ? l : 0.f,
+                   cluster_map(&sm.rx_bar, y));
   }
-  __syncthreads();
   dec_stamp(7);
-  if (!sm.is_last) return;
 
-#pragma unroll
-  for (int u = 0; u < ITEMS; ++u) {
-    const int idx = tid + u * kThreads;
-    if (idx < NREP * D / 2) {
-      const int r = idx / (D / 2), dp = idx % (D / 2);
-      const int64_t hr = hrow0 + (int64_t)r * S;
-      // every split wrote its partial this call (empty ones: m = -inf, zeros),
-      // so all loads go out in one round
-      float2 ml[S], ov[S];
-#pragma unroll
-      for (int xx = 0; xx < S; ++xx) {
-        ml[xx] = __ldcg(&p.ws_ml[hr + xx]);
-        ov[xx] = __ldcg(reinterpret_cast<const float2 *>(p.ws_o + (hr + xx) * D) + dp);
-      }
+  // the owner's merge, in ascending split order. Its wait outlasts every
+  // split's own copy waits (each batch, then the drain of a failed one), so a
+  // split that gave up still delivers before the owner does.
+  constexpr uint64_t kRxLimitNs = (uint64_t)(kMaxCI / CPB + 2) * kWaitLimitNs;
+  if (tid < E / 2) {
+    if (mbar_wait_cluster(&sm.rx_bar, 0, p.err, kRxLimitNs)) {
+      const int e0 = x * E + 2 * tid;
+      const int r = e0 / D, d = e0 % D;
       float Mx = -INFINITY;
 #pragma unroll
-      for (int xx = 0; xx < S; ++xx) Mx = fmaxf(Mx, ml[xx].x);
+      for (int xx = 0; xx < S; ++xx) Mx = fmaxf(Mx, sm.rx_ml[xx][r].x);
       float L = 0.f, o0 = 0.f, o1 = 0.f;
       if (Mx != -INFINITY) {
 #pragma unroll
         for (int xx = 0; xx < S; ++xx) {
-          if (ml[xx].x == -INFINITY) continue;
-          const float w = exp2f(ml[xx].x - Mx);
-          L = fmaf(ml[xx].y, w, L);
-          o0 = fmaf(ov[xx].x, w, o0);
-          o1 = fmaf(ov[xx].y, w, o1);
+          const float2 ml = sm.rx_ml[xx][r];
+          if (ml.x == -INFINITY) continue;
+          const float w = exp2f(ml.x - Mx);
+          L = fmaf(ml.y, w, L);
+          o0 = fmaf(sm.rx_o[xx][2 * tid], w, o0);
+          o1 = fmaf(sm.rx_o[xx][2 * tid + 1], w, o1);
         }
       }
       const float inv = (L > 0.f) ? 1.f / L : 0.f;
       T *orow = static_cast<T *>(p.out) + (int64_t)b * p.os_b + (int64_t)(h0 + r) * p.os_h;
-      orow[2 * dp] = from_float<T>(o0 * inv);
-      orow[2 * dp + 1] = from_float<T>(o1 * inv);
-      if (dp == 0 && p.lse)
+      orow[d] = from_float<T>(o0 * inv);
+      orow[d + 1] = from_float<T>(o1 * inv);
+      if (d == 0 && p.lse)
         p.lse[(int64_t)b * p.Hq + h0 + r] = (L > 0.f) ? (Mx + log2f(L)) * kLn2 : -INFINITY;
     }
   }
-  if (tid == 0) *tick = 0u;
   dec_stamp(8);
 }
 
@@ -770,10 +816,10 @@ mgqa_status launch_t(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeP
   auto kern = decode_kernel<T, D, NREP>;
   constexpr int smem = DecodeSmem<T, D, NREP>::total;
   static std::atomic<uint64_t> attr_done{0};
-  const mgqa_status st = ensure_smem_attr(kern, smem, attr_done, "decode kernel");
+  const mgqa_status st = ensure_cluster_attr(kern, smem, attr_done, "decode kernel");
   if (st != MGQA_OK) return st;
   dim3 grid(S, p.Hq / NREP, p.B);
-  const cudaError_t e = launch_pdl(kern, grid, dim3(kThreads), smem, s, mk, mv, p);
+  const cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kThreads), smem, s, S, mk, mv, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
@@ -798,35 +844,13 @@ int decode_heads_per_cta(int n_rep) {
   return 1;
 }
 
-// Tickets first, in a region of at least kDecodeTicketSlots entries that
-// nothing else ever writes and every call returns to zero: a workspace zeroed
-// once serves later calls of any shape with at most that many (request, head
-// group) pairs. Then the partial (m, l) and O of every (request, head, split).
-DecodeWsLayout decode_ws_layout(const mgqa_args &a) {
-  const int hpc = decode_heads_per_cta(a.Hq / a.Hkv);
-  const size_t pairs = (size_t)a.B * (a.Hq / hpc);
-  const size_t rows = (size_t)a.B * a.Hq * S;
-  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  DecodeWsLayout w;
-  w.tick = 0;
-  w.ml = up((pairs > kDecodeTicketSlots ? pairs : kDecodeTicketSlots) * sizeof(unsigned));
-  w.o = w.ml + up(rows * sizeof(float2));
-  w.total = w.o + up(rows * a.D * sizeof(float));
-  return w;
-}
-
-size_t decode_workspace_bytes(const mgqa_args &a) { return decode_ws_layout(a).total; }
-
-mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s) {
-  return launch_decode_append(a, nullptr, nullptr, nullptr, nullptr, nullptr, ws, ws_bytes, s);
+mgqa_status launch_decode(const mgqa_args &a, cudaStream_t s) {
+  return launch_decode_append(a, nullptr, nullptr, nullptr, nullptr, nullptr, s);
 }
 
 mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
                                  const int64_t *k_new_stride, const int64_t *v_new_stride,
-                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s,
-                                 const FusedRope &rope) {
-  const DecodeWsLayout L = decode_ws_layout(a);
-  if (ws_bytes < L.total) return fail(MGQA_ERR_INVALID_ARG, "decode workspace too small");
+                                 int32_t *kv_len_out, cudaStream_t s, const FusedRope &rope) {
   DecodeParams p{};
   p.q = a.q; p.k = a.k; p.v = a.v; p.out = a.out;
   p.qs_b = a.q_stride[0]; p.qs_h = a.q_stride[1];
@@ -839,10 +863,6 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
   p.lse = a.lse; p.err = a.dev_error;
   p.B = a.B; p.Hq = a.Hq; p.Hkv = a.Hkv; p.Lk = a.Lk; p.n_rep = a.Hq / a.Hkv;
   p.nch = (a.Lk + kDecodeChunk - 1) / kDecodeChunk;
-  char *base = static_cast<char *>(ws);
-  p.ws_tick = reinterpret_cast<unsigned *>(base + L.tick);
-  p.ws_ml = reinterpret_cast<float2 *>(base + L.ml);
-  p.ws_o = reinterpret_cast<float *>(base + L.o);
   p.rope = rope;
   p.append = k_new != nullptr;
   if (p.append) {
@@ -877,64 +897,12 @@ mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const vo
 
 }  // namespace mgqa
 
-// ---- decode with library-owned scratch -------------------------------------
-// For callers that cannot hand the library any device memory of its own: the
-// partial results and merge tickets of a call live in one fixed array that
-// every GPU loading this library keeps until the process exits.
-
-namespace mgqa {
-namespace {
-
-constexpr size_t kStaticScratchBytes = (size_t)MGQA_DECODE_STATIC_SCRATCH_BYTES;
-static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];  // device address of g_static_scratch, per device
-
-// Device address of the scratch array on the current device. The first call
-// on a device looks it up (with that device current) and caches it.
-mgqa_status static_scratch(void **out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return fail(MGQA_ERR_CUDA, "no usable current CUDA device");
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void *addr = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&addr, g_static_scratch);
-    if (e != cudaSuccess || addr == nullptr)
-      return fail(MGQA_ERR_CUDA, "cudaGetSymbolAddress of the decode scratch failed: %s",
-                  cudaGetErrorString(e));
-    g_scratch_addr[dev] = addr;
-  }
-  *out = g_scratch_addr[dev];
-  return MGQA_OK;
-}
-
-}  // namespace
-}  // namespace mgqa
+// ---- decode for callers that hand the library no device memory ------------
+// The kernel merges its splits on chip, so this needs no scratch of any kind:
+// it is the workspace-free form of masked_gqa_attn_decode.
 
 extern "C" mgqa_status masked_gqa_attn_decode_static(const mgqa_args *args, cudaStream_t stream) {
-  const size_t need = masked_gqa_attn_decode_workspace_size(args);
-  if (need == 0) return masked_gqa_attn_decode(args, nullptr, 0, stream);  // reports the bad argument
-  if (need > mgqa::kStaticScratchBytes)
-    return mgqa::fail(MGQA_ERR_UNSUPPORTED,
-                      "this decode needs %zu bytes of scratch; the library's fixed scratch holds %zu "
-                      "(pass a workspace to masked_gqa_attn_decode instead)",
-                      need, mgqa::kStaticScratchBytes);
-  void *ws = nullptr;
-  const mgqa::DecodeWsLayout lay = mgqa::decode_ws_layout(*args);
-  mgqa_status st = mgqa::static_scratch(&ws);
-  if (st != MGQA_OK) return st;
-  // The merge tickets must start at zero. The array is zero when the library
-  // loads and every call returns its tickets to zero, but a call cut short
-  // (its context lost mid-kernel) would not: clear this call's tickets on the
-  // caller's stream first.
-  const size_t pairs = (size_t)args->B * (args->Hq / mgqa::decode_heads_per_cta(args->Hq / args->Hkv));
-  if (cudaMemsetAsync(static_cast<char *>(ws) + lay.tick, 0, pairs * sizeof(unsigned), stream) !=
-      cudaSuccess)
-    return mgqa::fail(MGQA_ERR_CUDA, "clearing the decode scratch tickets failed");
-  return masked_gqa_attn_decode(args, ws, mgqa::kStaticScratchBytes, stream);
+  return masked_gqa_attn_decode(args, nullptr, 0, stream);
 }
 
 // ---- debug library entry point (include/masked_gqa_attn_debug.h) ------------

@@ -33,6 +33,44 @@ mgqa_status ensure_smem_attr(Kern kern, int bytes, std::atomic<uint64_t> &done, 
   return MGQA_OK;
 }
 
+// ensure_smem_attr for a kernel launched in clusters of up to 16 CTAs (past
+// the portable 8), spread over as many SMs as the GPU allows.
+template <typename Kern>
+mgqa_status ensure_cluster_attr(Kern kern, int bytes, std::atomic<uint64_t> &done, const char *what) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MGQA_ERR_CUDA, "no current CUDA device");
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return MGQA_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeClusterSchedulingPolicyPreference,
+                           cudaClusterSchedulingPolicySpread) != cudaSuccess)
+    return fail(MGQA_ERR_CUDA, "cudaFuncSetAttribute failed for the %s", what);
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return MGQA_OK;
+}
+
+// launch_pdl in thread-block clusters of cluster_x CTAs along x.
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl_cluster(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                               int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch with programmatic stream serialisation (the kernel itself calls
 // grid_dependency_wait() before touching global memory).
 template <typename Kern, typename... Args>
@@ -64,25 +102,21 @@ struct FusedRope {
 };
 
 // Decode: the cache is cut into chunks of kDecodeChunk absolute slots; the
-// kDecodeSplits CTAs of a (request, head group) own every kDecodeSplits-th chunk.
+// kDecodeSplits CTAs (one cluster) of a (request, head group) own every
+// kDecodeSplits-th chunk.
 constexpr int kDecodeChunk = 64;
 constexpr int kDecodeSplits = 16;
-// Ticket region at the start of a decode workspace: room for this many
-// (request, head group) pairs before the region grows with the shape.
-constexpr size_t kDecodeTicketSlots = 4096;
-// Longest static cache the decode kernel accepts (bounds its merge tables).
+// Longest static cache the decode kernel accepts (bounds its chunk masks).
 constexpr int kDecodeMaxLk = 32768;
+// Nominal workspace size reported for valid decode arguments: the kernel
+// merges on chip and never touches a workspace.
+constexpr size_t kDecodeWorkspaceBytes = 16;
 // Heads handled by one decode CTA (a divisor of Hq/Hkv, at most 8).
 int decode_heads_per_cta(int n_rep);
-struct DecodeWsLayout {
-  size_t tick, ml, o, total;  // byte offsets of the workspace regions; total size
-};
-DecodeWsLayout decode_ws_layout(const mgqa_args &a);
-size_t decode_workspace_bytes(const mgqa_args &a);
-mgqa_status launch_decode(const mgqa_args &a, void *ws, size_t ws_bytes, cudaStream_t s);
+mgqa_status launch_decode(const mgqa_args &a, cudaStream_t s);
 mgqa_status launch_decode_append(const mgqa_args &a, const void *k_new, const void *v_new,
                                  const int64_t *k_new_stride, const int64_t *v_new_stride,
-                                 int32_t *kv_len_out, void *ws, size_t ws_bytes, cudaStream_t s,
+                                 int32_t *kv_len_out, cudaStream_t s,
                                  const FusedRope &rope = FusedRope());
 
 // Packed-guidance row copies (pack or unpack one pair of sequences).

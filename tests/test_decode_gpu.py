@@ -25,8 +25,6 @@ def run_decode(M, wl, ws=None, lse=True, err=None):
     out = torch.empty_like(d["q"])
     lse_t = torch.empty(d["q"].shape[:3], dtype=torch.float32, device="cuda") if lse else None
     masks = {k: d[k] for k in ("mask_bits", "kv_len", "seg_q", "seg_k")}
-    if ws is None:
-        ws = M.new_decode_workspace(d["q"], d["k"], d["v"], **masks)
     M.masked_gqa_attn_decode(d["q"], d["k"], d["v"], out, workspace=ws, scale=wl.scale,
                              lse=lse_t, dev_error=err, **masks)
     torch.cuda.synchronize()
@@ -62,15 +60,16 @@ def test_masked_slots_refill_leaves_bits(M):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_repeated_calls_reuse_workspace(M):
+def test_repeated_calls_same_bits_workspace_untouched(M):
+    # the splits merge on chip: a workspace passed in is never read or
+    # written, and repeated calls give the same bits with or without one
     wl = W.static_cache_decode(variant="full", seed=4242)
-    o1, l1, ws = run_decode(M, wl)
+    o1, l1, _ = run_decode(M, wl)
+    ws = torch.full((1 << 16,), 0xAB, dtype=torch.uint8, device="cuda")
     for _ in range(3):
         o2, l2, _ = run_decode(M, wl, ws=ws)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    # the tickets (the workspace's first 4 bytes per (request, head group))
-    # are back at zero after every call
-    assert int(ws[:4 * 8 * 2].view(torch.int32).abs().sum()) == 0
+    assert bool(torch.all(ws == 0xAB))
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
@@ -132,28 +131,26 @@ def test_long_cache_many_batches(M, oracle_mod, dtype, B, Hq, Hkv, D):
     bitmask and filled-length forms stay bit-identical."""
     wl = W.static_cache_decode(seed=B + Hq + D, variant="span", B=B, Hq=Hq, Hkv=Hkv, D=D,
                                capacity=32768, lo=17000, hi=32768, dtype=dtype)
-    out, lse, ws = run_decode(M, wl)
+    out, lse, _ = run_decode(M, wl)
     ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
     assert_close_to_oracle(out, ref, dtype, f"long cache {B}/{Hq}/{Hkv}/{D}")
     assert_lse_close(lse, ref_lse, 1e-5 if dtype == torch.float32 else 1e-3)
-    assert int(ws[:256].abs().sum()) == 0  # the tickets are back at zero
     full = W.static_cache_decode(seed=B + Hq + D, variant="full", B=B, Hq=Hq, Hkv=Hkv, D=D,
                                  capacity=32768, lo=17000, hi=32768, dtype=dtype)
-    o2, l2, _ = run_decode(M, full, ws=ws)
+    o2, l2, _ = run_decode(M, full)
     assert torch.equal(out, o2) and torch.equal(lse, l2)
 
 
-def test_one_workspace_serves_shapes_back_to_back(M, oracle_mod):
-    """A workspace zeroed once serves later calls of other shapes (the merge
-    tickets live in a fixed region that every call returns to zero)."""
+def test_shapes_back_to_back(M, oracle_mod):
+    """Calls of different shapes (cluster grids of different sizes) in a row:
+    no state carries from one call to the next."""
     shapes = [dict(B=1, Hq=16, Hkv=2, D=64, capacity=32768, lo=20000, hi=32768),
               dict(B=2, Hq=8, Hkv=1, D=128, capacity=32768, lo=17000, hi=30000),
               dict(B=8, Hq=16, Hkv=2, D=64, capacity=8192, lo=256, hi=3100),
               dict(B=3, Hq=4, Hkv=4, D=128, capacity=5000, lo=1, hi=5000)]
-    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
     for i, kw in enumerate(shapes * 2):
         wl = W.static_cache_decode(seed=300 + i, variant="span", **kw)
-        out, lse, _ = run_decode(M, wl, ws=ws)
+        out, lse, _ = run_decode(M, wl)
         ref, ref_lse, _ = oracle_mod.attention(wl.q, wl.k, wl.v, scale=wl.scale, **wl.masks())
         assert_close_to_oracle(out, ref, torch.bfloat16, f"shape {i}")
         assert_lse_close(lse, ref_lse, 1e-3)
