@@ -314,22 +314,21 @@ def bench_fused_rope(M, dev, nsets=8):
         d = device_inputs(wd, dev)
         kn = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).to(dev)
         vn = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).to(dev)
-        ws = M.new_decode_workspace(d["q"], d["k"], d["v"], kv_len=d["kv_len"])
-        dsets.append((d, kn, vn, ws, torch.empty_like(d["kv_len"]), torch.empty_like(d["q"])))
+        dsets.append((d, kn, vn, torch.empty_like(d["kv_len"]), torch.empty_like(d["q"])))
     pos = [ds[0]["kv_len"][:, None].contiguous() for ds in dsets]
 
     def step_fused():
-        for d, kn, vn, ws, lo, out in dsets:
+        for d, kn, vn, lo, out in dsets:
             M.masked_gqa_attn_decode_append_rope(d["q"], d["k"], d["v"], kn, vn, d["kv_len"], out,
-                                                 workspace=ws, inv_freq=f64, q_norm_weight=w64,
+                                                 inv_freq=f64, q_norm_weight=w64,
                                                  k_norm_weight=w64, kv_len_out=lo, scale=wd.scale)
 
     def step_unfused():
-        for (d, kn, vn, ws, lo, out), p in zip(dsets, pos):
+        for (d, kn, vn, lo, out), p in zip(dsets, pos):
             M.masked_gqa_rope(d["q"], f64, positions=p, norm_weight=w64)
             M.masked_gqa_rope(kn, f64, positions=p, norm_weight=w64)
             M.masked_gqa_attn_decode_append(d["q"], d["k"], d["v"], kn, vn, d["kv_len"], out,
-                                            workspace=ws, kv_len_out=lo, scale=wd.scale)
+                                            kv_len_out=lo, scale=wd.scale)
 
     td_f = time_calls(step_fused) / DECODE_SETS
     td_u = time_calls(step_unfused) / DECODE_SETS
@@ -355,16 +354,14 @@ def bench_decode(M, wl, dev, steps, warmup, world, nsets=DECODE_SETS, calls=16):
         out = torch.empty_like(d["q"])
         a = make_args(M, d, out, wl)
         masks = {n: d[n] for n in ("mask_bits", "kv_len", "seg_q", "seg_k")}
-        ws = M.new_decode_workspace(d["q"], d["k"], d["v"], **masks)
-        sets.append((d, out, a, ws))
+        sets.append((d, out, a))
     L = M.lib()
     stream = torch.cuda.Stream(device=dev)
 
     def step():
         for c in range(calls):
-            d, out, a, ws = sets[c % nsets]
-            st = L.masked_gqa_attn_decode(ctypes.byref(a), ws.data_ptr(), ws.numel(),
-                                          stream.cuda_stream)
+            d, out, a = sets[c % nsets]
+            st = L.masked_gqa_attn_decode(ctypes.byref(a), None, 0, stream.cuda_stream)
             if st != 0:
                 raise RuntimeError(L.mgqa_last_error_detail())
 
@@ -383,7 +380,6 @@ def bench_decode_e2e(M, wl, dev, steps, warmup, world):
     oh = torch.empty_like(hq).pin_memory()
     a = make_args(M, d, out, wl)
     masks = {n: d[n] for n in ("mask_bits", "kv_len", "seg_q", "seg_k")}
-    ws = M.new_decode_workspace(d["q"], d["k"], d["v"], **masks)
     L = M.lib()
     stream = torch.cuda.Stream(device=dev)
 
@@ -392,8 +388,7 @@ def bench_decode_e2e(M, wl, dev, steps, warmup, world):
             d["q"].copy_(hq, non_blocking=True)
             if hl is not None:
                 d["kv_len"].copy_(hl, non_blocking=True)
-            st = L.masked_gqa_attn_decode(ctypes.byref(a), ws.data_ptr(), ws.numel(),
-                                          stream.cuda_stream)
+            st = L.masked_gqa_attn_decode(ctypes.byref(a), None, 0, stream.cuda_stream)
             if st != 0:
                 raise RuntimeError(L.mgqa_last_error_detail())
             oh.copy_(out, non_blocking=True)

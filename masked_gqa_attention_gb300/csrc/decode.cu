@@ -133,14 +133,17 @@ struct DecodeSmem {
     float q[NREP][D];
     float knew[D];
     float2 cs[D / 2];
+    float invf[D / 2];   // the rotation's inverse frequencies
+    float qw[D], kw[D];  // the q / k norm weights
   };
   static_assert((int)sizeof(Rot) <= CPB * CHB, "rotation rows fit in the K buffer");
   // byte offsets (the base is 1024-byte aligned)
   static constexpr int k_off = 0;
   static constexpr int v_off = CPB * CHB;
   static constexpr int misc_off = 2 * CPB * CHB;
-  struct Misc {
-    alignas(16) unsigned char rot[kMma ? 16 : sizeof(Rot)];
+  template <int ROTB>
+  struct MiscT {
+    alignas(16) unsigned char rot[ROTB];  // the rotation rows, when they live here
     float s[NREP][kMma ? 1 : CAPR];   // fp32 path: one batch's scores / weights
     float fo[NREP], fb[NREP];         // fp32 path
     float wmax[kWarps][NREP], wsum[kWarps][NREP];
@@ -153,6 +156,13 @@ struct DecodeSmem {
     alignas(8) uint64_t bar;          // one phase per batch
     alignas(8) uint64_t rx_bar;       // the partials of this CTA's outputs
   };
+  // The rotation rows live in this fixed region when the CTA still fits
+  // three to an SM with them there (<= 75 KB); then the first batch's copies
+  // go out before the rotation and land while it runs. Otherwise (the 16-bit
+  // types at D = 128) they use the K buffer, free until those copies.
+  static constexpr bool kRotMisc =
+      !kMma || misc_off + (int)sizeof(MiscT<(int)sizeof(Rot)>) + 1024 <= 75 * 1024;
+  using Misc = MiscT<kRotMisc ? (int)sizeof(Rot) : 16>;
   static constexpr int total = misc_off + (int)sizeof(Misc) + 1024;  // + alignment slack
   // byte address of 16-byte segment `seg` of positional row r (16-bit types)
   static MGQA_DEV uint32_t seg_off(int r, int seg) {
@@ -174,7 +184,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   unsigned char *kbuf = smem + Sm::k_off, *vbuf = smem + Sm::v_off;
   auto &sm = *reinterpret_cast<typename Sm::Misc *>(smem + Sm::misc_off);
-  auto &rot = *reinterpret_cast<typename Sm::Rot *>(Sm::kMma ? kbuf : sm.rot);
+  auto &rot = *reinterpret_cast<typename Sm::Rot *>(Sm::kRotMisc ? sm.rot : kbuf);
   float(*wo)[NREP][Sm::DP] = reinterpret_cast<float(*)[NREP][Sm::DP]>(kbuf);  // K, V: after the last batch
 
   const int x = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;  // x: rank in the cluster
@@ -229,16 +239,34 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
   constexpr int SEGS = D * (int)sizeof(T) / 16;  // 16-byte segments of a row
   static_assert(2 * SEGS <= kThreads && (!use_mma<T>() || NREP * SEGS <= kThreads),
                 "one thread per row segment");
-  // q lands in shared memory within this round trip (a load first used by
-  // the products could otherwise be scheduled next to them)
-  if (use_mma<T>() && !rope && tid < NREP * SEGS) {
-    const int h = tid / SEGS, sg = tid % SEGS;
-    reinterpret_cast<uint4 *>(sm.qh[h])[sg] =
-        reinterpret_cast<const uint4 *>(qb + (int64_t)(h0 + h) * p.qs_h)[sg];
+  // q (and a fused rotation's tables) land in shared memory within this
+  // round trip: every thread issues its few independent loads at once (a
+  // load first used later could otherwise be scheduled next to its use)
+  if constexpr (use_mma<T>()) {
+    if (tid < NREP * SEGS) {
+      const int h = tid / SEGS, sg = tid % SEGS;
+      reinterpret_cast<uint4 *>(sm.qh[h])[sg] =
+          reinterpret_cast<const uint4 *>(qb + (int64_t)(h0 + h) * p.qs_h)[sg];
+    }
+  } else {
+    constexpr int QV = NREP * D / 4;  // float4 pieces of the CTA's q rows
+#pragma unroll
+    for (int u = 0; u < (QV + kThreads - 1) / kThreads; ++u) {
+      const int i = tid + u * kThreads;
+      if (i < QV) {
+        const int h = i / (D / 4), c = i % (D / 4);
+        reinterpret_cast<float4 *>(rot.q[h])[c] =
+            reinterpret_cast<const float4 *>(qb + (int64_t)(h0 + h) * p.qs_h)[c];
+      }
+    }
   }
-  if (!use_mma<T>() || rope) {
-    for (int i = tid; i < NREP * D; i += kThreads)
-      rot.q[i / D][i % D] = to_float(qb[(int64_t)(h0 + i / D) * p.qs_h + i % D]);
+  int rope_pos = -1;  // the step's position when given explicitly
+  if (rope) {
+    static_assert(D <= kThreads, "one thread per feature");
+    if (tid < p.rope.half) rot.invf[tid] = __ldg(p.rope.inv_freq + tid);
+    if (tid < D && p.rope.q_norm) rot.qw[tid] = __ldg(p.rope.q_norm + tid);
+    if (tid < D && p.rope.k_norm) rot.kw[tid] = __ldg(p.rope.k_norm + tid);
+    if (p.rope.positions) rope_pos = __ldg(p.rope.positions + b);
   }
   uint32_t wbits[kCPW][2];
   int segk[kCPW][2];
@@ -322,71 +350,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
     }
   }
-  if (rope) {
-    // the step's query rows and new key row, normalised and rotated at the new
-    // token's position with the arithmetic of the standalone kernel
-    const int npos = p.rope.positions ? __ldg(p.rope.positions + b) : (pos >= 0 ? pos : kvl);
-    const bool krow = p.append && g < p.rope.k_heads;
-    if (krow)
-      for (int d = tid; d < D; d += kThreads) rot.knew[d] = to_float(sm.newk[d]);
-    for (int i = tid; i < p.rope.half; i += kThreads) {
-      float sn, cs;
-      rope_sincos(rope_theta(npos, __ldg(p.rope.inv_freq + i)), sn, cs);
-      rot.cs[i] = make_float2(cs, sn);
-    }
-    __syncthreads();
-    // RMS norm: one warp per row, lane partials over d = lane (mod 32)
-    for (int task = warp; task <= NREP; task += kWarps) {
-      const bool is_k = task == NREP;
-      const float *wn = is_k ? p.rope.k_norm : p.rope.q_norm;
-      if (!wn || (is_k ? !krow : h0 + task >= p.rope.q_heads)) continue;  // warp-uniform
-      float *row = is_k ? rot.knew : rot.q[task];
-      float part = 0.f;
-      for (int d = lane, k = 0; d < D; d += 32, ++k) part = rms_partial_add(part, row[d], k == 0);
-      const float rs = rms_scale(rms_butterfly_warp(part), D, p.rope.eps);
-      for (int d = lane; d < D; d += 32) row[d] = rms_apply(row[d], rs, __ldg(wn + d));
-    }
-    __syncthreads();
-    // rotation, then one rounding to the I/O type (q stays a float holding it)
-    for (int it = tid; it < (NREP + 1) * (D / 2); it += kThreads) {
-      const int task = it / (D / 2), i = it % (D / 2);
-      const bool is_k = task == NREP;
-      if (is_k ? !krow : h0 + task >= p.rope.q_heads) continue;
-      float *row = is_k ? rot.knew : rot.q[task];
-      const bool normed = is_k ? p.rope.k_norm != nullptr : p.rope.q_norm != nullptr;
-      if (i < p.rope.half) {
-        const int e0 = p.rope.interleaved ? 2 * i : i;
-        const int e1 = p.rope.interleaved ? 2 * i + 1 : i + p.rope.half;
-        float y0, y1;
-        rope_rotate(row[e0], row[e1], rot.cs[i].x, rot.cs[i].y, y0, y1);
-        if (is_k) {
-          sm.newk[e0] = from_float<T>(y0);
-          sm.newk[e1] = from_float<T>(y1);
-        } else {
-          row[e0] = to_float(from_float<T>(y0));
-          row[e1] = to_float(from_float<T>(y1));
-        }
-      } else if (normed) {  // features past rot_dim keep their normalised value
-        for (int d = 2 * p.rope.half + (i - p.rope.half); d < D; d += D / 2 - p.rope.half) {
-          if (is_k) sm.newk[d] = from_float<T>(row[d]);
-          else row[d] = to_float(from_float<T>(row[d]));
-        }
-      }
-    }
-    __syncthreads();
-    if constexpr (use_mma<T>()) {
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        if (gq < NREP) {
-          qa[kk][0] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq], rot.q[gq][kk * 16 + 2 * tq + 1]);
-          qa[kk][1] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq + 8], rot.q[gq][kk * 16 + 2 * tq + 9]);
-        }
-      // the rotation rows live in the K buffer: ordered before the copies
-      // that will overwrite it
-      fence_proxy_async_smem();
-      __syncthreads();
-    }
-  }
   // the non-empty chunks in ascending order: bit i set for chunk i (every warp
   // forms the same mask)
   const uint32_t nem = __ballot_sync(0xffffffffu, lane < nci && (sm.words[lane][0] | sm.words[lane][1]));
@@ -407,25 +370,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     return make_uint2(sm.words[chunk][0], sm.words[chunk][1]);
   };
 
-  // running state: mma path -- every lane holds the shared maximum of heads
-  // 2 tq and 2 tq + 1, its rows' part of their l and its fragment of O^T
-  // (rows: features, columns: heads); fp32 path -- per head in shared memory
-  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
-  float ot[use_mma<T>() ? D / 16 : 1][4];
-  if constexpr (use_mma<T>()) {
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
-  }
-  constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, feature pair) per thread
-  float o[ITEMS][2];
-#pragma unroll
-  for (int u = 0; u < ITEMS; ++u) o[u][0] = o[u][1] = 0.f;
-  bool ok = true;
-  int failed_bt = -1;
-
-  for (int bt = 0; bt < nbatch; ++bt) {
-    // ---- 2. gather: lane i of warp 0 holds chunk i; the chunk of rank
-    // bt * CPB + cs goes to chunk slot cs, after lane 0 armed the batch's bytes
+  // ---- 2. gather: lane i of warp 0 holds chunk i; the chunk of rank
+  // bt * CPB + cs goes to chunk slot cs, after lane 0 armed the batch's bytes
+  auto issue_batch = [&](int bt) {
     const int nbc = min(CPB, n_ne - bt * CPB);  // chunks in this batch
     if (warp == 0) {
       if (lane == 0) mbar_arrive_expect_tx(&sm.bar, (uint32_t)(nbc * 2 * Sm::CHB));
@@ -444,6 +391,114 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
       }
     }
     if (bt == 0) dec_stamp(3);
+  };
+  // the first batch goes out now unless the rotation rows still need the K buffer
+  const bool early = !rope || Sm::kRotMisc;
+  if (early && nbatch > 0) issue_batch(0);
+  if (rope) {
+    // the step's query rows and new key row, normalised and rotated at the new
+    // token's position with the arithmetic of the standalone kernel
+    const int npos = p.rope.positions ? rope_pos : (pos >= 0 ? pos : kvl);
+    const bool krow = p.append && g < p.rope.k_heads;
+    if constexpr (use_mma<T>())
+      for (int i = tid; i < NREP * D; i += kThreads) rot.q[i / D][i % D] = to_float(sm.qh[i / D][i % D]);
+    if (krow)
+      for (int d = tid; d < D; d += kThreads) rot.knew[d] = to_float(sm.newk[d]);
+    for (int i = tid; i < p.rope.half; i += kThreads) {
+      float sn, cs;
+      rope_sincos(rope_theta(npos, rot.invf[i]), sn, cs);
+      rot.cs[i] = make_float2(cs, sn);
+    }
+    __syncthreads();
+    // eight lanes per row (all NREP + 1 rows in one round): the RMS norm,
+    // then the rotation and one rounding to the I/O type (q stays a float
+    // holding it). Lane sl of a row forms the canonical lane partials sl,
+    // sl + 8, sl + 16, sl + 24 (x_d^2 over d = l mod 32) and combines them as
+    // the xor butterfly's first two steps (16, then 8) would; the steps 4, 2,
+    // 1 stay inside the eight lanes -- the standalone kernel's sum, bit for bit.
+    static_assert(NREP + 1 <= 4 * kWarps, "one eight-lane group per row");
+    {
+      const int task = warp * 4 + (lane >> 3), sl = lane & 7;
+      const bool is_k = task == NREP;
+      const bool active = task <= NREP && (is_k ? krow : h0 + task < p.rope.q_heads);
+      float *row = is_k ? rot.knew : rot.q[task < NREP ? task : 0];
+      const float *wn = is_k ? (p.rope.k_norm ? rot.kw : nullptr) : (p.rope.q_norm ? rot.qw : nullptr);
+      if (p.rope.q_norm || p.rope.k_norm) {  // uniform: the shuffles run in whole warps
+        const bool normed = active && wn;
+        float pl[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          pl[j] = 0.f;
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k)
+            pl[j] = normed ? rms_partial_add(pl[j], row[sl + 8 * j + 32 * k], k == 0) : 0.f;
+        }
+        float v = __fadd_rn(__fadd_rn(pl[0], pl[2]), __fadd_rn(pl[1], pl[3]));
+#pragma unroll
+        for (int o = 4; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        const float rs = rms_scale(v, D, p.rope.eps);
+        if (normed)
+          for (int d = sl; d < D; d += 8) row[d] = rms_apply(row[d], rs, wn[d]);
+      }
+      __syncwarp();
+      if (active) {
+        for (int i = sl; i < D / 2; i += 8) {
+          if (i < p.rope.half) {
+            const int e0 = p.rope.interleaved ? 2 * i : i;
+            const int e1 = p.rope.interleaved ? 2 * i + 1 : i + p.rope.half;
+            float y0, y1;
+            rope_rotate(row[e0], row[e1], rot.cs[i].x, rot.cs[i].y, y0, y1);
+            if (is_k) {
+              sm.newk[e0] = from_float<T>(y0);
+              sm.newk[e1] = from_float<T>(y1);
+            } else {
+              row[e0] = to_float(from_float<T>(y0));
+              row[e1] = to_float(from_float<T>(y1));
+            }
+          } else if (wn) {  // features past rot_dim keep their normalised value
+            for (int d = 2 * p.rope.half + (i - p.rope.half); d < D; d += D / 2 - p.rope.half) {
+              if (is_k) sm.newk[d] = from_float<T>(row[d]);
+              else row[d] = to_float(from_float<T>(row[d]));
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if constexpr (use_mma<T>()) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        if (gq < NREP) {
+          qa[kk][0] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq], rot.q[gq][kk * 16 + 2 * tq + 1]);
+          qa[kk][1] = pack2<T>(rot.q[gq][kk * 16 + 2 * tq + 8], rot.q[gq][kk * 16 + 2 * tq + 9]);
+        }
+      if constexpr (!Sm::kRotMisc) {
+        // the rotation rows live in the K buffer: ordered before the copies
+        // that will overwrite it
+        fence_proxy_async_smem();
+        __syncthreads();
+      }
+    }
+  }
+  // running state: mma path -- every lane holds the shared maximum of heads
+  // 2 tq and 2 tq + 1, its rows' part of their l and its fragment of O^T
+  // (rows: features, columns: heads); fp32 path -- per head in shared memory
+  float m_run[2] = {-INFINITY, -INFINITY}, l_part[2] = {0.f, 0.f};
+  float ot[use_mma<T>() ? D / 16 : 1][4];
+  if constexpr (use_mma<T>()) {
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) ot[mt][0] = ot[mt][1] = ot[mt][2] = ot[mt][3] = 0.f;
+  }
+  constexpr int ITEMS = (NREP * D / 2 + kThreads - 1) / kThreads;  // (head, feature pair) per thread
+  float o[ITEMS][2];
+#pragma unroll
+  for (int u = 0; u < ITEMS; ++u) o[u][0] = o[u][1] = 0.f;
+  bool ok = true;
+  int failed_bt = -1;
+
+  for (int bt = 0; bt < nbatch; ++bt) {
+    const int nbc = min(CPB, n_ne - bt * CPB);  // chunks in this batch
+    if (bt > 0 || !early) issue_batch(bt);
     ok = ok && mbar_wait(&sm.bar, bt & 1, p.err);
     ok = __syncthreads_and(ok);  // the batch landed, for every thread
     if (bt == 0) dec_stamp(4);

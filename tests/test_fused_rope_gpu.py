@@ -102,39 +102,49 @@ def test_prefill_fused_rope_equals_standalone_then_attention(M, oracle_mod, dtyp
     assert_lse_close(lse2, ref_lse, 2e-2)
 
 
+DECODE_ROPE = [  # Hq, Hkv, D, rot_dim
+    (16, 2, 64, 64),    # the static-cache decode heads: 8 query rows + the key row per CTA
+    (8, 2, 128, 64),    # partial rotary dim, 4 query rows per CTA
+    (4, 4, 128, 128),   # one query row per CTA
+]
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
-@pytest.mark.parametrize("norm", [False, True])
+@pytest.mark.parametrize("norm", ["none", "both", "q", "k"])
 @pytest.mark.parametrize("inter", [False, True])
-def test_decode_step_fused_rope_equals_standalone_then_append(M, oracle_mod, dtype, norm, inter):
-    wl = W.static_cache_decode(seed=71, variant="span", B=4, Hq=16, Hkv=2, D=64, capacity=3000,
-                               lo=100, hi=2900, dtype=dtype)
-    B, Hq, Hkv, _, Lk, D = wl.shape
-    f = inv_freq_table(D)
-    wq = norm_weight(3, D) if norm else None
-    wk = norm_weight(4, D) if norm else None
+@pytest.mark.parametrize("shape", DECODE_ROPE, ids=lambda c: "x".join(map(str, c)))
+def test_decode_step_fused_rope_equals_standalone_then_append(M, oracle_mod, dtype, norm, inter, shape):
+    Hq, Hkv, D, rot = shape
+    wl = W.static_cache_decode(seed=71 + D + Hq, variant="span", B=4, Hq=Hq, Hkv=Hkv, D=D,
+                               capacity=3000, lo=100, hi=2900, dtype=dtype)
+    B = wl.shape[0]
+    f = inv_freq_table(rot)
+    wq = norm_weight(3, D) if norm in ("both", "q") else None
+    wk = norm_weight(4, D) if norm in ("both", "k") else None
     g = torch.Generator().manual_seed(9)
     kn = torch.randn((B, Hkv, 1, D), generator=g).to(dtype)
     vn = torch.randn((B, Hkv, 1, D), generator=g).to(dtype)
     q, k, v, kvl = (t.cuda() for t in (wl.q, wl.k, wl.v, wl.kv_len))
     fd = f.cuda()
-    wqd = wq.cuda() if norm else None
-    wkd = wk.cuda() if norm else None
+    wqd = wq.cuda() if wq is not None else None
+    wkd = wk.cuda() if wk is not None else None
     pos = kvl.clone()  # the new token's position: its cache slot
     # unfused: rotate q and the new key row (positions [B, 1] = the slot), then append
     q_rot, kn_rot = q.clone(), kn.cuda().clone()
-    M.masked_gqa_rope(q_rot, fd, positions=pos[:, None].contiguous(), norm_weight=wqd, interleaved=inter)
-    M.masked_gqa_rope(kn_rot, fd, positions=pos[:, None].contiguous(), norm_weight=wkd, interleaved=inter)
+    M.masked_gqa_rope(q_rot, fd, positions=pos[:, None].contiguous(), rot_dim=rot, norm_weight=wqd,
+                      interleaved=inter)
+    M.masked_gqa_rope(kn_rot, fd, positions=pos[:, None].contiguous(), rot_dim=rot, norm_weight=wkd,
+                      interleaved=inter)
     k1, v1 = k.clone(), v.clone()
     len1 = torch.zeros_like(kvl)
-    ws = M.new_decode_workspace(q, k, v, kv_len=kvl)
-    o1 = M.masked_gqa_attn_decode_append(q_rot, k1, v1, kn_rot, vn.cuda(), kvl, workspace=ws,
-                                         kv_len_out=len1, scale=wl.scale)
+    o1 = M.masked_gqa_attn_decode_append(q_rot, k1, v1, kn_rot, vn.cuda(), kvl, kv_len_out=len1,
+                                         scale=wl.scale)
     # fused
     k2, v2 = k.clone(), v.clone()
     len2 = torch.zeros_like(kvl)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    o2 = M.masked_gqa_attn_decode_append_rope(q, k2, v2, kn.cuda(), vn.cuda(), kvl, workspace=ws,
-                                              inv_freq=fd, interleaved=inter, q_norm_weight=wqd,
+    o2 = M.masked_gqa_attn_decode_append_rope(q, k2, v2, kn.cuda(), vn.cuda(), kvl, inv_freq=fd,
+                                              rot_dim=rot, interleaved=inter, q_norm_weight=wqd,
                                               k_norm_weight=wkd, kv_len_out=len2, scale=wl.scale,
                                               dev_error=err)
     torch.cuda.synchronize()
@@ -143,8 +153,8 @@ def test_decode_step_fused_rope_equals_standalone_then_append(M, oracle_mod, dty
     assert torch.equal(len1, len2)
     # against the oracle: the cache after the append holds the rotated new row
     pos_c = wl.kv_len.clone()
-    q64 = oracle_qk(oracle_mod, wl.q, f, pos_c[:, None], D, Hq, inter, wq, 1e-6)
-    kn64 = oracle_qk(oracle_mod, kn, f, pos_c[:, None], D, Hkv, inter, wk, 1e-6)
+    q64 = oracle_qk(oracle_mod, wl.q, f, pos_c[:, None], rot, Hq, inter, wq, 1e-6)
+    kn64 = oracle_qk(oracle_mod, kn, f, pos_c[:, None], rot, Hkv, inter, wk, 1e-6)
     kc = wl.k.double().numpy().copy()
     vc = wl.v.double().numpy().copy()
     for b in range(B):
