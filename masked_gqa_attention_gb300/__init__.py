@@ -61,6 +61,7 @@ DEBUG_SYMBOLS = (
     "mgqa_debug_reset",
     "mgqa_debug_inject_prefill_stall",
     "mgqa_debug_decode_timeline",
+    "mgqa_debug_prefill_timeline",
 )
 DEBUG_NUM_COUNTERS = 4
 
@@ -188,6 +189,8 @@ def debug_lib() -> ctypes.CDLL:
         L.mgqa_debug_inject_prefill_stall.restype = ctypes.c_int
         L.mgqa_debug_decode_timeline.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
         L.mgqa_debug_decode_timeline.restype = ctypes.c_int
+        L.mgqa_debug_prefill_timeline.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
+        L.mgqa_debug_prefill_timeline.restype = ctypes.c_int
         _lib_debug = L
     return _lib_debug
 

@@ -74,7 +74,24 @@ __device__ DebugState g_dbg = {{0ull, 0ull, 0ull, 0ull}, -1, kWaitLimitNs};
 MGQA_DEV uint64_t wait_limit() { return *(volatile unsigned long long *)&g_dbg.wait_limit_ns; }
 MGQA_DEV int fault_tile() { return *(volatile int *)&g_dbg.fault_tile; }
 MGQA_DEV void dbg_count(int i, unsigned long long n = 1ull) { atomicAdd(&g_dbg.counters[i], n); }
+// per-CTA phase timeline (SM clock; slot 13: global timer at entry, 14: at
+// the end of head 0's epilogue, 15: SM id), read with mgqa_debug_prefill_timeline
+constexpr int kPreTlCtas = 1024, kPreTlStamps = 16;
+__device__ unsigned long long g_pre_tl[kPreTlCtas][kPreTlStamps];
+MGQA_DEV void pre_stamp(int k) {  // by the one thread that owns stamp k
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (cta >= (unsigned)kPreTlCtas) return;
+  g_pre_tl[cta][k] = clock64();
+  if (k == 0) {
+    g_pre_tl[cta][13] = globaltimer_ns();
+    unsigned sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    g_pre_tl[cta][15] = sm;
+  }
+  if (k == 7) g_pre_tl[cta][14] = globaltimer_ns();
+}
 #else
+MGQA_DEV void pre_stamp(int) {}
 MGQA_DEV uint64_t wait_limit() { return kWaitLimitNs; }
 MGQA_DEV int fault_tile() { return -1; }
 MGQA_DEV void dbg_count(int, unsigned long long = 1ull) {}
@@ -374,6 +391,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int rows = min(BM, p.Lq - row0);
 
   // ---- set-up that touches no global memory (may overlap the previous kernel)
+  if (tid == 0) pre_stamp(0);
   if (tid == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < STAGES; ++s) {
@@ -404,6 +422,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       all_bits[w] = 0xffffffffu;
     }
   grid_dependency_wait();
+  if (tid == 0) pre_stamp(1);
   const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
   const uint64_t lim = wait_limit();
 
@@ -550,6 +569,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (tid == 0) pre_stamp(2);
   const int nk = *nk_slot & 0x7fffffff;
   const uint32_t spec_miss = (*nk_slot < 0) ? 1u : 0u;  // stage 0 holds a stale tile 0
   const uint32_t tmem = *tmem_slot;
@@ -697,6 +717,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc::fence_after_sync();
         issue_s(t, 0, 0, D / 16);
       }
+      if (lane == 0) pre_stamp(3);
       // The MMA queue is shallow: an issuing thread stalls in it until the
       // pipe has nearly drained, so any wait between two groups of MMAs
       // leaves the pipe idle. The waits for the next tile's K and V therefore
@@ -722,6 +743,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
           issue_pv(t, st, kHalfPV, BN / 16, n == 0);
           if (leader) {
+            if (n == nk - 1 && t == NT - 1) pre_stamp(8);
             if (n == nk - 1) tc::mma_commit(bar_odone + t);  // read by the epilogue only
             if (t == NT - 1) tc::mma_commit(bar_vempty + st);
           }
@@ -800,6 +822,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // tensor-memory loads and stores
       if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err, lim);
       ok = __all_sync(0xffffffffu, ok);
+      if (n == 0 && t == 0 && tid == 128) pre_stamp(10);
       if (ok) {  // after a failed wait, tensor memory is left alone
         tc::fence_after_sync();
         if (neg) {
@@ -813,6 +836,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc::fence_before_sync();
       }
       mbar_arrive(bar_pfull + t);
+      if (n == 0 && t == 0 && tid == 128) pre_stamp(4);
     }
     // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
     // last S MMA completed) in the 128-byte-swizzled box layout, then written
@@ -823,6 +847,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = __all_sync(0xffffffffu, ok);
       tc::fence_after_sync();
       o_scale = (l > 0.f) ? 1.f / l : 0.f;
+      if (t == 0 && tid == 128) pre_stamp(5);
     } else if (ok) {
       ok = mbar_wait(bar_q, 0, p.err, lim);  // the Q load must land before the buffer is reused
     }
@@ -854,10 +879,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 4 + 4 * t && lane == 0 && MGQA_DCHECK(row0 < p.Lq && h0 + t < p.Hq, p.err)) {
       for (int c = 0; c < KB; ++c) tc::tma_store_4d(&tm_o, ob + c * BOX, c * 64, row0, h0 + t, b);
       tc::tma_store_commit_and_wait_read();
+      if (t == 0) pre_stamp(6);
     }
     if (row_ok && p.lse)
       p.lse[((int64_t)b * p.Hq + h0 + t) * p.Lq + i] =
           (l > 0.f) ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+    if (t == 0 && tid == 128) pre_stamp(7);
     role_end();
   }
 }
@@ -984,6 +1011,19 @@ extern "C" MGQA_API mgqa_status mgqa_debug_counters(uint64_t *out, int32_t n) {
   const cudaError_t e = cudaMemcpyFromSymbol(&st, g_dbg, sizeof(st));
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the debug state: %s", cudaGetErrorString(e));
   for (int i = 0; i < n; ++i) out[i] = st.counters[i];
+  return MGQA_OK;
+}
+
+extern "C" MGQA_API mgqa_status mgqa_debug_prefill_timeline(uint64_t *out, int32_t n_ctas) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (!out || n_ctas < 0 || n_ctas > kPreTlCtas)
+    return fail(MGQA_ERR_INVALID_ARG, "mgqa_debug_prefill_timeline: bad output or count");
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_pre_tl, (size_t)n_ctas * kPreTlStamps * sizeof(uint64_t));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the timeline: %s", cudaGetErrorString(e));
+  static const unsigned long long zeros[kPreTlCtas][kPreTlStamps] = {};
+  e = cudaMemcpyToSymbol(g_pre_tl, zeros, sizeof(zeros));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "clearing the timeline: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
 

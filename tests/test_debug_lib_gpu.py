@@ -116,3 +116,46 @@ def test_stall_arguments_are_checked(M):
     assert Ld.mgqa_debug_inject_prefill_stall(-1, 0) == M.MGQA_OK
     buf = (ctypes.c_uint64 * 8)()
     assert Ld.mgqa_debug_counters(buf, 8) == M.MGQA_ERR_INVALID_ARG
+
+
+def _timeline(fn, n):
+    buf = (ctypes.c_uint64 * (n * 16))()
+    assert fn(buf, n) == 0
+    import numpy as np
+    return np.array(buf, dtype=np.uint64).reshape(n, 16).astype(np.int64)
+
+
+def test_phase_timelines_are_ordered_and_cleared(M):
+    """The debug timelines (test equipment for finding where a kernel's time
+    goes): every CTA that ran records its phases in order on one SM clock, and
+    reading clears the record."""
+    Ld = M.debug_lib()
+    h = torch.cuda.current_stream().cuda_stream
+    # prefill: the padded-CFG shape (8 query tiles x 8 head pairs x 2 rows)
+    wl = W.padded_cfg(variant="kvlen")
+    d = to_device(wl)
+    _timeline(Ld.mgqa_debug_prefill_timeline, 1024)  # clear
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _prefill(Ld, M, d, wl, err)
+    torch.cuda.synchronize()
+    t = _timeline(Ld.mgqa_debug_prefill_timeline, 128)
+    # pairs ordered by causality (same thread, or an issue and its completion)
+    for k0, k1 in ((0, 1), (1, 2), (1, 3), (1, 10), (10, 4), (4, 5), (5, 6), (6, 7)):
+        assert (t[:, k1] >= t[:, k0]).all(), (k0, k1)
+    assert (t[:, 14] >= t[:, 13]).all() and (t[:, 0] > 0).all()
+    assert (_timeline(Ld.mgqa_debug_prefill_timeline, 128) == 0).all()
+    # decode: the static-cache shape (16 splits x 2 head groups x 8 requests)
+    wd = W.static_cache_decode(variant="span")
+    dd = to_device(wd)
+    out = torch.empty_like(dd["q"])
+    a = M.make_args(dd["q"], dd["k"], dd["v"], out, scale=wd.scale, kv_len=dd["kv_len"])
+    _timeline(Ld.mgqa_debug_decode_timeline, 256)
+    assert Ld.masked_gqa_attn_decode(ctypes.byref(a), None, 0, h) == 0
+    torch.cuda.synchronize()
+    t = _timeline(Ld.mgqa_debug_decode_timeline, 256)
+    ran = t[:, 3] > 0  # CTAs with at least one chunk
+    for k0, k1 in ((0, 1), (1, 2), (5, 6), (6, 7), (7, 8)):
+        assert (t[:, k1] >= t[:, k0]).all(), (k0, k1)
+    for k0, k1 in ((2, 3), (3, 4), (4, 5)):
+        assert (t[ran, k1] >= t[ran, k0]).all(), (k0, k1)
+    assert ran.any() and (_timeline(Ld.mgqa_debug_decode_timeline, 256) == 0).all()
