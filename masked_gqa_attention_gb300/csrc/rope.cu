@@ -7,10 +7,13 @@
 // built in fp32); OmniVoice page, "Memory & speed", packed_guidance paragraph
 // (positions restart at 0 for each packed sequence).
 //
-// One thread per (row b, position l, pair i): it forms theta = fl32(pos * f_i)
-// once, takes its sine and cosine (positions reach thousands of radians: the
-// shared reduced-argument sine and cosine of common.cuh) and rotates pair i
-// of every rotated head at (b, l).
+// Rows of 16-byte vectors take rope_vec_kernel (below); any other layout the
+// per-pair kernel: one thread per (row b, position l, pair i) forms
+// theta = fl32(pos * f_i) once, takes its sine and cosine (positions reach
+// thousands of radians: the shared reduced-argument sine and cosine of
+// common.cuh) and rotates pair i of every rotated head at (b, l). Both are
+// launched with programmatic dependent launch and read nothing before the
+// grid-dependency wait.
 // Consecutive threads take consecutive pairs, so each warp reads and writes
 // whole runs of a row (interleaved: one contiguous run; half-split: two).
 // The pairs of kHeadBatch heads are loaded before any is stored, so their
@@ -74,6 +77,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   const int i = (int)(idx % p.half);
   const int64_t bl = idx / p.half;
   const int l = (int)(bl % p.L), b = (int)(bl / p.L);
+  allow_dependents();
+  grid_dependency_wait();
   const int pos = p.positions ? __ldg(p.positions + bl) : l;
   float sn, cs;
   rope_sincos(rope_theta(pos, __ldg(p.inv_freq + i)), sn, cs);
@@ -96,6 +101,81 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   }
 }
 
+// Rows of 16-byte vectors (the x pointer and every stride 16-byte aligned,
+// the rotated span whole vectors): one thread per (row b, position l, group
+// of kVecHeads heads, vector of pairs). It takes the sines and cosines of its
+// pairs once, loads its vectors of every head in the group (half-split: the
+// first-half vector and its second-half partner) before storing any, and
+// moves 16 bytes per access; the arithmetic is the scalar kernel's.
+constexpr int kVecHeads = 4;
+
+template <typename T> MGQA_DEV void vec_to_float(const uint4 &u, float (&f)[16 / sizeof(T)]) {
+  unpack16_t<T>(u, f);
+}
+template <typename T> MGQA_DEV uint4 vec_from_float(const float (&f)[16 / sizeof(T)]) {
+  if constexpr (sizeof(T) == 4) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  } else {
+    return make_uint4(pack2<T>(f[0], f[1]), pack2<T>(f[2], f[3]), pack2<T>(f[4], f[5]),
+                      pack2<T>(f[6], f[7]));
+  }
+}
+
+template <typename T, bool INTER>
+__global__ void __launch_bounds__(kRopeThreads) rope_vec_kernel(const __grid_constant__ RopeParams p) {
+  constexpr int EPV = 16 / sizeof(T);          // elements per vector
+  constexpr int PPV = INTER ? EPV / 2 : EPV;   // pairs per vector (half-split: with its partner)
+  const int nvec = INTER ? 2 * p.half / EPV : p.half / EPV;
+  const int ngrp = (p.heads + kVecHeads - 1) / kVecHeads;
+  const int64_t idx = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x;
+  if (idx >= (int64_t)p.B * p.L * ngrp * nvec) return;
+  const int v = (int)(idx % nvec);
+  const int64_t r = idx / nvec;
+  const int grp = (int)(r % ngrp);
+  const int64_t bl = r / ngrp;
+  const int l = (int)(bl % p.L), b = (int)(bl / p.L);
+  allow_dependents();
+  grid_dependency_wait();  // x, positions and the table may come from the previous kernel
+  const int pos = p.positions ? __ldg(p.positions + bl) : l;
+  const int i0 = v * PPV;  // first pair of this vector
+  float sn[PPV], cs[PPV];
+#pragma unroll
+  for (int j = 0; j < PPV; ++j) rope_sincos(rope_theta(pos, __ldg(p.inv_freq + i0 + j)), sn[j], cs[j]);
+  const int e0 = INTER ? 2 * i0 : i0;  // first element of the vector
+  T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
+  uint4 va[kVecHeads], vb[kVecHeads];
+#pragma unroll
+  for (int u = 0; u < kVecHeads; ++u) {
+    const int h = grp * kVecHeads + u;
+    if (h < p.heads) {
+      const T *hr = row + (int64_t)h * p.s_h + e0;
+      va[u] = *reinterpret_cast<const uint4 *>(hr);
+      if (!INTER) vb[u] = *reinterpret_cast<const uint4 *>(hr + p.half);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kVecHeads; ++u) {
+    const int h = grp * kVecHeads + u;
+    if (h >= p.heads) continue;
+    T *hr = row + (int64_t)h * p.s_h + e0;
+    float a[EPV];
+    vec_to_float<T>(va[u], a);
+    if constexpr (INTER) {
+#pragma unroll
+      for (int j = 0; j < PPV; ++j) rope_rotate(a[2 * j], a[2 * j + 1], cs[j], sn[j], a[2 * j], a[2 * j + 1]);
+      *reinterpret_cast<uint4 *>(hr) = vec_from_float<T>(a);
+    } else {
+      float c[EPV];
+      vec_to_float<T>(vb[u], c);
+#pragma unroll
+      for (int j = 0; j < PPV; ++j) rope_rotate(a[j], c[j], cs[j], sn[j], a[j], c[j]);
+      *reinterpret_cast<uint4 *>(hr) = vec_from_float<T>(a);
+      *reinterpret_cast<uint4 *>(hr + p.half) = vec_from_float<T>(c);
+    }
+  }
+}
+
 // One warp per rotated head vector (b, l, h < heads): RMS normalisation over
 // the D features, then the rotation of the first rot_dim; D <= 256.
 constexpr int kNormWarps = 8;
@@ -111,6 +191,8 @@ rope_norm_kernel(const __grid_constant__ RopeParams p) {
   const int l = (int)(bl % p.L), b = (int)(bl / p.L);
   T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)h * p.s_h + (int64_t)l * p.s_l;
   float *buf = rowbuf[wl];
+  allow_dependents();
+  grid_dependency_wait();
   float part = 0.f;
   for (int d = lane, k = 0; d < p.D; d += 32, ++k) {
     const float x = to_float(row[d]);
@@ -139,8 +221,23 @@ mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
     const int64_t tasks = (int64_t)p.B * p.L * p.heads;
     const int64_t blocks = (tasks + kNormWarps - 1) / kNormWarps;
     if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
-    rope_norm_kernel<T><<<(unsigned)blocks, 32 * kNormWarps, 0, s>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(rope_norm_kernel<T>, dim3((unsigned)blocks), dim3(32 * kNormWarps), 0, s, p);
+    if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
+    return MGQA_OK;
+  }
+  // 16-byte vectors: aligned rows and a rotated span of whole vectors
+  constexpr int EPV = 16 / (int)sizeof(T);
+  const bool vec = (reinterpret_cast<uintptr_t>(p.x) % 16) == 0 && p.s_b % EPV == 0 &&
+                   p.s_h % EPV == 0 && p.s_l % EPV == 0 &&
+                   (p.interleaved ? (2 * p.half) % EPV == 0 : p.half % EPV == 0);
+  if (vec) {
+    const int64_t nvec = p.interleaved ? 2 * p.half / EPV : p.half / EPV;
+    const int64_t vtotal = (int64_t)p.B * p.L * ((p.heads + kVecHeads - 1) / kVecHeads) * nvec;
+    const int64_t vblocks = (vtotal + kRopeThreads - 1) / kRopeThreads;
+    if (vblocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
+    const cudaError_t e =
+        p.interleaved ? launch_pdl(rope_vec_kernel<T, true>, dim3((unsigned)vblocks), dim3(kRopeThreads), 0, s, p)
+                      : launch_pdl(rope_vec_kernel<T, false>, dim3((unsigned)vblocks), dim3(kRopeThreads), 0, s, p);
     if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
     return MGQA_OK;
   }
@@ -151,11 +248,9 @@ mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
   const bool paired = sizeof(T) == 2 && p.interleaved &&
                       (reinterpret_cast<uintptr_t>(p.x) % 4) == 0 && p.s_b % 2 == 0 &&
                       p.s_h % 2 == 0 && p.s_l % 2 == 0;
-  if (paired)
-    rope_kernel<T, sizeof(T) == 2><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
-  else
-    rope_kernel<T, false><<<(unsigned)blocks, kRopeThreads, 0, s>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      paired ? launch_pdl(rope_kernel<T, sizeof(T) == 2>, dim3((unsigned)blocks), dim3(kRopeThreads), 0, s, p)
+             : launch_pdl(rope_kernel<T, false>, dim3((unsigned)blocks), dim3(kRopeThreads), 0, s, p);
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }

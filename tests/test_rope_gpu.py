@@ -127,3 +127,30 @@ def test_reduced_sincos_error_bound(M):
     got = xd.cpu().double()[0, 0]
     err = torch.maximum((got[:, 0] - torch.cos(theta)).abs(), (got[:, 1] - torch.sin(theta)).abs())
     assert float(err.max()) <= 1e-6, float(err.max())
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("rot", [128, 64, 20])
+def test_rope_vector_and_scalar_paths_agree(M, oracle_mod, dtype, interleaved, rot):
+    """16-byte-aligned rows take the vector kernel, others the per-pair one:
+    the same bits either way (a view one element into a padded buffer is not
+    16-byte aligned; rot_dim 20 is not whole vectors and always takes the
+    per-pair kernel)."""
+    B, H, L, D, heads = 2, 6, 333, 128, 5
+    x = make_x(51 + rot, B, H, L, D, dtype)
+    f = inv_freq_table(rot)
+    g = torch.Generator().manual_seed(8)
+    pos = torch.randint(0, 8192, (B, L), generator=g, dtype=torch.int32)
+    pad = torch.zeros(B, H, L, D + 8, dtype=dtype)
+    pad[..., 1:D + 1] = x
+    a, p = x.cuda(), pad.cuda()
+    view = p[..., 1:D + 1]
+    for t in (a, view):
+        M.masked_gqa_rope(t, f.cuda(), positions=pos.cuda(), rot_dim=rot, heads=heads,
+                          interleaved=interleaved)
+    torch.cuda.synchronize()
+    assert torch.equal(a.cpu(), view.cpu())
+    assert torch.equal(p[..., 0].cpu(), pad[..., 0]) and torch.equal(p[..., D + 1:].cpu(), pad[..., D + 1:])
+    ref = oracle_mod.rope(x, inv_freq=f, positions=pos, rot_dim=rot, heads=heads, interleaved=interleaved)
+    assert_close_to_oracle(a, ref, dtype, f"rope rot {rot}")
