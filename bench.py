@@ -589,6 +589,8 @@ def run_gpu(args):
             print(json.dumps({"leg": "decode", "us_per_call": t * 1e6}))
             return 0
         maker, calls, nsets = {"prefill": (lambda: W.padded_cfg(variant="bits"), CFG_CALLS, PREFILL_SETS),
+                               "prefill_kvlen": (lambda: W.padded_cfg(variant="kvlen"), CFG_CALLS,
+                                                 PREFILL_SETS),
                                "packed": (W.packed_guidance, 32, PREFILL_SETS),
                                "dit": (lambda: W.dit_batch(B=args.rows or 32), DIT_CALLS, 1)}[args.only]
         secs, _ = bench_prefill_graph(M, maker(), dev, calls, nsets, args.steps, args.warmup, world)
@@ -771,7 +773,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mgqa", choices=["mgqa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "packed", "dit", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "prefill_kvlen", "packed", "dit", "decode"], default=None,
                     help="profiling aid: time only one workload (padded-CFG prefill, packed "
                          "guidance, DiT batch or the decode) and print its raw timing")
     ap.add_argument("--rows", type=int, default=None,

@@ -423,10 +423,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   grid_dependency_wait();
   if (tid == 0) pre_stamp(1);
-  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
-  const uint64_t lim = wait_limit();
 
   // ---- Q load, segment range of the query tile ----------------------------
+  // (the copies go out before anything waits on a global load)
   if (tid == 0) {
     // Q does not depend on the mask: start its load before classifying, and
     // key tile 0 with it (most masks keep it; checked after classifying)
@@ -446,6 +445,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc::tma_load_4d(smem + Lay::v_off + c * BOX, &tm_v, c * 64, 0, g, b, bar_vfull);
     }
   }
+  const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
+  const uint64_t lim = wait_limit();
   if (warp == 0) {
     if (p.mask.seg_q) {
       int mn = INT_MAX, mx = INT_MIN;
