@@ -467,6 +467,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   }
   __syncthreads();
+  if (tid == 0) pre_stamp(9);
 
   // ---- packed-bit mask: per-tile "some key allowed" / "all keys allowed" ---
   // Each warp reads whole mask rows (32 consecutive words per load), folds
@@ -512,6 +513,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncthreads();
   }
+  if (tid == 0) pre_stamp(11);
 
   // ---- classify key tiles: 0 empty, 1 partial, 2 full ----------------------
   for (int kt = warp; kt < p.nkt; kt += nwarps) {
@@ -553,6 +555,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (lane == 0) cls[kt] = ne ? (full ? 2 : 1) : 0;
   }
   __syncthreads();
+  if (tid == 0) pre_stamp(12);
   if (warp == 0) {
     int count = 0;
     for (int base = 0; base < p.nkt; base += 32) {

@@ -140,7 +140,8 @@ def test_phase_timelines_are_ordered_and_cleared(M):
     torch.cuda.synchronize()
     t = _timeline(Ld.mgqa_debug_prefill_timeline, 128)
     # pairs ordered by causality (same thread, or an issue and its completion)
-    for k0, k1 in ((0, 1), (1, 2), (1, 3), (1, 10), (10, 4), (4, 5), (5, 6), (6, 7)):
+    for k0, k1 in ((0, 1), (1, 9), (9, 11), (11, 12), (12, 2), (1, 3), (1, 10), (10, 4), (4, 5),
+                   (5, 6), (6, 7)):
         assert (t[:, k1] >= t[:, k0]).all(), (k0, k1)
     assert (t[:, 14] >= t[:, 13]).all() and (t[:, 0] > 0).all()
     assert (_timeline(Ld.mgqa_debug_prefill_timeline, 128) == 0).all()
