@@ -53,12 +53,13 @@ MGQA_API mgqa_status mgqa_debug_inject_prefill_stall(int32_t tile, uint64_t wait
  * clock at the kernel's phase boundaries 0..8 (entry; after the grid-
  * dependency wait; the allowed-slot words formed; the first batch's copies
  * issued; the first batch landed; every batch computed; the in-CTA merge; the
- * ticket taken; the merged output written, by the last CTA only), then at
- * four points inside the first batch of the 16-bit path: 9 (masked rows
- * fixed up), 10 (the shared maximum exchanged), 11 (this warp's scores and
- * maximum formed), 12 (the batch's bytes armed); the global timer (ns) at
- * entry and at the ticket, and the SM id. A stamp a CTA did not reach reads
- * 0. Reading clears the record for all CTAs. Synchronous. */
+ * partials sent to their owners in the cluster; this CTA's slice of the
+ * output merged and written), then at four points around the first batch of
+ * the 16-bit path: 9 (masked rows fixed up), 10 (the shared maximum
+ * exchanged), 11 (this warp's scores and maximum formed), 12 (the batch's
+ * bytes armed); the global timer (ns) at entry and at stamp 7, and the SM id.
+ * A stamp a CTA did not reach reads 0. Reading clears the record for all
+ * CTAs. Synchronous. */
 MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas);
 
 /* Per-CTA timeline of the tensor-core prefill launches since the previous
