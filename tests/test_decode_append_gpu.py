@@ -99,3 +99,33 @@ def test_full_cache_is_an_error_and_appends_nothing(M, oracle_mod):
     ref, _, _ = oracle_mod.attention(wl.q, kc, vc, scale=wl.scale,
                                      kv_len=torch.tensor([int(wl.kv_len[0]) + 1, Lk]))
     assert_close_to_oracle(out, ref, torch.bfloat16, "full cache")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("Hq,Hkv,D", [(16, 1, 128), (4, 4, 64), (12, 2, 64)],
+                         ids=lambda v: str(v))
+def test_append_head_groups_and_chunk_edges(M, oracle_mod, dtype, Hq, Hkv, D):
+    """Head groups that share a KV head (16 query heads on one: two groups, one
+    writer of the new row), one query head per group, and lengths at 64-slot
+    chunk edges and at the cache's last slot: the new row starts a chunk no
+    earlier step fetched, or fills the final slot."""
+    lens = [63, 64, 127, 999]
+    B, Lk = len(lens), 1000
+    g, q, k, v = W.random_qkv(91 + Hq + D, B, Hq, Hkv, 1, Lk, D, dtype)
+    kvl = torch.tensor(lens, dtype=torch.int32)
+    kn, vn = _step_inputs(2 + D, B, Hkv, D, dtype)
+    k2, v2 = k.clone(), v.clone()
+    for b, n in enumerate(lens):
+        k2[b, :, n] = kn[b, :, 0]
+        v2[b, :, n] = vn[b, :, 0]
+    qd, kd, vd, kvld = q.cuda(), k.cuda(), v.cuda(), kvl.cuda()
+    out_len = torch.zeros_like(kvld)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device="cuda")
+    out = M.masked_gqa_attn_decode_append(qd, kd, vd, kn.cuda(), vn.cuda(), kvld,
+                                          kv_len_out=out_len, scale=D ** -0.5, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(kd.cpu(), k2) and torch.equal(vd.cpu(), v2)
+    assert torch.equal(out_len.cpu(), kvl + 1)
+    ref, ref_lse, _ = oracle_mod.attention(q, k2, v2, scale=D ** -0.5, kv_len=kvl + 1)
+    assert_close_to_oracle(out, ref, dtype, f"append {Hq}/{Hkv}/{D}")
+    assert_lse_close(lse, ref_lse, 1e-5 if dtype == torch.float32 else 1e-3)
