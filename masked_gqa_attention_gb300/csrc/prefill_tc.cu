@@ -128,7 +128,9 @@ struct Layout {
   static constexpr int all_off = any_off + MAXKT / 8;  // uint32[MAXKT/32]: tile all allowed
   static constexpr int list_off = all_off + MAXKT / 8;  // uint16[MAXKT]
   static constexpr int cls_off = list_off + 2 * MAXKT;  // uint8[MAXKT]
-  static constexpr int total = cls_off + MAXKT;
+  // fused rotation: the inverse frequencies and the q norm weights, staged once
+  static constexpr int rope_off = (cls_off + MAXKT + 15) & ~15;  // float[D / 2] then float[D]
+  static constexpr int total = rope_off + (D / 2 + D) * 4;
   static constexpr int smem_bytes = total + 1024;   // slack for 1024-B alignment
   static constexpr int threads = 128 * (1 + NT);
   static constexpr int tmem_cols_used = NT * (BN + D);
@@ -200,7 +202,7 @@ template <> MGQA_DEV float half_of<__half>(uint32_t v, int hi) {
 // index is a constant (interleaved pairs stop at rp.half; half-split pairs
 // have HALF as a template argument), so the row stays in registers.
 template <int D, bool INTERLEAVED, int HALF>
-MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
+MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, const float *invf, int pos) {
   const int half = INTERLEAVED ? rp.half : HALF;
 #pragma unroll
   for (int i = 0; i < D / 2; ++i) {
@@ -208,7 +210,7 @@ MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
     const int e0 = INTERLEAVED ? 2 * i : i;
     const int e1 = INTERLEAVED ? 2 * i + 1 : i + half;
     float sn, cs, y0, y1;
-    rope_sincos(rope_theta(pos, __ldg(rp.inv_freq + i)), sn, cs);
+    rope_sincos(rope_theta(pos, invf[i]), sn, cs);
     rope_rotate(x[e0], x[e1], cs, sn, y0, y1);
     x[e0] = y0;
     x[e1] = y1;
@@ -217,9 +219,11 @@ MGQA_DEV void rope_row_pairs(float (&x)[D], const FusedRope &rp, int pos) {
 
 // RMS normalisation and rotary embedding of query row r of one head's tile
 // in shared memory (128-byte-swizzled 64-column boxes), in place: the same
-// arithmetic as the standalone rotary-embedding kernel.
+// arithmetic as the standalone rotary-embedding kernel. invf and qw are the
+// frequency table and the norm weights staged in shared memory.
 template <typename T, int D>
-MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &rp) {
+MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &rp,
+                         const float *invf, const float *qw) {
   float x[D];  // the row as floats (16-bit values are exact in fp32)
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
@@ -232,13 +236,13 @@ MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &r
   if (rp.q_norm) {
     const float rs = rms_scale(rms_sum_row<D>(x), D, rp.eps);
 #pragma unroll
-    for (int d = 0; d < D; ++d) x[d] = rms_apply(x[d], rs, __ldg(rp.q_norm + d));
+    for (int d = 0; d < D; ++d) x[d] = rms_apply(x[d], rs, qw[d]);
   }
   // half-split widths D/2, D/4, D/8 (the host refuses others)
-  if (rp.interleaved) rope_row_pairs<D, true, 0>(x, rp, pos);
-  else if (rp.half == D / 2) rope_row_pairs<D, false, D / 2>(x, rp, pos);
-  else if (rp.half == D / 4) rope_row_pairs<D, false, D / 4>(x, rp, pos);
-  else rope_row_pairs<D, false, D / 8>(x, rp, pos);
+  if (rp.interleaved) rope_row_pairs<D, true, 0>(x, rp, invf, pos);
+  else if (rp.half == D / 2) rope_row_pairs<D, false, D / 2>(x, rp, invf, pos);
+  else if (rp.half == D / 4) rope_row_pairs<D, false, D / 4>(x, rp, invf, pos);
+  else rope_row_pairs<D, false, D / 8>(x, rp, invf, pos);
 #pragma unroll
   for (int c = 0; c < D / 8; ++c)  // one rounding to the I/O type
     *reinterpret_cast<uint4 *>(tile + (c >> 3) * BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
@@ -447,6 +451,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   const int kvl = load_kv_len(p.mask.kv_len, b, p.Lk, p.err, qt == 0 && hp == 0 && tid == 0);
   const uint64_t lim = wait_limit();
+  float *rope_invf = reinterpret_cast<float *>(smem + Lay::rope_off);
+  float *rope_qw = rope_invf + D / 2;
+  if (ROPE && (warp == 2 || warp == 3)) {
+    // the rotation's tables, once per CTA (every query row reads them); every
+    // load is issued before any store
+    constexpr int NT3 = (D / 2 + D + 63) / 64;
+    float v[NT3];
+#pragma unroll
+    for (int u = 0; u < NT3; ++u) {
+      const int i = tid - 64 + 64 * u;
+      v[u] = 0.f;
+      if (i < D / 2) v[u] = i < p.rope.half ? __ldg(p.rope.inv_freq + i) : 0.f;
+      else if (i < D / 2 + D && p.rope.q_norm) v[u] = __ldg(p.rope.q_norm + (i - D / 2));
+    }
+#pragma unroll
+    for (int u = 0; u < NT3; ++u) {
+      const int i = tid - 64 + 64 * u;
+      if (i < D / 2 + D) rope_invf[i] = v[u];  // rope_qw follows rope_invf
+    }
+  }
   if (warp == 0) {
     if (p.mask.seg_q) {
       int mn = INT_MAX, mx = INT_MIN;
@@ -808,7 +832,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (ok) ok = mbar_wait(bar_q, 0, p.err, lim);
       if (ok && row_ok && h0 + t < p.rope.q_heads) {
         const int pos = p.rope.positions ? __ldg(p.rope.positions + (int64_t)b * p.Lq + i) : i;
-        rope_q_row<T, D>(smem + Lay::q_off + t * KB * BOX, r, pos, p.rope);
+        rope_q_row<T, D>(smem + Lay::q_off + t * KB * BOX, r, pos, p.rope, rope_invf, rope_qw);
       }
       fence_proxy_async_smem();  // the tensor core reads the tile through the async proxy
       mbar_arrive(bar_qrot + t);
