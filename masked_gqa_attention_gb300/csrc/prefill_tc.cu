@@ -427,6 +427,24 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   grid_dependency_wait();
   if (tid == 0) pre_stamp(1);
+  // packed-bit mask words of the first 32-word block (1024 keys) of this
+  // warp's rows, requested before anything else (the copies below move
+  // 64 KB or more per CTA; these few words should not queue behind them).
+  // At most 16 rows per warp (128 rows, >= 8 warps): every load in flight.
+  const int mW = (p.Lk + 31) >> 5;
+  auto mask_words = [&](int wb, uint32_t (&wv)[BM / 8]) {
+    const int w = wb + lane;
+    const int lim_k = p.Lk - 32 * w;
+    const uint32_t valid = w >= mW ? 0u : (lim_k >= 32 ? 0xffffffffu : ((1u << lim_k) - 1u));
+#pragma unroll
+    for (int k = 0; k < BM / 8; ++k) {
+      const int r = warp + k * nwarps;
+      const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
+      wv[k] = (r < rows && w < mW) ? (__ldg(mrow + w) & valid) : valid;
+    }
+  };
+  uint32_t wv0[BM / 8];
+  if (p.mask.bits) mask_words(0, wv0);
 
   // ---- Q load, segment range of the query tile ----------------------------
   // (the copies go out before anything waits on a global load)
@@ -494,23 +512,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (tid == 0) pre_stamp(9);
 
   // ---- packed-bit mask: per-tile "some key allowed" / "all keys allowed" ---
-  // Each warp reads whole mask rows (32 consecutive words per load), folds
-  // its rows per word, reduces the 4 words of a tile across lanes and merges
-  // into the CTA's bitsets.
+  // Each warp reads whole mask rows (32 consecutive words per load; the first
+  // block was requested right after the grid-dependency wait), folds its rows
+  // per word, reduces the 4 words of a tile across lanes and merges into the
+  // CTA's bitsets.
   if (p.mask.bits) {
-    const int W = (p.Lk + 31) >> 5;
+    const int W = mW;
     for (int wb = 0; wb < W; wb += 32) {
       const int w = wb + lane;
       const int lim = p.Lk - 32 * w;
       const uint32_t valid = w >= W ? 0u : (lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u));
       uint32_t o = 0u, a = 0xffffffffu;
-      // at most 16 rows per warp (128 rows, >= 8 warps): every load in flight
       uint32_t wv[BM / 8];
+      if (wb == 0) {
 #pragma unroll
-      for (int k = 0; k < BM / 8; ++k) {
-        const int r = warp + k * nwarps;
-        const uint32_t *mrow = p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + r) * p.mask.sq;
-        wv[k] = (r < rows && w < W) ? (__ldg(mrow + w) & valid) : valid;
+        for (int k = 0; k < BM / 8; ++k) wv[k] = wv0[k];
+      } else {
+        mask_words(wb, wv);
       }
 #pragma unroll
       for (int k = 0; k < BM / 8; ++k) {
