@@ -212,20 +212,35 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #endif
   const int h0 = hg * NREP;
   const int g = h0 / p.n_rep;
-  if (warp == 1 && lane < 8) {
-    // warm the L2 lines and page translations this CTA touches first
-    const char *pf = nullptr;
+  {
+    // before the grid-dependency wait, hints that move the lines this CTA
+    // reads first toward the L2 (nothing enters the SM; the L2 is the point
+    // of coherence, so a later write by the previous kernel still wins): q's
+    // rows, kv_len, the mask words and segment ids of every chunk of mine,
+    // and the K and V rows of my first chunk, which most calls fetch
     const int64_t r0 = (int64_t)x * C;
-    if (lane == 0) pf = static_cast<const char *>(p.q) + ((int64_t)b * p.qs_b + (int64_t)h0 * p.qs_h) * sizeof(T);
-    if (lane == 1 && p.kv_len) pf = reinterpret_cast<const char *>(p.kv_len + b);
-    if (lane == 2 && p.bits && r0 < p.Lk) pf = reinterpret_cast<const char *>(p.bits + (int64_t)b * p.ms_b + (r0 >> 5));
-    if (lane == 3 && r0 < p.Lk)
-      pf = static_cast<const char *>(p.k) + ((int64_t)b * p.ks_b + (int64_t)g * p.ks_h + r0 * p.ks_l) * sizeof(T);
-    if (lane == 4 && r0 < p.Lk)
-      pf = static_cast<const char *>(p.v) + ((int64_t)b * p.vs_b + (int64_t)g * p.vs_h + r0 * p.vs_l) * sizeof(T);
-    if (lane == 5) pf = static_cast<const char *>(p.out) + ((int64_t)b * p.os_b + (int64_t)h0 * p.os_h) * sizeof(T);
-    if (lane == 7 && p.seg_k && r0 < p.Lk) pf = reinterpret_cast<const char *>(p.seg_k + (int64_t)b * p.Lk + r0);
-    if (pf) prefetch_l2(pf);
+    if (tid < NREP)
+      prefetch_l2(static_cast<const char *>(p.q) + ((int64_t)b * p.qs_b + (int64_t)(h0 + tid) * p.qs_h) * sizeof(T));
+    if (tid == NREP && p.kv_len) prefetch_l2(p.kv_len + b);
+    const int nci0 = x < p.nch ? (p.nch - x + S - 1) / S : 0;
+    for (int i = tid; i < nci0; i += kThreads) {
+      const int64_t j0 = (int64_t)(x + S * i) * C;
+      if (p.bits) prefetch_l2(p.bits + (int64_t)b * p.ms_b + (j0 >> 5));
+      if (p.seg_k) {
+        prefetch_l2(p.seg_k + (int64_t)b * p.Lk + j0);
+        if (j0 + 32 < p.Lk) prefetch_l2(p.seg_k + (int64_t)b * p.Lk + j0 + 32);
+      }
+    }
+    constexpr int LPR = (D * (int)sizeof(T) + 127) / 128;  // 128-byte lines per row
+    for (int u = tid; u < 2 * C * LPR && r0 < p.Lk; u += kThreads) {
+      const int kv = u / (C * LPR), rr = (u / LPR) % C, ln = u % LPR;
+      if (r0 + rr < p.Lk) {
+        const char *base = static_cast<const char *>(kv ? p.v : p.k);
+        const int64_t off = kv ? (int64_t)b * p.vs_b + (int64_t)g * p.vs_h + (r0 + rr) * p.vs_l
+                               : (int64_t)b * p.ks_b + (int64_t)g * p.ks_h + (r0 + rr) * p.ks_l;
+        prefetch_l2(base + off * sizeof(T) + ln * 128);
+      }
+    }
   }
   grid_dependency_wait();  // everything below may read what the previous kernel wrote
   dec_stamp(1);
