@@ -13,7 +13,8 @@
 // thousands of radians: the shared reduced-argument sine and cosine of
 // common.cuh) and rotates pair i of every rotated head at (b, l). Both are
 // launched with programmatic dependent launch and read nothing before the
-// grid-dependency wait.
+// grid-dependency wait (the vector kernel only issues L2 prefetch hints for
+// its vectors there, which overlap the previous kernel's tail).
 // Consecutive threads take consecutive pairs, so each warp reads and writes
 // whole runs of a row (interleaved: one contiguous run; half-split: two).
 // The pairs of kHeadBatch heads are loaded before any is stored, so their
@@ -136,14 +137,24 @@ __global__ void __launch_bounds__(kRopeThreads) rope_vec_kernel(const __grid_con
   const int64_t bl = r / ngrp;
   const int l = (int)(bl % p.L), b = (int)(bl / p.L);
   allow_dependents();
+  const int i0 = v * PPV;              // first pair of this vector
+  const int e0 = INTER ? 2 * i0 : i0;  // first element of the vector
+  T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
+  // hints toward the L2 before the wait (the L2 is the point of coherence,
+  // so a later write by the previous kernel still wins)
+#pragma unroll
+  for (int u = 0; u < kVecHeads; ++u) {
+    const int h = grp * kVecHeads + u;
+    if (h < p.heads) {
+      prefetch_l2(row + (int64_t)h * p.s_h + e0);
+      if (!INTER) prefetch_l2(row + (int64_t)h * p.s_h + e0 + p.half);
+    }
+  }
   grid_dependency_wait();  // x, positions and the table may come from the previous kernel
   const int pos = p.positions ? __ldg(p.positions + bl) : l;
-  const int i0 = v * PPV;  // first pair of this vector
   float sn[PPV], cs[PPV];
 #pragma unroll
   for (int j = 0; j < PPV; ++j) rope_sincos(rope_theta(pos, __ldg(p.inv_freq + i0 + j)), sn[j], cs[j]);
-  const int e0 = INTER ? 2 * i0 : i0;  // first element of the vector
-  T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)l * p.s_l;
   uint4 va[kVecHeads], vb[kVecHeads];
 #pragma unroll
   for (int u = 0; u < kVecHeads; ++u) {
