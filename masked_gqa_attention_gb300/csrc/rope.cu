@@ -13,8 +13,8 @@
 // thousands of radians: the shared reduced-argument sine and cosine of
 // common.cuh) and rotates pair i of every rotated head at (b, l). Both are
 // launched with programmatic dependent launch and read nothing before the
-// grid-dependency wait (the vector kernel only issues L2 prefetch hints for
-// its vectors there, which overlap the previous kernel's tail).
+// grid-dependency wait (the vector and norm kernels only issue L2 prefetch
+// hints for their data there, which overlap the previous kernel's tail).
 // Consecutive threads take consecutive pairs, so each warp reads and writes
 // whole runs of a row (interleaved: one contiguous run; half-split: two).
 // The pairs of kHeadBatch heads are loaded before any is stored, so their
@@ -203,6 +203,8 @@ rope_norm_kernel(const __grid_constant__ RopeParams p) {
   T *row = static_cast<T *>(p.x) + (int64_t)b * p.s_b + (int64_t)h * p.s_h + (int64_t)l * p.s_l;
   float *buf = rowbuf[wl];
   allow_dependents();
+  if (lane * 128 < p.D * (int)sizeof(T))  // the row toward the L2 (a hint) before the wait
+    prefetch_l2(reinterpret_cast<const char *>(row) + lane * 128);
   grid_dependency_wait();
   float part = 0.f;
   for (int d = lane, k = 0; d < p.D; d += 32, ++k) {
