@@ -592,6 +592,7 @@ def run_gpu(args):
                                "prefill_kvlen": (lambda: W.padded_cfg(variant="kvlen"), CFG_CALLS,
                                                  PREFILL_SETS),
                                "packed": (W.packed_guidance, 32, PREFILL_SETS),
+                               "tiny": (W.tiny_fp32, 32, 8),
                                "dit": (lambda: W.dit_batch(B=args.rows or 32), DIT_CALLS, 1)}[args.only]
         secs, _ = bench_prefill_graph(M, maker(), dev, calls, nsets, args.steps, args.warmup, world)
         print(json.dumps({"leg": args.only, "us_per_call": secs / (args.steps * calls) * 1e6}))
@@ -773,7 +774,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mgqa", choices=["mgqa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["prefill", "prefill_kvlen", "packed", "dit", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "prefill_kvlen", "packed", "tiny", "dit", "decode"], default=None,
                     help="profiling aid: time only one workload (padded-CFG prefill, packed "
                          "guidance, DiT batch or the decode) and print its raw timing")
     ap.add_argument("--rows", type=int, default=None,

@@ -78,16 +78,27 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
     for (int w = 0; w < kKeys / 32; ++w) any |= mw[w];
     if (!__syncthreads_or(any != 0u)) continue;  // empty tile: K/V never read
 
-    for (int e = tid; e < kKeys * D; e += kThreads) {
-      const int jj = e / D, d = e % D;
-      const int j = j0 + jj;
-      float kv = 0.f, vv = 0.f;
-      if (j < p.Lk) {
-        kv = to_float(kb[(int64_t)j * p.ks[2] + d]);
-        vv = to_float(vb[(int64_t)j * p.vs[2] + d]);
+    {
+      // the tile's K and V rows as 16-byte pieces, every load issued before
+      // any store (rows are 16-byte aligned: the ABI's stride rule)
+      constexpr int PV = kKeys * D / 4 / kThreads;  // pieces of K (and of V) per thread
+      float4 kq[PV], vq[PV];
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const int e = (tid + u * kThreads) * 4;
+        const int jj = e / D, d = e % D, j = j0 + jj;
+        kq[u] = vq[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < p.Lk) {
+          kq[u] = *reinterpret_cast<const float4 *>(kb + (int64_t)j * p.ks[2] + d);
+          vq[u] = *reinterpret_cast<const float4 *>(vb + (int64_t)j * p.vs[2] + d);
+        }
       }
-      ks[e] = kv;
-      vs[e] = vv;
+#pragma unroll
+      for (int u = 0; u < PV; ++u) {
+        const int e = (tid + u * kThreads) * 4;
+        *reinterpret_cast<float4 *>(ks + e) = kq[u];
+        *reinterpret_cast<float4 *>(vs + e) = vq[u];
+      }
     }
     __syncthreads();
 
