@@ -453,6 +453,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (p.mask.bits && tid < rows)
       prefetch_l2(p.mask.bits + (int64_t)b * p.mask.sb + (int64_t)(row0 + tid) * p.mask.sq);
+    // and the other inputs of the tile classification: the row's kv_len, the
+    // query tile's segment ids and the row's key segment ids (32 per line)
+    if (p.mask.kv_len && tid == 0) prefetch_l2(p.mask.kv_len + b);
+    if (p.mask.seg_q) {
+      const int nq = (rows + 31) / 32, nkl = (p.Lk + 31) / 32;
+      for (int u = tid; u < nq + nkl; u += blockDim.x)
+        prefetch_l2(u < nq ? p.mask.seg_q + (int64_t)b * p.Lq + row0 + 32 * u
+                           : p.mask.seg_k + (int64_t)b * p.Lk + 32 * (u - nq));
+    }
   }
   grid_dependency_wait();
   if (tid == 0) pre_stamp(1);
