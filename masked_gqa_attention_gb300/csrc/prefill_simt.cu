@@ -8,12 +8,15 @@
 // mask, not causal, KV heads repeated) and "Memory & speed", packed_guidance
 // paragraph (block-diagonal mask).
 //
-// CTA = 64 query rows of one query head; two threads per row, each owning
-// half of the head dim. Keys advance in tiles of 64: a tile no row of the CTA
-// may attend to is skipped without reading K/V; otherwise K and V are staged
-// in shared memory, the 64 scores of a row are formed (the two halves summed
-// with one shuffle), masked to -inf, and folded into a running (max, sum, O)
-// with one rescale per tile.
+// CTA = 32 query rows of one query head; four threads per row, each owning a
+// quarter of the head dim. Keys advance in tiles of 64: a tile no row of the
+// CTA may attend to is skipped without reading K/V; otherwise K and V are
+// staged in shared memory, the 64 scores of a row are formed from 16-byte
+// shared-memory reads (the quarters summed with two shuffles), masked to
+// -inf, and folded into a running (max, sum, O) with one rescale per tile.
+// (Two threads per row and 4-byte reads measured 24.9 us on the tiny case:
+// every row re-reads the whole tile, so the shared-memory load instructions
+// were the limit.)
 #include <cmath>
 
 #include "common.cuh"
@@ -33,22 +36,28 @@ struct SimtParams {
   int B, Hq, Hkv, Lq, Lk, n_rep;
 };
 
-constexpr int kRows = 64;
+constexpr int kRows = 32;
 constexpr int kKeys = 64;
-constexpr int kThreads = 2 * kRows;
+constexpr int kTpr = 4;  // threads per row
+constexpr int kThreads = kTpr * kRows;
+// Shared-memory row of a K or V tile: the four quarters of the head dim, each
+// followed by 4 floats of padding, so the four threads of a row read four
+// different bank groups.
+template <int D> __host__ __device__ constexpr int row_floats() { return kTpr * (D / kTpr + 4); }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
 prefill_simt_kernel(const __grid_constant__ SimtParams p) {
   extern __shared__ __align__(16) float sh[];
-  float *ks = sh;                 // [kKeys][D]
-  float *vs = sh + kKeys * D;     // [kKeys][D]
-  constexpr int DH = D / 2;
+  constexpr int DH = D / kTpr;  // head-dim elements per thread
+  constexpr int RF = row_floats<D>();
+  float *ks = sh;                 // [kKeys][RF]
+  float *vs = sh + kKeys * RF;    // [kKeys][RF]
 
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = h / p.n_rep;
   const int tid = threadIdx.x;
-  const int row = tid >> 1, half = tid & 1;
+  const int row = tid / kTpr, part = tid % kTpr;
   const int i = qt * kRows + row;
   const bool row_ok = i < p.Lq;
   const int ic = row_ok ? i : p.Lq - 1;
@@ -60,7 +69,7 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
   const T *qrow = static_cast<const T *>(p.q) + b * p.qs[0] + h * p.qs[1] + (int64_t)ic * p.qs[2];
 #pragma unroll
   for (int d = 0; d < DH; ++d) {
-    q[d] = to_float(qrow[half * DH + d]) * p.scale_log2;
+    q[d] = to_float(qrow[part * DH + d]) * p.scale_log2;
     o[d] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -96,8 +105,10 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
 #pragma unroll
       for (int u = 0; u < PV; ++u) {
         const int e = (tid + u * kThreads) * 4;
-        *reinterpret_cast<float4 *>(ks + e) = kq[u];
-        *reinterpret_cast<float4 *>(vs + e) = vq[u];
+        const int jj = e / D, d = e % D;
+        const int off = jj * RF + (d / DH) * (DH + 4) + d % DH;
+        *reinterpret_cast<float4 *>(ks + off) = kq[u];
+        *reinterpret_cast<float4 *>(vs + off) = vq[u];
       }
     }
     __syncthreads();
@@ -106,11 +117,18 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
     float mt = -INFINITY;
 #pragma unroll
     for (int jj = 0; jj < kKeys; ++jj) {
-      const float *kr = ks + jj * D + half * DH;
+      const float4 *kr = reinterpret_cast<const float4 *>(ks + jj * RF + part * (DH + 4));
       float acc = 0.f;
 #pragma unroll
-      for (int d = 0; d < DH; ++d) acc = fmaf(q[d], kr[d], acc);
+      for (int d4 = 0; d4 < DH / 4; ++d4) {
+        const float4 kv = kr[d4];
+        acc = fmaf(q[4 * d4], kv.x, acc);
+        acc = fmaf(q[4 * d4 + 1], kv.y, acc);
+        acc = fmaf(q[4 * d4 + 2], kv.z, acc);
+        acc = fmaf(q[4 * d4 + 3], kv.w, acc);
+      }
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       const bool al = (mw[jj >> 5] >> (jj & 31)) & 1u;
       s[jj] = al ? acc : -INFINITY;
       mt = fmaxf(mt, s[jj]);
@@ -125,9 +143,15 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
       for (int jj = 0; jj < kKeys; ++jj) {
         const float pj = exp2f(s[jj] - m_new);  // masked: exp2(-inf) = 0
         l += pj;
-        const float *vr = vs + jj * D + half * DH;
+        const float4 *vr = reinterpret_cast<const float4 *>(vs + jj * RF + part * (DH + 4));
 #pragma unroll
-        for (int d = 0; d < DH; ++d) o[d] = fmaf(pj, vr[d], o[d]);
+        for (int d4 = 0; d4 < DH / 4; ++d4) {
+          const float4 vv = vr[d4];
+          o[4 * d4] = fmaf(pj, vv.x, o[4 * d4]);
+          o[4 * d4 + 1] = fmaf(pj, vv.y, o[4 * d4 + 1]);
+          o[4 * d4 + 2] = fmaf(pj, vv.z, o[4 * d4 + 2]);
+          o[4 * d4 + 3] = fmaf(pj, vv.w, o[4 * d4 + 3]);
+        }
       }
       m = m_new;
     }
@@ -138,8 +162,8 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
     const float inv = l > 0.f ? 1.f / l : 0.f;
     T *orow = static_cast<T *>(p.out) + b * p.os[0] + h * p.os[1] + (int64_t)i * p.os[2];
 #pragma unroll
-    for (int d = 0; d < DH; ++d) orow[half * DH + d] = from_float<T>(o[d] * inv);
-    if (p.lse && half == 0)
+    for (int d = 0; d < DH; ++d) orow[part * DH + d] = from_float<T>(o[d] * inv);
+    if (p.lse && part == 0)
       p.lse[((int64_t)b * p.Hq + h) * p.Lq + i] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
   }
 }
@@ -147,7 +171,7 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
 template <typename T, int D>
 mgqa_status launch_t(const SimtParams &p, cudaStream_t s) {
   auto kern = prefill_simt_kernel<T, D>;
-  const size_t smem = 2 * kKeys * D * sizeof(float);
+  const size_t smem = 2 * kKeys * row_floats<D>() * sizeof(float);
   static std::atomic<uint64_t> attr_done{0};
   const mgqa_status st = ensure_smem_attr(kern, (int)smem, attr_done, "fp32 prefill kernel");
   if (st != MGQA_OK) return st;
