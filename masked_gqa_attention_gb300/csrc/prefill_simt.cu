@@ -9,11 +9,12 @@
 // paragraph (block-diagonal mask).
 //
 // CTA = 32 query rows of one query head; four threads per row, each owning a
-// quarter of the head dim. Keys advance in tiles of 64: a tile no row of the
-// CTA may attend to is skipped without reading K/V; otherwise K and V are
-// staged in shared memory, the 64 scores of a row are formed from 16-byte
-// shared-memory reads (the quarters summed with two shuffles), masked to
-// -inf, and folded into a running (max, sum, O) with one rescale per tile.
+// quarter of the head dim. Keys advance in tiles of 64, double-buffered in
+// shared memory (tile j+1 is fetched by asynchronous copies while tile j is
+// computed); a tile no row of the CTA may attend to is not computed. The 64
+// scores of a row are formed from 16-byte shared-memory reads (the quarters
+// summed with two shuffles), masked to -inf, and folded into a running (max,
+// sum, O) with one rescale per tile.
 // (Two threads per row and 4-byte reads measured 24.9 us on the tiny case:
 // every row re-reads the whole tile, so the shared-memory load instructions
 // were the limit.)
@@ -51,8 +52,6 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
   extern __shared__ __align__(16) float sh[];
   constexpr int DH = D / kTpr;  // head-dim elements per thread
   constexpr int RF = row_floats<D>();
-  float *ks = sh;                 // [kKeys][RF]
-  float *vs = sh + kKeys * RF;    // [kKeys][RF]
 
   const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = h / p.n_rep;
@@ -77,85 +76,102 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
   const T *kb = static_cast<const T *>(p.k) + b * p.ks[0] + g * p.ks[1];
   const T *vb = static_cast<const T *>(p.v) + b * p.vs[0] + g * p.vs[1];
 
-  for (int j0 = 0; j0 < p.Lk; j0 += kKeys) {
-    uint32_t mw[kKeys / 32];
+  // K and V tiles in two shared-memory buffers: tile j+1's rows are fetched
+  // (16-byte asynchronous copies) and its mask words loaded while tile j is
+  // computed
+  auto buf_k = [&](int bf) { return sh + bf * 2 * kKeys * RF; };
+  auto buf_v = [&](int bf) { return sh + bf * 2 * kKeys * RF + kKeys * RF; };
+  auto fetch = [&](int j0, int bf) {
+    constexpr int PV = kKeys * D / 4 / kThreads;  // 16-byte pieces of K (and of V) per thread
+    float *kd = buf_k(bf), *vd = buf_v(bf);
+#pragma unroll
+    for (int u = 0; u < PV; ++u) {
+      const int e = (tid + u * kThreads) * 4;
+      const int jj = e / D, d = e % D, j = j0 + jj;
+      const int off = jj * RF + (d / DH) * (DH + 4) + d % DH;
+      if (j < p.Lk) {  // rows are 16-byte aligned: the ABI's stride rule
+        cp_async16(kd + off, kb + (int64_t)j * p.ks[2] + d);
+        cp_async16(vd + off, vb + (int64_t)j * p.vs[2] + d);
+      } else {
+        *reinterpret_cast<float4 *>(kd + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(vd + off) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    cp_async_commit();
+  };
+  auto mask_words = [&](int j0, uint32_t (&mw)[kKeys / 32]) {
 #pragma unroll
     for (int w = 0; w < kKeys / 32; ++w)
       mw[w] = row_ok ? mask_word(p.mask, b, ic, j0 + 32 * w, p.Lk, p.Lq, kvl, segq) : 0u;
+  };
+
+  uint32_t mw[kKeys / 32] = {0u, 0u};
+  if (p.Lk > 0) {
+    fetch(0, 0);
+    mask_words(0, mw);
+  }
+  for (int j0 = 0, bf = 0; j0 < p.Lk; j0 += kKeys, bf ^= 1) {
+    const int jn = j0 + kKeys;
+    uint32_t mwn[kKeys / 32] = {0u, 0u};
+    if (jn < p.Lk) {
+      fetch(jn, bf ^ 1);  // that buffer's last reader passed the barrier ending the previous tile
+      mask_words(jn, mwn);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
     uint32_t any = 0;
 #pragma unroll
     for (int w = 0; w < kKeys / 32; ++w) any |= mw[w];
-    if (!__syncthreads_or(any != 0u)) continue;  // empty tile: K/V never read
-
-    {
-      // the tile's K and V rows as 16-byte pieces, every load issued before
-      // any store (rows are 16-byte aligned: the ABI's stride rule)
-      constexpr int PV = kKeys * D / 4 / kThreads;  // pieces of K (and of V) per thread
-      float4 kq[PV], vq[PV];
-#pragma unroll
-      for (int u = 0; u < PV; ++u) {
-        const int e = (tid + u * kThreads) * 4;
-        const int jj = e / D, d = e % D, j = j0 + jj;
-        kq[u] = vq[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < p.Lk) {
-          kq[u] = *reinterpret_cast<const float4 *>(kb + (int64_t)j * p.ks[2] + d);
-          vq[u] = *reinterpret_cast<const float4 *>(vb + (int64_t)j * p.vs[2] + d);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < PV; ++u) {
-        const int e = (tid + u * kThreads) * 4;
-        const int jj = e / D, d = e % D;
-        const int off = jj * RF + (d / DH) * (DH + 4) + d % DH;
-        *reinterpret_cast<float4 *>(ks + off) = kq[u];
-        *reinterpret_cast<float4 *>(vs + off) = vq[u];
-      }
-    }
-    __syncthreads();
-
-    float s[kKeys];
-    float mt = -INFINITY;
-#pragma unroll
-    for (int jj = 0; jj < kKeys; ++jj) {
-      const float4 *kr = reinterpret_cast<const float4 *>(ks + jj * RF + part * (DH + 4));
-      float acc = 0.f;
-#pragma unroll
-      for (int d4 = 0; d4 < DH / 4; ++d4) {
-        const float4 kv = kr[d4];
-        acc = fmaf(q[4 * d4], kv.x, acc);
-        acc = fmaf(q[4 * d4 + 1], kv.y, acc);
-        acc = fmaf(q[4 * d4 + 2], kv.z, acc);
-        acc = fmaf(q[4 * d4 + 3], kv.w, acc);
-      }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      const bool al = (mw[jj >> 5] >> (jj & 31)) & 1u;
-      s[jj] = al ? acc : -INFINITY;
-      mt = fmaxf(mt, s[jj]);
-    }
-    const float m_new = fmaxf(m, mt);
-    if (m_new != -INFINITY) {
-      const float corr = exp2f(m - m_new);  // m == -inf gives 0
-      l *= corr;
-#pragma unroll
-      for (int d = 0; d < DH; ++d) o[d] *= corr;
+    // (also the barrier after which every thread's copies of this tile are visible)
+    if (__syncthreads_or(any != 0u)) {  // an empty tile is fetched ahead but never computed
+      const float *ks = buf_k(bf), *vs = buf_v(bf);
+      float s[kKeys];
+      float mt = -INFINITY;
 #pragma unroll
       for (int jj = 0; jj < kKeys; ++jj) {
-        const float pj = exp2f(s[jj] - m_new);  // masked: exp2(-inf) = 0
-        l += pj;
-        const float4 *vr = reinterpret_cast<const float4 *>(vs + jj * RF + part * (DH + 4));
+        const float4 *kr = reinterpret_cast<const float4 *>(ks + jj * RF + part * (DH + 4));
+        float acc = 0.f;
 #pragma unroll
         for (int d4 = 0; d4 < DH / 4; ++d4) {
-          const float4 vv = vr[d4];
-          o[4 * d4] = fmaf(pj, vv.x, o[4 * d4]);
-          o[4 * d4 + 1] = fmaf(pj, vv.y, o[4 * d4 + 1]);
-          o[4 * d4 + 2] = fmaf(pj, vv.z, o[4 * d4 + 2]);
-          o[4 * d4 + 3] = fmaf(pj, vv.w, o[4 * d4 + 3]);
+          const float4 kv = kr[d4];
+          acc = fmaf(q[4 * d4], kv.x, acc);
+          acc = fmaf(q[4 * d4 + 1], kv.y, acc);
+          acc = fmaf(q[4 * d4 + 2], kv.z, acc);
+          acc = fmaf(q[4 * d4 + 3], kv.w, acc);
         }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        const bool al = (mw[jj >> 5] >> (jj & 31)) & 1u;
+        s[jj] = al ? acc : -INFINITY;
+        mt = fmaxf(mt, s[jj]);
       }
-      m = m_new;
+      const float m_new = fmaxf(m, mt);
+      if (m_new != -INFINITY) {
+        const float corr = exp2f(m - m_new);  // m == -inf gives 0
+        l *= corr;
+#pragma unroll
+        for (int d = 0; d < DH; ++d) o[d] *= corr;
+#pragma unroll
+        for (int jj = 0; jj < kKeys; ++jj) {
+          const float pj = exp2f(s[jj] - m_new);  // masked: exp2(-inf) = 0
+          l += pj;
+          const float4 *vr = reinterpret_cast<const float4 *>(vs + jj * RF + part * (DH + 4));
+#pragma unroll
+          for (int d4 = 0; d4 < DH / 4; ++d4) {
+            const float4 vv = vr[d4];
+            o[4 * d4] = fmaf(pj, vv.x, o[4 * d4]);
+            o[4 * d4 + 1] = fmaf(pj, vv.y, o[4 * d4 + 1]);
+            o[4 * d4 + 2] = fmaf(pj, vv.z, o[4 * d4 + 2]);
+            o[4 * d4 + 3] = fmaf(pj, vv.w, o[4 * d4 + 3]);
+          }
+        }
+        m = m_new;
+      }
     }
-    __syncthreads();
+    __syncthreads();  // this buffer is refilled two tiles later
+#pragma unroll
+    for (int w = 0; w < kKeys / 32; ++w) mw[w] = mwn[w];
   }
 
   if (row_ok) {
@@ -171,7 +187,7 @@ prefill_simt_kernel(const __grid_constant__ SimtParams p) {
 template <typename T, int D>
 mgqa_status launch_t(const SimtParams &p, cudaStream_t s) {
   auto kern = prefill_simt_kernel<T, D>;
-  const size_t smem = 2 * kKeys * row_floats<D>() * sizeof(float);
+  const size_t smem = 2 * 2 * kKeys * row_floats<D>() * sizeof(float);  // two K/V buffers
   static std::atomic<uint64_t> attr_done{0};
   const mgqa_status st = ensure_smem_attr(kern, (int)smem, attr_done, "fp32 prefill kernel");
   if (st != MGQA_OK) return st;
