@@ -205,6 +205,20 @@ def test_random_cases_fp32(M, oracle_mod, mask, case):
     assert_lse_close(lse, ref_lse, 1e-5)
 
 
+@pytest.mark.parametrize("mask", ["none", "kvlen", "bits+kvlen"])
+@pytest.mark.parametrize("case", [(1, 2, 1, 33, 37, 64), (2, 2, 2, 64, 64, 128), (1, 4, 2, 1, 65, 64),
+                                  (2, 2, 1, 97, 191, 128)], ids=lambda c: "x".join(map(str, c)))
+def test_fp32_key_tile_edges(M, oracle_mod, mask, case):
+    """The fp32 kernel's double-buffered 64-key tiles at their edges: one
+    partial tile, exactly one full tile, one full tile and one key, a ragged
+    third tile; with key lengths that empty whole tiles of some rows."""
+    wl = W.random_case(sum(case) + 7, *case, dtype=torch.float32, mask=mask)
+    out, lse = run_prefill(M, wl)
+    ref, ref_lse = oracle(oracle_mod, wl)
+    assert_close_to_oracle(out, ref, torch.float32, f"fp32 {mask} {case}")
+    assert_lse_close(lse, ref_lse, 1e-5)
+
+
 def test_gqa_equals_repeated_heads(M):
     wl = W.random_case(5, 2, 8, 2, 200, 333, 128, dtype=torch.bfloat16, mask="bits")
     o1, l1 = run_prefill(M, wl)
