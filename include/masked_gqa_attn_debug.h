@@ -76,6 +76,19 @@ MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas);
  * Reading clears the record. Synchronous. */
 MGQA_API mgqa_status mgqa_debug_prefill_timeline(uint64_t *out, int32_t n_ctas);
 
+/* Per-key-tile event trace of the first n_ctas (<= 4) CTAs of the
+ * tensor-core prefill launches since the previous read, in launch order (x
+ * fastest), as written by the most recent launch: 64 tiles x 18 values per
+ * CTA (the SM clock), for the CTA's n-th non-empty key tile n < 64. Events
+ * 2t and 2t+1: the MMA warp begins issuing / has committed S_t(n) = Q_t K^T
+ * (head t); 4+2t and 5+2t: the same for O_t += P_t(n) V(n); 8+4t: softmax
+ * warpgroup t sees S_t(n) complete (its first warp); 9+4t: every warp of it
+ * has read the scores; 10+4t: the first warp's exponentials are done; 11+4t:
+ * every warp has handed P_t(n) over; 16 / 17: the producer has issued the
+ * loads of K(n) / V(n). An event not reached reads 0. Reading clears the
+ * record. Synchronous. */
+MGQA_API mgqa_status mgqa_debug_prefill_trace(uint64_t *out, int32_t n_ctas);
+
 #ifdef __cplusplus
 }
 #endif

@@ -62,6 +62,7 @@ DEBUG_SYMBOLS = (
     "mgqa_debug_inject_prefill_stall",
     "mgqa_debug_decode_timeline",
     "mgqa_debug_prefill_timeline",
+    "mgqa_debug_prefill_trace",
 )
 DEBUG_NUM_COUNTERS = 4
 
@@ -191,6 +192,8 @@ def debug_lib() -> ctypes.CDLL:
         L.mgqa_debug_decode_timeline.restype = ctypes.c_int
         L.mgqa_debug_prefill_timeline.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
         L.mgqa_debug_prefill_timeline.restype = ctypes.c_int
+        L.mgqa_debug_prefill_trace.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.c_int32]
+        L.mgqa_debug_prefill_trace.restype = ctypes.c_int
         _lib_debug = L
     return _lib_debug
 

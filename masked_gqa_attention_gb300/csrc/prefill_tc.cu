@@ -90,8 +90,29 @@ MGQA_DEV void pre_stamp(int k) {  // by the one thread that owns stamp k
   }
   if (k == 7) g_pre_tl[cta][14] = globaltimer_ns();
 }
+// per-tile event trace of the first CTAs (SM clock), read with
+// mgqa_debug_prefill_trace: for the n-th non-empty key tile, 2t / 2t+1 = the
+// MMA warp begins issuing / has committed S_t(n), 4+2t / 5+2t = the same for
+// O_t += P_t(n) V(n), 8+4t = softmax t sees S_t(n) (its first warp), 9+4t =
+// every warp has read it, 10+4t = the first warp's exponentials are done,
+// 11+4t = every warp has handed P_t(n) over; 16 / 17 = the producer has
+// issued K(n) / V(n)
+constexpr int kTrCtas = 4, kTrTiles = 64, kTrEvents = 18;
+__device__ unsigned long long g_pre_tr[kTrCtas][kTrTiles][kTrEvents];
+MGQA_DEV unsigned long long *tr_slot(int n, int ev) {
+  const unsigned cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  return (cta < (unsigned)kTrCtas && n < kTrTiles) ? &g_pre_tr[cta][n][ev] : nullptr;
+}
+MGQA_DEV void tr_stamp(int n, int ev) {
+  if (unsigned long long *s = tr_slot(n, ev)) *s = clock64();
+}
+MGQA_DEV void tr_stamp_max(int n, int ev) {  // the latest of several warps
+  if (unsigned long long *s = tr_slot(n, ev)) atomicMax(s, (unsigned long long)clock64());
+}
 #else
 MGQA_DEV void pre_stamp(int) {}
+MGQA_DEV void tr_stamp(int, int) {}
+MGQA_DEV void tr_stamp_max(int, int) {}
 MGQA_DEV uint64_t wait_limit() { return kWaitLimitNs; }
 MGQA_DEV int fault_tile() { return -1; }
 MGQA_DEV void dbg_count(int, unsigned long long = 1ull) {}
@@ -262,7 +283,7 @@ MGQA_DEV void rope_q_row(unsigned char *tile, int r, int pos, const FusedRope &r
 // PARTIAL: mw holds the row's allowed-key bits.
 template <typename T, int D, bool NEG, bool PARTIAL>
 MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN / 32], float sl2,
-                           float &m_used, float &l) {
+                           float &m_used, float &l, int n, int tr) {
   constexpr float MV = NEG ? INFINITY : -INFINITY;
   uint32_t sr[BN];
   float mr;
@@ -274,6 +295,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
       tc::tmem_ld32_red<!NEG>(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]),
                               red[c]);
     tc::tmem_wait_ld();
+    if (tr >= 0) tr_stamp_max(n, (tr & 0xff) + 1);
     mr = NEG ? fminf(fminf(red[0], red[1]), fminf(red[2], red[3]))
              : fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   } else {
@@ -281,6 +303,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
     for (int c = 0; c < BN / 32; ++c)
       tc::tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
     tc::tmem_wait_ld();
+    if (tr >= 0) tr_stamp_max(n, (tr & 0xff) + 1);
     float mx[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) mx[k] = MV;
@@ -354,6 +377,7 @@ MGQA_DEV void softmax_tile(uint32_t t_s, uint32_t t_o, const uint32_t (&mw)[BN /
   float s0, s1;
   tc::upk2(acc[0], s0, s1);
   l += s0 + s1;
+  if (tr >= 0 && (tr >> 8) == 0) tr_stamp(n, (tr & 0xff) + 2);
   tc::tmem_wait_st();
 }
 
@@ -697,12 +721,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (n >= STAGES && !(ok = mbar_wait(bar_kempty + st, (use - 1) & 1, p.err, lim))) break;
         mbar_arrive_expect_tx(bar_kfull + st, KB * BOX);
         k_issued = n + 1;
+        tr_stamp(n, 16);
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::k_off + (st * KB + c) * BOX, &tm_k, c * 64, kt * BN, g, b,
                           bar_kfull + st);
         if (n >= STAGES && !(ok = mbar_wait(bar_vempty + st, (use - 1) & 1, p.err, lim))) break;
         mbar_arrive_expect_tx(bar_vfull + st, KB * BOX);
         v_issued = n + 1;
+        tr_stamp(n, 17);
         for (int c = 0; c < KB; ++c)
           tc::tma_load_4d(smem + Lay::v_off + (st * KB + c) * BOX, &tm_v, c * 64, kt * BN, g, b,
                           bar_vfull + st);
@@ -799,7 +825,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // a fused rotary embedding rewrites the query tile first
         if (ROPE && !wait(bar_qrot + t, 0)) break;
         tc::fence_after_sync();
+        if (leader) tr_stamp(0, 2 * t);
         issue_s(t, 0, 0, D / 16);
+        if (leader) tr_stamp(0, 2 * t + 1);
       }
       if (lane == 0) pre_stamp(3);
       // The MMA queue is shallow: an issuing thread stalls in it until the
@@ -819,6 +847,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int t = 0; t < NT && ok; ++t) {
           if (!(t == 0 ? p0_seen : p1_seen) && !wait(bar_pfull + t, n & 1)) break;
           tc::fence_after_sync();
+          if (leader) tr_stamp(n, 4 + 2 * t);
           issue_pv(t, st, 0, kHalfPV, n == 0);
           if (has_next) {  // K(n+1) before head 0's S(n+1), V(n+1) before the next P.V
             if (t == 0 && !wait(bar_kfull + st1, par(st1, use1))) break;
@@ -830,9 +859,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (n == nk - 1 && t == NT - 1) pre_stamp(8);
             if (n == nk - 1) tc::mma_commit(bar_odone + t);  // read by the epilogue only
             if (t == NT - 1) tc::mma_commit(bar_vempty + st);
+            tr_stamp(n, 5 + 2 * t);
           }
           __syncwarp();
           if (has_next) {
+            if (leader) tr_stamp(n + 1, 2 * t);
             if (NT > 1 && t == NT - 1) {
               issue_s(t, st1, 0, kLateS);
               // a probe, not a wait: P_0(n+1) needs the softmax of head 0,
@@ -846,6 +877,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             } else {
               issue_s(t, st1, 0, D / 16);
             }
+            if (leader) tr_stamp(n + 1, 2 * t + 1);
           }
         }
       }
@@ -896,6 +928,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const bool neg = p.scale_log2 < 0.f;
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
+    const int tr = (lane == 0) ? ((8 + 4 * t) | (quarter << 8)) : -1;  // debug trace events
     for (int n = 0; n < nk; ++n) {
       const int ent = list[n];
       const int kt = ent & 0x7fff;
@@ -907,19 +940,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (ok) ok = mbar_wait(bar_sfull + t, n & 1, p.err, lim);
       ok = __all_sync(0xffffffffu, ok);
       if (n == 0 && t == 0 && tid == 128) pre_stamp(10);
+      if (tr >= 0 && quarter == 0) tr_stamp(n, 8 + 4 * t);
       if (ok) {  // after a failed wait, tensor memory is left alone
         tc::fence_after_sync();
         if (neg) {
-          if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l);
-          else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l);
+          if (partial) softmax_tile<T, D, true, true>(t_s, t_o, mw, sl2, m_used, l, n, tr);
+          else softmax_tile<T, D, true, false>(t_s, t_o, mw, sl2, m_used, l, n, tr);
         } else {
-          if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l);
-          else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l);
+          if (partial) softmax_tile<T, D, false, true>(t_s, t_o, mw, sl2, m_used, l, n, tr);
+          else softmax_tile<T, D, false, false>(t_s, t_o, mw, sl2, m_used, l, n, tr);
         }
         if (lane == 0) dbg_count(1);  // debug library: tiles processed (per warp)
         tc::fence_before_sync();
       }
       mbar_arrive(bar_pfull + t);
+      if (tr >= 0) tr_stamp_max(n, 11 + 4 * t);
       if (n == 0 && t == 0 && tid == 128) pre_stamp(4);
     }
     // epilogue: O / l -> bf16, staged in this head's Q buffer (free once its
@@ -1132,6 +1167,20 @@ extern "C" MGQA_API mgqa_status mgqa_debug_prefill_timeline(uint64_t *out, int32
   static const unsigned long long zeros[kPreTlCtas][kPreTlStamps] = {};
   e = cudaMemcpyToSymbol(g_pre_tl, zeros, sizeof(zeros));
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "clearing the timeline: %s", cudaGetErrorString(e));
+  return MGQA_OK;
+}
+
+extern "C" MGQA_API mgqa_status mgqa_debug_prefill_trace(uint64_t *out, int32_t n_ctas) {
+  using namespace mgqa;
+  clear_error_detail();
+  if (!out || n_ctas < 0 || n_ctas > kTrCtas)
+    return fail(MGQA_ERR_INVALID_ARG, "mgqa_debug_prefill_trace: bad output or count");
+  const size_t per_cta = (size_t)kTrTiles * kTrEvents * sizeof(uint64_t);
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_pre_tr, (size_t)n_ctas * per_cta);
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "reading the trace: %s", cudaGetErrorString(e));
+  static const unsigned long long zeros[kTrCtas][kTrTiles][kTrEvents] = {};
+  e = cudaMemcpyToSymbol(g_pre_tr, zeros, sizeof(zeros));
+  if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "clearing the trace: %s", cudaGetErrorString(e));
   return MGQA_OK;
 }
 

@@ -145,6 +145,25 @@ def test_phase_timelines_are_ordered_and_cleared(M):
         assert (t[:, k1] >= t[:, k0]).all(), (k0, k1)
     assert (t[:, 14] >= t[:, 13]).all() and (t[:, 0] > 0).all()
     assert (_timeline(Ld.mgqa_debug_prefill_timeline, 128) == 0).all()
+    # per-tile trace of the first CTAs (8 non-empty key tiles each in row 0)
+    import numpy as np
+    buf = (ctypes.c_uint64 * (4 * 64 * 18))()
+    assert Ld.mgqa_debug_prefill_trace(buf, 4) == 0  # clear
+    _prefill(Ld, M, d, wl, err)
+    torch.cuda.synchronize()
+    assert Ld.mgqa_debug_prefill_trace(buf, 4) == 0
+    tr = np.array(buf, dtype=np.uint64).reshape(4, 64, 18).astype(np.int64)
+    nk = 8
+    # (key tile 0's loads go out before the producer loop: no issue stamps)
+    assert (tr[:, :nk, :16] > 0).all() and (tr[:, 1:nk, 16:] > 0).all() and (tr[:, nk:, :] == 0).all()
+    for t in range(2):
+        e = tr[:, :nk]
+        # same thread, or an MMA commit before the completion the softmax sees
+        assert (e[..., 2 * t] <= e[..., 2 * t + 1]).all() and (e[..., 4 + 2 * t] <= e[..., 5 + 2 * t]).all()
+        assert (e[..., 2 * t + 1] <= e[..., 8 + 4 * t]).all() and (e[..., 8 + 4 * t] <= e[..., 10 + 4 * t]).all()
+        assert (e[..., 8 + 4 * t] <= e[..., 9 + 4 * t]).all()
+    assert Ld.mgqa_debug_prefill_trace(buf, 4) == 0
+    assert (np.array(buf, dtype=np.uint64) == 0).all()
     # decode: the static-cache shape (16 splits x 2 head groups x 8 requests)
     wd = W.static_cache_decode(variant="span")
     dd = to_device(wd)
