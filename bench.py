@@ -531,38 +531,62 @@ def run_reference(args):
 
 def bench_dit_e2e(M, wl, dev, calls, steps, warmup, world):
     """Through the C ABI from pinned host buffers: every call of a step copies
-    its q/k/v and segment ids in and its output back out."""
+    its q/k/v and segment ids in and its output back out. The calls are
+    pipelined the way a throughput user would run them: two device input and
+    output sets; call i+1's inputs go in on a copy stream and call i-1's output
+    comes out on another while call i computes (events order each buffer's
+    reuse), so the host link and the kernel overlap. (Spreading each copy over
+    several copy streams measured no faster: the host link is the limit.)"""
     import ctypes
     host = {n: (getattr(wl, n).pin_memory() if getattr(wl, n) is not None else None)
             for n in ("q", "k", "v", "mask_bits", "kv_len", "seg_q", "seg_k")}
-    d = {n: (torch.empty_like(t, device=dev) if t is not None else None) for n, t in host.items()}
-    out = torch.empty_like(d["q"])
-    out_host = torch.empty_like(host["q"]).pin_memory()
-    a = make_args(M, d, out, wl)
+    sets = []
+    for _ in range(2):
+        d = {n: (torch.empty_like(t, device=dev) if t is not None else None) for n, t in host.items()}
+        out = torch.empty_like(d["q"])
+        sets.append({"d": d, "out": out, "args": make_args(M, d, out, wl),
+                     "out_host": torch.empty_like(host["q"]).pin_memory()})
     L = M.lib()
-    stream = torch.cuda.Stream(device=dev)
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("in", "run", "out")}
     h2d = calls * sum(t.numel() * t.element_size() for t in host.values() if t is not None)
-    d2h = calls * out_host.numel() * out_host.element_size()
+    d2h = calls * sets[0]["out_host"].numel() * sets[0]["out_host"].element_size()
 
     def step():
-        with torch.cuda.stream(stream):
-            for _ in range(calls):
+        for i in range(calls):
+            b = i % 2
+            st = sets[b]
+            with torch.cuda.stream(s_in):  # inputs of call i, once call i-2 has read this set
+                s_in.wait_event(ev["run"][b])
                 for n, t in host.items():
                     if t is not None:
-                        d[n].copy_(t, non_blocking=True)
-                st = L.masked_gqa_attn_prefill(ctypes.byref(a), stream.cuda_stream)
-                if st != 0:
-                    raise RuntimeError(L.mgqa_last_error_detail())
-                out_host.copy_(out, non_blocking=True)
+                        st["d"][n].copy_(t, non_blocking=True)
+                ev["in"][b].record(s_in)
+            s_run.wait_event(ev["in"][b])
+            s_run.wait_event(ev["out"][b])  # call i-2's output has left this set
+            rc = L.masked_gqa_attn_prefill(ctypes.byref(st["args"]), s_run.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(L.mgqa_last_error_detail())
+            ev["run"][b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["run"][b])
+                st["out_host"].copy_(st["out"], non_blocking=True)
+                ev["out"][b].record(s_out)
 
+    main = torch.cuda.current_stream(dev)
     for _ in range(warmup):
         step()
+    torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(main)
+    for s in (s_in, s_run, s_out):
+        s.wait_event(e0)
     for _ in range(steps):
         step()
-    e1.record(stream)
+    for s in (s_in, s_run, s_out):
+        main.wait_stream(s)
+    e1.record(main)
     torch.cuda.synchronize()
     barrier(world)
     return e0.elapsed_time(e1) / 1e3, h2d, d2h
