@@ -371,40 +371,56 @@ def bench_decode(M, wl, dev, steps, warmup, world, nsets=DECODE_SETS, calls=16):
 
 def bench_decode_e2e(M, wl, dev, steps, warmup, world):
     """Per step: H2D of the new query and lengths, one decode call, D2H of the
-    output (the cache stays resident, as a static KV cache does)."""
+    output (the cache stays resident, as a static KV cache does). Steps run one
+    after another, as a token loop's do. The query and the lengths travel in
+    one pinned buffer (one copy), and the step is captured once in a CUDA
+    graph, as the pages' decode loop is."""
     import ctypes
     d = device_inputs(wl, dev)
-    hq = wl.q.pin_memory()
-    hl = wl.kv_len.pin_memory() if wl.kv_len is not None else None
+    qb = wl.q.numel() * wl.q.element_size()
+    nl = wl.kv_len.numel() if wl.kv_len is not None else 0
+    # [q bytes | kv_len bytes] on the host (pinned) and on the device
+    hbuf = torch.empty(qb + 4 * nl, dtype=torch.uint8).pin_memory()
+    hbuf[:qb].copy_(wl.q.contiguous().view(-1).view(torch.uint8))
+    if nl:
+        hbuf[qb:].copy_(wl.kv_len.contiguous().view(-1).view(torch.uint8))
+    dbuf = torch.empty(qb + 4 * nl, dtype=torch.uint8, device=dev)
+    d["q"] = dbuf[:qb].view(wl.q.dtype).view(wl.q.shape)
+    if nl:
+        d["kv_len"] = dbuf[qb:].view(torch.int32).view(wl.kv_len.shape)
     out = torch.empty_like(d["q"])
-    oh = torch.empty_like(hq).pin_memory()
+    oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     a = make_args(M, d, out, wl)
-    masks = {n: d[n] for n in ("mask_bits", "kv_len", "seg_q", "seg_k")}
     L = M.lib()
     stream = torch.cuda.Stream(device=dev)
 
     def step():
-        with torch.cuda.stream(stream):
-            d["q"].copy_(hq, non_blocking=True)
-            if hl is not None:
-                d["kv_len"].copy_(hl, non_blocking=True)
-            st = L.masked_gqa_attn_decode(ctypes.byref(a), None, 0, stream.cuda_stream)
-            if st != 0:
-                raise RuntimeError(L.mgqa_last_error_detail())
-            oh.copy_(out, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
+        st = L.masked_gqa_attn_decode(ctypes.byref(a), None, 0, stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(L.mgqa_last_error_detail())
+        oh.copy_(out, non_blocking=True)
 
-    for _ in range(warmup):
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
         step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        step()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
     torch.cuda.synchronize()
-    h2d = hq.numel() * hq.element_size() + (hl.numel() * 4 if hl is not None else 0)
-    d2h = oh.numel() * oh.element_size()
-    return e0.elapsed_time(e1) / 1e3 / steps, h2d, d2h
+    return e0.elapsed_time(e1) / 1e3 / steps, qb + 4 * nl, oh.numel() * oh.element_size()
 
 
 def traffic_from_profiles(kernel_file: str, workload: str = None):
