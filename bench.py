@@ -217,40 +217,49 @@ def bench_prefill_graph(M, wl, dev, calls, nsets, steps, warmup, world):
 def bench_rope(M, dev, reps=20, warmup=3, nsets=12):
     """Rotary embedding of the headline shapes' q [2,16,1024,128] and
     k [2,8,1024,128] (bf16, full rotary dim, positions = row index); one call =
-    q then k of one of `nsets` rotating sets. One pass over the sets is
-    captured in a CUDA graph (no host launch cost in the timed region) and
-    replayed. Returns (seconds per call, algorithmic bytes per call: every
-    rotated element read and written, plus the frequency table)."""
+    q and k of one of `nsets` rotating sets, rotated by one masked_gqa_rope_pair
+    launch (and, for comparison, by two masked_gqa_rope calls). One pass over
+    the sets is captured in a CUDA graph (no host launch cost in the timed
+    region) and replayed. Returns (seconds per call with the pair launch,
+    seconds per call with two calls, algorithmic bytes per call: every rotated
+    element read and written, plus the frequency table)."""
     import torch
     g = torch.Generator(device="cpu").manual_seed(1006)
     sets = [(torch.randn(2, 16, 1024, 128, generator=g).to(torch.bfloat16).to(dev),
              torch.randn(2, 8, 1024, 128, generator=g).to(torch.bfloat16).to(dev)) for _ in range(nsets)]
     f = (10000.0 ** (-torch.arange(0, 128, 2, dtype=torch.float64) / 128)).to(torch.float32).to(dev)
 
-    def one_pass():
-        for q, k in sets:
-            M.masked_gqa_rope(q, f)
-            M.masked_gqa_rope(k, f)
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        one_pass()  # warm-up and lazy set-up outside the capture
-    torch.cuda.current_stream().wait_stream(s)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        one_pass()
-    for _ in range(warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        graph.replay()
-    e1.record()
-    torch.cuda.synchronize()
+    def time_pass(pair):
+        def one_pass():
+            for q, k in sets:
+                if pair:
+                    M.masked_gqa_rope_pair(q, k, f)
+                else:
+                    M.masked_gqa_rope(q, f)
+                    M.masked_gqa_rope(k, f)
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            one_pass()  # warm-up and lazy set-up outside the capture
+        torch.cuda.current_stream().wait_stream(s)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one_pass()
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / (reps * nsets)
+
+    t_pair, t_two = time_pass(True), time_pass(False)
     q, k = sets[0]
     nbytes = 2 * (q.numel() + k.numel()) * q.element_size() + f.numel() * 4
-    return e0.elapsed_time(e1) / 1e3 / (reps * nsets), nbytes
+    return t_pair, t_two, nbytes
 
 
 def time_calls(fn, reps=20, warmup=3):
@@ -749,11 +758,12 @@ def run_gpu(args):
 
     # ---- rotary embedding of the padded-CFG q and k
     clocks.start()
-    t_rope, b_rope = bench_rope(M, dev)
+    t_rope, t_rope2, b_rope = bench_rope(M, dev)
     ck = clocks.stop()
     configs["rope_qk"] = {"workload": "rotary embedding of q [2,16,1024,128] and k [2,8,1024,128], "
-                                      "bf16, 12 rotating sets (144 MB > L2)",
-                          "us_per_call": t_rope * 1e6, "value": b_rope / t_rope / 1e9, "unit": "GB/s",
+                                      "bf16, 12 rotating sets (144 MB > L2); one pair launch per call",
+                          "us_per_call": t_rope * 1e6, "two_calls_us": t_rope2 * 1e6,
+                          "value": b_rope / t_rope / 1e9, "unit": "GB/s",
                           "roofline": {"bound": "hbm", "achieved": b_rope / t_rope / 1e9, "peak": hbm,
                                        "unit": "GB/s", "frac": b_rope / t_rope / 1e9 / hbm,
                                        "traffic": traffic_from_profiles("rope.cu"),

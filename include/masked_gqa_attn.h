@@ -54,7 +54,7 @@
 extern "C" {
 #endif
 
-#define MGQA_ABI_VERSION 5
+#define MGQA_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define MGQA_API __attribute__((visibility("default")))
@@ -238,6 +238,17 @@ typedef struct {
  * nothing, never synchronises; MGQA_OK once the kernel is enqueued. All
  * pointers are caller-owned device memory. */
 MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *args, cudaStream_t stream);
+
+/* q and k of one layer rotated by one launch: the same results, bit for bit,
+ * as masked_gqa_rope(q) followed by masked_gqa_rope(k). Each tensor has its
+ * own arguments (shape, strides, heads, norm weight, positions, table); both
+ * must have the same dtype. When the two take different kernels (for
+ * instance one with a norm weight and one without, or one with 16-byte rows
+ * and one without), or their elements overlap, the call makes one launch
+ * each, in that order. Errors as masked_gqa_rope (the detail names q or k);
+ * nothing is enqueued when either tensor's arguments are rejected. */
+MGQA_API mgqa_status masked_gqa_rope_pair(const mgqa_rope_args *q, const mgqa_rope_args *k,
+                                          cudaStream_t stream);
 
 /* The rotary embedding (and optional RMS normalisation) applied INSIDE an
  * attention call, to the query rows as they are loaded and, for the fused

@@ -34,6 +34,7 @@ __all__ = [
     "masked_gqa_attn_decode_append", "masked_gqa_pack_pair", "masked_gqa_unpack_pair",
     "debug_lib", "MGQA_ERR_DEVICE_CHECK", "MgqaQkRope", "make_qk_rope",
     "masked_gqa_attn_prefill_rope", "masked_gqa_attn_decode_append_rope", "masked_gqa_rope",
+    "masked_gqa_rope_pair",
 ]
 
 (MGQA_OK, MGQA_ERR_INVALID_ARG, MGQA_ERR_UNSUPPORTED, MGQA_ERR_CUDA, MGQA_ERR_TIMEOUT,
@@ -54,6 +55,7 @@ EXPORTED_SYMBOLS = (
     "masked_gqa_rope",
     "masked_gqa_attn_prefill_rope",
     "masked_gqa_attn_decode_append_rope",
+    "masked_gqa_rope_pair",
 )
 # exported by the debug library only (include/masked_gqa_attn_debug.h)
 DEBUG_SYMBOLS = (
@@ -152,6 +154,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.masked_gqa_attn_decode_static.restype = ctypes.c_int
     L.masked_gqa_rope.argtypes = [ctypes.POINTER(MgqaRopeArgs), P]
     L.masked_gqa_rope.restype = ctypes.c_int
+    L.masked_gqa_rope_pair.argtypes = [ctypes.POINTER(MgqaRopeArgs), ctypes.POINTER(MgqaRopeArgs), P]
+    L.masked_gqa_rope_pair.restype = ctypes.c_int
     L.mgqa_abi_version.argtypes = []
     L.mgqa_abi_version.restype = ctypes.c_int32
     L.masked_gqa_attn_prefill_rope.argtypes = [ctypes.POINTER(MgqaArgs), ctypes.POINTER(MgqaQkRope), P]
@@ -415,15 +419,7 @@ def masked_gqa_unpack_pair(packed, La, *, stream=None):
     return a, b
 
 
-def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, interleaved=False,
-                    norm_weight=None, norm_eps=1e-6, stream=None):
-    """Rotate x [B, H, L, D] (bf16, fp16 or fp32, head dim contiguous) in place by
-    rotary position embedding and return it: theta = fl32(position * inv_freq[i])
-    for pair i of the first rot_dim features (default D) of the first `heads`
-    heads (default H); positions int32 [B, L] (default: the row index);
-    inv_freq fp32 [rot_dim / 2]; interleaved pairs (2i, 2i+1) or half-split
-    pairs (i, i + rot_dim/2). norm_weight (fp32 [D], optional): RMS-normalise
-    each rotated head vector over its D features before the rotation."""
+def _rope_args(x, inv_freq, positions, rot_dim, heads, interleaved, norm_weight, norm_eps):
     _dev(x, "x")
     B, H, L, D = x.shape
     if x.stride(3) != 1:
@@ -451,8 +447,34 @@ def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, in
             raise ValueError(f"norm_weight must be a contiguous fp32 tensor of {D} values")
         a.norm_weight = norm_weight.data_ptr()
         a.norm_eps = float(norm_eps)
+    return a
+
+
+def masked_gqa_rope(x, inv_freq, *, positions=None, rot_dim=None, heads=None, interleaved=False,
+                    norm_weight=None, norm_eps=1e-6, stream=None):
+    """Rotate x [B, H, L, D] (bf16, fp16 or fp32, head dim contiguous) in place by
+    rotary position embedding and return it: theta = fl32(position * inv_freq[i])
+    for pair i of the first rot_dim features (default D) of the first `heads`
+    heads (default H); positions int32 [B, L] (default: the row index);
+    inv_freq fp32 [rot_dim / 2]; interleaved pairs (2i, 2i+1) or half-split
+    pairs (i, i + rot_dim/2). norm_weight (fp32 [D], optional): RMS-normalise
+    each rotated head vector over its D features before the rotation."""
+    a = _rope_args(x, inv_freq, positions, rot_dim, heads, interleaved, norm_weight, norm_eps)
     _check(lib().masked_gqa_rope(ctypes.byref(a), _stream_handle(stream)))
     return x
+
+
+def masked_gqa_rope_pair(q, k, inv_freq, *, positions=None, rot_dim=None, q_heads=None,
+                         k_heads=None, interleaved=False, q_norm_weight=None, k_norm_weight=None,
+                         norm_eps=1e-6, stream=None):
+    """Rotate q and k (same dtype; [B, H, L, D] each, head dim contiguous) in
+    place with one launch, as masked_gqa_rope(q, ...) then masked_gqa_rope(k,
+    ...) would (same bits): the same table and positions, each its own head
+    count (default all) and optional norm weight. Returns (q, k)."""
+    aq = _rope_args(q, inv_freq, positions, rot_dim, q_heads, interleaved, q_norm_weight, norm_eps)
+    ak = _rope_args(k, inv_freq, positions, rot_dim, k_heads, interleaved, k_norm_weight, norm_eps)
+    _check(lib().masked_gqa_rope_pair(ctypes.byref(aq), ctypes.byref(ak), _stream_handle(stream)))
+    return q, k
 
 
 def make_qk_rope(inv_freq, D, *, positions=None, rot_dim=None, interleaved=False, q_heads,

@@ -71,8 +71,8 @@ MGQA_DEV void store_pair(T *r, int e0, int e1, float a, float c) {
 }
 
 template <typename T, bool PAIRED>
-__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeParams p) {
-  const int64_t idx = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x;
+MGQA_DEV void rope_body(const RopeParams &p, int64_t blk) {
+  const int64_t idx = blk * kRopeThreads + threadIdx.x;
   const int64_t total = (int64_t)p.B * p.L * p.half;
   if (idx >= total) return;
   const int i = (int)(idx % p.half);
@@ -124,12 +124,12 @@ template <typename T> MGQA_DEV uint4 vec_from_float(const float (&f)[16 / sizeof
 }
 
 template <typename T, bool INTER>
-__global__ void __launch_bounds__(kRopeThreads) rope_vec_kernel(const __grid_constant__ RopeParams p) {
+MGQA_DEV void rope_vec_body(const RopeParams &p, int64_t blk) {
   constexpr int EPV = 16 / sizeof(T);          // elements per vector
   constexpr int PPV = INTER ? EPV / 2 : EPV;   // pairs per vector (half-split: with its partner)
   const int nvec = INTER ? 2 * p.half / EPV : p.half / EPV;
   const int ngrp = (p.heads + kVecHeads - 1) / kVecHeads;
-  const int64_t idx = (int64_t)blockIdx.x * kRopeThreads + threadIdx.x;
+  const int64_t idx = blk * kRopeThreads + threadIdx.x;
   if (idx >= (int64_t)p.B * p.L * ngrp * nvec) return;
   const int v = (int)(idx % nvec);
   const int64_t r = idx / nvec;
@@ -191,11 +191,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_vec_kernel(const __grid_con
 // the D features, then the rotation of the first rot_dim; D <= 256.
 constexpr int kNormWarps = 8;
 template <typename T>
-__global__ void __launch_bounds__(32 * kNormWarps)
-rope_norm_kernel(const __grid_constant__ RopeParams p) {
+MGQA_DEV void rope_norm_body(const RopeParams &p, int64_t blk) {
   __shared__ float rowbuf[kNormWarps][256];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const int64_t task = (int64_t)blockIdx.x * kNormWarps + wl;  // (b, l, h) with h fastest
+  const int64_t task = blk * kNormWarps + wl;  // (b, l, h) with h fastest
   if (task >= (int64_t)p.B * p.L * p.heads) return;             // warp-uniform
   const int h = (int)(task % p.heads);
   const int64_t bl = task / p.heads;
@@ -228,15 +227,39 @@ rope_norm_kernel(const __grid_constant__ RopeParams p) {
   for (int d = 2 * p.half + lane; d < p.D; d += 32) row[d] = from_float<T>(buf[d]);
 }
 
+// Every kernel rotates one tensor (p1 unused, nb0 = the grid) or two in one
+// launch: blocks below nb0 take p0, the rest p1 (q and k of one layer).
+template <typename T, bool PAIRED>
+__global__ void __launch_bounds__(kRopeThreads)
+rope_kernel(const __grid_constant__ RopeParams p0, const __grid_constant__ RopeParams p1, unsigned nb0) {
+  if (blockIdx.x < nb0) rope_body<T, PAIRED>(p0, blockIdx.x);
+  else rope_body<T, PAIRED>(p1, blockIdx.x - nb0);
+}
+template <typename T, bool INTER>
+__global__ void __launch_bounds__(kRopeThreads)
+rope_vec_kernel(const __grid_constant__ RopeParams p0, const __grid_constant__ RopeParams p1, unsigned nb0) {
+  if (blockIdx.x < nb0) rope_vec_body<T, INTER>(p0, blockIdx.x);
+  else rope_vec_body<T, INTER>(p1, blockIdx.x - nb0);
+}
 template <typename T>
-mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
+__global__ void __launch_bounds__(32 * kNormWarps)
+rope_norm_kernel(const __grid_constant__ RopeParams p0, const __grid_constant__ RopeParams p1, unsigned nb0) {
+  if (blockIdx.x < nb0) rope_norm_body<T>(p0, blockIdx.x);
+  else rope_norm_body<T>(p1, blockIdx.x - nb0);
+}
+
+// The kernel a tensor takes, and its grid.
+enum class RopeKind { kNorm, kVecInter, kVecHalf, kScalarPaired, kScalar };
+struct RopePlan {
+  RopeKind kind;
+  int64_t blocks;
+};
+
+template <typename T>
+RopePlan plan_t(const RopeParams &p) {
   if (p.norm_w) {
     const int64_t tasks = (int64_t)p.B * p.L * p.heads;
-    const int64_t blocks = (tasks + kNormWarps - 1) / kNormWarps;
-    if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
-    const cudaError_t e = launch_pdl(rope_norm_kernel<T>, dim3((unsigned)blocks), dim3(32 * kNormWarps), 0, s, p);
-    if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
-    return MGQA_OK;
+    return {RopeKind::kNorm, (tasks + kNormWarps - 1) / kNormWarps};
   }
   // 16-byte vectors: aligned rows and a rotated span of whole vectors
   constexpr int EPV = 16 / (int)sizeof(T);
@@ -246,60 +269,98 @@ mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
   if (vec) {
     const int64_t nvec = p.interleaved ? 2 * p.half / EPV : p.half / EPV;
     const int64_t vtotal = (int64_t)p.B * p.L * ((p.heads + kVecHeads - 1) / kVecHeads) * nvec;
-    const int64_t vblocks = (vtotal + kRopeThreads - 1) / kRopeThreads;
-    if (vblocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
-    const cudaError_t e =
-        p.interleaved ? launch_pdl(rope_vec_kernel<T, true>, dim3((unsigned)vblocks), dim3(kRopeThreads), 0, s, p)
-                      : launch_pdl(rope_vec_kernel<T, false>, dim3((unsigned)vblocks), dim3(kRopeThreads), 0, s, p);
-    if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
-    return MGQA_OK;
+    return {p.interleaved ? RopeKind::kVecInter : RopeKind::kVecHalf,
+            (vtotal + kRopeThreads - 1) / kRopeThreads};
   }
   const int64_t total = (int64_t)p.B * p.L * p.half;
-  const int64_t blocks = (total + kRopeThreads - 1) / kRopeThreads;
-  if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
   // interleaved 16-bit pairs as 32-bit words: every row start 4-byte aligned
   const bool paired = sizeof(T) == 2 && p.interleaved &&
                       (reinterpret_cast<uintptr_t>(p.x) % 4) == 0 && p.s_b % 2 == 0 &&
                       p.s_h % 2 == 0 && p.s_l % 2 == 0;
-  const cudaError_t e =
-      paired ? launch_pdl(rope_kernel<T, sizeof(T) == 2>, dim3((unsigned)blocks), dim3(kRopeThreads), 0, s, p)
-             : launch_pdl(rope_kernel<T, false>, dim3((unsigned)blocks), dim3(kRopeThreads), 0, s, p);
+  return {paired ? RopeKind::kScalarPaired : RopeKind::kScalar, (total + kRopeThreads - 1) / kRopeThreads};
+}
+
+// One launch of kind k over grid blocks, the first nb0 of them for p0.
+template <typename T>
+mgqa_status launch_kind(RopeKind k, const RopeParams &p0, const RopeParams &p1, int64_t nb0,
+                        int64_t blocks, cudaStream_t s) {
+  if (blocks > 0x7fffffffLL) return fail(MGQA_ERR_UNSUPPORTED, "rope: too many rows");
+  const dim3 grid((unsigned)blocks);
+  const unsigned n0 = (unsigned)nb0;
+  cudaError_t e = cudaSuccess;
+  switch (k) {
+    case RopeKind::kNorm:
+      e = launch_pdl(rope_norm_kernel<T>, grid, dim3(32 * kNormWarps), 0, s, p0, p1, n0);
+      break;
+    case RopeKind::kVecInter:
+      e = launch_pdl(rope_vec_kernel<T, true>, grid, dim3(kRopeThreads), 0, s, p0, p1, n0);
+      break;
+    case RopeKind::kVecHalf:
+      e = launch_pdl(rope_vec_kernel<T, false>, grid, dim3(kRopeThreads), 0, s, p0, p1, n0);
+      break;
+    case RopeKind::kScalarPaired:
+      e = launch_pdl(rope_kernel<T, sizeof(T) == 2>, grid, dim3(kRopeThreads), 0, s, p0, p1, n0);
+      break;
+    case RopeKind::kScalar:
+      e = launch_pdl(rope_kernel<T, false>, grid, dim3(kRopeThreads), 0, s, p0, p1, n0);
+      break;
+  }
   if (e != cudaSuccess) return fail(MGQA_ERR_CUDA, "rope launch: %s", cudaGetErrorString(e));
   return MGQA_OK;
+}
+
+template <typename T>
+mgqa_status launch_t(const RopeParams &p, cudaStream_t s) {
+  const RopePlan pl = plan_t<T>(p);
+  return launch_kind<T>(pl.kind, p, p, pl.blocks, pl.blocks, s);
+}
+
+// Two tensors: one launch when they take the same kernel and their elements
+// do not overlap (overlapping ones are rotated one after the other, as two
+// calls would), else one launch each.
+template <typename T>
+mgqa_status launch_pair_t(const RopeParams &p0, const RopeParams &p1, bool disjoint, cudaStream_t s) {
+  const RopePlan a = plan_t<T>(p0), b = plan_t<T>(p1);
+  if (disjoint && a.kind == b.kind) return launch_kind<T>(a.kind, p0, p1, a.blocks, a.blocks + b.blocks, s);
+  const mgqa_status st = launch_kind<T>(a.kind, p0, p0, a.blocks, a.blocks, s);
+  if (st != MGQA_OK) return st;
+  return launch_kind<T>(b.kind, p1, p1, b.blocks, b.blocks, s);
 }
 
 }  // namespace
 }  // namespace mgqa
 
-extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStream_t stream) {
-  using namespace mgqa;
-  clear_error_detail();
-  if (!a) return fail(MGQA_ERR_INVALID_ARG, "args is null");
+namespace mgqa {
+namespace {
+
+// Host-side checks of one tensor's arguments; fills p.
+mgqa_status rope_params(const mgqa_rope_args *a, RopeParams &p, const char *what) {
+  if (!a) return fail(MGQA_ERR_INVALID_ARG, "%s: args is null", what);
   if (a->dtype != MGQA_BF16 && a->dtype != MGQA_FP16 && a->dtype != MGQA_FP32)
-    return fail(MGQA_ERR_INVALID_ARG, "rope: unknown dtype");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: unknown dtype", what);
   if (a->B < 1 || a->H < 1 || a->L < 1 || a->D < 2)
-    return fail(MGQA_ERR_INVALID_ARG, "rope: B, H, L must be >= 1 and D >= 2");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: B, H, L must be >= 1 and D >= 2", what);
   if (a->rot_dim < 2 || a->rot_dim > a->D || (a->rot_dim & 1))
-    return fail(MGQA_ERR_INVALID_ARG, "rope: rot_dim must be even and in [2, D]");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: rot_dim must be even and in [2, D]", what);
   if (a->heads < 1 || a->heads > a->H)
-    return fail(MGQA_ERR_INVALID_ARG, "rope: heads must be in [1, H]");
-  if (!a->x || !a->inv_freq) return fail(MGQA_ERR_INVALID_ARG, "rope: x or inv_freq is null");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: heads must be in [1, H]", what);
+  if (!a->x || !a->inv_freq) return fail(MGQA_ERR_INVALID_ARG, "%s: x or inv_freq is null", what);
   if (a->norm_weight && (a->D > 256 || !(a->norm_eps >= 0.f) || !std::isfinite(a->norm_eps) ||
                          reinterpret_cast<uintptr_t>(a->norm_weight) % 4 != 0))
-    return fail(MGQA_ERR_INVALID_ARG, "rope: the norm needs D <= 256, a finite eps >= 0 and an "
-                                      "aligned fp32 weight");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: the norm needs D <= 256, a finite eps >= 0 and an "
+                                      "aligned fp32 weight", what);
   const size_t es = a->dtype == MGQA_FP32 ? 4 : 2;
   if (reinterpret_cast<uintptr_t>(a->x) % es != 0 ||
       reinterpret_cast<uintptr_t>(a->inv_freq) % 4 != 0 ||
       (a->positions && reinterpret_cast<uintptr_t>(a->positions) % 4 != 0))
-    return fail(MGQA_ERR_INVALID_ARG, "rope: misaligned pointer");
+    return fail(MGQA_ERR_INVALID_ARG, "%s: misaligned pointer", what);
   // a zero stride over a dimension of extent > 1 would rotate shared elements
   // more than once (or from two threads at once)
   const int ext[3] = {a->B, a->H, a->L};
   for (int t = 0; t < 3; ++t)
     if (a->x_stride[t] < 0 || (a->x_stride[t] == 0 && ext[t] > 1))
-      return fail(MGQA_ERR_INVALID_ARG, "rope: stride %d must be positive", t);
-  RopeParams p{};
+      return fail(MGQA_ERR_INVALID_ARG, "%s: stride %d must be positive", what, t);
+  p = RopeParams{};
   p.x = a->x;
   p.s_b = a->x_stride[0]; p.s_h = a->x_stride[1]; p.s_l = a->x_stride[2];
   p.positions = a->positions;
@@ -308,7 +369,47 @@ extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStr
   p.interleaved = a->interleaved != 0;
   p.norm_w = a->norm_weight;
   p.eps = a->norm_eps;
+  return MGQA_OK;
+}
+
+// [first, last] byte addresses of the elements a tensor's view spans
+void rope_span(const mgqa_rope_args *a, uintptr_t &lo, uintptr_t &hi) {
+  const size_t es = a->dtype == MGQA_FP32 ? 4 : 2;
+  const int64_t last = (int64_t)(a->B - 1) * a->x_stride[0] + (int64_t)(a->H - 1) * a->x_stride[1] +
+                       (int64_t)(a->L - 1) * a->x_stride[2] + (a->D - 1);
+  lo = reinterpret_cast<uintptr_t>(a->x);
+  hi = lo + (uintptr_t)last * es + (es - 1);
+}
+
+}  // namespace
+}  // namespace mgqa
+
+extern "C" MGQA_API mgqa_status masked_gqa_rope(const mgqa_rope_args *a, cudaStream_t stream) {
+  using namespace mgqa;
+  clear_error_detail();
+  RopeParams p;
+  const mgqa_status st = rope_params(a, p, "rope");
+  if (st != MGQA_OK) return st;
   if (a->dtype == MGQA_BF16) return launch_t<__nv_bfloat16>(p, stream);
   if (a->dtype == MGQA_FP16) return launch_t<__half>(p, stream);
   return launch_t<float>(p, stream);
+}
+
+extern "C" MGQA_API mgqa_status masked_gqa_rope_pair(const mgqa_rope_args *q, const mgqa_rope_args *k,
+                                                     cudaStream_t stream) {
+  using namespace mgqa;
+  clear_error_detail();
+  RopeParams pq, pk;
+  mgqa_status st = rope_params(q, pq, "rope pair (q)");
+  if (st != MGQA_OK) return st;
+  st = rope_params(k, pk, "rope pair (k)");
+  if (st != MGQA_OK) return st;
+  if (q->dtype != k->dtype) return fail(MGQA_ERR_INVALID_ARG, "rope pair: q and k dtypes differ");
+  uintptr_t q0, q1, k0, k1;
+  rope_span(q, q0, q1);
+  rope_span(k, k0, k1);
+  const bool disjoint = q1 < k0 || k1 < q0;
+  if (q->dtype == MGQA_BF16) return launch_pair_t<__nv_bfloat16>(pq, pk, disjoint, stream);
+  if (q->dtype == MGQA_FP16) return launch_pair_t<__half>(pq, pk, disjoint, stream);
+  return launch_pair_t<float>(pq, pk, disjoint, stream);
 }

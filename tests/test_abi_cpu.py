@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(L):
     for name in declared_symbols():
         assert hasattr(L, name), name
-    assert L.mgqa_abi_version() == 5
+    assert L.mgqa_abi_version() == 6
     assert L.mgqa_status_string(M.MGQA_ERR_TIMEOUT) == b"device wait timed out"
     assert b"debug" in L.mgqa_status_string(M.MGQA_ERR_DEVICE_CHECK)
 

@@ -154,3 +154,63 @@ def test_rope_vector_and_scalar_paths_agree(M, oracle_mod, dtype, interleaved, r
     assert torch.equal(p[..., 0].cpu(), pad[..., 0]) and torch.equal(p[..., D + 1:].cpu(), pad[..., D + 1:])
     ref = oracle_mod.rope(x, inv_freq=f, positions=pos, rot_dim=rot, heads=heads, interleaved=interleaved)
     assert_close_to_oracle(a, ref, dtype, f"rope rot {rot}")
+
+
+PAIR_CASES = [  # q shape, k shape, rot_dim, q_heads, k_heads, q norm, k norm, k as a strided view
+    ((2, 16, 1024, 128), (2, 8, 1024, 128), 128, 16, 8, False, False, False),  # one vector launch
+    ((2, 16, 300, 128), (2, 8, 300, 128), 64, 16, 8, True, True, False),       # one norm launch
+    ((1, 4, 77, 64), (1, 2, 77, 64), 64, 4, 2, True, False, False),            # norm and vector: two
+    ((1, 4, 77, 64), (1, 2, 77, 66), 64, 3, 2, False, False, True),            # vector and scalar: two
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("interleaved", [True, False])
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: "x".join(map(str, c[0] + c[1])) + f"_{c[5]}{c[6]}{c[7]}")
+def test_rope_pair_equals_two_calls(M, dtype, interleaved, case):
+    """q and k in one launch (or two, when they take different kernels) give
+    the bits of masked_gqa_rope on q followed by masked_gqa_rope on k."""
+    qs, ks, rot, qh, kh, qn, kn, kview = case
+    f = inv_freq_table(rot).cuda()
+    g = torch.Generator().manual_seed(sum(qs) + sum(ks) + rot)
+    pos = torch.randint(0, 4096, (qs[0], qs[2]), generator=g, dtype=torch.int32).cuda()
+    q = make_x(11 + rot, *qs, dtype).cuda()
+    kfull = make_x(12 + rot, *ks, dtype).cuda()
+    k = kfull[..., :qs[3]] if kview else kfull  # a view whose rows are not 16-byte multiples
+    wq = (torch.rand(qs[3], generator=g) + 0.5).cuda() if qn else None
+    wk = (torch.rand(qs[3], generator=g) + 0.5).cuda() if kn else None
+    q1, k1 = q.clone(), k.clone()
+    M.masked_gqa_rope(q1, f, positions=pos, rot_dim=rot, heads=qh, interleaved=interleaved, norm_weight=wq)
+    M.masked_gqa_rope(k1, f, positions=pos, rot_dim=rot, heads=kh, interleaved=interleaved, norm_weight=wk)
+    M.masked_gqa_rope_pair(q, k, f, positions=pos, rot_dim=rot, q_heads=qh, k_heads=kh,
+                           interleaved=interleaved, q_norm_weight=wq, k_norm_weight=wk)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q1) and torch.equal(k, k1)
+    if kview:  # the features past the view are untouched
+        assert torch.equal(kfull[..., qs[3]:], make_x(12 + rot, *ks, dtype).cuda()[..., qs[3]:])
+
+
+def test_rope_pair_overlapping_tensors_rotate_in_turn(M):
+    """When q and k share elements the pair call rotates them one after the
+    other, as two calls would (here: the same tensor, rotated twice)."""
+    f = inv_freq_table(64).cuda()
+    x = make_x(21, 1, 4, 100, 64, torch.bfloat16).cuda()
+    ref = x.clone()
+    M.masked_gqa_rope(ref, f)
+    M.masked_gqa_rope(ref, f)
+    M.masked_gqa_rope_pair(x, x, f)
+    torch.cuda.synchronize()
+    assert torch.equal(x, ref)
+
+
+def test_rope_pair_rejects_mixed_dtypes_and_bad_args(M):
+    f = inv_freq_table(64).cuda()
+    q = make_x(1, 1, 2, 8, 64, torch.bfloat16).cuda()
+    k = make_x(2, 1, 2, 8, 64, torch.float16).cuda()
+    before = q.clone()
+    with pytest.raises(M.MgqaError):
+        M.masked_gqa_rope_pair(q, k, f)
+    with pytest.raises(M.MgqaError):
+        M.masked_gqa_rope_pair(q, q.clone(), f, k_heads=3)  # heads > H
+    torch.cuda.synchronize()
+    assert torch.equal(q, before)  # nothing was enqueued
