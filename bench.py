@@ -334,8 +334,7 @@ def bench_fused_rope(M, dev, nsets=8):
 
     def step_unfused():
         for (d, kn, vn, lo, out), p in zip(dsets, pos):
-            M.masked_gqa_rope(d["q"], f64, positions=p, norm_weight=w64)
-            M.masked_gqa_rope(kn, f64, positions=p, norm_weight=w64)
+            M.masked_gqa_rope_pair(d["q"], kn, f64, positions=p, q_norm_weight=w64, k_norm_weight=w64)
             M.masked_gqa_attn_decode_append(d["q"], d["k"], d["v"], kn, vn, d["kv_len"], out,
                                             kv_len_out=lo, scale=wd.scale)
 
@@ -780,7 +779,8 @@ def run_gpu(args):
         "workload": "rotary embedding with the q/k RMS norm (fp32 table, half-split pairs, all heads) "
                     "inside the call: padded-CFG prefill (kv_len form; q rotated in the kernel, k "
                     "already rotated) and the static-cache decode step with its append (q and the new "
-                    "key row rotated in the kernel), each against masked_gqa_rope + the plain call",
+                    "key row rotated in the kernel), each against the standalone rotation (decode step: "
+                    "q and the key row in one masked_gqa_rope_pair launch) + the plain call",
         "prefill_fused_us": tp_f * 1e6, "prefill_unfused_us": tp_u * 1e6,
         "prefill_fused_TFLOP_s": wr.flops() / tp_f / 1e12,
         "decode_step_fused_us": td_f * 1e6, "decode_step_unfused_us": td_u * 1e6,
