@@ -192,6 +192,23 @@ def test_rope_rejects_bad_arguments(L, mutate):
     assert L.masked_gqa_rope(ctypes.byref(a), None) == M.MGQA_ERR_INVALID_ARG
     assert L.mgqa_last_error_detail() != b""
     assert L.masked_gqa_rope(None, None) == M.MGQA_ERR_INVALID_ARG
+    # the pair entry checks both tensors before anything is enqueued and names the bad one
+    good = _valid_rope()
+    good.x = 1 << 24
+    assert L.masked_gqa_rope_pair(ctypes.byref(a), ctypes.byref(good), None) == M.MGQA_ERR_INVALID_ARG
+    assert b"(q)" in L.mgqa_last_error_detail()
+    assert L.masked_gqa_rope_pair(ctypes.byref(good), ctypes.byref(a), None) == M.MGQA_ERR_INVALID_ARG
+    assert b"(k)" in L.mgqa_last_error_detail()
+
+
+def test_rope_pair_rejects_mixed_dtypes_and_null(L):
+    q, k = _valid_rope(), _valid_rope()
+    k.x = 1 << 24
+    k.dtype = M.MGQA_FP16
+    assert L.masked_gqa_rope_pair(ctypes.byref(q), ctypes.byref(k), None) == M.MGQA_ERR_INVALID_ARG
+    assert b"dtypes differ" in L.mgqa_last_error_detail()
+    assert L.masked_gqa_rope_pair(ctypes.byref(q), None, None) == M.MGQA_ERR_INVALID_ARG
+    assert L.masked_gqa_rope_pair(None, ctypes.byref(q), None) == M.MGQA_ERR_INVALID_ARG
 
 
 def test_plain_c_program_links_and_calls_the_library(L, tmp_path):
