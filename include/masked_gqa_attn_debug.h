@@ -68,7 +68,7 @@ MGQA_API mgqa_status mgqa_debug_decode_timeline(uint64_t *out, int32_t n_ctas);
  * CTA -- the SM clock at 0 (entry), 1 (after the grid-dependency wait), 9
  * (the first copies issued and the segment range formed), 11 (the packed-bit
  * mask folded into per-tile bits), 12 (every key tile classified), 2 (the
- * non-empty tile list built), 3 (the first score MMAs issued), 10 (head 0's
+ * non-empty tiles counted), 3 (the first score MMAs issued), 10 (head 0's
  * first scores complete), 4 (head 0's first P handed over), 8 (the last P.V
  * MMAs issued), 5 (head 0's output complete), 6 (head 0's output tile
  * stored), 7 (head 0's epilogue done); the global timer (ns) at entry and at

@@ -146,14 +146,13 @@ struct Layout {
   static constexpr int n_bars = 1 + 4 * STAGES + 3 * NT + 2 + NT;
   static constexpr int misc_off = bar_off + 8 * n_bars;
   static constexpr int tmem_slot = misc_off;        // uint32
-  static constexpr int nk_slot = misc_off + 4;      // int32 (nk; bit 31: speculation missed)
   static constexpr int seg_slot = misc_off + 8;     // int32 x2 (min, max of seg_q)
   static constexpr int any_off = misc_off + 16;     // uint32[MAXKT/32]: tile has an allowed bit
   static constexpr int all_off = any_off + MAXKT / 8;  // uint32[MAXKT/32]: tile all allowed
-  static constexpr int list_off = all_off + MAXKT / 8;  // uint16[MAXKT]
-  static constexpr int cls_off = list_off + 2 * MAXKT;  // uint8[MAXKT]
+  static constexpr int ne_off = all_off + MAXKT / 8;   // uint32[MAXKT/32]: tile is non-empty
+  static constexpr int full_off = ne_off + MAXKT / 8;  // uint32[MAXKT/32]: tile needs no masking
   // fused rotation: the inverse frequencies and the q norm weights, staged once
-  static constexpr int rope_off = (cls_off + MAXKT + 15) & ~15;  // float[D / 2] then float[D]
+  static constexpr int rope_off = (full_off + MAXKT / 8 + 15) & ~15;  // float[D / 2] then float[D]
   static constexpr int total = rope_off + (D / 2 + D) * 4;
   static constexpr int smem_bytes = total + 1024;   // slack for 1024-B alignment
   static constexpr int threads = 128 * (1 + NT);
@@ -163,6 +162,17 @@ struct Layout {
                                         : tmem_cols_used <= 256 ? 256 : 512;
   static_assert(tmem_cols_used <= 512, "tensor memory");
 };
+
+// The first non-empty key tile after `prev` (-1: the first), or nkt.
+MGQA_DEV int next_tile(const uint32_t *ne, int prev, int nkt) {
+  int kt = prev + 1;
+  while (kt < nkt) {
+    const uint32_t w = ne[kt >> 5] >> (kt & 31);
+    if (w) return kt + __ffs(w) - 1;
+    kt = (kt | 31) + 1;
+  }
+  return nkt;
+}
 
 // Allowed-key words of one query row for a partial key tile (keys k0..k0+127).
 // Segment ids: each lane loads 4 of the tile's key ids (coalesced) and the
@@ -406,12 +416,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t *bar_drain = bar_spec + 1;
   uint64_t *bar_qrot = bar_drain + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Lay::tmem_slot);
-  int *nk_slot = reinterpret_cast<int *>(smem + Lay::nk_slot);
   int *seg_slot = reinterpret_cast<int *>(smem + Lay::seg_slot);
-  uint16_t *list = reinterpret_cast<uint16_t *>(smem + Lay::list_off);
   uint32_t *any_bits = reinterpret_cast<uint32_t *>(smem + Lay::any_off);
   uint32_t *all_bits = reinterpret_cast<uint32_t *>(smem + Lay::all_off);
-  uint8_t *cls = smem + Lay::cls_off;
+  uint32_t *ne_bits = reinterpret_cast<uint32_t *>(smem + Lay::ne_off);
+  uint32_t *full_bits = reinterpret_cast<uint32_t *>(smem + Lay::full_off);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
@@ -447,11 +456,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     allow_dependents();
   }
   if (warp == 1) tc::tmem_alloc(tmem_slot, Lay::tmem_cols);
-  if (p.mask.bits)
-    for (int w = tid; w < (p.nkt + 31) / 32; w += blockDim.x) {
+  for (int w = tid; w < (p.nkt + 31) / 32; w += blockDim.x) {
+    ne_bits[w] = 0u;
+    full_bits[w] = 0u;
+    if (p.mask.bits) {
       any_bits[w] = 0u;
       all_bits[w] = 0xffffffffu;
     }
+  }
   if (p.warm) {
     // before the grid-dependency wait, hints that move this CTA's first reads
     // toward the L2 (nothing enters the SM; the L2 is the point of coherence,
@@ -619,7 +631,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
   if (tid == 0) pre_stamp(11);
 
-  // ---- classify key tiles: 0 empty, 1 partial, 2 full ----------------------
+  // ---- classify key tiles: non-empty (ne_bits), and of those full (no masking)
   for (int kt = warp; kt < p.nkt; kt += nwarps) {
     const int k0 = kt * BN;
     bool ne = k0 < p.Lk;
@@ -656,30 +668,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (qmx < 0 || mx < 0 || qmx < mn || mx < qmn) ne = false;
       full = full && qmn == qmx && mn == mx && qmn == mn && qmn >= 0;
     }
-    if (lane == 0) cls[kt] = ne ? (full ? 2 : 1) : 0;
-  }
-  __syncthreads();
-  if (tid == 0) pre_stamp(12);
-  if (warp == 0) {
-    int count = 0;
-    for (int base = 0; base < p.nkt; base += 32) {
-      const int kt = base + lane;
-      const int c = kt < p.nkt ? cls[kt] : 0;
-      const uint32_t bal = __ballot_sync(0xffffffffu, c != 0);
-      const int pos = count + __popc(bal & ((1u << lane) - 1u));
-      if (c != 0) list[pos] = (uint16_t)(kt | (c == 1 ? 0x8000 : 0));
-      count += __popc(bal);
+    if (lane == 0 && ne) {
+      atomicOr(&ne_bits[kt >> 5], 1u << (kt & 31));
+      if (full) atomicOr(&full_bits[kt >> 5], 1u << (kt & 31));
     }
-    // speculation missed when the first non-empty tile is not tile 0
-    const bool miss = count == 0 || (list[0] & 0x7fff) != 0;
-    if (lane == 0) *nk_slot = count | (miss ? (int)0x80000000 : 0);
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  if (tid == 0) pre_stamp(12);
+  // every warp counts the non-empty tiles itself (no list, no second barrier);
+  // the roles walk the bitsets in order (next_tile)
+  int nk;
+  {
+    int cnt = 0;
+    for (int w = lane; w < (p.nkt + 31) / 32; w += 32) cnt += __popc(ne_bits[w]);
+    nk = __reduce_add_sync(0xffffffffu, cnt);
+  }
   if (tid == 0) pre_stamp(2);
-  const int nk = *nk_slot & 0x7fffffff;
-  const uint32_t spec_miss = (*nk_slot < 0) ? 1u : 0u;  // stage 0 holds a stale tile 0
+  // speculation missed when the first non-empty tile is not tile 0: stage 0
+  // then holds a stale tile 0
+  const uint32_t spec_miss = (nk == 0 || (ne_bits[0] & 1u) == 0u) ? 1u : 0u;
   const uint32_t tmem = *tmem_slot;
   const uint32_t sm_base = smem_u32(smem);
   bool ok = true;
@@ -695,9 +704,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if constexpr (NT == 2) tc::regs_dec<104>();
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      // list entries whose K (V) load has been issued; entry 0's went out
+      // non-empty tiles whose K (V) load has been issued; tile 0's went out
       // speculatively unless the speculation missed, in which case stage 0
-      // was armed once more than the entries say
+      // was armed once more than the tiles say
       int k_issued = (nk > 0 && !spec_miss) ? 1 : 0, v_issued = k_issued;
       const int extra0 = (nk == 0 || spec_miss) ? 1 : 0;
       if (nk == 0 || spec_miss) {
@@ -710,9 +719,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // consumers' bounded waits then give up and report MGQA_ERR_TIMEOUT)
       const int stop_at = fault_tile();
       // (an L2 prefetch of the tiles ahead of their loads measured no faster)
+      int kt = -1;  // the current non-empty tile
       for (int n = 0; n < nk && ok; ++n) {
         const int st = n % STAGES, use = n / STAGES;
-        const int kt = list[n] & 0x7fff;
+        kt = next_tile(ne_bits, kt, p.nkt);
         if (n == 0 && !spec_miss) continue;  // tile 0 is already on its way
         if (n == stop_at) break;
         if (!MGQA_DCHECK(kt * BN < p.Lk && g < p.Hkv, p.err)) break;
@@ -929,10 +939,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     const int tr = (lane == 0) ? ((8 + 4 * t) | (quarter << 8)) : -1;  // debug trace events
+    int kt = -1;  // the current non-empty tile
     for (int n = 0; n < nk; ++n) {
-      const int ent = list[n];
-      const int kt = ent & 0x7fff;
-      const bool partial = (ent & 0x8000) != 0;
+      kt = next_tile(ne_bits, kt, p.nkt);
+      const bool partial = !((full_bits[kt >> 5] >> (kt & 31)) & 1u);
       uint32_t mw[BN / 32] = {0u, 0u, 0u, 0u};
       if (partial) tile_mask_words(p, b, ic, row_ok, kt * BN, kvl, segq, lane, mw);
       // warp-uniform outcome: the tile pass below is made of warp-wide
