@@ -66,7 +66,7 @@ typedef enum {
   MGQA_OK = 0,
   MGQA_ERR_INVALID_ARG = 1,  /* bad pointer, shape, stride, alignment or scale;
                                 on the device: kv_len < 0 or kv_len > Lk */
-  MGQA_ERR_UNSUPPORTED = 2,  /* valid request this build has no kernel for */
+  MGQA_ERR_UNSUPPORTED = 2,  /* valid request the library has no kernel for */
   MGQA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
   MGQA_ERR_TIMEOUT = 4,      /* device: a bounded pipeline wait gave up */
   MGQA_ERR_DEVICE_CHECK = 5  /* device, debug library only: a bounds or alignment
